@@ -1,0 +1,22 @@
+"""fp64 CPU oracle for paged, prefix-shared, mixed-batch attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import, call or
+execute this package: only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` use it.  It shares no code with the CUDA
+library (no kernels, headers, helpers or tables) and never takes an input or
+an expected value from it.
+
+What it computes (``attention.paged_attention``), for every request r, new
+token j and query head h (kv head g = h // G, G = Hq / Hkv):
+
+    o[r, j, h] = sum_{p <= c_r + j} softmax_p(scale * q[r, j, h] . k[r, p, g]) v[r, p, g]
+
+with c_r the request's cached length and k[r, p, g] read through the paged
+block table.  Every function is pinned by ``tests/test_oracle_pins.py``
+against something other than itself (brute force on unpaged copies, closed
+forms, invariances); none is "parity unpinned".
+"""
+from .attention import (  # noqa: F401
+    reference_scatter, gather_request_kv, paged_attention, dense_attention_loops,
+    attention_partial, lse_merge, split_kv_attention,
+)
