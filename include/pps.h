@@ -1,0 +1,264 @@
+/*
+ * pps.h -- C ABI of the paged, prefix-shared, mixed-batch attention library
+ * (libpps.so, hand-written CUDA for sm_103a).
+ *
+ * The library computes, for one batch that mixes prefill chunks, single-token
+ * decode rows and multi-token speculative-verify rows, exact causal GQA
+ * attention over a paged KV cache whose pages may be shared between requests
+ * by a radix-tree prefix cache:
+ *
+ *   o[r, j, h] = sum_{p <= c_r + j} softmax_p(scale * q[r, j, h] . k[r, p, h / G]) v[r, p, h / G]
+ *
+ * for every request r, new token j (absolute position c_r + j, c_r = tokens
+ * cached before the step) and query head h, G = num_q_heads / num_kv_heads.
+ *
+ * Sources (page title and section):
+ *  - XY-Serve review, "Tackling the Dynamicity in a Production LLM Serving
+ *    System with SOTA Optimizations via Hybrid Prefill/Decode/Verify
+ *    Scheduling on Efficient Meta-kernels" (pith.science/paper/ABCKJ6RF):
+ *    "Core claim" (token-budgeted P/D/V batch; workload decomposition into
+ *    tile tasks recorded in token and task tables; one matmul-softmax-matmul
+ *    meta-kernel; mask sparsity skips invalid tiles), "What carries the
+ *    argument" (tiles sorted by computational area and assigned to cores
+ *    symmetrically round-robin), "Assumptions & free parameters" (PagedAttention
+ *    block table with radix-tree reuse and copy-on-write; online softmax equals
+ *    plain softmax; padded scores excluded).
+ *  - SGLang review, "SGLang: Efficient Execution of Structured Language Model
+ *    Programs" (pith.science/p/2312.07104), "Core claim": RadixAttention reuses
+ *    the KV cache of shared prefixes across requests.
+ *
+ * Conventions for every call:
+ *  - bf16 means IEEE bfloat16 (2 bytes), little endian.  All tensors are dense
+ *    and row-major with the shapes given; no strides are accepted.
+ *  - "device" pointers point to memory of the current CUDA device; "host"
+ *    pointers to ordinary (pageable or pinned) host memory.
+ *  - The caller owns every buffer it passes.  The library keeps no pointer to
+ *    them after a call returns, except that work it enqueued on `stream` still
+ *    reads/writes them until that work completes.
+ *  - Calls never throw and never abort.  They return PPS_OK (0) or a negative
+ *    pps_status.  Argument errors are detected on the host before anything is
+ *    enqueued.  Errors that only the GPU can see (a page id read from a device
+ *    array that is out of range) are recorded in a device error word; read it
+ *    with pps_get_device_error().  Kernels never trap.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Work is enqueued asynchronously on it.
+ *  - Supported shapes: head_dim in {64, 128}; page_size in {16, 32, 64, 128};
+ *    G = num_q_heads / num_kv_heads in {1, 2, 4, 8}.
+ */
+#ifndef PPS_H_
+#define PPS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t pps_status;
+
+#define PPS_OK 0
+#define PPS_ERR_INVALID_ARGUMENT (-1)  /* null pointer, negative size, mismatched shapes   */
+#define PPS_ERR_UNSUPPORTED (-2)       /* head_dim / page_size / G outside the supported set */
+#define PPS_ERR_PAGE_TABLE (-3)        /* indptr not monotone, page list too short, id out of range */
+#define PPS_ERR_WORKSPACE (-4)         /* workspace null or smaller than the plan requires  */
+#define PPS_ERR_CUDA (-5)              /* a CUDA runtime/driver call failed                 */
+#define PPS_ERR_NO_MEMORY (-6)         /* host allocation failed                            */
+#define PPS_ERR_SCRATCH_LIMIT (-7)     /* reserved for entry points with a fixed scratch cap */
+
+/* Device error word values (pps_get_device_error).  0 = no error. */
+#define PPS_DEV_ERR_APPEND_PAGE_ID 1     /* kv_append read a page id outside [0, num_pages)   */
+#define PPS_DEV_ERR_APPEND_PAGE_LIST 2   /* kv_append position beyond the request's page list */
+#define PPS_DEV_ERR_APPEND_REQUEST 3     /* kv_append token not inside q_indptr's range       */
+#define PPS_DEV_ERR_WAIT_TIMEOUT 4       /* a bounded pipeline wait in a kernel ran out       */
+
+/*
+ * The paged KV pool: two caller-owned device arrays, bf16,
+ * [num_pages, num_kv_heads, page_size, head_dim] (all slots of one page and
+ * one kv head are contiguous: page_size * head_dim * 2 bytes).
+ * Logical position p of request r lives in page
+ * page_indices[page_indptr[r] + p / page_size], slot p % page_size
+ * (PagedAttention block table; XY-Serve review, "Assumptions & free
+ * parameters").  Requests that share a cached prefix list the same page ids.
+ */
+typedef struct pps_pool {
+  void* k;
+  void* v;
+  int32_t num_pages;
+  int32_t num_kv_heads;
+  int32_t page_size;
+  int32_t head_dim;
+} pps_pool;
+
+/*
+ * pps_kv_append -- write this step's new K/V rows into their pool pages.
+ *
+ * New token j of request r (row q_indptr[r] + j of k_new / v_new) goes to
+ * logical position cached_len[r] + j.  Definition: the paged block table of
+ * the XY-Serve review ("Assumptions & free parameters") with chunked-prefill,
+ * decode and verify rows appended the same way ("Core claim").
+ *
+ *  pool          host pointer to the pool descriptor (its k/v are device).
+ *  k_new, v_new  device, bf16 [num_new_tokens, num_kv_heads, head_dim].
+ *  q_indptr      device int32 [num_requests + 1], q_indptr[0] = 0, nondecreasing,
+ *                q_indptr[num_requests] = num_new_tokens.
+ *  cached_len    device int32 [num_requests].
+ *  page_indptr   device int32 [num_requests + 1]; page_indices device int32 [nnz].
+ * The copy is bit exact.  Because the tables are device arrays the host only
+ * checks sizes and pointers; a page id or position out of range is skipped
+ * and recorded in the device error word (PPS_DEV_ERR_APPEND_*).
+ * Rows of different requests must not map to the same slot (undefined order).
+ */
+pps_status pps_kv_append(const pps_pool* pool, const void* k_new, const void* v_new,
+                         const int32_t* q_indptr, const int32_t* cached_len,
+                         const int32_t* page_indptr, const int32_t* page_indices,
+                         int32_t num_requests, int32_t num_new_tokens, void* stream);
+
+/* Optional planner knobs; pass NULL for defaults.  Zero fields take defaults. */
+typedef struct pps_plan_options {
+  int32_t num_sms;          /* SMs to balance over; 0 = query the current device (152 if none) */
+  int32_t bw_chunk_tokens;  /* KV tokens per split-KV task on the bandwidth path; 0 = adaptive    */
+  int32_t mma_chunk_tokens; /* KV tokens per tensor-core task (multiple of 128); 0 = adaptive     */
+  int32_t flags;            /* PPS_PLAN_* bits                                                   */
+} pps_plan_options;
+
+#define PPS_PLAN_NO_GROUPS 1      /* do not merge shared-prefix pages into group tasks            */
+#define PPS_PLAN_CUDA_CORES_ONLY 2 /* route every task to the CUDA-core kernel (no tcgen05 tiles) */
+
+typedef struct pps_plan pps_plan;
+
+/*
+ * pps_attn_plan -- decompose one batch into a work-sorted tile task table.
+ *
+ * Host-only (no CUDA call unless opts->num_sms is 0 and a device exists).
+ * Follows the XY-Serve review's workload decomposition and task reordering
+ * ("Core claim", "What carries the argument"):
+ *  1. a radix tree over each request's fully cached page ids finds runs of
+ *     pages shared by >= 2 requests (SGLang review, "Core claim"); each run
+ *     becomes one group task per kv head that attends all of its members'
+ *     query rows against those pages, so shared pages are read once per group;
+ *  2. each request's remaining positions (private pages and this step's new
+ *     tokens, causal) become request tasks;
+ *  3. tasks with few query rows go to the bandwidth (split-KV, CUDA-core)
+ *     kernel, wider ones to the tcgen05 tensor-core kernel in 128-row tiles;
+ *     fully masked causal tiles are never created;
+ *  4. tasks are sorted by work (rows x KV tokens) in descending order;
+ *  5. every (token, head) covered by more than one task gets partial slots
+ *     that a merge kernel combines by log-sum-exp.
+ *
+ *  q_indptr     host int32 [num_requests + 1]: new-token offsets (q_indptr[0] = 0).
+ *  kv_len       host int32 [num_requests]: cached + new tokens of each request.
+ *  page_indptr  host int32 [num_requests + 1]; page_indices host int32 [nnz]
+ *               (identical ids in two requests' lists mean shared pages).
+ *  num_pages    pool size, for range checks.
+ *  sm_scale     softmax scale (normally 1/sqrt(head_dim)); must be finite.
+ * On success *out_plan owns a host copy of everything the kernels need and
+ * *out_workspace_bytes is the device workspace pps_attn_run requires.
+ * The input arrays may be freed or changed after the call returns.
+ * Errors: PPS_ERR_INVALID_ARGUMENT, PPS_ERR_UNSUPPORTED, PPS_ERR_PAGE_TABLE,
+ * PPS_ERR_NO_MEMORY; *out_plan is then NULL.
+ */
+pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_len,
+                         const int32_t* page_indptr, const int32_t* page_indices,
+                         int32_t num_requests, int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t page_size, int32_t num_pages, float sm_scale,
+                         const pps_plan_options* opts, pps_plan** out_plan,
+                         size_t* out_workspace_bytes);
+
+/*
+ * pps_attn_run -- the mixed-batch attention.
+ *
+ *  q          device bf16 [num_new_tokens, num_q_heads, head_dim].
+ *  pool       host descriptor; its pages must already hold every row the step
+ *             attends to (call pps_kv_append first for this step's rows).
+ *  out        device bf16 [num_new_tokens, num_q_heads, head_dim]; every row is
+ *             written.
+ *  workspace  device, >= the plan's workspace bytes, 256-byte aligned; holds the
+ *             uploaded task table and fp32 partials.  It must not be used by
+ *             other work in flight on another stream.
+ * Enqueues: one host-to-device copy of the task table (from the plan's host
+ * memory; the call returns only after the source has been consumed, so the
+ * plan may be destroyed right after), then up to three kernels (bandwidth
+ * tasks, tensor-core tasks, partial merge).  A plan may be run any number of
+ * times.
+ */
+pps_status pps_attn_run(const pps_plan* plan, const void* q, const pps_pool* pool, void* out,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Same as pps_attn_run, and records caller-created CUDA events (cudaEvent_t
+ * passed as void*, any may be NULL) on `stream` immediately before and after
+ * each kernel class: events[2*i] / events[2*i+1] for i = PPS_KERNEL_*.
+ * A class that has no work this step records both events back to back. */
+#define PPS_KERNEL_BANDWIDTH 0
+#define PPS_KERNEL_TENSOR 1
+#define PPS_KERNEL_MERGE 2
+#define PPS_NUM_KERNEL_CLASSES 3
+pps_status pps_attn_run_events(const pps_plan* plan, const void* q, const pps_pool* pool,
+                               void* out, void* workspace, size_t workspace_bytes, void* stream,
+                               void* const* events);
+
+/* Frees a plan (host memory only).  NULL is accepted. */
+pps_status pps_plan_destroy(pps_plan* plan);
+
+/* Plan summary, for tests and reports. */
+typedef struct pps_plan_info {
+  int32_t num_requests, num_tokens, num_q_heads, num_kv_heads, head_dim, page_size;
+  int32_t num_groups;          /* shared-prefix group nodes found                       */
+  int64_t num_bw_tasks;        /* bandwidth-kernel tasks (all kv heads)                 */
+  int64_t num_mma_tasks;       /* tensor-core tasks (all kv heads)                      */
+  int64_t num_partials;        /* partial slots (per token; x num_q_heads rows each)    */
+  int64_t num_merge_tokens;    /* tokens whose rows are combined by the merge kernel    */
+  int64_t table_bytes;         /* bytes of the device task table                        */
+  int64_t workspace_bytes;
+  int64_t kv_bytes_unique;     /* K+V bytes of distinct (page, kv head, valid slot)      */
+  int64_t kv_bytes_read;       /* K+V bytes the tasks read (shared runs counted once)    */
+  double flops_mma;            /* 4*d per visible (query row, key) pair on tensor tasks  */
+  double flops_total;          /* same over all tasks                                   */
+} pps_plan_info;
+pps_status pps_plan_get_info(const pps_plan* plan, pps_plan_info* info);
+
+/*
+ * Read-only views of the plan's tables (host memory owned by the plan, valid
+ * until pps_plan_destroy).  Task records are PPS_TASK_INTS int32 each:
+ *   [0] row_off    first entry of this task's tokens in the ROWS array
+ *   [1] n_tok      number of query tokens (rows = n_tok * G)
+ *   [2] kv_head
+ *   [3] page_off   offset of the request's page list in the PAGES array
+ *   [4] kv_begin   first logical KV position read
+ *   [5] kv_end     one past the last logical KV position read
+ *   [6] causal     token i of the task sees positions <= causal + i
+ *                  (PPS_NO_CAUSAL: no causal limit inside [kv_begin, kv_end))
+ *   [7] out_pid    -1: write final output rows; else token i writes partial
+ *                  slot out_pid + i (rows (out_pid + i) * num_q_heads + h)
+ * MERGE_INDPTR / MERGE_PIDS list, for each token in MERGE_TOKENS, its partials.
+ */
+#define PPS_TASK_INTS 8
+#define PPS_NO_CAUSAL 0x3fffffff
+#define PPS_ARRAY_BW_TASKS 0
+#define PPS_ARRAY_MMA_TASKS 1
+#define PPS_ARRAY_ROWS 2
+#define PPS_ARRAY_PAGES 3
+#define PPS_ARRAY_MERGE_TOKENS 4
+#define PPS_ARRAY_MERGE_INDPTR 5
+#define PPS_ARRAY_MERGE_PIDS 6
+pps_status pps_plan_get_array(const pps_plan* plan, int32_t which, const int32_t** data,
+                              int64_t* count);
+
+/* Reads the current device's error word into *code (0 = none); if `clear`
+ * is nonzero, resets it to 0.  Synchronous (waits for the device). */
+pps_status pps_get_device_error(int32_t* code, int32_t clear);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t pps_launch_count(void);
+
+/* Static description of a status code (never NULL). */
+const char* pps_status_string(pps_status status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int32_t pps_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PPS_H_ */

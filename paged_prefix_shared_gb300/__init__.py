@@ -1,0 +1,258 @@
+"""Python binding of libpps.so: paged, prefix-shared, mixed-batch attention
+for GB300 (sm_103a).
+
+Argument marshalling only: every step of the attention path runs in the
+library's CUDA kernels.  PyTorch provides device memory and streams.  The
+binding raises ``PPSError`` when the library is missing or a call fails; there
+is no fallback.
+
+    plan = attn_plan(q_indptr, kv_len, page_indptr, page_indices, Hq, Hkv, d, P, num_pages)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    kv_append(pool_k, pool_v, k_new, v_new, q_indptr_d, cached_len_d, page_indptr_d, page_indices_d)
+    attn_run(plan, q, pool_k, pool_v, out, ws)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import numpy as np
+
+__all__ = [
+    "PPSError", "Plan", "lib", "build", "kv_append", "attn_plan", "attn_run", "plan_destroy",
+    "get_device_error", "launch_count", "status_string", "version", "LIB_PATH",
+    "PLAN_NO_GROUPS", "PLAN_CUDA_CORES_ONLY", "KERNEL_BANDWIDTH", "KERNEL_TENSOR", "KERNEL_MERGE",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpps.so")
+
+PLAN_NO_GROUPS = 1
+PLAN_CUDA_CORES_ONLY = 2
+KERNEL_BANDWIDTH, KERNEL_TENSOR, KERNEL_MERGE = 0, 1, 2
+NUM_KERNEL_CLASSES = 3
+TASK_INTS = 8
+NO_CAUSAL = 0x3FFFFFFF
+ARRAYS = {"bw_tasks": 0, "mma_tasks": 1, "rows": 2, "pages": 3, "merge_tokens": 4,
+          "merge_indptr": 5, "merge_pids": 6}
+
+
+class PPSError(RuntimeError):
+    pass
+
+
+class _Pool(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_pages", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32)]
+
+
+class _PlanOptions(ctypes.Structure):
+    _fields_ = [("num_sms", ctypes.c_int32), ("bw_chunk_tokens", ctypes.c_int32),
+                ("mma_chunk_tokens", ctypes.c_int32), ("flags", ctypes.c_int32)]
+
+
+class _PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_requests", "num_tokens", "num_q_heads", "num_kv_heads", "head_dim", "page_size",
+        "num_groups")] + [(n, ctypes.c_int64) for n in (
+            "num_bw_tasks", "num_mma_tasks", "num_partials", "num_merge_tokens", "table_bytes",
+            "workspace_bytes", "kv_bytes_unique", "kv_bytes_read")] + [
+        ("flops_mma", ctypes.c_double), ("flops_total", ctypes.c_double)]
+
+
+_lib = None
+_I32P = ctypes.POINTER(ctypes.c_int32)
+
+
+def build(force: bool = False) -> str:
+    """Compile libpps.so in place (nvcc, sm_103a)."""
+    from .build import build as _build
+    return _build(force=force)
+
+
+def lib():
+    """The loaded library (raises PPSError if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise PPSError(f"{LIB_PATH} is missing: build it with paged_prefix_shared_gb300.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    L.pps_kv_append.argtypes = [ctypes.POINTER(_Pool), vp, vp, vp, vp, vp, vp, i32, i32, vp]
+    L.pps_attn_plan.argtypes = [_I32P, _I32P, _I32P, _I32P, i32, i32, i32, i32, i32, i32,
+                                ctypes.c_float, ctypes.POINTER(_PlanOptions),
+                                ctypes.POINTER(vp), ctypes.POINTER(sz)]
+    L.pps_attn_run.argtypes = [vp, vp, ctypes.POINTER(_Pool), vp, vp, sz, vp]
+    L.pps_attn_run_events.argtypes = [vp, vp, ctypes.POINTER(_Pool), vp, vp, sz, vp,
+                                      ctypes.POINTER(vp)]
+    L.pps_plan_destroy.argtypes = [vp]
+    L.pps_plan_get_info.argtypes = [vp, ctypes.POINTER(_PlanInfo)]
+    L.pps_plan_get_array.argtypes = [vp, i32, ctypes.POINTER(_I32P), ctypes.POINTER(ctypes.c_int64)]
+    L.pps_get_device_error.argtypes = [_I32P, i32]
+    L.pps_launch_count.restype = ctypes.c_uint64
+    L.pps_status_string.restype = ctypes.c_char_p
+    L.pps_status_string.argtypes = [i32]
+    L.pps_version.restype = i32
+    for f in (L.pps_kv_append, L.pps_attn_plan, L.pps_attn_run, L.pps_attn_run_events,
+              L.pps_plan_destroy, L.pps_plan_get_info, L.pps_plan_get_array,
+              L.pps_get_device_error):
+        f.restype = i32
+    _lib = L
+    return L
+
+
+def status_string(code: int) -> str:
+    return lib().pps_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise PPSError(f"{what}: {status_string(code)} ({code})")
+
+
+def version() -> int:
+    return int(lib().pps_version())
+
+
+def launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(lib().pps_launch_count())
+
+
+def _host_i32(a):
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return a, a.ctypes.data_as(_I32P)
+
+
+def _dev(t, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise PPSError("tensors must be contiguous CUDA tensors")
+    if dtype is not None and t.dtype != dtype:
+        raise PPSError(f"expected {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _pool(pool_k, pool_v):
+    import torch
+    if pool_k.shape != pool_v.shape or pool_k.dim() != 4:
+        raise PPSError("pool_k / pool_v must both be [num_pages, Hkv, page_size, head_dim]")
+    n, h, p, d = pool_k.shape
+    return _Pool(_dev(pool_k, torch.bfloat16), _dev(pool_v, torch.bfloat16), n, h, p, d)
+
+
+def kv_append(pool_k, pool_v, k_new, v_new, q_indptr, cached_len, page_indptr, page_indices,
+              stream=None):
+    """pps_kv_append: all arguments are CUDA tensors (int32 tables, bf16 rows)."""
+    import torch
+    pool = _pool(pool_k, pool_v)
+    R = int(cached_len.shape[0])
+    T = int(k_new.shape[0])
+    _check(lib().pps_kv_append(ctypes.byref(pool), _dev(k_new, torch.bfloat16),
+                               _dev(v_new, torch.bfloat16), _dev(q_indptr, torch.int32),
+                               _dev(cached_len, torch.int32), _dev(page_indptr, torch.int32),
+                               _dev(page_indices, torch.int32), R, T, _stream(stream)),
+           "pps_kv_append")
+
+
+class Plan:
+    """Owner of a pps_plan (host memory); freed by destroy() or garbage collection."""
+
+    def __init__(self, handle, workspace_bytes):
+        self._h = handle
+        self.workspace_bytes = int(workspace_bytes)
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise PPSError("plan already destroyed")
+        return self._h
+
+    def info(self) -> dict:
+        inf = _PlanInfo()
+        _check(lib().pps_plan_get_info(self.handle, ctypes.byref(inf)), "pps_plan_get_info")
+        return {n: getattr(inf, n) for n, _ in _PlanInfo._fields_}
+
+    def array(self, name) -> np.ndarray:
+        ptr = _I32P()
+        cnt = ctypes.c_int64()
+        _check(lib().pps_plan_get_array(self.handle, ARRAYS[name], ctypes.byref(ptr),
+                                        ctypes.byref(cnt)), "pps_plan_get_array")
+        if cnt.value == 0:
+            a = np.zeros(0, dtype=np.int32)
+        else:
+            a = np.ctypeslib.as_array(ptr, shape=(cnt.value,)).copy()
+        return a.reshape(-1, TASK_INTS) if name.endswith("tasks") else a
+
+    def destroy(self):
+        if self._h is not None:
+            lib().pps_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def attn_plan(q_indptr, kv_len, page_indptr, page_indices, num_q_heads, num_kv_heads, head_dim,
+              page_size, num_pages, sm_scale=None, num_sms=0, bw_chunk_tokens=0,
+              mma_chunk_tokens=0, flags=0) -> Plan:
+    """pps_attn_plan on host int32 arrays (numpy or lists)."""
+    qi, qi_p = _host_i32(q_indptr)
+    kl, kl_p = _host_i32(kv_len)
+    pi, pi_p = _host_i32(page_indptr)
+    px, px_p = _host_i32(page_indices if len(page_indices) else np.zeros(1, np.int32))
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(head_dim)
+    opts = _PlanOptions(int(num_sms), int(bw_chunk_tokens), int(mma_chunk_tokens), int(flags))
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    _check(lib().pps_attn_plan(qi_p, kl_p, pi_p, px_p, len(kl), int(num_q_heads),
+                               int(num_kv_heads), int(head_dim), int(page_size), int(num_pages),
+                               float(sm_scale), ctypes.byref(opts), ctypes.byref(h),
+                               ctypes.byref(ws)), "pps_attn_plan")
+    return Plan(h, ws.value)
+
+
+def plan_destroy(plan: Plan):
+    plan.destroy()
+
+
+def attn_run(plan: Plan, q, pool_k, pool_v, out, workspace, stream=None, events=None):
+    """pps_attn_run (or pps_attn_run_events when `events` is a list of
+    2 * NUM_KERNEL_CLASSES torch.cuda.Event objects / None)."""
+    import torch
+    pool = _pool(pool_k, pool_v)
+    ws = _dev(workspace)
+    nbytes = workspace.numel() * workspace.element_size()
+    if events is None:
+        code = lib().pps_attn_run(plan.handle, _dev(q, torch.bfloat16), ctypes.byref(pool),
+                                  _dev(out, torch.bfloat16), ws, nbytes, _stream(stream))
+    else:
+        handles = []
+        for e in events:
+            if e is not None and not e.cuda_event:
+                e.record()          # torch creates the CUDA event on first record
+            handles.append(ctypes.c_void_p(e.cuda_event) if e is not None else None)
+        arr = (ctypes.c_void_p * (2 * NUM_KERNEL_CLASSES))(*handles)
+        code = lib().pps_attn_run_events(plan.handle, _dev(q, torch.bfloat16), ctypes.byref(pool),
+                                         _dev(out, torch.bfloat16), ws, nbytes, _stream(stream),
+                                         arr)
+    _check(code, "pps_attn_run")
+
+
+def get_device_error(clear: bool = True) -> int:
+    code = ctypes.c_int32()
+    _check(lib().pps_get_device_error(ctypes.byref(code), int(bool(clear))), "pps_get_device_error")
+    return int(code.value)

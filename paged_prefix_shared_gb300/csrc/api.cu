@@ -1,0 +1,188 @@
+// C ABI of libpps.so (declared in include/pps.h): argument checks, task-table
+// upload and kernel launches.  Every step of the attention path runs in this
+// library's kernels; there is no host fallback.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "pps_internal.h"
+
+// Device error word (one per device that loads the library).
+__device__ int32_t g_pps_device_error = 0;
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+int32_t* g_err_ptr[kMaxDevices] = {nullptr};
+std::mutex g_err_mu;
+
+// Device address of the error word on the current device (looked up once per device).
+int32_t* error_word(cudaError_t* status) {
+  int dev = 0;
+  *status = cudaGetDevice(&dev);
+  if (*status != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    *status = cudaGetSymbolAddress(&p, g_pps_device_error);
+    if (*status != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = (int32_t*)p;
+  }
+  return g_err_ptr[dev];
+}
+
+bool pool_ok(const pps_pool* p) {
+  return p && p->k && p->v && p->num_pages > 0 && p->num_kv_heads > 0 &&
+         (p->page_size == 16 || p->page_size == 32 || p->page_size == 64 || p->page_size == 128) &&
+         (p->head_dim == 64 || p->head_dim == 128);
+}
+
+pps_status run_impl(const pps_plan* plan, const void* q, const pps_pool* pool, void* out,
+                    void* workspace, size_t workspace_bytes, void* stream, void* const* events) {
+  if (!plan || !pool || (plan->num_tokens > 0 && (!q || !out))) return PPS_ERR_INVALID_ARGUMENT;
+  if (!pool_ok(pool)) return pool && (pool->head_dim != 64 && pool->head_dim != 128) ?
+                                  PPS_ERR_UNSUPPORTED : PPS_ERR_INVALID_ARGUMENT;
+  const pps::Shape& s = plan->shape;
+  if (pool->num_kv_heads != s.num_kv_heads || pool->page_size != s.page_size ||
+      pool->head_dim != s.head_dim || pool->num_pages < s.num_pages)
+    return PPS_ERR_INVALID_ARGUMENT;
+  if (!workspace || workspace_bytes < plan->workspace_bytes || ((uintptr_t)workspace & 255))
+    return PPS_ERR_WORKSPACE;
+  if (((uintptr_t)q & 15) || ((uintptr_t)out & 15) || ((uintptr_t)pool->k & 15) ||
+      ((uintptr_t)pool->v & 15))
+    return PPS_ERR_INVALID_ARGUMENT;
+  cudaError_t e;
+  int32_t* err = error_word(&e);
+  if (!err) return PPS_ERR_CUDA;
+  auto st = (cudaStream_t)stream;
+  auto rec = [&](int i) {
+    if (events && events[i]) return cudaEventRecord((cudaEvent_t)events[i], st);
+    return cudaSuccess;
+  };
+  if (plan->num_tokens == 0) {
+    for (int i = 0; i < 2 * PPS_NUM_KERNEL_CLASSES; ++i)
+      if (rec(i) != cudaSuccess) return PPS_ERR_CUDA;
+    return PPS_OK;
+  }
+  char* ws = (char*)workspace;
+  // The plan's table is pageable host memory: the copy returns once the
+  // source has been staged, so the plan may be freed as soon as we return.
+  e = cudaMemcpyAsync(ws, plan->image.data(), plan->image.size() * 4, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return PPS_ERR_CUDA;
+  const int32_t* base = (const int32_t*)ws;
+  const auto& L = plan->layout;
+  pps::DeviceTables t;
+  t.bw_tasks = (const pps::Task*)(base + L.bw_tasks);
+  t.mma_tasks = (const pps::Task*)(base + L.mma_tasks);
+  t.rows = base + L.rows;
+  t.pages = base + L.pages;
+  t.merge_tokens = base + L.merge_tokens;
+  t.merge_indptr = base + L.merge_indptr;
+  t.merge_pids = base + L.merge_pids;
+  t.o_part = (float*)(ws + plan->table_bytes);
+  t.lse_part = (float*)(ws + plan->table_bytes + plan->partial_o_bytes);
+
+  if (rec(2 * PPS_KERNEL_BANDWIDTH) != cudaSuccess) return PPS_ERR_CUDA;
+  if (pps::launch_bw_attention(s, t, plan->num_bw, q, *pool, out, err, stream)) return PPS_ERR_CUDA;
+  if (rec(2 * PPS_KERNEL_BANDWIDTH + 1) != cudaSuccess) return PPS_ERR_CUDA;
+  if (rec(2 * PPS_KERNEL_TENSOR) != cudaSuccess) return PPS_ERR_CUDA;
+  if (plan->num_mma &&
+      pps::launch_mma_attention(s, t, plan->num_mma, q, *pool, out, err, stream))
+    return PPS_ERR_CUDA;
+  if (rec(2 * PPS_KERNEL_TENSOR + 1) != cudaSuccess) return PPS_ERR_CUDA;
+  if (rec(2 * PPS_KERNEL_MERGE) != cudaSuccess) return PPS_ERR_CUDA;
+  if (pps::launch_merge(s, t, plan->num_merge_tokens, out, stream)) return PPS_ERR_CUDA;
+  if (rec(2 * PPS_KERNEL_MERGE + 1) != cudaSuccess) return PPS_ERR_CUDA;
+  return PPS_OK;
+}
+
+}  // namespace
+
+namespace pps {
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 0; }
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+}  // namespace pps
+
+extern "C" {
+
+pps_status pps_kv_append(const pps_pool* pool, const void* k_new, const void* v_new,
+                         const int32_t* q_indptr, const int32_t* cached_len,
+                         const int32_t* page_indptr, const int32_t* page_indices,
+                         int32_t num_requests, int32_t num_new_tokens, void* stream) {
+  if (!pool || num_requests < 0 || num_new_tokens < 0) return PPS_ERR_INVALID_ARGUMENT;
+  if (pool->head_dim != 64 && pool->head_dim != 128) return PPS_ERR_UNSUPPORTED;
+  if (!pool_ok(pool)) return PPS_ERR_INVALID_ARGUMENT;
+  if (num_new_tokens == 0) return PPS_OK;
+  if (num_requests == 0 || !k_new || !v_new || !q_indptr || !cached_len || !page_indptr ||
+      !page_indices)
+    return PPS_ERR_INVALID_ARGUMENT;
+  if (((uintptr_t)k_new & 15) || ((uintptr_t)v_new & 15) || ((uintptr_t)pool->k & 15) ||
+      ((uintptr_t)pool->v & 15))
+    return PPS_ERR_INVALID_ARGUMENT;
+  cudaError_t e;
+  int32_t* err = error_word(&e);
+  if (!err) return PPS_ERR_CUDA;
+  return pps::launch_kv_append(*pool, k_new, v_new, q_indptr, cached_len, page_indptr,
+                               page_indices, num_requests, num_new_tokens, err, stream)
+             ? PPS_ERR_CUDA : PPS_OK;
+}
+
+pps_status pps_attn_run(const pps_plan* plan, const void* q, const pps_pool* pool, void* out,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  return run_impl(plan, q, pool, out, workspace, workspace_bytes, stream, nullptr);
+}
+
+pps_status pps_attn_run_events(const pps_plan* plan, const void* q, const pps_pool* pool,
+                               void* out, void* workspace, size_t workspace_bytes, void* stream,
+                               void* const* events) {
+  return run_impl(plan, q, pool, out, workspace, workspace_bytes, stream, events);
+}
+
+pps_status pps_get_device_error(int32_t* code, int32_t clear) {
+  if (!code) return PPS_ERR_INVALID_ARGUMENT;
+  *code = 0;
+  if (cudaMemcpyFromSymbol(code, g_pps_device_error, sizeof(int32_t)) != cudaSuccess)
+    return PPS_ERR_CUDA;
+  if (clear) {
+    const int32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_pps_device_error, &zero, sizeof(int32_t)) != cudaSuccess)
+      return PPS_ERR_CUDA;
+  }
+  return PPS_OK;
+}
+
+uint64_t pps_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* pps_status_string(pps_status s) {
+  switch (s) {
+    case PPS_OK: return "ok";
+    case PPS_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case PPS_ERR_UNSUPPORTED: return "unsupported head_dim, page_size or head ratio";
+    case PPS_ERR_PAGE_TABLE: return "malformed page table";
+    case PPS_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case PPS_ERR_CUDA: return "CUDA call failed";
+    case PPS_ERR_NO_MEMORY: return "host allocation failed";
+    case PPS_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch limit";
+    default: return "unknown status";
+  }
+}
+
+int32_t pps_version(void) { return 100; }
+
+}  // extern "C"

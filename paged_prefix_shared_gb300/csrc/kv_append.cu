@@ -1,0 +1,95 @@
+// kv_append: scatter this step's new K/V rows into their pool pages.
+//
+// Definition: PagedAttention block table (XY-Serve review, "Assumptions & free
+// parameters"); new token j of request r is written at logical position
+// cached_len[r] + j, i.e. page page_indices[page_indptr[r] + p / P], slot p % P.
+//
+// One warp per (token, kv head): lanes copy the head_dim-long K row and V row
+// with 16-byte vector loads/stores (head_dim 128 -> 16 lanes per row, K and V
+// in the two half-warps).  Pure data movement: bit exact by construction.
+#include <cuda_runtime.h>
+
+#include "pps_internal.h"
+
+namespace {
+
+__device__ __forceinline__ void set_error(int32_t* err, int32_t code) {
+  atomicCAS(err, 0, code);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) kv_append_kernel(
+    int4* __restrict__ pool_k, int4* __restrict__ pool_v, const int4* __restrict__ k_new,
+    const int4* __restrict__ v_new, const int32_t* __restrict__ q_indptr,
+    const int32_t* __restrict__ cached_len, const int32_t* __restrict__ page_indptr,
+    const int32_t* __restrict__ page_indices, int32_t num_requests, int32_t num_tokens,
+    int32_t num_kv_heads, int32_t page_size, int32_t num_pages, int32_t* __restrict__ err) {
+  constexpr int kVec = D * 2 / 16;                  // int4 per row (8 or 16)
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int t = warp / num_kv_heads;
+  const int h = warp - t * num_kv_heads;
+  if (t >= num_tokens) return;
+  // request of token t: last r with q_indptr[r] <= t
+  int lo = 0, hi = num_requests;                    // invariant: q_indptr[lo] <= t < q_indptr[hi]
+  if (q_indptr[0] > t || q_indptr[num_requests] <= t) {
+    if (lane == 0) set_error(err, PPS_DEV_ERR_APPEND_REQUEST);
+    return;
+  }
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (q_indptr[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int r = lo;
+  const int p = cached_len[r] + (t - q_indptr[r]);
+  const int pi = p / page_size;
+  const int npg = page_indptr[r + 1] - page_indptr[r];
+  if (p < 0 || pi >= npg) {
+    if (lane == 0) set_error(err, PPS_DEV_ERR_APPEND_PAGE_LIST);
+    return;
+  }
+  const int page = page_indices[page_indptr[r] + pi];
+  if (page < 0 || page >= num_pages) {
+    if (lane == 0) set_error(err, PPS_DEV_ERR_APPEND_PAGE_ID);
+    return;
+  }
+  const int slot = p - pi * page_size;
+  const size_t dst = (((size_t)page * num_kv_heads + h) * page_size + slot) * kVec;
+  const size_t src = ((size_t)t * num_kv_heads + h) * kVec;
+  if (kVec == 16) {
+    if (lane < 16) pool_k[dst + lane] = __ldg(k_new + src + lane);
+    else pool_v[dst + lane - 16] = __ldg(v_new + src + lane - 16);
+  } else {
+    if (lane < kVec) pool_k[dst + lane] = __ldg(k_new + src + lane);
+    else if (lane < 2 * kVec) pool_v[dst + lane - kVec] = __ldg(v_new + src + lane - kVec);
+  }
+}
+
+}  // namespace
+
+namespace pps {
+
+int launch_kv_append(const pps_pool& pool, const void* k_new, const void* v_new,
+                     const int32_t* q_indptr, const int32_t* cached_len,
+                     const int32_t* page_indptr, const int32_t* page_indices,
+                     int32_t num_requests, int32_t num_new_tokens, int32_t* err, void* stream) {
+  const int64_t warps = (int64_t)num_new_tokens * pool.num_kv_heads;
+  if (warps == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (warps * 32 + threads - 1) / threads;
+  auto s = (cudaStream_t)stream;
+  if (pool.head_dim == 128)
+    kv_append_kernel<128><<<(unsigned)blocks, threads, 0, s>>>(
+        (int4*)pool.k, (int4*)pool.v, (const int4*)k_new, (const int4*)v_new, q_indptr,
+        cached_len, page_indptr, page_indices, num_requests, num_new_tokens, pool.num_kv_heads,
+        pool.page_size, pool.num_pages, err);
+  else
+    kv_append_kernel<64><<<(unsigned)blocks, threads, 0, s>>>(
+        (int4*)pool.k, (int4*)pool.v, (const int4*)k_new, (const int4*)v_new, q_indptr,
+        cached_len, page_indptr, page_indices, num_requests, num_new_tokens, pool.num_kv_heads,
+        pool.page_size, pool.num_pages, err);
+  count_launch();
+  return (int)cudaGetLastError();
+}
+
+}  // namespace pps

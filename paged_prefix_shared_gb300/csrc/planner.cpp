@@ -1,0 +1,433 @@
+// Host tile planner: turns one mixed prefill/decode/verify batch into a
+// work-sorted task table (pps_attn_plan).
+//
+// Follows the XY-Serve review (pith.science/paper/ABCKJ6RF): "Core claim"
+// (every stage's attention decomposed into tile tasks recorded in tables),
+// "What carries the argument" (tiles sorted by computational area before they
+// are handed to cores), and the SGLang review (pith.science/p/2312.07104),
+// "Core claim" (RadixAttention: requests that share a cached prefix share its
+// KV).  Shared runs of pages are found with a radix tree over page ids, built
+// here from the lexicographically sorted page lists and their longest common
+// prefixes.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <numeric>
+
+#include "pps_internal.h"
+
+namespace {
+
+using pps::Task;
+
+struct Segment {       // KV positions [kv_begin, kv_end) of one page list, with query tokens
+  int32_t row_off;     // first token in the rows array
+  int32_t n_tok;
+  int32_t page_off;
+  int32_t kv_begin, kv_end;
+  bool causal;         // private segment: token i sees positions <= c + i
+  int32_t c;
+  int32_t key;         // request id (private) or R + group id (group), for stable ordering
+};
+
+struct TaskSet {       // emitted once per kv head
+  int32_t row_off, n_tok, page_off, kv_begin, kv_end, causal;
+  int32_t key, tile, chunk;
+  bool mma;
+  int64_t work;
+  int32_t out_pid;
+};
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool pow2_in(int32_t v, std::initializer_list<int32_t> set) {
+  for (int32_t s : set) if (v == s) return true;
+  return false;
+}
+
+// Radix tree over page-id sequences: requests sorted lexicographically by their
+// fully cached page lists; lcp[i] = common prefix (in pages) of sorted[i-1] and
+// sorted[i].  Every maximal run sharing more than `depth` pages is a node.
+struct RadixBuilder {
+  const std::vector<int32_t>& sorted;
+  const std::vector<int32_t>& lcp;
+  std::vector<std::pair<std::vector<int32_t>, std::pair<int32_t, int32_t>>> groups;  // members, [d0, d1)
+  std::vector<int32_t>& group_end;  // per request: deepest grouped page
+
+  void build(int32_t lo, int32_t hi, int32_t depth) {
+    int32_t i = lo;
+    while (i < hi) {
+      int32_t j = i + 1;
+      int32_t common = INT32_MAX;
+      while (j < hi && lcp[j] > depth) {
+        common = std::min(common, lcp[j]);
+        ++j;
+      }
+      if (j - i >= 2) {
+        std::vector<int32_t> members(sorted.begin() + i, sorted.begin() + j);
+        std::sort(members.begin(), members.end());
+        for (int32_t r : members) group_end[r] = std::max(group_end[r], common);
+        groups.push_back({std::move(members), {depth, common}});
+        build(i, j, common);
+      }
+      i = j;
+    }
+  }
+};
+
+}  // namespace
+
+extern "C" pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_len,
+                                    const int32_t* page_indptr, const int32_t* page_indices,
+                                    int32_t num_requests, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                                    int32_t num_pages, float sm_scale,
+                                    const pps_plan_options* opts, pps_plan** out_plan,
+                                    size_t* out_workspace_bytes) {
+  if (out_plan) *out_plan = nullptr;
+  if (out_workspace_bytes) *out_workspace_bytes = 0;
+  if (!out_plan || !out_workspace_bytes || num_requests < 0 || !q_indptr || !page_indptr ||
+      (num_requests > 0 && !kv_len) || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_pages < 0 || !std::isfinite(sm_scale))
+    return PPS_ERR_INVALID_ARGUMENT;
+  if (num_q_heads % num_kv_heads) return PPS_ERR_INVALID_ARGUMENT;
+  const int32_t G = num_q_heads / num_kv_heads;
+  if (!pow2_in(G, {1, 2, 4, 8}) || !pow2_in(head_dim, {64, 128}) ||
+      !pow2_in(page_size, {16, 32, 64, 128}))
+    return PPS_ERR_UNSUPPORTED;
+  const int32_t R = num_requests, P = page_size;
+  if (q_indptr[0] != 0 || page_indptr[0] != 0) return PPS_ERR_INVALID_ARGUMENT;
+  for (int32_t r = 0; r < R; ++r) {
+    if (q_indptr[r + 1] < q_indptr[r]) return PPS_ERR_INVALID_ARGUMENT;
+    if (page_indptr[r + 1] < page_indptr[r]) return PPS_ERR_PAGE_TABLE;
+    const int32_t q = q_indptr[r + 1] - q_indptr[r];
+    if (kv_len[r] < q) return PPS_ERR_INVALID_ARGUMENT;
+    const int64_t need = ceil_div(kv_len[r], P);
+    if (page_indptr[r + 1] - page_indptr[r] < need) return PPS_ERR_PAGE_TABLE;
+    for (int64_t i = 0; i < need; ++i) {
+      const int32_t pg = page_indices[page_indptr[r] + i];
+      if (pg < 0 || pg >= num_pages) return PPS_ERR_PAGE_TABLE;
+    }
+  }
+  const int64_t nnz = page_indptr[R];
+  if (nnz > 0 && !page_indices) return PPS_ERR_INVALID_ARGUMENT;
+
+  pps_plan_options o{};
+  if (opts) o = *opts;
+  int32_t num_sms = o.num_sms;
+  if (num_sms <= 0) num_sms = pps::device_sm_count();
+  if (num_sms <= 0) num_sms = 152;
+  const bool use_mma = pps::mma_path_available() && !(o.flags & PPS_PLAN_CUDA_CORES_ONLY);
+  const bool use_groups = !(o.flags & PPS_PLAN_NO_GROUPS);
+
+  pps_plan* plan = new (std::nothrow) pps_plan;
+  if (!plan) return PPS_ERR_NO_MEMORY;
+  try {
+    plan->shape = {num_q_heads, num_kv_heads, head_dim, page_size, G, num_pages, sm_scale, 0};
+    plan->num_requests = R;
+    plan->num_tokens = q_indptr[R];
+    plan->use_mma = use_mma;
+    const int32_t T = q_indptr[R];
+
+    // ---- 1. radix grouping over fully cached pages --------------------------------
+    std::vector<int32_t> group_end(R, 0);
+    std::vector<std::pair<std::vector<int32_t>, std::pair<int32_t, int32_t>>> groups;
+    if (use_groups) {
+      std::vector<int32_t> full(R, 0), cand;
+      for (int32_t r = 0; r < R; ++r) {
+        const int32_t q = q_indptr[r + 1] - q_indptr[r];
+        const int32_t c = kv_len[r] - q;
+        full[r] = c / P;
+        if (q > 0 && full[r] > 0) cand.push_back(r);
+      }
+      auto seq = [&](int32_t r) { return page_indices + page_indptr[r]; };
+      std::sort(cand.begin(), cand.end(), [&](int32_t a, int32_t b) {
+        const int32_t n = std::min(full[a], full[b]);
+        const int32_t* pa = seq(a);
+        const int32_t* pb = seq(b);
+        for (int32_t i = 0; i < n; ++i)
+          if (pa[i] != pb[i]) return pa[i] < pb[i];
+        if (full[a] != full[b]) return full[a] < full[b];
+        return a < b;
+      });
+      std::vector<int32_t> lcp(cand.size(), 0);
+      for (size_t i = 1; i < cand.size(); ++i) {
+        const int32_t a = cand[i - 1], b = cand[i];
+        const int32_t n = std::min(full[a], full[b]);
+        int32_t k = 0;
+        while (k < n && seq(a)[k] == seq(b)[k]) ++k;
+        lcp[i] = k;
+      }
+      RadixBuilder rb{cand, lcp, {}, group_end};
+      rb.build(0, (int32_t)cand.size(), 0);
+      groups = std::move(rb.groups);
+    }
+    plan->num_groups = (int32_t)groups.size();
+
+    // ---- 2. segments ---------------------------------------------------------------
+    std::vector<int32_t> rows;
+    rows.reserve((size_t)T * 2);
+    std::vector<Segment> segs;
+    for (size_t g = 0; g < groups.size(); ++g) {
+      const auto& mem = groups[g].first;
+      Segment s{};
+      s.row_off = (int32_t)rows.size();
+      for (int32_t r : mem)
+        for (int32_t t = q_indptr[r]; t < q_indptr[r + 1]; ++t) rows.push_back(t);
+      s.n_tok = (int32_t)rows.size() - s.row_off;
+      s.page_off = page_indptr[mem[0]];
+      s.kv_begin = groups[g].second.first * P;
+      s.kv_end = groups[g].second.second * P;
+      s.causal = false;
+      s.c = 0;
+      s.key = R + (int32_t)g;
+      segs.push_back(s);
+    }
+    for (int32_t r = 0; r < R; ++r) {
+      const int32_t q = q_indptr[r + 1] - q_indptr[r];
+      if (q == 0) continue;
+      Segment s{};
+      s.row_off = (int32_t)rows.size();
+      for (int32_t t = q_indptr[r]; t < q_indptr[r + 1]; ++t) rows.push_back(t);
+      s.n_tok = q;
+      s.page_off = page_indptr[r];
+      s.kv_begin = group_end[r] * P;
+      s.kv_end = kv_len[r];
+      s.causal = true;
+      s.c = kv_len[r] - q;
+      s.key = r;
+      segs.push_back(s);
+    }
+
+    // ---- 3. tiles and split-KV chunks ----------------------------------------------
+    const int32_t bw_max_tok = std::max(1, 8 / G);          // decode-like rows stay on CUDA cores
+    const int32_t bw_tile_tok = std::max(1, pps::kBwMaxRows / G);
+    const int32_t mma_tile_tok = pps::kMmaRows / G;
+    auto is_mma = [&](const Segment& s) { return use_mma && s.n_tok > bw_max_tok; };
+    auto tile_tok_of = [&](const Segment& s) {
+      if (is_mma(s)) return mma_tile_tok;
+      return s.n_tok <= bw_max_tok ? s.n_tok : bw_tile_tok;
+    };
+    // Spans before chunking: [a, b) split into chunks; the last chunk runs to `end`.
+    struct Span { int32_t a, b, end; };
+    auto span_of = [&](const Segment& s, int32_t i0, int32_t i1) {
+      if (!s.causal) return Span{s.kv_begin, s.kv_end, s.kv_end};
+      return Span{s.kv_begin, s.c + i0 + 1, std::min(s.kv_end, s.c + i1)};
+    };
+    int64_t bw_kv = 0, mma_kv = 0, mma_tiles = 0;
+    for (const auto& s : segs) {
+      const int32_t tt = tile_tok_of(s);
+      for (int32_t i0 = 0; i0 < s.n_tok; i0 += tt) {
+        const Span sp = span_of(s, i0, std::min(s.n_tok, i0 + tt));
+        if (is_mma(s)) { mma_kv += sp.end - sp.a; ++mma_tiles; }
+        else bw_kv += sp.end - sp.a;
+      }
+    }
+    int32_t bw_chunk = o.bw_chunk_tokens;
+    if (bw_chunk <= 0) {
+      const int64_t want = ceil_div(bw_kv * num_kv_heads, (int64_t)num_sms * 6);
+      bw_chunk = (int32_t)std::min<int64_t>(512, std::max<int64_t>(128, want));
+    }
+    bw_chunk = (int32_t)(ceil_div(bw_chunk, P) * P);
+    int32_t mma_chunk = o.mma_chunk_tokens;
+    if (mma_chunk <= 0) {
+      mma_chunk = 1 << 30;
+      const int64_t target = 2LL * num_sms;
+      if (mma_tiles * num_kv_heads > 0 && mma_tiles * num_kv_heads < target) {
+        const int64_t want = ceil_div(mma_kv * num_kv_heads, target);
+        mma_chunk = (int32_t)std::max<int64_t>(512, want);
+      }
+    }
+    mma_chunk = (int32_t)std::min<int64_t>(1 << 30, ceil_div(mma_chunk, pps::kMmaKvTile) * pps::kMmaKvTile);
+
+    std::vector<TaskSet> sets;
+    for (const auto& s : segs) {
+      const bool mma = is_mma(s);
+      const int32_t tt = tile_tok_of(s);
+      const int32_t chunk = mma ? mma_chunk : bw_chunk;
+      int32_t tile = 0;
+      for (int32_t i0 = 0; i0 < s.n_tok; i0 += tt, ++tile) {
+        const int32_t i1 = std::min(s.n_tok, i0 + tt);
+        const Span sp = span_of(s, i0, i1);
+        const int64_t nch = std::max<int64_t>(1, ceil_div(sp.b - sp.a, chunk));
+        for (int64_t k = 0; k < nch; ++k) {
+          TaskSet ts{};
+          ts.row_off = s.row_off + i0;
+          ts.n_tok = i1 - i0;
+          ts.page_off = s.page_off;
+          ts.kv_begin = sp.a + (int32_t)(k * chunk);
+          ts.kv_end = (k == nch - 1) ? sp.end : ts.kv_begin + chunk;
+          ts.causal = s.causal ? s.c + i0 : PPS_NO_CAUSAL;
+          ts.key = s.key;
+          ts.tile = tile;
+          ts.chunk = (int32_t)k;
+          ts.mma = mma;
+          const int64_t rows_eff = mma ? pps::kMmaRows : (int64_t)ts.n_tok * G;
+          ts.work = rows_eff * (ts.kv_end - ts.kv_begin);
+          ts.out_pid = -1;
+          sets.push_back(ts);
+        }
+      }
+    }
+
+    // ---- 4. partial slots and merge lists ------------------------------------------
+    std::vector<int32_t> pieces(T, 0);
+    for (const auto& ts : sets)
+      for (int32_t i = 0; i < ts.n_tok; ++i) ++pieces[rows[ts.row_off + i]];
+    std::vector<std::vector<int32_t>> tok_pids(T);
+    int64_t next_pid = 0;
+    for (auto& ts : sets) {
+      bool direct = true;
+      for (int32_t i = 0; i < ts.n_tok; ++i) direct &= pieces[rows[ts.row_off + i]] == 1;
+      if (direct) continue;
+      ts.out_pid = (int32_t)next_pid;
+      for (int32_t i = 0; i < ts.n_tok; ++i) tok_pids[rows[ts.row_off + i]].push_back((int32_t)(next_pid + i));
+      next_pid += ts.n_tok;
+    }
+    std::vector<int32_t> m_tok, m_ptr{0}, m_pid;
+    for (int32_t t = 0; t < T; ++t) {
+      if (tok_pids[t].empty()) continue;
+      m_tok.push_back(t);
+      m_pid.insert(m_pid.end(), tok_pids[t].begin(), tok_pids[t].end());
+      m_ptr.push_back((int32_t)m_pid.size());
+    }
+
+    // ---- 5. sort by work (descending), deterministic ties ---------------------------
+    std::stable_sort(sets.begin(), sets.end(), [](const TaskSet& a, const TaskSet& b) {
+      if (a.mma != b.mma) return a.mma < b.mma;
+      if (a.work != b.work) return a.work > b.work;
+      if (a.key != b.key) return a.key < b.key;
+      if (a.tile != b.tile) return a.tile < b.tile;
+      return a.chunk < b.chunk;
+    });
+    std::vector<Task> bw, mm;
+    for (const auto& ts : sets) {
+      if (!ts.mma) plan->shape.bw_rows_max = std::max(plan->shape.bw_rows_max, ts.n_tok * G);
+      for (int32_t h = 0; h < num_kv_heads; ++h) {
+        Task t{ts.row_off, ts.n_tok, h, ts.page_off, ts.kv_begin, ts.kv_end, ts.causal, ts.out_pid};
+        (ts.mma ? mm : bw).push_back(t);
+      }
+    }
+
+    // ---- 6. statistics ---------------------------------------------------------------
+    const int64_t tok_bytes = 2LL * num_kv_heads * head_dim * 2;   // K+V, all kv heads
+    {
+      std::vector<uint8_t> seen((size_t)num_pages, 0);
+      int64_t slots = 0;
+      for (int32_t r = 0; r < R; ++r) {
+        const int64_t need = ceil_div(kv_len[r], P);
+        for (int64_t i = 0; i < need; ++i) {
+          const int32_t pg = page_indices[page_indptr[r] + i];
+          const int32_t valid = (int32_t)std::min<int64_t>(P, kv_len[r] - i * P);
+          if (valid > seen[pg]) { slots += valid - seen[pg]; seen[pg] = (uint8_t)std::min(valid, 255); }
+        }
+      }
+      plan->kv_bytes_unique = slots * tok_bytes;
+    }
+    double fl_tot = 0, fl_mma = 0;
+    int64_t read = 0;
+    for (const auto& ts : sets) {
+      double pairs = 0;
+      for (int32_t i = 0; i < ts.n_tok; ++i) {
+        const int64_t lim = std::min<int64_t>(ts.kv_end, (int64_t)ts.causal + i + 1);
+        pairs += (double)std::max<int64_t>(0, lim - ts.kv_begin);
+      }
+      const double f = pairs * num_q_heads * 4.0 * head_dim;
+      fl_tot += f;
+      if (ts.mma) fl_mma += f;
+      read += (int64_t)(ts.kv_end - ts.kv_begin) * tok_bytes;
+    }
+    plan->flops_total = fl_tot;
+    plan->flops_mma = fl_mma;
+    plan->kv_bytes_read = read;
+
+    // ---- 7. table image ----------------------------------------------------------------
+    auto al = [](int64_t n) { return (n + 63) / 64 * 64; };
+    pps::TableLayout L;
+    int64_t off = 0;
+    L.bw_tasks = off;      off += al((int64_t)bw.size() * PPS_TASK_INTS);
+    L.mma_tasks = off;     off += al((int64_t)mm.size() * PPS_TASK_INTS);
+    L.rows = off;          off += al((int64_t)rows.size());
+    L.pages = off;         off += al(nnz);
+    L.merge_tokens = off;  off += al((int64_t)m_tok.size());
+    L.merge_indptr = off;  off += al((int64_t)m_ptr.size());
+    L.merge_pids = off;    off += al((int64_t)m_pid.size());
+    L.total_ints = off;
+    plan->layout = L;
+    plan->image.assign((size_t)std::max<int64_t>(off, 64), 0);
+    int32_t* img = plan->image.data();
+    if (!bw.empty()) std::memcpy(img + L.bw_tasks, bw.data(), bw.size() * sizeof(Task));
+    if (!mm.empty()) std::memcpy(img + L.mma_tasks, mm.data(), mm.size() * sizeof(Task));
+    if (!rows.empty()) std::memcpy(img + L.rows, rows.data(), rows.size() * 4);
+    if (nnz) std::memcpy(img + L.pages, page_indices, (size_t)nnz * 4);
+    if (!m_tok.empty()) std::memcpy(img + L.merge_tokens, m_tok.data(), m_tok.size() * 4);
+    std::memcpy(img + L.merge_indptr, m_ptr.data(), m_ptr.size() * 4);
+    if (!m_pid.empty()) std::memcpy(img + L.merge_pids, m_pid.data(), m_pid.size() * 4);
+
+    plan->num_bw = (int64_t)bw.size();
+    plan->num_mma = (int64_t)mm.size();
+    plan->num_partials = next_pid;
+    plan->num_merge_tokens = (int64_t)m_tok.size();
+    plan->num_merge_pids = (int64_t)m_pid.size();
+    plan->num_rows = (int64_t)rows.size();
+    plan->num_pages_listed = nnz;
+    auto al256 = [](size_t n) { return (n + 255) / 256 * 256; };
+    plan->table_bytes = al256(plan->image.size() * 4);
+    plan->partial_o_bytes = al256((size_t)next_pid * num_q_heads * head_dim * 4);
+    plan->partial_lse_bytes = al256((size_t)next_pid * num_q_heads * 4);
+    plan->workspace_bytes = plan->table_bytes + plan->partial_o_bytes + plan->partial_lse_bytes;
+  } catch (const std::bad_alloc&) {
+    delete plan;
+    return PPS_ERR_NO_MEMORY;
+  }
+  *out_plan = plan;
+  *out_workspace_bytes = plan->workspace_bytes;
+  return PPS_OK;
+}
+
+extern "C" pps_status pps_plan_destroy(pps_plan* plan) {
+  delete plan;
+  return PPS_OK;
+}
+
+extern "C" pps_status pps_plan_get_info(const pps_plan* p, pps_plan_info* info) {
+  if (!p || !info) return PPS_ERR_INVALID_ARGUMENT;
+  std::memset(info, 0, sizeof(*info));
+  info->num_requests = p->num_requests;
+  info->num_tokens = p->num_tokens;
+  info->num_q_heads = p->shape.num_q_heads;
+  info->num_kv_heads = p->shape.num_kv_heads;
+  info->head_dim = p->shape.head_dim;
+  info->page_size = p->shape.page_size;
+  info->num_groups = p->num_groups;
+  info->num_bw_tasks = p->num_bw;
+  info->num_mma_tasks = p->num_mma;
+  info->num_partials = p->num_partials;
+  info->num_merge_tokens = p->num_merge_tokens;
+  info->table_bytes = (int64_t)p->table_bytes;
+  info->workspace_bytes = (int64_t)p->workspace_bytes;
+  info->kv_bytes_unique = p->kv_bytes_unique;
+  info->kv_bytes_read = p->kv_bytes_read;
+  info->flops_mma = p->flops_mma;
+  info->flops_total = p->flops_total;
+  return PPS_OK;
+}
+
+extern "C" pps_status pps_plan_get_array(const pps_plan* p, int32_t which, const int32_t** data,
+                                         int64_t* count) {
+  if (!p || !data || !count) return PPS_ERR_INVALID_ARGUMENT;
+  const int32_t* img = p->image.data();
+  const auto& L = p->layout;
+  switch (which) {
+    case PPS_ARRAY_BW_TASKS: *data = img + L.bw_tasks; *count = p->num_bw * PPS_TASK_INTS; break;
+    case PPS_ARRAY_MMA_TASKS: *data = img + L.mma_tasks; *count = p->num_mma * PPS_TASK_INTS; break;
+    case PPS_ARRAY_ROWS: *data = img + L.rows; *count = p->num_rows; break;
+    case PPS_ARRAY_PAGES: *data = img + L.pages; *count = p->num_pages_listed; break;
+    case PPS_ARRAY_MERGE_TOKENS: *data = img + L.merge_tokens; *count = p->num_merge_tokens; break;
+    case PPS_ARRAY_MERGE_INDPTR: *data = img + L.merge_indptr; *count = p->num_merge_tokens + 1; break;
+    case PPS_ARRAY_MERGE_PIDS: *data = img + L.merge_pids; *count = p->num_merge_pids; break;
+    default: return PPS_ERR_INVALID_ARGUMENT;
+  }
+  return PPS_OK;
+}

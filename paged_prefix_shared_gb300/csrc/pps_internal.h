@@ -1,0 +1,103 @@
+// Internal declarations shared by the host planner, the C ABI and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "pps.h"
+
+namespace pps {
+
+// One unit of work for one kv head (layout documented in pps.h, PPS_TASK_INTS).
+struct Task {
+  int32_t row_off;
+  int32_t n_tok;
+  int32_t kv_head;
+  int32_t page_off;
+  int32_t kv_begin;
+  int32_t kv_end;
+  int32_t causal;
+  int32_t out_pid;
+};
+static_assert(sizeof(Task) == PPS_TASK_INTS * 4, "task record size");
+
+// Limits of the kernels.
+constexpr int kBwMaxRows = 16;      // query rows (tokens x G) per bandwidth task
+constexpr int kMmaRows = 128;       // query rows per tensor-core tile (TMEM lanes)
+constexpr int kMmaKvTile = 128;     // KV positions per tensor-core step
+
+// Offsets (in int32 units) of the sections of the uploaded task table.
+struct TableLayout {
+  int64_t bw_tasks = 0, mma_tasks = 0, rows = 0, pages = 0;
+  int64_t merge_tokens = 0, merge_indptr = 0, merge_pids = 0;
+  int64_t total_ints = 0;
+};
+
+// Everything the device needs for one run, resolved to device addresses.
+struct DeviceTables {
+  const Task* bw_tasks;
+  const Task* mma_tasks;
+  const int32_t* rows;
+  const int32_t* pages;
+  const int32_t* merge_tokens;
+  const int32_t* merge_indptr;
+  const int32_t* merge_pids;
+  float* o_part;     // [num_partials, Hq, d]
+  float* lse_part;   // [num_partials, Hq] (log2 domain)
+};
+
+struct Shape {
+  int32_t num_q_heads, num_kv_heads, head_dim, page_size, group;  // group = G
+  int32_t num_pages;
+  float sm_scale;
+  int32_t bw_rows_max;   // largest n_tok * G over bandwidth tasks
+};
+
+}  // namespace pps
+
+struct pps_plan {
+  pps::Shape shape;
+  int32_t num_requests = 0;
+  int32_t num_tokens = 0;
+  int32_t num_groups = 0;
+  int64_t num_bw = 0, num_mma = 0, num_partials = 0, num_merge_tokens = 0, num_merge_pids = 0;
+  int64_t num_rows = 0, num_pages_listed = 0;
+  pps::TableLayout layout;
+  std::vector<int32_t> image;   // host copy of the device table
+  size_t table_bytes = 0;       // bytes of `image`, rounded to 256
+  size_t partial_o_bytes = 0;
+  size_t partial_lse_bytes = 0;
+  size_t workspace_bytes = 0;
+  int64_t kv_bytes_unique = 0, kv_bytes_read = 0;
+  double flops_mma = 0, flops_total = 0;
+  bool use_mma = false;
+};
+
+namespace pps {
+
+// Kernel launchers (defined in the .cu files).  All return cudaSuccess (0) or
+// the launch error.  `err` is the device error word of the current device.
+int launch_kv_append(const pps_pool& pool, const void* k_new, const void* v_new,
+                     const int32_t* q_indptr, const int32_t* cached_len,
+                     const int32_t* page_indptr, const int32_t* page_indices,
+                     int32_t num_requests, int32_t num_new_tokens, int32_t* err, void* stream);
+
+int launch_bw_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
+                        const pps_pool& pool, void* out, int32_t* err, void* stream);
+
+int launch_mma_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
+                         const pps_pool& pool, void* out, int32_t* err, void* stream);
+
+int launch_merge(const Shape& s, const DeviceTables& t, int64_t num_merge_tokens, void* out,
+                 void* stream);
+
+bool mma_path_available();
+
+// SM count of the current device, or 0 when no device is usable.
+int device_sm_count();
+
+// Counts every kernel launch (pps_launch_count).
+void count_launch();
+
+}  // namespace pps

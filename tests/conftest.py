@@ -25,3 +25,12 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def pps():
+    """The binding, with libpps.so built in place (nvcc cross-compiles without a GPU)."""
+    import paged_prefix_shared_gb300 as m
+    m.build()
+    m.lib()
+    return m

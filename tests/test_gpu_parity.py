@@ -1,0 +1,198 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerance, on bf16 outputs: max abs <= 2e-2 and mean abs <= 2e-3 against
+fp64.  kv_append is compared bit for bit with the oracle's scatter.  Inputs
+come from the seeded generators only; expected values only from ``oracle``.
+Every pool slot that holds no row (slots past a request's length, unused
+pages) is NaN, so reading one would show up as a NaN output.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_run import errors, run_workload, to_device
+from oracle_run import oracle_steps, oracle_tokens
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS = 2e-2, 2e-3
+
+KW = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16, keep_segments=False)
+
+
+def small_cases():
+    """Sizes the oracle finishes in seconds, spanning several KV blocks, row
+    tiles and chunks, with ragged tails."""
+    return {
+        "tiny_mixed": lambda: workloads.tiny_mixed(),
+        "decode_heavy": lambda: workloads.decode_heavy(num_requests=24, kv_lo=1, kv_hi=1500, **KW),
+        "radix_sharing": lambda: workloads.radix_sharing(groups=2, root=256, branch=64, pairs=2,
+                                                         tail_lo=1, tail_hi=300, **KW),
+        "mixed_budget": lambda: workloads.mixed_budget(budget=400, prefill_q=190, prefill_cached=77,
+                                                       num_verify=6, mu=5.0, sigma=1.0,
+                                                       clip_lo=1, clip_hi=3000, **KW),
+        "long_prefill": lambda: workloads.long_prefill(num_requests=2, chunk=300, num_chunks=3,
+                                                       **dict(KW, page_size=64)),
+        "d64_g8": lambda: workloads.mixed_budget(budget=120, prefill_q=70, prefill_cached=5,
+                                                 num_verify=3, mu=4.0, sigma=1.0, clip_lo=1,
+                                                 clip_hi=700, num_q_heads=16, num_kv_heads=2,
+                                                 head_dim=64, page_size=32),
+        "g1_p128": lambda: workloads.mixed_budget(budget=100, prefill_q=40, prefill_cached=200,
+                                                  num_verify=3, mu=4.0, sigma=1.0, clip_lo=1,
+                                                  clip_hi=700, num_q_heads=4, num_kv_heads=4,
+                                                  head_dim=128, page_size=128),
+    }
+
+
+_CACHE = {}
+
+
+def _small(name):
+    if name not in _CACHE:
+        wl = small_cases()[name]()
+        _CACHE[name] = (wl, oracle_steps(wl))
+    return _CACHE[name]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(pps):
+    assert torch.cuda.is_available()
+    return pps
+
+
+@pytest.mark.parametrize("name", list(small_cases()))
+def test_kv_append_bit_exact(name):
+    wl, (_, (ok, ov)) = _small(name)
+    _, (gk, gv), _ = run_workload(wl)
+    assert torch.equal(gk.cpu().view(torch.int16), ok.view(torch.int16))
+    assert torch.equal(gv.cpu().view(torch.int16), ov.view(torch.int16))
+
+
+@pytest.mark.parametrize("flags", [0, 1, 2])
+@pytest.mark.parametrize("name", list(small_cases()))
+def test_parity_small(name, flags):
+    wl, (ref, _) = _small(name)
+    outs, _, plans = run_workload(wl, flags=flags)
+    for s, (o, r) in enumerate(zip(outs, ref)):
+        assert torch.isfinite(o).all(), f"step {s}: non-finite output (a NaN slot was read?)"
+        mx, mean = errors(o, r)
+        assert mx <= MAX_ABS and mean <= MEAN_ABS, (s, mx, mean, plans[s].info())
+
+
+@pytest.mark.parametrize("chunk", [16, 64, 200])
+def test_parity_forced_split(chunk):
+    wl, (ref, _) = _small("mixed_budget")
+    outs, _, _ = run_workload(wl, bw_chunk_tokens=chunk, mma_chunk_tokens=128)
+    mx, mean = errors(outs[0], ref[0])
+    assert mx <= MAX_ABS and mean <= MEAN_ABS
+
+
+def test_page_order_is_bit_invariant():
+    wl, _ = _small("radix_sharing")
+    rng = np.random.default_rng(11)
+    perm = rng.permutation(wl.pool_k.shape[0])
+    inv = torch.as_tensor(np.argsort(perm))
+    steps = []
+    for st in wl.steps:
+        L = st.layout
+        nl = workloads.Layout(L.num_q_heads, L.num_kv_heads, L.head_dim, L.page_size, L.num_pages,
+                              L.q_indptr, L.cached_len, L.kv_len, L.page_indptr,
+                              perm[L.page_indices].astype(np.int32))
+        steps.append(workloads.Step(nl, st.q, st.k_new, st.v_new))
+    wl2 = workloads.Workload(wl.name, wl.pool_k.index_select(0, inv), wl.pool_v.index_select(0, inv),
+                             steps)
+    a, _, _ = run_workload(wl)
+    b, _, _ = run_workload(wl2)
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+
+
+def test_empty_and_degenerate_rows():
+    # request 0: no new tokens; request 1: a single token with nothing cached
+    # (output = its own V row); request 2: 3 new tokens on a 1-token cache.
+    wl = workloads.build_workload("edge", num_q_heads=8, num_kv_heads=2, head_dim=64, page_size=16,
+                                  shared_lens=[], requests=[([], 5, [0]), ([], 0, [1]),
+                                                            ([], 1, [3])], seed=9)
+    ref, _ = oracle_steps(wl)
+    outs, _, _ = run_workload(wl)
+    mx, mean = errors(outs[0], ref[0])
+    assert mx <= MAX_ABS and mean <= MEAN_ABS
+    v = wl.steps[0].v_new.double().numpy()
+    np.testing.assert_allclose(outs[0][0].double().cpu().numpy(),
+                               np.repeat(v[0], 4, axis=0), atol=1e-2)
+
+
+def test_empty_batch():
+    wl = workloads.build_workload("empty", num_q_heads=8, num_kv_heads=2, head_dim=64, page_size=16,
+                                  shared_lens=[], requests=[([], 5, [0])], seed=9)
+    outs, _, plans = run_workload(wl)
+    assert outs[0].numel() == 0 and plans[0].info()["num_bw_tasks"] == 0
+
+
+def test_kv_append_flags_bad_page_id_on_device(pps):
+    wl = workloads.tiny_mixed()
+    pk, pv, steps = to_device(wl)
+    st = steps[0]
+    bad = st["tabs"]["page_indices"].clone()
+    bad[:] = 10_000                                  # every page id out of range
+    before = pk.clone()
+    pps.get_device_error(clear=True)
+    pps.kv_append(pk, pv, st["k_new"], st["v_new"], st["tabs"]["q_indptr"],
+                  st["tabs"]["cached_len"], st["tabs"]["page_indptr"], bad)
+    torch.cuda.synchronize()
+    assert pps.get_device_error(clear=True) == 1     # PPS_DEV_ERR_APPEND_PAGE_ID
+    assert torch.equal(pk.view(torch.int16), before.view(torch.int16))
+    # the context is still usable
+    outs, _, _ = run_workload(wl)
+    assert torch.isfinite(outs[0]).all()
+
+
+def test_run_rejects_small_workspace(pps):
+    wl = workloads.tiny_mixed()
+    pk, pv, steps = to_device(wl)
+    L = steps[0]["layout"]
+    plan = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices, 8, 2, 64, 16, 64)
+    ws = torch.empty(plan.workspace_bytes - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pps.PPSError, match="workspace"):
+        pps.attn_run(plan, steps[0]["q"], pk, pv, torch.empty_like(steps[0]["q"]), ws)
+
+
+# --- full sizes, sampled rows ------------------------------------------------
+
+FULL = ["tiny_mixed", "decode_heavy", "radix_sharing", "mixed_budget", "long_prefill"]
+
+
+def _sample_tokens(L, n, seed):
+    T = L.num_tokens
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(T, size=min(n, T), replace=False).tolist())
+    pick |= {0, T - 1}
+    # every request's last token (the longest causal row)
+    pick |= set((L.q_indptr[1:] - 1)[L.q_len > 0][:8].tolist())
+    return np.array(sorted(pick))
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_parity_full_size_sampled(pps, name):
+    if name == "long_prefill" and not pps_has_mma(pps):
+        pytest.skip("long prefill at full size needs the tensor-core path")
+    wl = workloads.make(name, device="cuda")
+    outs, _, plans = run_workload(wl)
+    for s, st in enumerate(wl.steps):
+        L = st.layout
+        assert torch.isfinite(outs[s]).all()
+        toks = _sample_tokens(L, 24, 100 + s) if name != "tiny_mixed" else np.arange(L.num_tokens)
+        ref = oracle_tokens(wl, s, toks)
+        mx, mean = errors(outs[s][torch.as_tensor(toks, device="cuda")], ref)
+        assert mx <= MAX_ABS and mean <= MEAN_ABS, (name, s, mx, mean)
+    del wl, outs
+    torch.cuda.empty_cache()
+
+
+def pps_has_mma(pps):
+    L = workloads.tiny_mixed(values=False).layout
+    plan = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices, 8, 2, 64, 16, 64)
+    return plan.info()["num_mma_tasks"] > 0

@@ -1,0 +1,159 @@
+"""Host planner (pps_attn_plan) checks, CPU only.
+
+Coverage is the planner's correctness contract: across all tasks, every
+(new token, kv head, KV position the token may see) is read exactly once and
+nothing else is read; the page ids a task reads for a token are that token's
+own request's page ids (group tasks read one member's list for all members);
+tokens read by more than one task get partial slots and a merge list, tokens
+read once are written directly.
+"""
+import time
+
+import numpy as np
+import pytest
+
+import workloads
+
+
+def _plan(pps, L, **kw):
+    return pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices, L.num_q_heads,
+                         L.num_kv_heads, L.head_dim, L.page_size, L.num_pages, **kw)
+
+
+def check_plan(pps, L, plan):
+    rows = plan.array("rows")
+    pages = plan.array("pages")
+    tasks = np.concatenate([plan.array("bw_tasks"), plan.array("mma_tasks")])
+    R, T, Hkv, P = L.num_requests, L.num_tokens, L.num_kv_heads, L.page_size
+    req_of = np.searchsorted(L.q_indptr, np.arange(T), side="right") - 1
+    cover = {t: np.zeros((Hkv, int(L.kv_len[req_of[t]])), np.int32) for t in range(T)}
+    per_token_tasks = {t: [] for t in range(T)}
+    for (row_off, n_tok, h, page_off, b, e, causal, pid) in tasks:
+        assert 0 <= h < Hkv and b < e
+        for i in range(n_tok):
+            t = int(rows[row_off + i])
+            r = int(req_of[t])
+            lim = min(e, causal + i + 1)
+            assert lim > b, "a task row that sees nothing"
+            cover[t][h, b:lim] += 1
+            own = L.page_indices[L.page_indptr[r]:L.page_indptr[r + 1]]
+            pos = np.arange(b, lim)
+            assert np.array_equal(pages[page_off + pos // P], own[pos // P])
+            per_token_tasks[t].append((h, pid, i))
+    for t in range(T):
+        r = int(req_of[t])
+        j = t - int(L.q_indptr[r])
+        vis = int(L.cached_len[r]) + j + 1
+        assert (cover[t][:, :vis] == 1).all(), f"token {t} not covered exactly once"
+        assert (cover[t][:, vis:] == 0).all(), f"token {t} reads beyond its causal limit"
+    # partials / merge bookkeeping
+    m_tok = plan.array("merge_tokens")
+    m_ptr = plan.array("merge_indptr")
+    m_pid = plan.array("merge_pids")
+    merged = {int(t): set(m_pid[m_ptr[k]:m_ptr[k + 1]].tolist()) for k, t in enumerate(m_tok)}
+    info = plan.info()
+    for t in range(T):
+        lst = per_token_tasks[t]
+        per_head = len(lst) // Hkv
+        assert len(lst) == per_head * Hkv
+        if per_head == 1:
+            assert all(pid == -1 for _, pid, _ in lst) and t not in merged
+        else:
+            assert all(pid >= 0 for _, pid, _ in lst)
+            pids = {pid + i for _, pid, i in lst}
+            assert merged[t] == pids and len(pids) == per_head
+            assert all(0 <= p < info["num_partials"] for p in pids)
+    # work-sorted (descending) inside each kernel class
+    G = L.num_q_heads // Hkv
+    for name, rows_eff in (("bw_tasks", None), ("mma_tasks", 128)):
+        tk = plan.array(name)
+        if len(tk):
+            w = (tk[:, 1] * G if rows_eff is None else rows_eff) * (tk[:, 5] - tk[:, 4])
+            assert (np.diff(w) <= 0).all()
+    return info
+
+
+SMALL = dict(num_q_heads=8, num_kv_heads=2, head_dim=64, page_size=16, values=False)
+
+
+@pytest.mark.parametrize("flags", [0, 1, 2])
+@pytest.mark.parametrize("name,kw", [
+    ("tiny_mixed", dict(values=False)),
+    ("decode_heavy", dict(num_requests=5, kv_lo=1, kv_hi=700, **SMALL)),
+    ("radix_sharing", dict(groups=3, root=64, branch=32, pairs=2, tail_lo=1, tail_hi=80, **SMALL)),
+    ("mixed_budget", dict(budget=200, prefill_q=100, prefill_cached=40, num_verify=5,
+                          mu=4.0, sigma=1.0, clip_lo=1, clip_hi=600, **SMALL)),
+    ("long_prefill", dict(num_requests=2, chunk=300, num_chunks=3, **SMALL)),
+])
+def test_plan_covers_every_visible_key_once(pps, name, kw, flags):
+    wl = workloads.make(name, **kw)
+    for st in wl.steps:
+        plan = _plan(pps, st.layout, flags=flags, num_sms=4)
+        check_plan(pps, st.layout, plan)
+
+
+@pytest.mark.parametrize("chunk", [16, 48, 128])
+def test_forced_small_chunks_still_cover(pps, chunk):
+    wl = workloads.make("mixed_budget", budget=120, prefill_q=40, prefill_cached=33, num_verify=4,
+                        mu=4.0, sigma=1.0, clip_lo=1, clip_hi=500, **SMALL)
+    plan = _plan(pps, wl.layout, bw_chunk_tokens=chunk, mma_chunk_tokens=128)
+    info = check_plan(pps, wl.layout, plan)
+    assert info["num_partials"] > 0
+
+
+def test_groups_detected(pps):
+    plan = _plan(pps, workloads.tiny_mixed(values=False).layout)
+    assert plan.info()["num_groups"] == 1      # the 2-page prefix shared by all four requests
+    wl = workloads.radix_sharing(groups=3, root=64, branch=32, pairs=2, tail_lo=1, tail_hi=80,
+                                 **SMALL)
+    info = _plan(pps, wl.layout).info()
+    assert info["num_groups"] == 3 * (1 + 2)   # per subtree: the root and two pair branches
+    assert _plan(pps, wl.layout, flags=pps.PLAN_NO_GROUPS).info()["num_groups"] == 0
+    # shared pages are read once per group: bytes read < bytes read without groups
+    a = _plan(pps, wl.layout).info()["kv_bytes_read"]
+    b = _plan(pps, wl.layout, flags=pps.PLAN_NO_GROUPS).info()["kv_bytes_read"]
+    assert a < b
+
+
+def test_unique_bytes_of_full_radix_workload(pps):
+    L = workloads.radix_sharing(values=False).layout
+    info = _plan(pps, L).info()
+    tok_bytes = 2 * 8 * 128 * 2
+    # 8 roots of 2048 + 32 branches of 512 + private tails (+1 new token each)
+    tails = int((L.kv_len - 2048 - 512).sum())
+    assert info["kv_bytes_unique"] == (8 * 2048 + 32 * 512 + tails) * tok_bytes
+    if info["num_mma_tasks"]:
+        # wide groups run as one 128-row tensor-core tile: every shared page read once
+        assert info["kv_bytes_read"] == info["kv_bytes_unique"]
+    else:
+        # CUDA cores only: a root group of 8 decode rows x G=4 needs two 16-row tiles
+        assert info["kv_bytes_read"] == info["kv_bytes_unique"] + 8 * 2048 * tok_bytes
+
+
+def test_plan_is_deterministic(pps):
+    L = workloads.radix_sharing(groups=2, root=64, branch=32, pairs=2, tail_lo=1, tail_hi=80,
+                                **SMALL).layout
+    a, b = _plan(pps, L), _plan(pps, L)
+    for name in ("bw_tasks", "mma_tasks", "rows", "merge_tokens", "merge_pids"):
+        assert np.array_equal(a.array(name), b.array(name))
+
+
+def test_zero_length_requests_contribute_no_rows(pps):
+    q_indptr = np.array([0, 0, 3, 3], np.int32)
+    kv_len = np.array([10, 7, 0], np.int32)
+    page_indptr = np.array([0, 1, 2, 2], np.int32)
+    plan = pps.attn_plan(q_indptr, kv_len, page_indptr, np.array([0, 1], np.int32), 8, 2, 64, 16, 2)
+    rows = plan.array("rows")
+    assert set(rows.tolist()) == {0, 1, 2}
+
+
+@pytest.mark.parametrize("name", ["decode_heavy", "mixed_budget", "long_prefill", "radix_sharing"])
+def test_full_size_plans_fast(pps, name):
+    wl = workloads.make(name, values=False)
+    for st in wl.steps:
+        t0 = time.perf_counter()
+        plan = _plan(pps, st.layout)
+        dt = time.perf_counter() - t0
+        info = plan.info()
+        assert info["workspace_bytes"] > 0
+        assert dt < 3.0, f"planning {name} took {dt:.3f}s"

@@ -103,7 +103,7 @@ def _round_bf16(x: torch.Tensor) -> torch.Tensor:
 
 def build_workload(name, *, num_q_heads, num_kv_heads, head_dim, page_size,
                    shared_lens, requests, seed, num_pages=None, pool_factor=1.25,
-                   device="cpu", keep_segments=False):
+                   device="cpu", keep_segments=False, values=True):
     """Draw one workload.
 
     ``shared_lens[i]`` is the length (a multiple of ``page_size``) of shared
@@ -111,7 +111,8 @@ def build_workload(name, *, num_q_heads, num_kv_heads, head_dim, page_size,
     ``(shared_path, private_cached, q_lens)``: the shared segment ids the
     request's cache starts with, in order, then the length of its private
     cached tail, then its new-token count at each step (one entry per step).
-    The private tail's pages also hold the request's new tokens.
+    The private tail's pages also hold the request's new tokens.  With
+    ``values=False`` only the layouts are drawn (tensors are None).
     """
     P = page_size
     rng = np.random.default_rng(seed)
@@ -144,6 +145,9 @@ def build_workload(name, *, num_q_heads, num_kv_heads, head_dim, page_size,
         off += n
 
     Hkv, Hq, d = num_kv_heads, num_q_heads, head_dim
+    if not values:
+        return _layouts_only(name, requests, shared_lens, seg_pages, req_segments, n_steps,
+                             Hq, Hkv, d, P, num_pages)
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     nan = float("nan")
@@ -201,6 +205,28 @@ def build_workload(name, *, num_q_heads, num_kv_heads, head_dim, page_size,
                     req_segments, shared)
 
 
+def _layouts_only(name, requests, shared_lens, seg_pages, req_segments, n_steps, Hq, Hkv, d, P,
+                  num_pages):
+    steps = []
+    q_done = [0] * len(requests)
+    for s in range(n_steps):
+        q_len = np.array([r[2][s] for r in requests], dtype=np.int64)
+        cached = np.array([sum(shared_lens[i] for i in r[0]) + r[1] + q_done[j]
+                           for j, r in enumerate(requests)], dtype=np.int64)
+        kv_len = cached + q_len
+        q_indptr = np.concatenate([[0], np.cumsum(q_len)]).astype(np.int32)
+        plists = [np.concatenate([seg_pages[i] for i in segs])[: -(-int(kv_len[j]) // P)]
+                  for j, segs in enumerate(req_segments)]
+        page_indptr = np.concatenate([[0], np.cumsum([len(p) for p in plists])]).astype(np.int32)
+        page_indices = (np.concatenate(plists) if plists else np.zeros(0)).astype(np.int32)
+        steps.append(Step(Layout(Hq, Hkv, d, P, num_pages, q_indptr, cached.astype(np.int32),
+                                 kv_len.astype(np.int32), page_indptr, page_indices),
+                          None, None, None))
+        for j in range(len(requests)):
+            q_done[j] += int(q_len[j])
+    return Workload(name, None, None, steps, None, None, req_segments, [])
+
+
 def contiguous_kv(wl: Workload, r: int, upto_step: int | None = None):
     """Request ``r``'s K and V rows in logical order ([n, Hkv, d] each), built
     from the drawn segments and new rows without any page table (needs
@@ -223,7 +249,7 @@ def contiguous_kv(wl: Workload, r: int, upto_step: int | None = None):
 # The five synthetic workloads (full sizes are the defaults).
 
 
-def tiny_mixed(seed=0, device="cpu", keep_segments=True):
+def tiny_mixed(seed=0, device="cpu", keep_segments=True, values=True):
     """4 requests, 8/2 heads, d=64, P=16; cached {37,64,100,129} all starting
     with one shared 32-token (2-page) prefix; new tokens {1 decode, 1 decode,
     4 verify, 16 prefill chunk}; 64-page pool in random page order."""
@@ -232,12 +258,12 @@ def tiny_mixed(seed=0, device="cpu", keep_segments=True):
     reqs = [([0], c - 32, [q]) for c, q in zip(cached, qs)]
     return build_workload("tiny_mixed", num_q_heads=8, num_kv_heads=2, head_dim=64,
                           page_size=16, shared_lens=[32], requests=reqs, seed=seed,
-                          num_pages=64, device=device, keep_segments=keep_segments)
+                          num_pages=64, device=device, keep_segments=keep_segments, values=values)
 
 
 def decode_heavy(seed=1, device="cpu", num_requests=256, kv_lo=512, kv_hi=4096,
                  num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
-                 keep_segments=False):
+                 keep_segments=False, values=True):
     """Decode rows only (q_len 1), cached length uniform in [kv_lo, kv_hi],
     no sharing, pages scattered over a pool 1.25x the pages needed."""
     rng = np.random.default_rng(seed)
@@ -246,12 +272,12 @@ def decode_heavy(seed=1, device="cpu", num_requests=256, kv_lo=512, kv_hi=4096,
     return build_workload("decode_heavy", num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                           head_dim=head_dim, page_size=page_size, shared_lens=[],
                           requests=reqs, seed=seed + 1000, device=device,
-                          keep_segments=keep_segments)
+                          keep_segments=keep_segments, values=values)
 
 
 def radix_sharing(seed=2, device="cpu", groups=8, root=2048, branch=512, pairs=4,
                   tail_lo=64, tail_hi=1024, num_q_heads=32, num_kv_heads=8,
-                  head_dim=128, page_size=16, keep_segments=False):
+                  head_dim=128, page_size=16, keep_segments=False, values=True):
     """Decode rows in ``groups`` radix subtrees: each subtree has one root
     segment shared by ``2*pairs`` requests and ``pairs`` branch segments each
     shared by two of them, then a private tail uniform in [tail_lo, tail_hi]."""
@@ -269,13 +295,13 @@ def radix_sharing(seed=2, device="cpu", groups=8, root=2048, branch=512, pairs=4
     return build_workload("radix_sharing", num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                           head_dim=head_dim, page_size=page_size, shared_lens=shared_lens,
                           requests=reqs, seed=seed + 1000, device=device,
-                          keep_segments=keep_segments)
+                          keep_segments=keep_segments, values=values)
 
 
 def mixed_budget(seed=3, device="cpu", budget=8192, prefill_q=2048, prefill_cached=1024,
                  num_verify=24, verify_lo=4, verify_hi=8, mu=7.0, sigma=1.0,
                  clip_lo=16, clip_hi=16384, num_q_heads=32, num_kv_heads=8,
-                 head_dim=128, page_size=16, keep_segments=False):
+                 head_dim=128, page_size=16, keep_segments=False, values=True):
     """One prefill chunk, ``num_verify`` speculative-verify rows, and the rest
     of the token budget as decode rows; verify/decode cached lengths are
     round(lognormal(mu, sigma)) clipped to [clip_lo, clip_hi]."""
@@ -292,19 +318,19 @@ def mixed_budget(seed=3, device="cpu", budget=8192, prefill_q=2048, prefill_cach
     return build_workload("mixed_budget", num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                           head_dim=head_dim, page_size=page_size, shared_lens=[],
                           requests=reqs, seed=seed + 1000, device=device,
-                          keep_segments=keep_segments)
+                          keep_segments=keep_segments, values=values)
 
 
 def long_prefill(seed=4, device="cpu", num_requests=4, chunk=8192, num_chunks=4,
                  num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=64,
-                 keep_segments=False):
+                 keep_segments=False, values=True):
     """``num_requests`` prompts prefilled as ``num_chunks`` causal chunks of
     ``chunk`` tokens; chunk c attends to every earlier chunk's pages."""
     reqs = [([], 0, [chunk] * num_chunks) for _ in range(num_requests)]
     return build_workload("long_prefill", num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                           head_dim=head_dim, page_size=page_size, shared_lens=[],
                           requests=reqs, seed=seed + 1000, device=device,
-                          keep_segments=keep_segments)
+                          keep_segments=keep_segments, values=values)
 
 
 WORKLOADS = {
