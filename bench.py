@@ -179,8 +179,11 @@ def run_pps(args):
     pps.build()
     pps.lib()
 
-    wl = workloads.make(args.workload, device=dev) if args.workload != "decode_heavy" else \
-        workloads.decode_heavy(seed=1 + 1000 * rank, device=dev)
+    if args.workload == "decode_heavy":
+        wl = workloads.decode_heavy(seed=1 + 1000 * rank, device=dev,
+                                    num_requests=args.requests or 256)
+    else:
+        wl = workloads.make(args.workload, device=dev)
     # device-resident inputs
     # The library appends into a copy; the drawn pool stays as the generator
     # made it (the CPU baseline starts from it).  Re-appending the same rows
@@ -320,7 +323,8 @@ def run_pps(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, seeded layouts; no dataset)",
-        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}" +
+                   (f" [{args.requests} requests]" if args.requests else ""),
                    "tokens_per_step": tokens, "kv_bytes_unique_per_step": kv_unique,
                    "l2": "inputs larger than L2 (KV pool >> 129 MB), no flush"
                    if kv_unique > 4 * 129e6 else "KV smaller than L2: warm-L2 figure",
@@ -429,6 +433,9 @@ def main():
     ap.add_argument("--impl", default="pps", choices=["pps", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--requests", type=int, default=0,
+                    help="decode_heavy only: number of requests (default 256); for small "
+                         "profiling captures")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

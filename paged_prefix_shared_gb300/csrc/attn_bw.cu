@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include "pps_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace {
 
@@ -189,6 +190,342 @@ __global__ void __launch_bounds__(kThreads) bw_attention_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// v2: TMA bulk-copy pipeline, one 16-position sub-block per consumer warp step.
+//
+// A producer warp streams the task's K and V rows 16 positions at a time
+// (2 x 16 x d x 2 bytes per stage; a page of P >= 16 slots is P/16 sub-blocks)
+// with cp.async.bulk into an 8-stage ring; four consumer warps take
+// sub-blocks round robin.  In a consumer warp, LPT lanes share one KV row
+// (EL head_dim elements each, two 16-byte chunks at stride LPT so shared
+// memory reads are conflict free), TPW rows are processed per step.  The R
+// partial dot products of a lane are reduce-scattered across its LPT lanes
+// (log2(LPT) shuffles in all, each lane ends with the full score of one
+// row), the online softmax keeps a per-warp reference max (rescaled only when
+// it rises by more than 2^8), and P.V accumulates into registers with packed
+// fp32x2 FMAs.  Four warps' states are merged through shared memory at the end.
+
+constexpr int kBw2Stages = 8;
+constexpr int kBw2Sub = 16;                   // KV positions per stage
+constexpr int kBw2Consumers = 4;
+constexpr int kBw2Threads = (kBw2Consumers + 1) * 32;
+
+template <int D, int R>
+struct Bw2 {
+  static constexpr int EL = (R >= 8) ? 8 : 16;            // head_dim elements per lane
+  static constexpr int LPT = D / EL;                      // lanes per KV row
+  static constexpr int TPW = 32 / LPT;                    // KV rows per warp step
+  static constexpr int ITERS = kBw2Sub / TPW;
+  static constexpr int CH = EL / 8;                       // 16-byte chunks per lane
+  static constexpr int STAGE = 2 * kBw2Sub * D * 2;       // K then V
+  static constexpr int SMEM = kBw2Stages * STAGE;
+  static_assert(R <= LPT, "one row per lane after the reduce-scatter");
+  static_assert(4 * R * (D + 2) * 4 <= SMEM, "combine area fits in the ring");
+};
+
+// Reduce-scatter of V[0..CUR) over lanes xor O, O/2, ..., 1: each halving step
+// sends half of the values to the partner lane and keeps the other half.
+template <int CUR, int O>
+__device__ __forceinline__ void reduce_scatter(float* v, int lane) {
+  if constexpr (O >= 1) {
+    if constexpr (CUR > 1) {
+      constexpr int H = CUR / 2;
+      const bool up = (lane & O) != 0;
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const float send = up ? v[i] : v[i + H];
+        const float keep = up ? v[i + H] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+      }
+      reduce_scatter<H, O / 2>(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+      reduce_scatter<1, O / 2>(v, lane);
+    }
+  }
+}
+// Row whose full score lane `lane` holds after reduce_scatter<R, LPT/2>.
+template <int CUR, int O>
+__device__ __forceinline__ int rs_row(int lane) {
+  if constexpr (O >= 1 && CUR > 1) return ((lane & O) ? CUR / 2 : 0) + rs_row<CUR / 2, O / 2>(lane);
+  else return 0;
+}
+// Lane (within its LPT group) that holds row r.
+template <int R, int LPT>
+__device__ __forceinline__ int rs_lane(int r) {
+  int l = 0;
+#pragma unroll
+  for (int k = 1; (R >> k) >= 1; ++k)
+    if (r & (R >> k)) l += LPT >> k;
+  return l;
+}
+
+__device__ __forceinline__ float fast_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+template <int D, int R>
+__global__ void __launch_bounds__(kBw2Threads) bw2_attention_kernel(
+    const pps::Task* __restrict__ tasks, const int32_t* __restrict__ rows,
+    const int32_t* __restrict__ pages, const __nv_bfloat16* __restrict__ q,
+    const __nv_bfloat16* __restrict__ pool_k, const __nv_bfloat16* __restrict__ pool_v,
+    __nv_bfloat16* __restrict__ out, float* __restrict__ o_part, float* __restrict__ lse_part,
+    int32_t* __restrict__ err, int32_t num_q_heads, int32_t num_kv_heads, int32_t G,
+    int32_t page_size, float qk_scale) {
+  using C = Bw2<D, R>;
+  constexpr int EL = C::EL, LPT = C::LPT, TPW = C::TPW, ITERS = C::ITERS, CH = C::CH;
+  extern __shared__ __align__(128) uint8_t bw2_smem[];
+  __shared__ uint64_t full[kBw2Stages], empty[kBw2Stages];
+  __shared__ volatile int abort_flag;
+
+  const pps::Task task = tasks[blockIdx.x];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nrows = task.n_tok * G;
+  const int n_sub = (task.kv_end - task.kv_begin + kBw2Sub - 1) / kBw2Sub;
+  if (tid == 0) {
+    for (int s = 0; s < kBw2Stages; ++s) {
+      sm100::mbar_init(sm100::smem_u32(&full[s]), 1);
+      sm100::mbar_init(sm100::smem_u32(&empty[s]), 1);
+    }
+    abort_flag = 0;
+    sm100::fence_mbar_init();
+  }
+  __syncthreads();
+
+  // per-warp online-softmax state (consumer warps), merged after the loop
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[R][EL];
+  const int grp = lane / LPT, sub = lane % LPT;
+  const int my_row = rs_row<R, LPT / 2>(lane);
+
+  if (warp == kBw2Consumers) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const size_t head_stride = (size_t)page_size * D;
+      const uint32_t half = kBw2Sub * D * 2;
+      int issued = 0;
+      for (int k = 0; k < n_sub; ++k) {
+        const int s = k % kBw2Stages, use = k / kBw2Stages;
+        if (use > 0 && !sm100::mbar_wait(sm100::smem_u32(&empty[s]), (use - 1) & 1)) {
+          atomicCAS(err, 0, PPS_DEV_ERR_WAIT_TIMEOUT);
+          abort_flag = 1;
+          break;
+        }
+        if (abort_flag) break;
+        const int pos0 = task.kv_begin + k * kBw2Sub;
+        const int page = pages[task.page_off + pos0 / page_size];
+        const size_t off = ((size_t)page * num_kv_heads + task.kv_head) * head_stride +
+                           (size_t)(pos0 % page_size) * D;
+        const uint32_t bar = sm100::smem_u32(&full[s]);
+        const uint32_t dst = sm100::smem_u32(bw2_smem + s * C::STAGE);
+        sm100::mbar_expect_tx(bar, 2 * half);
+        bulk_g2s(dst, pool_k + off, half, bar);
+        bulk_g2s(dst + half, pool_v + off, half, bar);
+        issued = k + 1;
+      }
+      // every started copy lands before the CTA may exit
+      for (int k = (issued > kBw2Stages ? issued - kBw2Stages : 0); k < issued; ++k)
+        sm100::mbar_wait(sm100::smem_u32(&full[k % kBw2Stages]), (k / kBw2Stages) & 1);
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    const int h0 = task.kv_head * G;
+    float qr[R][EL];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const bool real = r < nrows;
+      const int t = real ? rows[task.row_off + r / G] : 0;
+      const __nv_bfloat16* src = q + ((size_t)t * num_q_heads + h0 + (real ? r % G : 0)) * D;
+#pragma unroll
+      for (int j = 0; j < CH; ++j) {
+        float f[8];
+        const int4 v = real ? __ldg(reinterpret_cast<const int4*>(src + (sub + j * LPT) * 8))
+                            : make_int4(0, 0, 0, 0);
+        bf16x8_to_f32(v, f);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) qr[r][j * 8 + x] = f[x] * qk_scale;
+      }
+#pragma unroll
+      for (int e = 0; e < EL; ++e) acc[r][e] = 0.f;
+    }
+    const int lim0 = task.causal;                 // row 0 (first token) has the smallest limit
+    const int my_lim = task.causal + my_row / G;
+    for (int k = warp; k < n_sub; k += kBw2Consumers) {
+      const int s = k % kBw2Stages;
+      const bool got = sm100::mbar_wait(sm100::smem_u32(&full[s]), (k / kBw2Stages) & 1) && !abort_flag;
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) { atomicCAS(err, 0, PPS_DEV_ERR_WAIT_TIMEOUT); abort_flag = 1; }
+        break;
+      }
+      const int pos0 = task.kv_begin + k * kBw2Sub;
+      const bool fast = (pos0 + kBw2Sub <= task.kv_end) && (pos0 + kBw2Sub - 1 <= lim0);
+      const uint8_t* kb = bw2_smem + s * C::STAGE;
+      const uint8_t* vb = kb + kBw2Sub * D * 2;
+      float sc[ITERS];
+#pragma unroll
+      for (int it = 0; it < ITERS; ++it) {
+        const int t = it * TPW + grp;
+        float kf[EL];
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+          const int4 v = *reinterpret_cast<const int4*>(kb + t * D * 2 + (sub + j * LPT) * 16);
+          bf16x8_to_f32(v, kf + j * 8);
+        }
+        float d[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < EL; e += 2)
+            a = __ffma2_rn(make_float2(qr[r][e], qr[r][e + 1]), make_float2(kf[e], kf[e + 1]), a);
+          d[r] = a.x + a.y;
+        }
+        reduce_scatter<R, LPT / 2>(d, lane);
+        float sv = d[0];
+        if (!fast) {
+          const int pos = pos0 + t;
+          if (pos >= task.kv_end || pos > my_lim) sv = -INFINITY;
+        }
+        sc[it] = sv;
+      }
+      // block max over the sub-block's rows (lanes of the same row, other groups)
+      float mx = sc[0];
+#pragma unroll
+      for (int it = 1; it < ITERS; ++it) mx = fmaxf(mx, sc[it]);
+#pragma unroll
+      for (int o = LPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const bool need = (mx > m_run + 8.f) || (m_run == -INFINITY && mx != -INFINITY);
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? fmaxf(mx, m_run) : m_run;
+        const float alpha = (m_run == -INFINITY) ? 0.f : fast_ex2(m_run - m_new);
+        m_run = m_new;
+        l_run *= alpha;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float a = __shfl_sync(0xffffffffu, alpha, rs_lane<R, LPT>(r));
+#pragma unroll
+          for (int e = 0; e < EL; ++e) acc[r][e] *= a;
+        }
+      }
+      const float msub = (m_run == -INFINITY) ? 0.f : m_run;
+      float ls = 0.f;
+#pragma unroll
+      for (int it = 0; it < ITERS; ++it) {
+        sc[it] = fast_ex2(sc[it] - msub);
+        ls += sc[it];
+      }
+#pragma unroll
+      for (int o = LPT; o < 32; o <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+      l_run += ls;
+      // P.V
+#pragma unroll
+      for (int it = 0; it < ITERS; ++it) {
+        const int t = it * TPW + grp;
+        float vf[EL];
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+          const int4 v = *reinterpret_cast<const int4*>(vb + t * D * 2 + (sub + j * LPT) * 16);
+          bf16x8_to_f32(v, vf + j * 8);
+        }
+        if (!fast && pos0 + t >= task.kv_end) {
+#pragma unroll
+          for (int e = 0; e < EL; ++e) vf[e] = 0.f;   // rows past the end may hold NaN
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float pr = __shfl_sync(0xffffffffu, sc[it], grp * LPT + rs_lane<R, LPT>(r));
+#pragma unroll
+          for (int e = 0; e < EL; e += 2) {
+            const float2 o2 = __ffma2_rn(make_float2(pr, pr), make_float2(vf[e], vf[e + 1]),
+                                         make_float2(acc[r][e], acc[r][e + 1]));
+            acc[r][e] = o2.x;
+            acc[r][e + 1] = o2.y;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) sm100::mbar_arrive(sm100::smem_u32(&empty[s]));
+    }
+    // sum the TPW row groups of the warp
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int e = 0; e < EL; ++e)
+#pragma unroll
+        for (int o = LPT; o < 32; o <<= 1) acc[r][e] += __shfl_xor_sync(0xffffffffu, acc[r][e], o);
+  }
+  __syncthreads();   // ring no longer in use: reuse it for the cross-warp merge
+  float* cm = reinterpret_cast<float*>(bw2_smem);                 // [4][R] max
+  float* cl = cm + kBw2Consumers * R;                         // [4][R] sum
+  float* co = cl + kBw2Consumers * R;                         // [4][R][D]
+  if (warp < kBw2Consumers) {
+    if (grp == 0) {
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int j = 0; j < CH; ++j)
+#pragma unroll
+          for (int x = 0; x < 8; ++x)
+            co[(warp * R + r) * D + (sub + j * LPT) * 8 + x] = acc[r][j * 8 + x];
+    }
+    if (lane == rs_lane<R, LPT>(my_row) && grp == 0) {
+      cm[warp * R + my_row] = m_run;
+      cl[warp * R + my_row] = l_run;
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < nrows * D; idx += kBw2Threads) {
+    const int r = idx / D, c = idx - (idx / D) * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kBw2Consumers; ++w) M = fmaxf(M, cm[w * R + r]);
+    float o = 0.f, l = 0.f;
+#pragma unroll
+    for (int w = 0; w < kBw2Consumers; ++w) {
+      const float mw = cm[w * R + r];
+      const float sw = (mw == -INFINITY) ? 0.f : fast_ex2(mw - M);
+      o += sw * co[(w * R + r) * D + c];
+      l += sw * cl[w * R + r];
+    }
+    const float val = l > 0.f ? o / l : 0.f;
+    const int i = r / G, h = task.kv_head * G + r % G;
+    if (task.out_pid < 0) {
+      out[((size_t)rows[task.row_off + i] * num_q_heads + h) * D + c] = __float2bfloat16_rn(val);
+    } else {
+      const size_t prow = (size_t)(task.out_pid + i) * num_q_heads + h;
+      o_part[prow * D + c] = val;
+      if (c == 0) lse_part[prow] = l > 0.f ? M + log2f(l) : -INFINITY;
+    }
+  }
+}
+
+template <int D, int R>
+int launch_v2(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const void* q,
+              const pps_pool& pool, void* out, int32_t* err, cudaStream_t st) {
+  auto kern = bw2_attention_kernel<D, R>;
+  constexpr int smem = Bw2<D, R>::SMEM;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return (int)e;
+  }
+  kern<<<(unsigned)n, kBw2Threads, smem, st>>>(
+      t.bw_tasks, t.rows, t.pages, (const __nv_bfloat16*)q, (const __nv_bfloat16*)pool.k,
+      (const __nv_bfloat16*)pool.v, (__nv_bfloat16*)out, t.o_part, t.lse_part, err,
+      s.num_q_heads, s.num_kv_heads, s.group, s.page_size, s.sm_scale * kLog2e);
+  pps::count_launch();
+  return (int)cudaGetLastError();
+}
+
 template <int D, int R>
 int launch_t(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const void* q,
              const pps_pool& pool, void* out, cudaStream_t st) {
@@ -213,18 +550,19 @@ int launch_t(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const v
 namespace pps {
 
 int launch_bw_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
-                        const pps_pool& pool, void* out, int32_t* /*err*/, void* stream) {
+                        const pps_pool& pool, void* out, int32_t* err, void* stream) {
   if (num_tasks == 0) return cudaSuccess;
   auto st = (cudaStream_t)stream;
   // The planner caps rows per task at kBwMaxRows; pick the smallest instance.
+  // Up to 8 rows: the pipelined v2 kernel; 9..16 rows (CUDA-core-only plans): v1.
   const int rows = s.bw_rows_max;
   if (s.head_dim == 128) {
-    if (rows <= 4) return launch_t<128, 4>(s, t, num_tasks, q, pool, out, st);
-    if (rows <= 8) return launch_t<128, 8>(s, t, num_tasks, q, pool, out, st);
+    if (rows <= 4) return launch_v2<128, 4>(s, t, num_tasks, q, pool, out, err, st);
+    if (rows <= 8) return launch_v2<128, 8>(s, t, num_tasks, q, pool, out, err, st);
     return launch_t<128, 16>(s, t, num_tasks, q, pool, out, st);
   }
-  if (rows <= 4) return launch_t<64, 4>(s, t, num_tasks, q, pool, out, st);
-  if (rows <= 8) return launch_t<64, 8>(s, t, num_tasks, q, pool, out, st);
+  if (rows <= 4) return launch_v2<64, 4>(s, t, num_tasks, q, pool, out, err, st);
+  if (rows <= 8) return launch_v2<64, 8>(s, t, num_tasks, q, pool, out, err, st);
   return launch_t<64, 16>(s, t, num_tasks, q, pool, out, st);
 }
 
