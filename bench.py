@@ -182,6 +182,8 @@ def run_pps(args):
     if args.workload == "decode_heavy":
         wl = workloads.decode_heavy(seed=1 + 1000 * rank, device=dev,
                                     num_requests=args.requests or 256)
+    elif args.workload == "long_prefill" and args.requests:
+        wl = workloads.long_prefill(device=dev, num_requests=args.requests)
     else:
         wl = workloads.make(args.workload, device=dev)
     # device-resident inputs
@@ -434,8 +436,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--requests", type=int, default=0,
-                    help="decode_heavy only: number of requests (default 256); for small "
-                         "profiling captures")
+                    help="decode_heavy / long_prefill: number of requests (default 256 / 4); "
+                         "for small profiling captures")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

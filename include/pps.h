@@ -248,6 +248,17 @@ pps_status pps_plan_get_array(const pps_plan* plan, int32_t which, const int32_t
  * is nonzero, resets it to 0.  Synchronous (waits for the device). */
 pps_status pps_get_device_error(int32_t* code, int32_t clear);
 
+/*
+ * pps_selftest_wait_timeout -- diagnostic for the kernels' bounded waits.
+ * Launches one CTA that waits on a shared-memory mbarrier that nothing ever
+ * arrives at, with the same bounded wait the pipelined kernels use, limited to
+ * `limit_ns` nanoseconds (clamped to [1 us, 1 s]).  When the limit runs out the
+ * kernel records PPS_DEV_ERR_WAIT_TIMEOUT in the device error word and returns;
+ * the context stays usable.  No counterpart on the pages (a test hook for the
+ * failure path).
+ */
+pps_status pps_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t pps_launch_count(void);
 

@@ -67,7 +67,7 @@ _I32P = ctypes.POINTER(ctypes.c_int32)
 
 def build(force: bool = False) -> str:
     """Compile libpps.so in place (nvcc, sm_103a)."""
-    from .build import build as _build
+    from .builder import build as _build
     return _build(force=force)
 
 
@@ -91,6 +91,8 @@ def lib():
     L.pps_plan_get_info.argtypes = [vp, ctypes.POINTER(_PlanInfo)]
     L.pps_plan_get_array.argtypes = [vp, i32, ctypes.POINTER(_I32P), ctypes.POINTER(ctypes.c_int64)]
     L.pps_get_device_error.argtypes = [_I32P, i32]
+    L.pps_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    L.pps_selftest_wait_timeout.restype = i32
     L.pps_launch_count.restype = ctypes.c_uint64
     L.pps_status_string.restype = ctypes.c_char_p
     L.pps_status_string.argtypes = [i32]
@@ -256,3 +258,9 @@ def get_device_error(clear: bool = True) -> int:
     code = ctypes.c_int32()
     _check(lib().pps_get_device_error(ctypes.byref(code), int(bool(clear))), "pps_get_device_error")
     return int(code.value)
+
+
+def selftest_wait_timeout(limit_ns: int = 10_000_000, stream=None):
+    """Launch the bounded-wait diagnostic kernel (see pps_selftest_wait_timeout)."""
+    _check(lib().pps_selftest_wait_timeout(int(limit_ns), _stream(stream)),
+           "pps_selftest_wait_timeout")

@@ -2,7 +2,7 @@
 planner with g++, linked with nvcc (static CUDA runtime, no libcuda link; the
 driver API is reached through cudaGetDriverEntryPoint).
 
-    python -m paged_prefix_shared_gb300.build      # or build() from Python
+    python -m paged_prefix_shared_gb300.builder    # or build() from Python
 """
 from __future__ import annotations
 

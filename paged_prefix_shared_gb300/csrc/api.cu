@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "pps_internal.h"
+#include "sm100_ptx.cuh"
 
 // Device error word (one per device that loads the library).
 __device__ int32_t g_pps_device_error = 0;
@@ -101,6 +102,18 @@ pps_status run_impl(const pps_plan* plan, const void* q, const pps_pool* pool, v
   return PPS_OK;
 }
 
+// One thread waits on an mbarrier that never completes; the bounded wait gives
+// up after `limit_ns` and the kernel reports it.
+__global__ void wait_timeout_selftest_kernel(int32_t* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    sm100::mbar_init(sm100::smem_u32(&bar), 1);
+    sm100::fence_mbar_init();
+    if (!sm100::mbar_wait(sm100::smem_u32(&bar), 0, limit_ns))
+      atomicCAS(err, 0, PPS_DEV_ERR_WAIT_TIMEOUT);
+  }
+}
+
 }  // namespace
 
 namespace pps {
@@ -165,6 +178,17 @@ pps_status pps_get_device_error(int32_t* code, int32_t clear) {
       return PPS_ERR_CUDA;
   }
   return PPS_OK;
+}
+
+pps_status pps_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  if (limit_ns < 1000) limit_ns = 1000;
+  if (limit_ns > 1000000000ull) limit_ns = 1000000000ull;
+  cudaError_t e;
+  int32_t* err = error_word(&e);
+  if (!err) return PPS_ERR_CUDA;
+  wait_timeout_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(err, limit_ns);
+  pps::count_launch();
+  return cudaGetLastError() == cudaSuccess ? PPS_OK : PPS_ERR_CUDA;
 }
 
 uint64_t pps_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

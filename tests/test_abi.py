@@ -75,3 +75,22 @@ def test_empty_batch_plans(pps):
     info = plan.info()
     assert info["num_bw_tasks"] == 0 and info["num_mma_tasks"] == 0
     plan.destroy()
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without libpps.so the binding raises; it never falls back to another path."""
+    import subprocess
+    import sys
+    code = (
+        "import sys; sys.path.insert(0, %r)\n"
+        "import paged_prefix_shared_gb300 as p\n"
+        "p.LIB_PATH = %r\n"
+        "try:\n"
+        "    p.attn_plan([0, 1], [1], [0, 1], [0], 8, 2, 64, 16, 1)\n"
+        "except p.PPSError as e:\n"
+        "    print('raised:', e)\n"
+        "    sys.exit(0)\n"
+        "sys.exit(3)\n" % (ROOT, str(tmp_path / "absent" / "libpps.so")))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "missing" in r.stdout

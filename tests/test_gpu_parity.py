@@ -196,3 +196,13 @@ def pps_has_mma(pps):
     L = workloads.tiny_mixed(values=False).layout
     plan = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices, 8, 2, 64, 16, 64)
     return plan.info()["num_mma_tasks"] > 0
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(pps):
+    pps.get_device_error(clear=True)
+    pps.selftest_wait_timeout(20_000_000)            # 20 ms; nothing ever arrives
+    torch.cuda.synchronize()
+    assert pps.get_device_error(clear=True) == 4     # PPS_DEV_ERR_WAIT_TIMEOUT
+    outs, _, _ = run_workload(workloads.tiny_mixed())
+    assert torch.isfinite(outs[0]).all()
+    assert pps.get_device_error(clear=True) == 0
