@@ -64,7 +64,7 @@ typedef int32_t pps_status;
 #define PPS_ERR_WORKSPACE (-4)         /* workspace null or smaller than the plan requires  */
 #define PPS_ERR_CUDA (-5)              /* a CUDA runtime/driver call failed                 */
 #define PPS_ERR_NO_MEMORY (-6)         /* host allocation failed                            */
-#define PPS_ERR_SCRATCH_LIMIT (-7)     /* reserved for entry points with a fixed scratch cap */
+#define PPS_ERR_SCRATCH_LIMIT (-7)     /* plan needs more than the fixed no-alloc scratch    */
 
 /* Device error word values (pps_get_device_error).  0 = no error. */
 #define PPS_DEV_ERR_APPEND_PAGE_ID 1     /* kv_append read a page id outside [0, num_pages)   */
@@ -196,6 +196,32 @@ pps_status pps_attn_run(const pps_plan* plan, const void* q, const pps_pool* poo
 pps_status pps_attn_run_events(const pps_plan* plan, const void* q, const pps_pool* pool,
                                void* out, void* workspace, size_t workspace_bytes, void* stream,
                                void* const* events);
+
+/*
+ * pps_attn_run_noalloc -- pps_attn_run for callers that cannot allocate device
+ * memory.  The paper has no counterpart; this is an integration aid.
+ *
+ * Some callers cannot call cudaMalloc: a plugin inside an engine that owns all
+ * device memory and offers no workspace, or a latency-critical loop that must
+ * not reach cudaMalloc / cudaFree (they can synchronize the device).  This call
+ * takes the same plan, q, pool and out as pps_attn_run, but instead of a
+ * caller workspace it uses a fixed array of PPS_NOALLOC_SCRATCH_BYTES that the
+ * library keeps in device memory (every GPU that loads the library holds that
+ * array until the process exits).  It allocates nothing.
+ *
+ *  - A plan whose workspace_bytes exceeds PPS_NOALLOC_SCRATCH_BYTES is
+ *    rejected with PPS_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the one array.  It keeps the previous call's contents;
+ *    nothing in it needs to start at zero.  Calls whose work overlaps on the
+ *    GPU (different streams, or different host threads) race on the array:
+ *    order them on one stream or synchronize between them.
+ */
+#define PPS_NOALLOC_SCRATCH_BYTES (32u << 20)
+pps_status pps_attn_run_noalloc(const pps_plan* plan, const void* q, const pps_pool* pool,
+                                void* out, void* stream);
 
 /* Frees a plan (host memory only).  NULL is accepted. */
 pps_status pps_plan_destroy(pps_plan* plan);

@@ -87,6 +87,8 @@ def lib():
     L.pps_attn_run.argtypes = [vp, vp, ctypes.POINTER(_Pool), vp, vp, sz, vp]
     L.pps_attn_run_events.argtypes = [vp, vp, ctypes.POINTER(_Pool), vp, vp, sz, vp,
                                       ctypes.POINTER(vp)]
+    L.pps_attn_run_noalloc.argtypes = [vp, vp, ctypes.POINTER(_Pool), vp, vp]
+    L.pps_attn_run_noalloc.restype = i32
     L.pps_plan_destroy.argtypes = [vp]
     L.pps_plan_get_info.argtypes = [vp, ctypes.POINTER(_PlanInfo)]
     L.pps_plan_get_array.argtypes = [vp, i32, ctypes.POINTER(_I32P), ctypes.POINTER(ctypes.c_int64)]
@@ -264,3 +266,18 @@ def selftest_wait_timeout(limit_ns: int = 10_000_000, stream=None):
     """Launch the bounded-wait diagnostic kernel (see pps_selftest_wait_timeout)."""
     _check(lib().pps_selftest_wait_timeout(int(limit_ns), _stream(stream)),
            "pps_selftest_wait_timeout")
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def attn_run_noalloc(plan: Plan, q, pool_k, pool_v, out, stream=None):
+    """pps_attn_run_noalloc: pps_attn_run without a caller workspace, for callers
+    that cannot allocate device memory.  Uses the library's fixed
+    NOALLOC_SCRATCH_BYTES device array; plans that need more are rejected
+    (PPSError).  Calls that overlap on the GPU race on that one array."""
+    import torch
+    pool = _pool(pool_k, pool_v)
+    _check(lib().pps_attn_run_noalloc(plan.handle, _dev(q, torch.bfloat16), ctypes.byref(pool),
+                                      _dev(out, torch.bfloat16), _stream(stream)),
+           "pps_attn_run_noalloc")

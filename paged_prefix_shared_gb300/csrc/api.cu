@@ -202,7 +202,7 @@ const char* pps_status_string(pps_status s) {
     case PPS_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case PPS_ERR_CUDA: return "CUDA call failed";
     case PPS_ERR_NO_MEMORY: return "host allocation failed";
-    case PPS_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch limit";
+    case PPS_ERR_SCRATCH_LIMIT: return "plan needs more than the fixed no-alloc scratch";
     default: return "unknown status";
   }
 }
