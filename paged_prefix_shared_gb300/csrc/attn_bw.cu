@@ -14,6 +14,7 @@
 // (3) P.V accumulated in registers.  A final cross-warp reduction writes the
 // bf16 output row or an fp32 partial (o normalised, lse in log2 units).
 #include <cuda_bf16.h>
+#include <algorithm>
 #include <cuda_runtime.h>
 
 #include "pps_internal.h"
@@ -191,23 +192,25 @@ __global__ void __launch_bounds__(kThreads) bw_attention_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// v2: TMA bulk-copy pipeline, one 16-position sub-block per consumer warp step.
+// Pipelined, persistent kernel (tasks of up to 8 query rows).
 //
-// A producer warp streams the task's K and V rows 16 positions at a time
-// (2 x 16 x d x 2 bytes per stage; a page of P >= 16 slots is P/16 sub-blocks)
-// with cp.async.bulk into an 8-stage ring; four consumer warps take
-// sub-blocks round robin.  In a consumer warp, LPT lanes share one KV row
-// (EL head_dim elements each, two 16-byte chunks at stride LPT so shared
-// memory reads are conflict free), TPW rows are processed per step.  The R
+// One CTA per SM (8 warps: 7 consumers + 1 producer) loops over its share of
+// the work-sorted task list.  The producer streams each task's query rows and
+// its K and V rows 16 positions at a time (2 x 16 x d x 2 bytes per stage; a
+// page of P >= 16 slots is P/16 sub-blocks) with cp.async.bulk into a
+// 16-stage ring, running ahead across task boundaries.  Consumer warps take a
+// task's sub-blocks round robin.  In a consumer warp, LPT lanes share one KV
+// row (EL head_dim elements each, 16-byte chunks at stride LPT so shared
+// memory reads are conflict free) and TPW rows are processed per step.  The R
 // partial dot products of a lane are reduce-scattered across its LPT lanes
 // (log2(LPT) shuffles in all, each lane ends with the full score of one
 // row), the online softmax keeps a per-warp reference max (rescaled only when
-// it rises by more than 2^8), and P.V accumulates into registers with packed
-// fp32x2 FMAs.  Four warps' states are merged through shared memory at the end.
+// it rises by more than 2^8), and P.V accumulates in registers with packed
+// fp32x2 FMAs.  The warps' states are merged through shared memory per task.
 
-constexpr int kBw2Stages = 8;
+constexpr int kBw2Stages = 16;
 constexpr int kBw2Sub = 16;                   // KV positions per stage
-constexpr int kBw2Consumers = 4;
+constexpr int kBw2Consumers = 7;
 constexpr int kBw2Threads = (kBw2Consumers + 1) * 32;
 
 template <int D, int R>
@@ -218,9 +221,7 @@ struct Bw2 {
   static constexpr int ITERS = kBw2Sub / TPW;
   static constexpr int CH = EL / 8;                       // 16-byte chunks per lane
   static constexpr int STAGE = 2 * kBw2Sub * D * 2;       // K then V
-  static constexpr int SMEM = kBw2Stages * STAGE;
   static_assert(R <= LPT, "one row per lane after the reduce-scatter");
-  static_assert(4 * R * (D + 2) * 4 <= SMEM, "combine area fits in the ring");
 };
 
 // Reduce-scatter of V[0..CUR) over lanes xor O, O/2, ..., 1: each halving step
@@ -274,111 +275,166 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Persistent CTAs: CTA b takes tasks b, 2C-1-b, 2C+b, 4C-1-b, ... of the
+// work-sorted list (symmetric round robin over C CTAs, the assignment the
+// XY-Serve review's "What carries the argument" describes for sorted tiles).
+__device__ __forceinline__ int snake_task(int ti, int b, int C) {
+  return ti * C + ((ti & 1) ? (C - 1 - b) : b);
+}
+
 template <int D, int R>
-__global__ void __launch_bounds__(kBw2Threads) bw2_attention_kernel(
-    const pps::Task* __restrict__ tasks, const int32_t* __restrict__ rows,
+struct Bw3Smem {
+  using C = Bw2<D, R>;
+  static constexpr int ring = 0;
+  static constexpr int qbuf = kBw2Stages * C::STAGE;             // 2 x [R][D] bf16
+  static constexpr int qbuf_bytes = R * D * 2;
+  static constexpr int comb = qbuf + 2 * ((qbuf_bytes + 127) / 128 * 128);
+  static constexpr int comb_bytes = kBw2Consumers * R * (D + 2) * 4;
+  static constexpr int total = comb + comb_bytes;
+};
+
+template <int D, int R>
+__global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
+    const pps::Task* __restrict__ tasks, int32_t num_tasks, const int32_t* __restrict__ rows,
     const int32_t* __restrict__ pages, const __nv_bfloat16* __restrict__ q,
     const __nv_bfloat16* __restrict__ pool_k, const __nv_bfloat16* __restrict__ pool_v,
     __nv_bfloat16* __restrict__ out, float* __restrict__ o_part, float* __restrict__ lse_part,
     int32_t* __restrict__ err, int32_t num_q_heads, int32_t num_kv_heads, int32_t G,
     int32_t page_size, float qk_scale) {
   using C = Bw2<D, R>;
+  using S = Bw3Smem<D, R>;
   constexpr int EL = C::EL, LPT = C::LPT, TPW = C::TPW, ITERS = C::ITERS, CH = C::CH;
   extern __shared__ __align__(128) uint8_t bw2_smem[];
-  __shared__ uint64_t full[kBw2Stages], empty[kBw2Stages];
+  __shared__ uint64_t full[kBw2Stages], empty[kBw2Stages], qfull[2], qempty[2];
   __shared__ volatile int abort_flag;
 
-  const pps::Task task = tasks[blockIdx.x];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nrows = task.n_tok * G;
-  const int n_sub = (task.kv_end - task.kv_begin + kBw2Sub - 1) / kBw2Sub;
+  const int b = blockIdx.x, nctas = gridDim.x;
   if (tid == 0) {
     for (int s = 0; s < kBw2Stages; ++s) {
       sm100::mbar_init(sm100::smem_u32(&full[s]), 1);
       sm100::mbar_init(sm100::smem_u32(&empty[s]), 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      sm100::mbar_init(sm100::smem_u32(&qfull[i]), 1);
+      sm100::mbar_init(sm100::smem_u32(&qempty[i]), kBw2Consumers);
+    }
     abort_flag = 0;
     sm100::fence_mbar_init();
   }
   __syncthreads();
-
-  // per-warp online-softmax state (consumer warps), merged after the loop
-  float m_run = -INFINITY, l_run = 0.f;
-  float acc[R][EL];
-  const int grp = lane / LPT, sub = lane % LPT;
-  const int my_row = rs_row<R, LPT / 2>(lane);
+  auto fail = [&]() {
+    atomicCAS(err, 0, PPS_DEV_ERR_WAIT_TIMEOUT);
+    abort_flag = 1;
+  };
 
   if (warp == kBw2Consumers) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       const size_t head_stride = (size_t)page_size * D;
       const uint32_t half = kBw2Sub * D * 2;
-      int issued = 0;
-      for (int k = 0; k < n_sub; ++k) {
-        const int s = k % kBw2Stages, use = k / kBw2Stages;
-        if (use > 0 && !sm100::mbar_wait(sm100::smem_u32(&empty[s]), (use - 1) & 1)) {
-          atomicCAS(err, 0, PPS_DEV_ERR_WAIT_TIMEOUT);
-          abort_flag = 1;
-          break;
+      int gk = 0, t;
+      for (int ti = 0; (t = snake_task(ti, b, nctas)) < num_tasks && !abort_flag; ++ti) {
+        const pps::Task task = tasks[t];
+        // this task's query rows (G heads of one token are contiguous)
+        const int qb = ti & 1, quse = ti >> 1;
+        if (quse > 0 && !sm100::mbar_wait(sm100::smem_u32(&qempty[qb]), (quse - 1) & 1)) { fail(); break; }
+        const uint32_t qbar = sm100::smem_u32(&qfull[qb]);
+        const uint32_t tok_bytes = (uint32_t)G * D * 2;
+        sm100::mbar_expect_tx(qbar, tok_bytes * task.n_tok);
+        for (int i = 0; i < task.n_tok; ++i)
+          bulk_g2s(sm100::smem_u32(bw2_smem + S::qbuf + qb * ((S::qbuf_bytes + 127) / 128 * 128)) +
+                       i * tok_bytes,
+                   q + ((size_t)rows[task.row_off + i] * num_q_heads + task.kv_head * G) * D,
+                   tok_bytes, qbar);
+        const int n_sub = (task.kv_end - task.kv_begin + kBw2Sub - 1) / kBw2Sub;
+        for (int k = 0; k < n_sub; ++k, ++gk) {
+          const int s = gk % kBw2Stages, use = gk / kBw2Stages;
+          if (use > 0 && !sm100::mbar_wait(sm100::smem_u32(&empty[s]), (use - 1) & 1)) { fail(); break; }
+          if (abort_flag) break;
+          const int pos0 = task.kv_begin + k * kBw2Sub;
+          const int page = pages[task.page_off + pos0 / page_size];
+          const size_t off = ((size_t)page * num_kv_heads + task.kv_head) * head_stride +
+                             (size_t)(pos0 % page_size) * D;
+          const uint32_t bar = sm100::smem_u32(&full[s]);
+          const uint32_t dst = sm100::smem_u32(bw2_smem + S::ring + s * C::STAGE);
+          sm100::mbar_expect_tx(bar, 2 * half);
+          bulk_g2s(dst, pool_k + off, half, bar);
+          bulk_g2s(dst + half, pool_v + off, half, bar);
         }
-        if (abort_flag) break;
-        const int pos0 = task.kv_begin + k * kBw2Sub;
-        const int page = pages[task.page_off + pos0 / page_size];
-        const size_t off = ((size_t)page * num_kv_heads + task.kv_head) * head_stride +
-                           (size_t)(pos0 % page_size) * D;
-        const uint32_t bar = sm100::smem_u32(&full[s]);
-        const uint32_t dst = sm100::smem_u32(bw2_smem + s * C::STAGE);
-        sm100::mbar_expect_tx(bar, 2 * half);
-        bulk_g2s(dst, pool_k + off, half, bar);
-        bulk_g2s(dst + half, pool_v + off, half, bar);
-        issued = k + 1;
       }
       // every started copy lands before the CTA may exit
-      for (int k = (issued > kBw2Stages ? issued - kBw2Stages : 0); k < issued; ++k)
+      for (int k = (gk > kBw2Stages ? gk - kBw2Stages : 0); k < gk; ++k)
         sm100::mbar_wait(sm100::smem_u32(&full[k % kBw2Stages]), (k / kBw2Stages) & 1);
     }
-  } else {
-    // ---------------------------------------------------------------- consumers
-    const int h0 = task.kv_head * G;
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int grp = lane / LPT, sub = lane % LPT;
+  const int my_row = rs_row<R, LPT / 2>(lane);
+  float* cm = reinterpret_cast<float*>(bw2_smem + S::comb);   // [warps][R] max
+  float* cl = cm + kBw2Consumers * R;                          // [warps][R] sum
+  float* co = cl + kBw2Consumers * R;                          // [warps][R][D]
+  int gk = 0, t;
+  for (int ti = 0; (t = snake_task(ti, b, nctas)) < num_tasks; ++ti) {
+    const pps::Task task = tasks[t];
+    const int nrows = task.n_tok * G;
+    const int n_sub = (task.kv_end - task.kv_begin + kBw2Sub - 1) / kBw2Sub;
+    bool live = !abort_flag;
+    // query rows from the producer's buffer
+    const int qb = ti & 1;
+    if (live) {
+      const bool got = sm100::mbar_wait(sm100::smem_u32(&qfull[qb]), (ti >> 1) & 1);
+      if (!__all_sync(0xffffffffu, got)) { if (lane == 0) fail(); live = false; }
+    }
     float qr[R][EL];
+    const uint8_t* qs = bw2_smem + S::qbuf + qb * ((S::qbuf_bytes + 127) / 128 * 128);
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const bool real = r < nrows;
-      const int t = real ? rows[task.row_off + r / G] : 0;
-      const __nv_bfloat16* src = q + ((size_t)t * num_q_heads + h0 + (real ? r % G : 0)) * D;
 #pragma unroll
       for (int j = 0; j < CH; ++j) {
         float f[8];
-        const int4 v = real ? __ldg(reinterpret_cast<const int4*>(src + (sub + j * LPT) * 8))
-                            : make_int4(0, 0, 0, 0);
+        const int4 v = (live && r < nrows)
+                           ? *reinterpret_cast<const int4*>(qs + r * D * 2 + (sub + j * LPT) * 16)
+                           : make_int4(0, 0, 0, 0);
         bf16x8_to_f32(v, f);
 #pragma unroll
         for (int x = 0; x < 8; ++x) qr[r][j * 8 + x] = f[x] * qk_scale;
       }
+    }
+    __syncwarp();
+    if (lane == 0) sm100::mbar_arrive(sm100::smem_u32(&qempty[qb]));
+
+    float m_run = -INFINITY, l_run = 0.f;
+    float acc[R][EL];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int e = 0; e < EL; ++e) acc[r][e] = 0.f;
-    }
-    const int lim0 = task.causal;                 // row 0 (first token) has the smallest limit
+    const int lim0 = task.causal;
     const int my_lim = task.causal + my_row / G;
-    for (int k = warp; k < n_sub; k += kBw2Consumers) {
-      const int s = k % kBw2Stages;
-      const bool got = sm100::mbar_wait(sm100::smem_u32(&full[s]), (k / kBw2Stages) & 1) && !abort_flag;
+    for (int k = warp; live && k < n_sub; k += kBw2Consumers) {
+      const int g = gk + k;
+      const int s = g % kBw2Stages;
+      const bool got = sm100::mbar_wait(sm100::smem_u32(&full[s]), (g / kBw2Stages) & 1) && !abort_flag;
       if (!__all_sync(0xffffffffu, got)) {
-        if (lane == 0) { atomicCAS(err, 0, PPS_DEV_ERR_WAIT_TIMEOUT); abort_flag = 1; }
+        if (lane == 0) fail();
+        live = false;
         break;
       }
       const int pos0 = task.kv_begin + k * kBw2Sub;
       const bool fast = (pos0 + kBw2Sub <= task.kv_end) && (pos0 + kBw2Sub - 1 <= lim0);
-      const uint8_t* kb = bw2_smem + s * C::STAGE;
+      const uint8_t* kb = bw2_smem + S::ring + s * C::STAGE;
       const uint8_t* vb = kb + kBw2Sub * D * 2;
       float sc[ITERS];
 #pragma unroll
       for (int it = 0; it < ITERS; ++it) {
-        const int t = it * TPW + grp;
+        const int tt = it * TPW + grp;
         float kf[EL];
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
-          const int4 v = *reinterpret_cast<const int4*>(kb + t * D * 2 + (sub + j * LPT) * 16);
+          const int4 v = *reinterpret_cast<const int4*>(kb + tt * D * 2 + (sub + j * LPT) * 16);
           bf16x8_to_f32(v, kf + j * 8);
         }
         float d[R];
@@ -393,12 +449,11 @@ __global__ void __launch_bounds__(kBw2Threads) bw2_attention_kernel(
         reduce_scatter<R, LPT / 2>(d, lane);
         float sv = d[0];
         if (!fast) {
-          const int pos = pos0 + t;
+          const int pos = pos0 + tt;
           if (pos >= task.kv_end || pos > my_lim) sv = -INFINITY;
         }
         sc[it] = sv;
       }
-      // block max over the sub-block's rows (lanes of the same row, other groups)
       float mx = sc[0];
 #pragma unroll
       for (int it = 1; it < ITERS; ++it) mx = fmaxf(mx, sc[it]);
@@ -427,17 +482,16 @@ __global__ void __launch_bounds__(kBw2Threads) bw2_attention_kernel(
 #pragma unroll
       for (int o = LPT; o < 32; o <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
       l_run += ls;
-      // P.V
 #pragma unroll
       for (int it = 0; it < ITERS; ++it) {
-        const int t = it * TPW + grp;
+        const int tt = it * TPW + grp;
         float vf[EL];
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
-          const int4 v = *reinterpret_cast<const int4*>(vb + t * D * 2 + (sub + j * LPT) * 16);
+          const int4 v = *reinterpret_cast<const int4*>(vb + tt * D * 2 + (sub + j * LPT) * 16);
           bf16x8_to_f32(v, vf + j * 8);
         }
-        if (!fast && pos0 + t >= task.kv_end) {
+        if (!fast && pos0 + tt >= task.kv_end) {
 #pragma unroll
           for (int e = 0; e < EL; ++e) vf[e] = 0.f;   // rows past the end may hold NaN
         }
@@ -456,19 +510,17 @@ __global__ void __launch_bounds__(kBw2Threads) bw2_attention_kernel(
       __syncwarp();
       if (lane == 0) sm100::mbar_arrive(sm100::smem_u32(&empty[s]));
     }
-    // sum the TPW row groups of the warp
+    gk += n_sub;
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int e = 0; e < EL; ++e)
 #pragma unroll
         for (int o = LPT; o < 32; o <<= 1) acc[r][e] += __shfl_xor_sync(0xffffffffu, acc[r][e], o);
-  }
-  __syncthreads();   // ring no longer in use: reuse it for the cross-warp merge
-  float* cm = reinterpret_cast<float*>(bw2_smem);                 // [4][R] max
-  float* cl = cm + kBw2Consumers * R;                         // [4][R] sum
-  float* co = cl + kBw2Consumers * R;                         // [4][R][D]
-  if (warp < kBw2Consumers) {
+
+    // merge the consumer warps' states (named barrier: consumer warps only,
+    // the producer keeps streaming the next task meanwhile)
+    asm volatile("bar.sync 1, %0;" ::"r"(kBw2Consumers * 32) : "memory");
     if (grp == 0) {
 #pragma unroll
       for (int r = 0; r < R; ++r)
@@ -477,34 +529,34 @@ __global__ void __launch_bounds__(kBw2Threads) bw2_attention_kernel(
 #pragma unroll
           for (int x = 0; x < 8; ++x)
             co[(warp * R + r) * D + (sub + j * LPT) * 8 + x] = acc[r][j * 8 + x];
+      if (lane == rs_lane<R, LPT>(my_row)) {
+        cm[warp * R + my_row] = m_run;
+        cl[warp * R + my_row] = l_run;
+      }
     }
-    if (lane == rs_lane<R, LPT>(my_row) && grp == 0) {
-      cm[warp * R + my_row] = m_run;
-      cl[warp * R + my_row] = l_run;
-    }
-  }
-  __syncthreads();
-  for (int idx = tid; idx < nrows * D; idx += kBw2Threads) {
-    const int r = idx / D, c = idx - (idx / D) * D;
-    float M = -INFINITY;
+    asm volatile("bar.sync 1, %0;" ::"r"(kBw2Consumers * 32) : "memory");
+    for (int idx = tid; idx < nrows * D; idx += kBw2Consumers * 32) {
+      const int r = idx / D, c = idx - (idx / D) * D;
+      float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kBw2Consumers; ++w) M = fmaxf(M, cm[w * R + r]);
-    float o = 0.f, l = 0.f;
+      for (int w = 0; w < kBw2Consumers; ++w) M = fmaxf(M, cm[w * R + r]);
+      float o = 0.f, l = 0.f;
 #pragma unroll
-    for (int w = 0; w < kBw2Consumers; ++w) {
-      const float mw = cm[w * R + r];
-      const float sw = (mw == -INFINITY) ? 0.f : fast_ex2(mw - M);
-      o += sw * co[(w * R + r) * D + c];
-      l += sw * cl[w * R + r];
-    }
-    const float val = l > 0.f ? o / l : 0.f;
-    const int i = r / G, h = task.kv_head * G + r % G;
-    if (task.out_pid < 0) {
-      out[((size_t)rows[task.row_off + i] * num_q_heads + h) * D + c] = __float2bfloat16_rn(val);
-    } else {
-      const size_t prow = (size_t)(task.out_pid + i) * num_q_heads + h;
-      o_part[prow * D + c] = val;
-      if (c == 0) lse_part[prow] = l > 0.f ? M + log2f(l) : -INFINITY;
+      for (int w = 0; w < kBw2Consumers; ++w) {
+        const float mw = cm[w * R + r];
+        const float sw = (mw == -INFINITY) ? 0.f : fast_ex2(mw - M);
+        o += sw * co[(w * R + r) * D + c];
+        l += sw * cl[w * R + r];
+      }
+      const float val = l > 0.f ? o / l : 0.f;
+      const int i = r / G, h = task.kv_head * G + r % G;
+      if (task.out_pid < 0) {
+        out[((size_t)rows[task.row_off + i] * num_q_heads + h) * D + c] = __float2bfloat16_rn(val);
+      } else {
+        const size_t prow = (size_t)(task.out_pid + i) * num_q_heads + h;
+        o_part[prow * D + c] = val;
+        if (c == 0) lse_part[prow] = l > 0.f ? M + log2f(l) : -INFINITY;
+      }
     }
   }
 }
@@ -513,15 +565,22 @@ template <int D, int R>
 int launch_v2(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const void* q,
               const pps_pool& pool, void* out, int32_t* err, cudaStream_t st) {
   auto kern = bw2_attention_kernel<D, R>;
-  constexpr int smem = Bw2<D, R>::SMEM;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return (int)e;
-  }
-  kern<<<(unsigned)n, kBw2Threads, smem, st>>>(
-      t.bw_tasks, t.rows, t.pages, (const __nv_bfloat16*)q, (const __nv_bfloat16*)pool.k,
-      (const __nv_bfloat16*)pool.v, (__nv_bfloat16*)out, t.o_part, t.lse_part, err,
-      s.num_q_heads, s.num_kv_heads, s.group, s.page_size, s.sm_scale * kLog2e);
+  constexpr int smem = Bw3Smem<D, R>::total;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return (int)e;
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return (int)e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return (int)e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBw2Threads, smem)) !=
+      cudaSuccess)
+    return (int)e;
+  const int64_t grid = std::min<int64_t>(n, (int64_t)sms * std::max(per_sm, 1));
+  kern<<<(unsigned)grid, kBw2Threads, smem, st>>>(
+      t.bw_tasks, (int32_t)n, t.rows, t.pages, (const __nv_bfloat16*)q,
+      (const __nv_bfloat16*)pool.k, (const __nv_bfloat16*)pool.v, (__nv_bfloat16*)out, t.o_part,
+      t.lse_part, err, s.num_q_heads, s.num_kv_heads, s.group, s.page_size,
+      s.sm_scale * kLog2e);
   pps::count_launch();
   return (int)cudaGetLastError();
 }

@@ -14,46 +14,48 @@
 
 namespace {
 
-// One CTA per merged token; each warp takes query heads h = warp, warp + 4, ...
-// and each lane owns D/32 consecutive output columns.
+// One warp per (merged token, query head); each lane owns D/32 consecutive
+// output columns.  Enough independent warps to cover the memory latency of
+// the few partial rows each one reads.
 template <int D>
-__global__ void __launch_bounds__(128) merge_kernel(
+__global__ void __launch_bounds__(256) merge_kernel(
     const int32_t* __restrict__ tokens, const int32_t* __restrict__ indptr,
     const int32_t* __restrict__ pids, const float* __restrict__ o_part,
-    const float* __restrict__ lse_part, __nv_bfloat16* __restrict__ out, int32_t num_q_heads) {
+    const float* __restrict__ lse_part, __nv_bfloat16* __restrict__ out, int32_t num_q_heads,
+    int64_t num_rows) {
   constexpr int kPer = D / 32;
-  const int m = blockIdx.x;
+  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= num_rows) return;
+  const int m = (int)(wid / num_q_heads), h = (int)(wid - (int64_t)m * num_q_heads);
   const int t = tokens[m];
   const int a = indptr[m], b = indptr[m + 1];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int h = warp; h < num_q_heads; h += 4) {
-    float M = -INFINITY;
-    for (int i = a; i < b; ++i) M = fmaxf(M, __ldg(lse_part + (size_t)pids[i] * num_q_heads + h));
-    float acc[kPer];
+  float M = -INFINITY;
+  for (int i = a; i < b; ++i) M = fmaxf(M, __ldg(lse_part + (size_t)pids[i] * num_q_heads + h));
+  float acc[kPer];
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-    float wsum = 0.f;
-    for (int i = a; i < b; ++i) {
-      const size_t row = (size_t)pids[i] * num_q_heads + h;
-      const float l = __ldg(lse_part + row);
-      const float w = (l == -INFINITY) ? 0.f : exp2f(l - M);
-      wsum += w;
-      const float* src = o_part + row * D + lane * kPer;
-      if constexpr (kPer == 4) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(src));
-        acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
-      } else {
-        static_assert(kPer == 2, "head_dim 64 or 128");
-        const float2 v = __ldg(reinterpret_cast<const float2*>(src));
-        acc[0] += w * v.x; acc[1] += w * v.y;
-      }
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  for (int i = a; i < b; ++i) {
+    const size_t row = (size_t)pids[i] * num_q_heads + h;
+    const float l = __ldg(lse_part + row);
+    const float w = (l == -INFINITY) ? 0.f : exp2f(l - M);
+    wsum += w;
+    const float* src = o_part + row * D + lane * kPer;
+    if constexpr (kPer == 4) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(src));
+      acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+    } else {
+      static_assert(kPer == 2, "head_dim 64 or 128");
+      const float2 v = __ldg(reinterpret_cast<const float2*>(src));
+      acc[0] += w * v.x; acc[1] += w * v.y;
     }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    __nv_bfloat16* dst = out + ((size_t)t * num_q_heads + h) * D + lane * kPer;
-#pragma unroll
-    for (int e = 0; e < kPer; e += 2)
-      *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
   }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat16* dst = out + ((size_t)t * num_q_heads + h) * D + lane * kPer;
+#pragma unroll
+  for (int e = 0; e < kPer; e += 2)
+    *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
 }
 
 }  // namespace
@@ -64,14 +66,16 @@ int launch_merge(const Shape& s, const DeviceTables& t, int64_t num_merge_tokens
                  void* stream) {
   if (num_merge_tokens == 0) return cudaSuccess;
   auto st = (cudaStream_t)stream;
+  const int64_t rows = num_merge_tokens * s.num_q_heads;
+  const unsigned blocks = (unsigned)((rows * 32 + 255) / 256);
   if (s.head_dim == 128)
-    merge_kernel<128><<<(unsigned)num_merge_tokens, 128, 0, st>>>(
-        t.merge_tokens, t.merge_indptr, t.merge_pids, t.o_part, t.lse_part,
-        (__nv_bfloat16*)out, s.num_q_heads);
+    merge_kernel<128><<<blocks, 256, 0, st>>>(t.merge_tokens, t.merge_indptr, t.merge_pids,
+                                               t.o_part, t.lse_part, (__nv_bfloat16*)out,
+                                               s.num_q_heads, rows);
   else
-    merge_kernel<64><<<(unsigned)num_merge_tokens, 128, 0, st>>>(
-        t.merge_tokens, t.merge_indptr, t.merge_pids, t.o_part, t.lse_part,
-        (__nv_bfloat16*)out, s.num_q_heads);
+    merge_kernel<64><<<blocks, 256, 0, st>>>(t.merge_tokens, t.merge_indptr, t.merge_pids,
+                                              t.o_part, t.lse_part, (__nv_bfloat16*)out,
+                                              s.num_q_heads, rows);
   count_launch();
   return (int)cudaGetLastError();
 }
