@@ -307,6 +307,10 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
   extern __shared__ __align__(128) uint8_t bw2_smem[];
   __shared__ uint64_t full[kBw2Stages], empty[kBw2Stages], qfull[2], qempty[2];
   __shared__ volatile int abort_flag;
+  // Per task (double-buffered with the query rows): the task record and its
+  // token ids, written by the producer so consumers never wait on global loads.
+  __shared__ pps::Task tinfo[2];
+  __shared__ int32_t ttok[2][R];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x, nctas = gridDim.x;
@@ -330,41 +334,72 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
 
   if (warp == kBw2Consumers) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      const size_t head_stride = (size_t)page_size * D;
-      const uint32_t half = kBw2Sub * D * 2;
-      int gk = 0, t;
-      for (int ti = 0; (t = snake_task(ti, b, nctas)) < num_tasks && !abort_flag; ++ti) {
-        const pps::Task task = tasks[t];
-        // this task's query rows (G heads of one token are contiguous)
-        const int qb = ti & 1, quse = ti >> 1;
-        if (quse > 0 && !sm100::mbar_wait(sm100::smem_u32(&qempty[qb]), (quse - 1) & 1)) { fail(); break; }
-        const uint32_t qbar = sm100::smem_u32(&qfull[qb]);
-        const uint32_t tok_bytes = (uint32_t)G * D * 2;
-        sm100::mbar_expect_tx(qbar, tok_bytes * task.n_tok);
-        for (int i = 0; i < task.n_tok; ++i)
-          bulk_g2s(sm100::smem_u32(bw2_smem + S::qbuf + qb * ((S::qbuf_bytes + 127) / 128 * 128)) +
-                       i * tok_bytes,
-                   q + ((size_t)rows[task.row_off + i] * num_q_heads + task.kv_head * G) * D,
-                   tok_bytes, qbar);
-        const int n_sub = (task.kv_end - task.kv_begin + kBw2Sub - 1) / kBw2Sub;
-        for (int k = 0; k < n_sub; ++k, ++gk) {
-          const int s = gk % kBw2Stages, use = gk / kBw2Stages;
-          if (use > 0 && !sm100::mbar_wait(sm100::smem_u32(&empty[s]), (use - 1) & 1)) { fail(); break; }
-          if (abort_flag) break;
-          const int pos0 = task.kv_begin + k * kBw2Sub;
-          const int page = pages[task.page_off + pos0 / page_size];
-          const size_t off = ((size_t)page * num_kv_heads + task.kv_head) * head_stride +
-                             (size_t)(pos0 % page_size) * D;
-          const uint32_t bar = sm100::smem_u32(&full[s]);
-          const uint32_t dst = sm100::smem_u32(bw2_smem + S::ring + s * C::STAGE);
-          sm100::mbar_expect_tx(bar, 2 * half);
-          bulk_g2s(dst, pool_k + off, half, bar);
-          bulk_g2s(dst + half, pool_v + off, half, bar);
+    // The whole warp walks the CTA's tasks: lanes fetch 32 page ids at a time
+    // (one coalesced load instead of a dependent load per sub-block) and lane 0
+    // issues the bulk copies.
+    const size_t head_stride = (size_t)page_size * D;
+    const uint32_t half = kBw2Sub * D * 2;
+    int gk = 0, t;
+    bool ok = true;
+    for (int ti = 0; ok && (t = snake_task(ti, b, nctas)) < num_tasks; ++ti) {
+      const pps::Task task = tasks[t];
+      const int qb = ti & 1, quse = ti >> 1;
+      if (lane == 0) {
+        ok = !(quse > 0 && !sm100::mbar_wait(sm100::smem_u32(&qempty[qb]), (quse - 1) & 1)) &&
+             !abort_flag;
+        if (ok) {
+          tinfo[qb] = task;
+          for (int i = 0; i < task.n_tok; ++i) ttok[qb][i] = rows[task.row_off + i];
+          const uint32_t qbar = sm100::smem_u32(&qfull[qb]);
+          const uint32_t tok_bytes = (uint32_t)G * D * 2;
+          sm100::mbar_expect_tx(qbar, tok_bytes * task.n_tok);   // releases tinfo / ttok
+          for (int i = 0; i < task.n_tok; ++i)
+            bulk_g2s(sm100::smem_u32(bw2_smem + S::qbuf + qb * ((S::qbuf_bytes + 127) / 128 * 128)) +
+                         i * tok_bytes,
+                     q + ((size_t)ttok[qb][i] * num_q_heads + task.kv_head * G) * D, tok_bytes,
+                     qbar);
+        } else {
+          fail();
         }
       }
-      // every started copy lands before the CTA may exit
-      for (int k = (gk > kBw2Stages ? gk - kBw2Stages : 0); k < gk; ++k)
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      const int n_sub = (task.kv_end - task.kv_begin + kBw2Sub - 1) / kBw2Sub;
+      for (int k0 = 0; ok && k0 < n_sub; k0 += 32) {
+        int my_page = 0, my_slot = 0;
+        if (k0 + lane < n_sub) {
+          const int pos0 = task.kv_begin + (k0 + lane) * kBw2Sub;
+          my_page = pages[task.page_off + pos0 / page_size];
+          my_slot = pos0 % page_size;
+        }
+        const int cnt = min(32, n_sub - k0);
+        for (int j = 0; j < cnt; ++j, ++gk) {
+          const int page = __shfl_sync(0xffffffffu, my_page, j);
+          const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+          if (lane == 0) {
+            const int s = gk % kBw2Stages, use = gk / kBw2Stages;
+            ok = !(use > 0 && !sm100::mbar_wait(sm100::smem_u32(&empty[s]), (use - 1) & 1)) &&
+                 !abort_flag;
+            if (ok) {
+              const size_t off = ((size_t)page * num_kv_heads + task.kv_head) * head_stride +
+                                 (size_t)slot * D;
+              const uint32_t bar = sm100::smem_u32(&full[s]);
+              const uint32_t dst = sm100::smem_u32(bw2_smem + S::ring + s * C::STAGE);
+              sm100::mbar_expect_tx(bar, 2 * half);
+              bulk_g2s(dst, pool_k + off, half, bar);
+              bulk_g2s(dst + half, pool_v + off, half, bar);
+            } else {
+              fail();
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+        }
+      }
+    }
+    // every started copy lands before the CTA may exit
+    if (lane == 0) {
+      const int issued = gk;   // stages whose copies were issued
+      for (int k = (issued > kBw2Stages ? issued - kBw2Stages : 0); k < issued; ++k)
         sm100::mbar_wait(sm100::smem_u32(&full[k % kBw2Stages]), (k / kBw2Stages) & 1);
     }
     return;
@@ -378,16 +413,19 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
   float* co = cl + kBw2Consumers * R;                          // [warps][R][D]
   int gk = 0, t;
   for (int ti = 0; (t = snake_task(ti, b, nctas)) < num_tasks; ++ti) {
-    const pps::Task task = tasks[t];
-    const int nrows = task.n_tok * G;
-    const int n_sub = (task.kv_end - task.kv_begin + kBw2Sub - 1) / kBw2Sub;
     bool live = !abort_flag;
-    // query rows from the producer's buffer
+    // task record, token ids and query rows from the producer's buffers
     const int qb = ti & 1;
     if (live) {
       const bool got = sm100::mbar_wait(sm100::smem_u32(&qfull[qb]), (ti >> 1) & 1);
       if (!__all_sync(0xffffffffu, got)) { if (lane == 0) fail(); live = false; }
     }
+    const pps::Task task = live ? tinfo[qb] : tasks[t];
+    int32_t tok[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) tok[i] = (live && i < task.n_tok) ? ttok[qb][i] : 0;
+    const int nrows = task.n_tok * G;
+    const int n_sub = (task.kv_end - task.kv_begin + kBw2Sub - 1) / kBw2Sub;
     float qr[R][EL];
     const uint8_t* qs = bw2_smem + S::qbuf + qb * ((S::qbuf_bytes + 127) / 128 * 128);
 #pragma unroll
@@ -550,8 +588,12 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
       }
       const float val = l > 0.f ? o / l : 0.f;
       const int i = r / G, h = task.kv_head * G + r % G;
+      if (!live) continue;
+      int ti_tok = tok[0];
+#pragma unroll
+      for (int x = 1; x < R; ++x) if (x == i) ti_tok = tok[x];
       if (task.out_pid < 0) {
-        out[((size_t)rows[task.row_off + i] * num_q_heads + h) * D + c] = __float2bfloat16_rn(val);
+        out[((size_t)ti_tok * num_q_heads + h) * D + c] = __float2bfloat16_rn(val);
       } else {
         const size_t prow = (size_t)(task.out_pid + i) * num_q_heads + h;
         o_part[prow * D + c] = val;
