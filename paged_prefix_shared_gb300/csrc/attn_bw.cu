@@ -212,6 +212,7 @@ constexpr int kBw2Stages = 16;
 constexpr int kBw2Sub = 16;                   // KV positions per stage
 constexpr int kBw2Consumers = 7;
 constexpr int kBw2Threads = (kBw2Consumers + 1) * 32;
+constexpr int kIssueLanes = 8;                // producer lanes issuing copies at once
 
 template <int D, int R>
 struct Bw2 {
@@ -363,44 +364,44 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      // K/V sub-blocks in batches of kIssueLanes: lane j loads the page id of
+      // sub-block k0 + j, waits for its ring stage and issues its two copies.
+      // A single issuing thread cannot keep 4 KB copies in flight fast enough
+      // to saturate HBM; several lanes issuing at once can.
       const int n_sub = (task.kv_end - task.kv_begin + kBw2Sub - 1) / kBw2Sub;
-      for (int k0 = 0; ok && k0 < n_sub; k0 += 32) {
-        int my_page = 0, my_slot = 0;
-        if (k0 + lane < n_sub) {
+      for (int k0 = 0; ok && k0 < n_sub; k0 += kIssueLanes) {
+        const int cnt = min(kIssueLanes, n_sub - k0);
+        bool good = true;
+        if (lane < cnt) {
+          const int g = gk + lane;
+          const int st = g % kBw2Stages, use = g / kBw2Stages;
           const int pos0 = task.kv_begin + (k0 + lane) * kBw2Sub;
-          my_page = pages[task.page_off + pos0 / page_size];
-          my_slot = pos0 % page_size;
-        }
-        const int cnt = min(32, n_sub - k0);
-        for (int j = 0; j < cnt; ++j, ++gk) {
-          const int page = __shfl_sync(0xffffffffu, my_page, j);
-          const int slot = __shfl_sync(0xffffffffu, my_slot, j);
-          if (lane == 0) {
-            const int s = gk % kBw2Stages, use = gk / kBw2Stages;
-            ok = !(use > 0 && !sm100::mbar_wait(sm100::smem_u32(&empty[s]), (use - 1) & 1)) &&
-                 !abort_flag;
-            if (ok) {
-              const size_t off = ((size_t)page * num_kv_heads + task.kv_head) * head_stride +
-                                 (size_t)slot * D;
-              const uint32_t bar = sm100::smem_u32(&full[s]);
-              const uint32_t dst = sm100::smem_u32(bw2_smem + S::ring + s * C::STAGE);
-              sm100::mbar_expect_tx(bar, 2 * half);
-              bulk_g2s(dst, pool_k + off, half, bar);
-              bulk_g2s(dst + half, pool_v + off, half, bar);
-            } else {
-              fail();
-            }
+          const int page = pages[task.page_off + pos0 / page_size];
+          if (use > 0 && !sm100::mbar_wait(sm100::smem_u32(&empty[st]), (use - 1) & 1)) {
+            good = false;
+          } else if (abort_flag) {
+            good = false;
+          } else {
+            const size_t off = ((size_t)page * num_kv_heads + task.kv_head) * head_stride +
+                               (size_t)(pos0 % page_size) * D;
+            const uint32_t bar = sm100::smem_u32(&full[st]);
+            const uint32_t dst = sm100::smem_u32(bw2_smem + S::ring + st * C::STAGE);
+            sm100::mbar_expect_tx(bar, 2 * half);
+            bulk_g2s(dst, pool_k + off, half, bar);
+            bulk_g2s(dst + half, pool_v + off, half, bar);
           }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
+          if (!good) fail();
         }
+        ok = __all_sync(0xffffffffu, good);
+        gk += cnt;
       }
     }
-    // every started copy lands before the CTA may exit
+    // every started copy lands before the CTA may exit (after a failed wait
+    // some of the last stages were never armed: short bounded waits there)
     if (lane == 0) {
-      const int issued = gk;   // stages whose copies were issued
-      for (int k = (issued > kBw2Stages ? issued - kBw2Stages : 0); k < issued; ++k)
-        sm100::mbar_wait(sm100::smem_u32(&full[k % kBw2Stages]), (k / kBw2Stages) & 1);
+      for (int k = (gk > kBw2Stages ? gk - kBw2Stages : 0); k < gk; ++k)
+        sm100::mbar_wait(sm100::smem_u32(&full[k % kBw2Stages]), (k / kBw2Stages) & 1,
+                         ok ? 2000000000ull : 10000000ull);
     }
     return;
   }

@@ -134,8 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // A wait whose outcome is the same for every lane of the warp (the warp then
   // either goes on to warp-collective tcgen05 ld/st together or leaves together).
-  auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
-    const bool ok = mbar_wait(smem_u32(bar), parity) && !abort_flag;
+  auto warp_wait = [&](uint64_t* bar, uint32_t parity, bool needed = true) {
+    const bool ok = (!needed || mbar_wait(smem_u32(bar), parity)) && !abort_flag;
     return __all_sync(0xffffffffu, ok);
   };
 
@@ -276,46 +276,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 4) {
     // ------------------------------------------------------------- TMA producer
+    // Lane 0 arms each stage's barrier with the tile's byte count, then one
+    // lane per (page, 64-column block) issues its box: a single issuing thread
+    // cannot issue small TMA loads fast enough to keep the tensor core fed.
     if (lane == 0) {
       prefetch_tmap(&tmk);
       prefetch_tmap(&tmv);
-      const int P = p.page_size;
-      const uint32_t box_bytes = (uint32_t)P * 128u;
-      int issued = 0;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % kStages, use = j / kStages;
-        const int t0 = task.kv_begin + j * kTile;
-        const int valid = min(kTile, task.kv_end - t0);
-        const int npg = (valid + P - 1) / P;
-        const uint32_t bytes = (uint32_t)(npg * KB) * box_bytes;
-        if (use > 0 && !mbar_wait(smem_u32(&bars.k_empty[st]), (use - 1) & 1)) { fail(); break; }
-        if (abort_flag) break;
-        const uint32_t kf = smem_u32(&bars.k_full[st]);
-        mbar_expect_tx(kf, bytes);
-        for (int pg = 0; pg < npg; ++pg) {
-          const int page = p.pages[task.page_off + (t0 + pg * P) / P];
-#pragma unroll
-          for (int kb = 0; kb < KB; ++kb)
-            tma_load_4d(k_base + st * Lay::kTileBytes + kb * 16384 + pg * P * 128, &tmk, kb * 64, 0,
-                        task.kv_head, page, kf);
-        }
-        if (use > 0 && !mbar_wait(smem_u32(&bars.v_empty[st]), (use - 1) & 1)) { fail(); break; }
-        const uint32_t vf = smem_u32(&bars.v_full[st]);
-        mbar_expect_tx(vf, bytes);
-        for (int pg = 0; pg < npg; ++pg) {
-          const int page = p.pages[task.page_off + (t0 + pg * P) / P];
-#pragma unroll
-          for (int kb = 0; kb < KB; ++kb)
-            tma_load_4d(v_base + st * Lay::kTileBytes + kb * 16384 + pg * P * 128, &tmv, kb * 64, 0,
-                        task.kv_head, page, vf);
-        }
-        issued = j + 1;
-      }
-      // Before the CTA can exit, every load it started must have landed.
+    }
+    const int P = p.page_size;
+    const uint32_t box_bytes = (uint32_t)P * 128u;
+    int issued = 0;
+    bool ok = true;
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      const int st = j % kStages, use = j / kStages;
+      const int t0 = task.kv_begin + j * kTile;
+      const int valid = min(kTile, task.kv_end - t0);
+      const int npg = (valid + P - 1) / P;
+      const uint32_t bytes = (uint32_t)(npg * KB) * box_bytes;
+      const int pg = lane / KB, kb = lane % KB;
+      const bool mine = lane < npg * KB;
+      const int page = mine ? p.pages[task.page_off + (t0 + pg * P) / P] : 0;
+      const uint32_t kf = smem_u32(&bars.k_full[st]);
+      if (!warp_wait(&bars.k_empty[st], (use - 1) & 1, use > 0)) { fail(); ok = false; break; }
+      if (lane == 0) mbar_expect_tx(kf, bytes);
+      __syncwarp();
+      if (mine)
+        tma_load_4d(k_base + st * Lay::kTileBytes + kb * 16384 + pg * P * 128, &tmk, kb * 64, 0,
+                    task.kv_head, page, kf);
+      const uint32_t vf = smem_u32(&bars.v_full[st]);
+      if (!warp_wait(&bars.v_empty[st], (use - 1) & 1, use > 0)) { fail(); ok = false; break; }
+      if (lane == 0) mbar_expect_tx(vf, bytes);
+      __syncwarp();
+      if (mine)
+        tma_load_4d(v_base + st * Lay::kTileBytes + kb * 16384 + pg * P * 128, &tmv, kb * 64, 0,
+                    task.kv_head, page, vf);
+      issued = j + 1;
+    }
+    // Before the CTA can exit, every load it started must have landed.
+    if (lane == 0) {
       for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j) {
         const int st = j % kStages, use = j / kStages;
-        mbar_wait(smem_u32(&bars.k_full[st]), use & 1);
-        mbar_wait(smem_u32(&bars.v_full[st]), use & 1);
+        mbar_wait(smem_u32(&bars.k_full[st]), use & 1, ok ? 2000000000ull : 10000000ull);
+        mbar_wait(smem_u32(&bars.v_full[st]), use & 1, ok ? 2000000000ull : 10000000ull);
       }
     }
   } else {
