@@ -208,9 +208,15 @@ __global__ void __launch_bounds__(kThreads) bw_attention_kernel(
 // it rises by more than 2^8), and P.V accumulates in registers with packed
 // fp32x2 FMAs.  The warps' states are merged through shared memory per task.
 
-constexpr int kBw2Stages = 16;
 constexpr int kBw2Sub = 16;                   // KV positions per stage
 constexpr int kBw2Consumers = 7;
+// Every consumer warp owns kStagesPerWarp ring stages: sub-block g of the
+// CTA's stream goes to warp g % kBw2Consumers, stage (g / kBw2Consumers) %
+// kStagesPerWarp of that warp.  With one consumer per stage, waiting in order,
+// a stage's full barrier is never waited on more than one phase ahead (its
+// parity bit alone then identifies the phase).
+constexpr int kStagesPerWarp = 3;
+constexpr int kBw2Stages = kBw2Consumers * kStagesPerWarp;
 constexpr int kBw2Threads = (kBw2Consumers + 1) * 32;
 constexpr int kIssueLanes = 8;                // producer lanes issuing copies at once
 
@@ -373,8 +379,10 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
         const int cnt = min(kIssueLanes, n_sub - k0);
         bool good = true;
         if (lane < cnt) {
-          const int g = gk + lane;
-          const int st = g % kBw2Stages, use = g / kBw2Stages;
+          const int g = gk + k0 + lane;
+          const int wi = g / kBw2Consumers;                 // index within its warp's stream
+          const int st = (g % kBw2Consumers) * kStagesPerWarp + wi % kStagesPerWarp;
+          const int use = wi / kStagesPerWarp;
           const int pos0 = task.kv_begin + (k0 + lane) * kBw2Sub;
           const int page = pages[task.page_off + pos0 / page_size];
           if (use > 0 && !sm100::mbar_wait(sm100::smem_u32(&empty[st]), (use - 1) & 1)) {
@@ -393,15 +401,18 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
           if (!good) fail();
         }
         ok = __all_sync(0xffffffffu, good);
-        gk += cnt;
       }
+      gk += n_sub;
     }
     // every started copy lands before the CTA may exit (after a failed wait
     // some of the last stages were never armed: short bounded waits there)
     if (lane == 0) {
-      for (int k = (gk > kBw2Stages ? gk - kBw2Stages : 0); k < gk; ++k)
-        sm100::mbar_wait(sm100::smem_u32(&full[k % kBw2Stages]), (k / kBw2Stages) & 1,
+      for (int g = (gk > kBw2Stages ? gk - kBw2Stages : 0); g < gk; ++g) {
+        const int wi = g / kBw2Consumers;
+        const int st = (g % kBw2Consumers) * kStagesPerWarp + wi % kStagesPerWarp;
+        sm100::mbar_wait(sm100::smem_u32(&full[st]), (wi / kStagesPerWarp) & 1,
                          ok ? 2000000000ull : 10000000ull);
+      }
     }
     return;
   }
@@ -453,10 +464,13 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
       for (int e = 0; e < EL; ++e) acc[r][e] = 0.f;
     const int lim0 = task.causal;
     const int my_lim = task.causal + my_row / G;
-    for (int k = warp; live && k < n_sub; k += kBw2Consumers) {
-      const int g = gk + k;
-      const int s = g % kBw2Stages;
-      const bool got = sm100::mbar_wait(sm100::smem_u32(&full[s]), (g / kBw2Stages) & 1) && !abort_flag;
+    const int first = (warp - gk % kBw2Consumers + kBw2Consumers) % kBw2Consumers;
+    for (int k = first; live && k < n_sub; k += kBw2Consumers) {
+      const int g = gk + k;                                  // g % kBw2Consumers == warp
+      const int wi = g / kBw2Consumers;
+      const int s = warp * kStagesPerWarp + wi % kStagesPerWarp;
+      const bool got =
+          sm100::mbar_wait(sm100::smem_u32(&full[s]), (wi / kStagesPerWarp) & 1) && !abort_flag;
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) fail();
         live = false;

@@ -74,13 +74,27 @@ def test_kv_append_bit_exact(name):
 
 @pytest.mark.parametrize("flags", [0, 1, 2])
 @pytest.mark.parametrize("name", list(small_cases()))
-def test_parity_small(name, flags):
+def test_parity_small(pps, name, flags):
     wl, (ref, _) = _small(name)
+    pps.get_device_error(clear=True)
     outs, _, plans = run_workload(wl, flags=flags)
+    assert pps.get_device_error(clear=True) == 0
     for s, (o, r) in enumerate(zip(outs, ref)):
         assert torch.isfinite(o).all(), f"step {s}: non-finite output (a NaN slot was read?)"
         mx, mean = errors(o, r)
         assert mx <= MAX_ABS and mean <= MEAN_ABS, (s, mx, mean, plans[s].info())
+
+
+@pytest.mark.parametrize("chunk", [512, 2048])
+def test_parity_long_tasks(pps, chunk):
+    """Tasks of hundreds of sub-blocks per CTA (consumer warps drift apart)."""
+    wl = workloads.decode_heavy(num_requests=16, kv_lo=3000, kv_hi=6000, seed=5, **KW)
+    ref, _ = oracle_steps(wl)
+    pps.get_device_error(clear=True)
+    outs, _, plans = run_workload(wl, bw_chunk_tokens=chunk, num_sms=4)
+    assert pps.get_device_error(clear=True) == 0
+    mx, mean = errors(outs[0], ref[0])
+    assert mx <= MAX_ABS and mean <= MEAN_ABS, (mx, mean)
 
 
 @pytest.mark.parametrize("chunk", [16, 64, 200])
@@ -180,7 +194,9 @@ def test_parity_full_size_sampled(pps, name):
     if name == "long_prefill" and not pps_has_mma(pps):
         pytest.skip("long prefill at full size needs the tensor-core path")
     wl = workloads.make(name, device="cuda")
+    pps.get_device_error(clear=True)
     outs, _, plans = run_workload(wl)
+    assert pps.get_device_error(clear=True) == 0     # no bounded wait ran out
     for s, st in enumerate(wl.steps):
         L = st.layout
         assert torch.isfinite(outs[s]).all()
