@@ -1,30 +1,40 @@
 // Tensor-core attention tiles (tcgen05 + TMEM + TMA) for tasks with many query
 // rows: prefill chunks, speculative-verify rows and wide shared-prefix groups.
 //
-// The matmul-softmax-matmul tile of the XY-Serve review ("Core claim"; Fig. 10
-// pipeline of meta-attention) re-designed for sm_103a.  One CTA runs one task:
-// 128 query rows (128 / G tokens x the G query heads of one kv head, so every
-// K/V tile feeds all G heads) against the task's KV range in tiles of 128
-// positions.  Fully masked causal tiles never reach the kernel (the planner
-// stops each tile's KV range at its last token's causal limit; Fig. 11
-// mask-aware computation).
+// The matmul-softmax-matmul tile of the XY-Serve review ("Core claim"; Fig. 10,
+// pipeline of meta-attention, where the cube works on one tile while the
+// vector unit runs the softmax of another) re-designed for sm_103a.
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread m owns query row m = TMEM lane m.  Loads Q into
-//              shared memory, turns S into P (online softmax in log2 units,
-//              fp32), rescales O in TMEM when its reference max moves up by
-//              more than 2^8, and writes the output or the partial (o, lse).
-//   warp 4     TMA producer: K and V tiles, one 64-column box per page and
-//              half of head_dim, into a 2-stage ring (128-byte swizzle).
-//   warp 5     MMA issuer: S = Q K^T into one of two TMEM buffers, then
-//              O += P V (P from shared memory, V MN-major), commits to mbarriers.
-// Every mbarrier wait is bounded; on timeout the kernel records
-// PPS_DEV_ERR_WAIT_TIMEOUT, stops issuing work and still frees TMEM.
+// A task holds up to 256 query rows of one kv head: two 128-row tiles A and B
+// (row = token * G + head, so every K/V tile feeds all G heads) that share the
+// task's KV range.  The tensor core alternates between them: while softmax
+// warpgroup A turns S_A into P_A, the MMA warp runs PV_B and QK_B on tile B,
+// and the other way round.  Each tile skips the KV tiles past its own causal
+// limit, and fully masked tiles never exist (the planner stops each task's
+// range at its last token's limit; Fig. 11, mask-aware computation).
+//
+// Warp roles (320 threads, one persistent CTA per SM taking tasks in
+// symmetric round-robin order over the work-sorted list):
+//   warps 0-3  softmax A, warps 4-7 softmax B: thread m of a warpgroup owns
+//              query row m = TMEM lane m.  It loads its Q row into 128-byte
+//              swizzled shared memory, reads S in two passes over TMEM (row max,
+//              then exp2 / sum / bf16 pack), writes P over S's own columns,
+//              rescales O in TMEM when its reference max rises by more than 2^8,
+//              and writes the output row or the partial (o, lse).
+//   warp 8     TMA producer: K and V tiles of 128 positions (one box per page
+//              and 64-column block, issued by one lane each) into a 2-stage ring.
+//   warp 9     MMA issuer: S_X = Q_X K^T (both K-major in shared memory) and
+//              O_X += P_X V (P from TMEM, V MN-major in shared memory), in the
+//              order PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1).
+// TMEM (512 columns): S_A | S_B | O_A | O_B.  Every mbarrier wait is bounded;
+// on timeout the kernel records PPS_DEV_ERR_WAIT_TIMEOUT, stops issuing work,
+// drains what it issued and still frees TMEM.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "pps_internal.h"
@@ -34,13 +44,17 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 192;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
 constexpr int kStages = 2;
-constexpr int kTile = 128;                    // KV positions per tile = query rows per task
+constexpr int kTile = 128;                    // KV positions per tile = query rows per tile
 constexpr float kRescaleThreshold = 8.f;      // log2 units
 
 struct MmaParams {
   const pps::Task* tasks;
+  int32_t num_tasks;
   const int32_t* rows;
   const int32_t* pages;
   const __nv_bfloat16* q;
@@ -56,7 +70,7 @@ struct MmaParams {
 
 struct Bars {
   uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
-  uint64_t s_full[2], s_free[2], p_full, o_done, q_full, drain;
+  uint64_t s_full[2], p_full[2], o_done[2], q_full, drain;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -65,17 +79,54 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ int snake_task(int ti, int b, int C) {
+  return ti * C + ((ti & 1) ? (C - 1 - b) : b);
+}
+
+// OR of `pred` over the 256 softmax threads (named barrier 1); every softmax
+// thread gets the same answer.
+__device__ __forceinline__ bool softmax_barrier_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n"
+      " bar.red.or.pred po, 1, 256, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
 template <int D>
 struct Layout {
   static constexpr int KB = D / 64;                  // 64-column blocks of head_dim
   static constexpr int kTileBytes = KB * 16384;      // 128 rows x D bf16
-  static constexpr int q_off = 0;
-  static constexpr int k_off = q_off + kTileBytes;
+  static constexpr int q_off = 0;                    // Q_A, Q_B
+  static constexpr int k_off = q_off + 2 * kTileBytes;
   static constexpr int v_off = k_off + kStages * kTileBytes;
-  static constexpr int p_off = v_off + kStages * kTileBytes;
-  static constexpr int bytes = p_off + 2 * 16384;    // P: 128 rows x 128 positions bf16
+  static constexpr int bytes = v_off + kStages * kTileBytes;
   static constexpr int smem_alloc = bytes + 1024;    // slack for 1024-byte alignment
 };
+
+// Per task and tile X: real rows and the number of 128-position KV tiles the
+// tile attends to (its last token's causal limit may end before the task's).
+struct TileRange {
+  int rows;
+  int n_tiles;
+};
+__device__ __forceinline__ TileRange tile_range(const pps::Task& t, int X, int G) {
+  const int n_rows = t.n_tok * G;
+  TileRange r;
+  r.rows = min(max(n_rows - X * 128, 0), 128);
+  if (r.rows == 0) {
+    r.n_tiles = 0;
+    return r;
+  }
+  const int last_tok = (X * 128 + r.rows - 1) / G;
+  int end = t.kv_end;
+  if (t.causal != PPS_NO_CAUSAL) end = min(end, t.causal + last_tok + 1);
+  r.n_tiles = (end - t.kv_begin + kTile - 1) / kTile;
+  return r;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -90,14 +141,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ volatile int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const pps::Task task = p.tasks[blockIdx.x];
+  const int b = blockIdx.x, nctas = gridDim.x;
   const int G = p.G;
-  const int n_rows = task.n_tok * G;
-  const int n_tiles = (task.kv_end - task.kv_begin + kTile - 1) / kTile;
   const uint32_t q_base = smem_u32(smem + Lay::q_off);
   const uint32_t k_base = smem_u32(smem + Lay::k_off);
   const uint32_t v_base = smem_u32(smem + Lay::v_off);
-  const uint32_t p_base = smem_u32(smem + Lay::p_off);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -106,18 +154,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars.v_full[s]), 1);
       mbar_init(smem_u32(&bars.v_empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&bars.s_full[b]), 1);
-      mbar_init(smem_u32(&bars.s_free[b]), 4);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_u32(&bars.s_full[x]), 1);
+      mbar_init(smem_u32(&bars.p_full[x]), 4);
+      mbar_init(smem_u32(&bars.o_done[x]), 1);
     }
-    mbar_init(smem_u32(&bars.p_full), 4);
-    mbar_init(smem_u32(&bars.o_done), 1);
-    mbar_init(smem_u32(&bars.q_full), 4);
+    mbar_init(smem_u32(&bars.q_full), kSoftmaxWarps);
     mbar_init(smem_u32(&bars.drain), 1);
     abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&tmem_base), 512);
     tmem_relinquish();
   }
@@ -125,159 +172,175 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = tmem_base;
-  const uint32_t tm_s[2] = {tm, tm + 128};
-  const uint32_t tm_o = tm + 256;
 
   auto fail = [&]() {
     atomicCAS(p.err, 0, PPS_DEV_ERR_WAIT_TIMEOUT);
     abort_flag = 1;
   };
   // A wait whose outcome is the same for every lane of the warp (the warp then
-  // either goes on to warp-collective tcgen05 ld/st together or leaves together).
+  // goes on to warp-collective tcgen05 ld/st together, or leaves together).
   auto warp_wait = [&](uint64_t* bar, uint32_t parity, bool needed = true) {
     const bool ok = (!needed || mbar_wait(smem_u32(bar), parity)) && !abort_flag;
     return __all_sync(0xffffffffu, ok);
   };
 
-  if (warp < 4) {
+  if (warp < kSoftmaxWarps) {
     // ------------------------------------------------------------- softmax warps
-    const int m = tid;                               // query row = TMEM lane
-    const int i = m / G, g = m - (m / G) * G;
-    const bool real = m < n_rows;
-    const int h = task.kv_head * G + g;
-    const int tok = real ? p.rows[task.row_off + i] : 0;
-    // Q row -> swizzled shared memory (zeros for padding rows)
-    {
-      const int4* src = reinterpret_cast<const int4*>(p.q + ((size_t)tok * p.num_q_heads + h) * D);
+    const int X = warp >> 2;                        // tile of this warpgroup
+    const int m = tid & 127;                        // row within the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tm_s = tm + X * 128;             // S_X, and P_X over its first 64 columns
+    const uint32_t tm_o = tm + 256 + X * D;         // O_X
+    uint8_t* q_tile = smem + Lay::q_off + X * Lay::kTileBytes;
+    int sx = 0, ox = 0;                             // phases consumed on s_full[X] / o_done[X]
+    for (int ti = 0;; ++ti) {
+      const int t = snake_task(ti, b, nctas);
+      // Both warpgroups start a task together (and stop together): neither can
+      // run a task ahead and complete the next task's q_full phase alone.
+      if (softmax_barrier_or(t >= p.num_tasks || abort_flag)) break;
+      const pps::Task task = p.tasks[t];
+      const TileRange tr = tile_range(task, X, G);
+      const int r = X * 128 + m;                    // row within the task
+      const bool real = m < tr.rows;
+      const int i = r / G, g = r - (r / G) * G;
+      const int h = task.kv_head * G + g;
+      const int tok = real ? p.rows[task.row_off + i] : 0;
+      // Q row -> swizzled shared memory (zeros for padding rows).  Every MMA of
+      // the previous task completed before its epilogues, which precede this.
+      {
+        const int4* src = reinterpret_cast<const int4*>(p.q + ((size_t)tok * p.num_q_heads + h) * D);
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const int4 v = real ? __ldg(src + c) : make_int4(0, 0, 0, 0);
-        *reinterpret_cast<int4*>(smem + Lay::q_off + (c / 8) * 16384 + sw128(m, c % 8)) = v;
-      }
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&bars.q_full));
-
-    const int lim = real ? task.causal + i : -1;     // last visible position (inclusive)
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    float m_ref = -INFINITY, l_sum = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      const int b = j & 1;
-      const int t0 = task.kv_begin + j * kTile;
-      if (!warp_wait(&bars.s_full[b], (j >> 1) & 1)) { fail(); ok = false; break; }
-      tc_fence_after();
-      float s[kTile];
-#pragma unroll
-      for (int c0 = 0; c0 < kTile; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tm_s[b] + lane_off + c0, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 32; ++c) s[c0 + c] = __uint_as_float(r[c]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars.s_free[b]));
-
-      const int bound = min(task.kv_end - t0, lim - t0 + 1);   // columns c < bound are visible
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kTile; ++c) {
-        s[c] = (c < bound) ? s[c] * p.qk_scale : -INFINITY;
-        mx = fmaxf(mx, s[c]);
-      }
-      float m_use = m_ref, alpha = 1.f;
-      if (mx > m_ref + kRescaleThreshold || m_ref == -INFINITY) {
-        m_use = fmaxf(mx, m_ref);
-        alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_use);
-      }
-      const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < kTile; ++c) {
-        s[c] = ex2(s[c] - m_sub);                    // exp2(-inf) = 0 for masked columns
-        rs += s[c];
-      }
-      l_sum = l_sum * alpha + rs;
-      m_ref = m_use;
-      // PV of the previous tile must be done before P and O are touched.
-      if (j > 0) {
-        if (!warp_wait(&bars.o_done, (j - 1) & 1)) { fail(); ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(tm_o + lane_off + c0, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-            tmem_st32(tm_o + lane_off + c0, r);
-          }
-          tmem_wait_st();
+        for (int c = 0; c < D / 8; ++c) {
+          const int4 v = real ? __ldg(src + c) : make_int4(0, 0, 0, 0);
+          *reinterpret_cast<int4*>(q_tile + (c / 8) * 16384 + sw128(m, c % 8)) = v;
         }
-      }
-      // P row (bf16) -> swizzled shared memory, K-major over the tile's positions
-#pragma unroll
-      for (int c = 0; c < kTile / 8; ++c) {
-        int4 v;
-        v.x = (int)pack_bf16(s[8 * c + 0], s[8 * c + 1]);
-        v.y = (int)pack_bf16(s[8 * c + 2], s[8 * c + 3]);
-        v.z = (int)pack_bf16(s[8 * c + 4], s[8 * c + 5]);
-        v.w = (int)pack_bf16(s[8 * c + 6], s[8 * c + 7]);
-        *reinterpret_cast<int4*>(smem + Lay::p_off + (c / 8) * 16384 + sw128(m, c % 8)) = v;
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars.p_full));
-    }
-    // epilogue: O / l
-    if (ok && n_tiles > 0) {
-      if (!warp_wait(&bars.o_done, (n_tiles - 1) & 1)) {
-        fail();
-      } else {
+      if (lane == 0) mbar_arrive(smem_u32(&bars.q_full));
+      if (tr.n_tiles == 0) continue;
+
+      const int lim = real ? task.causal + i : -1;  // last visible position (inclusive)
+      float m_ref = -INFINITY, l_sum = 0.f;
+      bool ok = true;
+      for (int j = 0; j < tr.n_tiles; ++j, ++sx) {
+        const int t0 = task.kv_begin + j * kTile;
+        if (!warp_wait(&bars.s_full[X], sx & 1)) { fail(); ok = false; break; }
         tc_fence_after();
-        const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-        const bool direct = task.out_pid < 0;
-        const size_t prow = direct ? 0 : (size_t)(task.out_pid + i) * p.num_q_heads + h;
+        const int bound = min(task.kv_end - t0, lim - t0 + 1);     // columns c < bound visible
+        const bool full = __all_sync(0xffffffffu, bound >= kTile);
+        // pass 1: row max of the raw scores
+        float mx = -INFINITY;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(tm_o + lane_off + c0, r);
+        for (int c0 = 0; c0 < kTile; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tm_s + lane_off + c0, rr);
           tmem_wait_ld();
-          if (real) {
-            if (direct) {
-              __nv_bfloat16* dst = p.out + ((size_t)tok * p.num_q_heads + h) * D + c0;
+          if (full) {
 #pragma unroll
-              for (int c = 0; c < 32; c += 8) {
-                int4 v;
-                v.x = (int)pack_bf16(__uint_as_float(r[c + 0]) * inv, __uint_as_float(r[c + 1]) * inv);
-                v.y = (int)pack_bf16(__uint_as_float(r[c + 2]) * inv, __uint_as_float(r[c + 3]) * inv);
-                v.z = (int)pack_bf16(__uint_as_float(r[c + 4]) * inv, __uint_as_float(r[c + 5]) * inv);
-                v.w = (int)pack_bf16(__uint_as_float(r[c + 6]) * inv, __uint_as_float(r[c + 7]) * inv);
-                *reinterpret_cast<int4*>(dst + c) = v;
-              }
-            } else {
-              float* dst = p.o_part + prow * D + c0;
+            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(rr[c]));
+          } else {
 #pragma unroll
-              for (int c = 0; c < 32; c += 4)
-                *reinterpret_cast<float4*>(dst + c) =
-                    make_float4(__uint_as_float(r[c]) * inv, __uint_as_float(r[c + 1]) * inv,
-                                __uint_as_float(r[c + 2]) * inv, __uint_as_float(r[c + 3]) * inv);
-            }
+            for (int c = 0; c < 32; ++c)
+              if (c0 + c < bound) mx = fmaxf(mx, __uint_as_float(rr[c]));
           }
         }
-        if (real && !direct)
-          p.lse_part[prow] = l_sum > 0.f ? m_ref + __log2f(l_sum) : -INFINITY;
+        const float mxs = (mx == -INFINITY) ? -INFINITY : mx * p.qk_scale;
+        float m_use = m_ref, alpha = 1.f;
+        if (mxs > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mxs != -INFINITY)) {
+          m_use = fmaxf(mxs, m_ref);
+          alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_use);
+        }
+        // O rescale: the PV of this tile's previous KV tile completed before
+        // this S was delivered (one in-order tcgen05 stream; the commit behind
+        // s_full covers both).
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tm_o + lane_off + c0, rr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
+            tmem_st32(tm_o + lane_off + c0, rr);
+          }
+        }
+        m_ref = m_use;
+        const float msub = (m_use == -INFINITY) ? 0.f : m_use;
+        // pass 2: P = exp2(s * scale - m), bf16 pairs over S's first 64 columns
+        // (columns already read: chunk c0 writes columns c0/2 .. c0/2 + 15)
+        float rs = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < kTile; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tm_s + lane_off + c0, rr);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float a = ex2(fmaf(__uint_as_float(rr[c]), p.qk_scale, -msub));
+            float bb = ex2(fmaf(__uint_as_float(rr[c + 1]), p.qk_scale, -msub));
+            if (!full) {
+              if (c0 + c >= bound) a = 0.f;
+              if (c0 + c + 1 >= bound) bb = 0.f;
+            }
+            rs += a + bb;
+            pk[c / 2] = pack_bf16(a, bb);
+          }
+          tmem_st16(tm_s + lane_off + c0 / 2, pk);
+        }
+        l_sum = l_sum * alpha + rs;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[X]));
       }
+      if (!ok) continue;                            // the next task barrier sees the abort
+      // epilogue: O / l once the task's last PV on this tile is done
+      if (!warp_wait(&bars.o_done[X], ox & 1)) {
+        fail();
+        continue;
+      }
+      ++ox;
+      tc_fence_after();
+      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      const bool direct = task.out_pid < 0;
+      const size_t prow = direct ? 0 : (size_t)(task.out_pid + i) * p.num_q_heads + h;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tm_o + lane_off + c0, rr);
+        tmem_wait_ld();
+        if (real) {
+          if (direct) {
+            __nv_bfloat16* dst = p.out + ((size_t)tok * p.num_q_heads + h) * D + c0;
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+              int4 v;
+              v.x = (int)pack_bf16(__uint_as_float(rr[c + 0]) * inv, __uint_as_float(rr[c + 1]) * inv);
+              v.y = (int)pack_bf16(__uint_as_float(rr[c + 2]) * inv, __uint_as_float(rr[c + 3]) * inv);
+              v.z = (int)pack_bf16(__uint_as_float(rr[c + 4]) * inv, __uint_as_float(rr[c + 5]) * inv);
+              v.w = (int)pack_bf16(__uint_as_float(rr[c + 6]) * inv, __uint_as_float(rr[c + 7]) * inv);
+              *reinterpret_cast<int4*>(dst + c) = v;
+            }
+          } else {
+            float* dst = p.o_part + prow * D + c0;
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              *reinterpret_cast<float4*>(dst + c) =
+                  make_float4(__uint_as_float(rr[c]) * inv, __uint_as_float(rr[c + 1]) * inv,
+                              __uint_as_float(rr[c + 2]) * inv, __uint_as_float(rr[c + 3]) * inv);
+          }
+        }
+      }
+      if (real && !direct) p.lse_part[prow] = l_sum > 0.f ? m_ref + __log2f(l_sum) : -INFINITY;
+      tc_fence_before();       // the O reads finish before the next task's first PV
     }
-  } else if (warp == 4) {
+  } else if (warp == kProducerWarp) {
     // ------------------------------------------------------------- TMA producer
-    // Lane 0 arms each stage's barrier with the tile's byte count, then one
-    // lane per (page, 64-column block) issues its box: a single issuing thread
+    // Lane 0 arms a stage's barrier with the tile's byte count, then one lane
+    // per (page, 64-column block) issues its box: a single issuing thread
     // cannot issue small TMA loads fast enough to keep the tensor core fed.
     if (lane == 0) {
       prefetch_tmap(&tmk);
@@ -285,98 +348,145 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int P = p.page_size;
     const uint32_t box_bytes = (uint32_t)P * 128u;
-    int issued = 0;
+    int it = 0;                                     // KV tiles loaded by this CTA
     bool ok = true;
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      const int st = j % kStages, use = j / kStages;
-      const int t0 = task.kv_begin + j * kTile;
-      const int valid = min(kTile, task.kv_end - t0);
-      const int npg = (valid + P - 1) / P;
-      const uint32_t bytes = (uint32_t)(npg * KB) * box_bytes;
-      const int pg = lane / KB, kb = lane % KB;
-      const bool mine = lane < npg * KB;
-      const int page = mine ? p.pages[task.page_off + (t0 + pg * P) / P] : 0;
-      const uint32_t kf = smem_u32(&bars.k_full[st]);
-      if (!warp_wait(&bars.k_empty[st], (use - 1) & 1, use > 0)) { fail(); ok = false; break; }
-      if (lane == 0) mbar_expect_tx(kf, bytes);
-      __syncwarp();
-      if (mine)
-        tma_load_4d(k_base + st * Lay::kTileBytes + kb * 16384 + pg * P * 128, &tmk, kb * 64, 0,
-                    task.kv_head, page, kf);
-      const uint32_t vf = smem_u32(&bars.v_full[st]);
-      if (!warp_wait(&bars.v_empty[st], (use - 1) & 1, use > 0)) { fail(); ok = false; break; }
-      if (lane == 0) mbar_expect_tx(vf, bytes);
-      __syncwarp();
-      if (mine)
-        tma_load_4d(v_base + st * Lay::kTileBytes + kb * 16384 + pg * P * 128, &tmv, kb * 64, 0,
-                    task.kv_head, page, vf);
-      issued = j + 1;
+    int t;
+    for (int ti = 0; ok && (t = snake_task(ti, b, nctas)) < p.num_tasks; ++ti) {
+      const pps::Task task = p.tasks[t];
+      const int n_tiles = max(tile_range(task, 0, G).n_tiles, tile_range(task, 1, G).n_tiles);
+      for (int j = 0; j < n_tiles; ++j, ++it) {
+        const int st = it % kStages, use = it / kStages;
+        const int t0 = task.kv_begin + j * kTile;
+        const int valid = min(kTile, task.kv_end - t0);
+        const int npg = (valid + P - 1) / P;
+        const uint32_t bytes = (uint32_t)(npg * KB) * box_bytes;
+        const int pg = lane / KB, kb = lane % KB;
+        const bool mine = lane < npg * KB;
+        const int page = mine ? p.pages[task.page_off + (t0 + pg * P) / P] : 0;
+        const uint32_t kf = smem_u32(&bars.k_full[st]);
+        if (!warp_wait(&bars.k_empty[st], (use - 1) & 1, use > 0)) { fail(); ok = false; break; }
+        if (lane == 0) mbar_expect_tx(kf, bytes);
+        __syncwarp();
+        if (mine)
+          tma_load_4d(k_base + st * Lay::kTileBytes + kb * 16384 + pg * P * 128, &tmk, kb * 64, 0,
+                      task.kv_head, page, kf);
+        const uint32_t vf = smem_u32(&bars.v_full[st]);
+        if (!warp_wait(&bars.v_empty[st], (use - 1) & 1, use > 0)) { fail(); ok = false; break; }
+        if (lane == 0) mbar_expect_tx(vf, bytes);
+        __syncwarp();
+        if (mine)
+          tma_load_4d(v_base + st * Lay::kTileBytes + kb * 16384 + pg * P * 128, &tmv, kb * 64, 0,
+                      task.kv_head, page, vf);
+      }
     }
-    // Before the CTA can exit, every load it started must have landed.
+    // every load this CTA started lands before it may exit
     if (lane == 0) {
-      for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j) {
+      const uint64_t lim = ok ? 2000000000ull : 10000000ull;
+      for (int j = (it > kStages ? it - kStages : 0); j < it; ++j) {
         const int st = j % kStages, use = j / kStages;
-        mbar_wait(smem_u32(&bars.k_full[st]), use & 1, ok ? 2000000000ull : 10000000ull);
-        mbar_wait(smem_u32(&bars.v_full[st]), use & 1, ok ? 2000000000ull : 10000000ull);
+        mbar_wait(smem_u32(&bars.k_full[st]), use & 1, lim);
+        mbar_wait(smem_u32(&bars.v_full[st]), use & 1, lim);
       }
     }
   } else {
     // ------------------------------------------------------------- MMA issuer
     constexpr uint32_t id_qk = idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t id_pv = idesc_bf16(128, D, 0, 1);
-    bool ok = warp_wait(&bars.q_full, 0);
-    if (!ok) fail();
-    for (int j = 0; ok && j <= n_tiles; ++j) {
-      if (j < n_tiles) {
-        const int st = j % kStages, b = j & 1;
-        if (!warp_wait(&bars.k_full[st], (j / kStages) & 1)) { fail(); break; }
-        if (j >= 2 && !warp_wait(&bars.s_free[b], ((j - 2) >> 1) & 1)) { fail(); break; }
+    int it = 0;                                     // KV tiles consumed (ring position)
+    int px[2] = {0, 0};                             // phases consumed on p_full[X]
+    int qn = 0;                                     // phases consumed on q_full
+    bool ok = true;
+    int t;
+    auto qk = [&](int X, int st) {
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t qt = q_base + X * Lay::kTileBytes;
+        const uint32_t kt = k_base + st * Lay::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
+          umma_ss(tm + X * 128, smem_desc(qt + off, 16, 1024), smem_desc(kt + off, 16, 1024), id_qk,
+                  ks > 0);
+        }
+        umma_commit(smem_u32(&bars.s_full[X]));
+      }
+      __syncwarp();
+    };
+    auto pv = [&](int X, int st, bool first, bool last_of_task) {
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t vt = v_base + st * Lay::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks)
+          umma_ts(tm + 256 + X * D, tm + X * 128 + ks * 8, smem_desc(vt + ks * 2048, 16384, 1024),
+                  id_pv, (!first || ks > 0) ? 1u : 0u);
+        if (last_of_task) umma_commit(smem_u32(&bars.o_done[X]));
+      }
+      __syncwarp();
+    };
+    // V rows past the task's last position may hold anything (NaN included);
+    // P is 0 there, and 0 * NaN would poison O, so clear them.
+    auto clear_v_tail = [&](int st, int valid) {
+      uint8_t* vt = smem + Lay::v_off + st * Lay::kTileBytes;
+      const int rows = kTile - valid;
+      for (int idx = lane; idx < rows * 8 * KB; idx += 32) {
+        const int kb = idx / (rows * 8);
+        const int rem = idx - kb * rows * 8;
+        *reinterpret_cast<int4*>(vt + kb * 16384 + (valid + rem / 8) * 128 + (rem % 8) * 16) =
+            make_int4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    };
+    for (int ti = 0; ok && (t = snake_task(ti, b, nctas)) < p.num_tasks; ++ti) {
+      const pps::Task task = p.tasks[t];
+      const int nt[2] = {tile_range(task, 0, G).n_tiles, tile_range(task, 1, G).n_tiles};
+      const int n_tiles = max(nt[0], nt[1]);
+      if (!warp_wait(&bars.q_full, qn & 1)) { fail(); ok = false; break; }
+      ++qn;
+      // QK of the first KV tile for both query tiles
+      {
+        const int st = it % kStages;
+        if (!warp_wait(&bars.k_full[st], (it / kStages) & 1)) { fail(); ok = false; break; }
+        for (int X = 0; X < 2; ++X)
+          if (nt[X] > 0) qk(X, st);
+        tc_fence_after();
+        if (lane == 0) umma_commit(smem_u32(&bars.k_empty[st]));   // K_0 used by both QKs
+        __syncwarp();
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = (it + j) % kStages;
+        const int stn = (it + j + 1) % kStages;
+        const bool next = j + 1 < n_tiles;
+        const int valid = min(kTile, task.kv_end - (task.kv_begin + j * kTile));
+        bool v_ready = false, k_ready = false;
+        for (int X = 0; X < 2; ++X) {
+          if (j >= nt[X]) continue;
+          if (!warp_wait(&bars.p_full[X], px[X] & 1)) { fail(); ok = false; break; }
+          ++px[X];
+          if (!v_ready) {
+            if (!warp_wait(&bars.v_full[st], ((it + j) / kStages) & 1)) { fail(); ok = false; break; }
+            if (valid < kTile) clear_v_tail(st, valid);
+            v_ready = true;
+          }
+          pv(X, st, j == 0, j + 1 == nt[X]);
+          if (j + 1 < nt[X]) {
+            if (!k_ready) {
+              if (!warp_wait(&bars.k_full[stn], ((it + j + 1) / kStages) & 1)) { fail(); ok = false; break; }
+              k_ready = true;
+            }
+            qk(X, stn);
+          }
+        }
+        if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t kt = k_base + st * Lay::kTileBytes;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
-            umma_ss(tm_s[b], smem_desc(q_base + off, 16, 1024), smem_desc(kt + off, 16, 1024),
-                    id_qk, ks > 0);
-          }
-          umma_commit(smem_u32(&bars.s_full[b]));
-          umma_commit(smem_u32(&bars.k_empty[st]));
+          umma_commit(smem_u32(&bars.v_empty[st]));                 // V_j no longer needed
+          if (next) umma_commit(smem_u32(&bars.k_empty[stn]));      // K_{j+1} used by its QKs
         }
         __syncwarp();
       }
-      if (j >= 1) {
-        const int jj = j - 1, st = jj % kStages;
-        if (!warp_wait(&bars.p_full, jj & 1)) { fail(); break; }
-        if (!warp_wait(&bars.v_full[st], (jj / kStages) & 1)) { fail(); break; }
-        const int valid = min(kTile, task.kv_end - (task.kv_begin + jj * kTile));
-        if (valid < kTile) {
-          // Rows past the task's last position may hold anything (NaN included);
-          // P is 0 there, and 0 * NaN would poison O, so clear them.
-          uint8_t* vt = smem + Lay::v_off + st * Lay::kTileBytes;
-          for (int idx = lane; idx < (kTile - valid) * 8 * KB; idx += 32) {
-            const int kb = idx / ((kTile - valid) * 8);
-            const int rem = idx - kb * (kTile - valid) * 8;
-            const int r = valid + rem / 8, c = rem % 8;
-            *reinterpret_cast<int4*>(vt + kb * 16384 + r * 128 + c * 16) = make_int4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t vt = v_base + st * Lay::kTileBytes;
-#pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks) {
-            const uint32_t aoff = (ks / 4) * 16384 + (ks % 4) * 32;
-            umma_ss(tm_o, smem_desc(p_base + aoff, 16, 1024), smem_desc(vt + ks * 2048, 16384, 1024),
-                    id_pv, (jj > 0 || ks > 0) ? 1u : 0u);
-          }
-          umma_commit(smem_u32(&bars.o_done));
-          umma_commit(smem_u32(&bars.v_empty[st]));
-        }
-        __syncwarp();
-      }
+      it += n_tiles;
     }
     // Every MMA this warp issued has completed before TMEM is freed.
     if (lane == 0) {
@@ -388,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tm, 512);
   }
@@ -435,10 +545,15 @@ int launch_t(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const v
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Layout<D>::smem_alloc);
   if (e != cudaSuccess) return (int)e;
-  MmaParams prm{t.mma_tasks, t.rows, t.pages, (const __nv_bfloat16*)q, (__nv_bfloat16*)out,
-                t.o_part, t.lse_part, err, s.num_q_heads, s.group, s.page_size,
-                s.sm_scale * 1.4426950408889634f};
-  kern<<<(unsigned)n, kThreads, Layout<D>::smem_alloc, st>>>(mk, mv, prm);
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return (int)e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return (int)e;
+  const int64_t grid = std::min<int64_t>(n, sms);
+  MmaParams prm{t.mma_tasks, (int32_t)n, t.rows, t.pages, (const __nv_bfloat16*)q,
+                (__nv_bfloat16*)out, t.o_part, t.lse_part, err, s.num_q_heads, s.group,
+                s.page_size, s.sm_scale * 1.4426950408889634f};
+  kern<<<(unsigned)grid, kThreads, Layout<D>::smem_alloc, st>>>(mk, mv, prm);
   pps::count_launch();
   return (int)cudaGetLastError();
 }

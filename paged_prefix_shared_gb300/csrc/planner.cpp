@@ -203,7 +203,7 @@ extern "C" pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_l
     // ---- 3. tiles and split-KV chunks ----------------------------------------------
     const int32_t bw_max_tok = std::max(1, 8 / G);          // decode-like rows stay on CUDA cores
     const int32_t bw_tile_tok = std::max(1, pps::kBwMaxRows / G);
-    const int32_t mma_tile_tok = pps::kMmaRows / G;
+    const int32_t mma_tile_tok = pps::kMmaTaskRows / G;
     auto is_mma = [&](const Segment& s) { return use_mma && s.n_tok > bw_max_tok; };
     auto tile_tok_of = [&](const Segment& s) {
       if (is_mma(s)) return mma_tile_tok;
@@ -266,7 +266,7 @@ extern "C" pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_l
           ts.tile = tile;
           ts.chunk = (int32_t)k;
           ts.mma = mma;
-          const int64_t rows_eff = mma ? pps::kMmaRows : (int64_t)ts.n_tok * G;
+          const int64_t rows_eff = mma ? pps::kMmaTaskRows : (int64_t)ts.n_tok * G;
           ts.work = rows_eff * (ts.kv_end - ts.kv_begin);
           ts.out_pid = -1;
           sets.push_back(ts);

@@ -25,6 +25,7 @@ static_assert(sizeof(Task) == PPS_TASK_INTS * 4, "task record size");
 // Limits of the kernels.
 constexpr int kBwMaxRows = 16;      // query rows (tokens x G) per bandwidth task
 constexpr int kMmaRows = 128;       // query rows per tensor-core tile (TMEM lanes)
+constexpr int kMmaTaskRows = 256;   // query rows per tensor-core task (two tiles sharing K/V)
 constexpr int kMmaKvTile = 128;     // KV positions per tensor-core step
 
 // Offsets (in int32 units) of the sections of the uploaded task table.
