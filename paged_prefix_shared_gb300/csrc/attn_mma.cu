@@ -17,10 +17,11 @@
 // symmetric round-robin order over the work-sorted list):
 //   warps 0-3  softmax A, warps 4-7 softmax B: thread m of a warpgroup owns
 //              query row m = TMEM lane m.  It loads its Q row into 128-byte
-//              swizzled shared memory, reads S in two passes over TMEM (row max,
-//              then exp2 / sum / bf16 pack), writes P over S's own columns,
-//              rescales O in TMEM when its reference max rises by more than 2^8,
-//              and writes the output row or the partial (o, lse).
+//              swizzled shared memory, turns its S row into P in one pass over
+//              TMEM against its running reference max (two passes, and an O
+//              rescale in TMEM, only when a score exceeds that reference by more
+//              than 2^8), writes P as bf16 over S's own columns, and writes the
+//              output row or the partial (o, lse).
 //   warp 8     TMA producer: K and V tiles of 128 positions (one box per page
 //              and 64-column block, issued by one lane each) into a 2-stage ring.
 //   warp 9     MMA issuer: S_X = Q_X K^T (both K-major in shared memory) and
@@ -222,7 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tr.n_tiles == 0) continue;
 
       const int lim = real ? task.causal + i : -1;  // last visible position (inclusive)
-      float m_ref = -INFINITY, l_sum = 0.f;
+      // Padding rows see no key: any finite reference keeps their P at 0 and
+      // keeps them off the exact path below.
+      float m_ref = real ? -INFINITY : 0.f, l_sum = 0.f;
       bool ok = true;
       for (int j = 0; j < tr.n_tiles; ++j, ++sx) {
         const int t0 = task.kv_begin + j * kTile;
@@ -230,66 +233,104 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int bound = min(task.kv_end - t0, lim - t0 + 1);     // columns c < bound visible
         const bool full = __all_sync(0xffffffffu, bound >= kTile);
-        // pass 1: row max of the raw scores
-        float mx = -INFINITY;
+        uint32_t pk[kTile / 2];                    // P row, bf16 pairs, stored once verified
+        float rs = 0.f, alpha = 1.f, m_use = m_ref;
+        // One pass against the running reference max: P = exp2(s * scale - m_ref).
+        // Valid unless some score exceeds the reference by the rescale threshold
+        // (rare once a row has seen a tile); then the exact two-pass path below.
+        bool exact = __any_sync(0xffffffffu, m_ref == -INFINITY);
+        if (!exact) {
+          float mx = -INFINITY;
 #pragma unroll
-        for (int c0 = 0; c0 < kTile; c0 += 32) {
-          uint32_t rr[32];
-          tmem_ld32(tm_s + lane_off + c0, rr);
-          tmem_wait_ld();
-          if (full) {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(rr[c]));
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (c0 + c < bound) mx = fmaxf(mx, __uint_as_float(rr[c]));
-          }
-        }
-        const float mxs = (mx == -INFINITY) ? -INFINITY : mx * p.qk_scale;
-        float m_use = m_ref, alpha = 1.f;
-        if (mxs > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mxs != -INFINITY)) {
-          m_use = fmaxf(mxs, m_ref);
-          alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_use);
-        }
-        // O rescale: the PV of this tile's previous KV tile completed before
-        // this S was delivered (one in-order tcgen05 stream; the commit behind
-        // s_full covers both).
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = 0; c0 < kTile; c0 += 32) {
             uint32_t rr[32];
-            tmem_ld32(tm_o + lane_off + c0, rr);
+            tmem_ld32(tm_s + lane_off + c0, rr);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
-            tmem_st32(tm_o + lane_off + c0, rr);
+            for (int c = 0; c < 32; c += 2) {
+              float sa = __uint_as_float(rr[c]), sb = __uint_as_float(rr[c + 1]);
+              if (!full) {
+                if (c0 + c >= bound) sa = -INFINITY;
+                if (c0 + c + 1 >= bound) sb = -INFINITY;
+              }
+              mx = fmaxf(mx, fmaxf(sa, sb));
+              const float a = ex2(fmaf(sa, p.qk_scale, -m_ref));
+              const float bb = ex2(fmaf(sb, p.qk_scale, -m_ref));
+              rs += a + bb;
+              pk[(c0 + c) / 2] = pack_bf16(a, bb);
+            }
+          }
+          const float mxs = (mx == -INFINITY) ? -INFINITY : mx * p.qk_scale;
+          exact = __any_sync(0xffffffffu, mxs > m_ref + kRescaleThreshold);
+          if (!exact) {
+            // P over S's first 64 columns (S has been read in full above)
+#pragma unroll
+            for (int c0 = 0; c0 < kTile / 2; c0 += 16) {
+              uint32_t w[16];
+#pragma unroll
+              for (int c = 0; c < 16; ++c) w[c] = pk[c0 + c];
+              tmem_st16(tm_s + lane_off + c0, w);
+            }
+          }
+        }
+        if (exact) {
+          // pass 1: row max of the raw scores
+          float mx = -INFINITY;
+#pragma unroll
+          for (int c0 = 0; c0 < kTile; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tm_s + lane_off + c0, rr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (full || c0 + c < bound) mx = fmaxf(mx, __uint_as_float(rr[c]));
+          }
+          const float mxs = (mx == -INFINITY) ? -INFINITY : mx * p.qk_scale;
+          m_use = m_ref;
+          alpha = 1.f;
+          if (mxs > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mxs != -INFINITY)) {
+            m_use = fmaxf(mxs, m_ref);
+            alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_use);
+          }
+          // O rescale: the PV of this tile's previous KV tile completed before
+          // this S was delivered (one in-order tcgen05 stream; the commit behind
+          // s_full covers both).
+          if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t rr[32];
+              tmem_ld32(tm_o + lane_off + c0, rr);
+              tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
+              tmem_st32(tm_o + lane_off + c0, rr);
+            }
+          }
+          const float msub = (m_use == -INFINITY) ? 0.f : m_use;
+          // pass 2: P = exp2(s * scale - m); chunk c0 is stored over columns
+          // c0/2 .. c0/2 + 15, all of which this pass has already read
+          rs = 0.f;
+#pragma unroll
+          for (int c0 = 0; c0 < kTile; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tm_s + lane_off + c0, rr);
+            tmem_wait_ld();
+            uint32_t w[16];
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              float a = ex2(fmaf(__uint_as_float(rr[c]), p.qk_scale, -msub));
+              float bb = ex2(fmaf(__uint_as_float(rr[c + 1]), p.qk_scale, -msub));
+              if (!full) {
+                if (c0 + c >= bound) a = 0.f;
+                if (c0 + c + 1 >= bound) bb = 0.f;
+              }
+              rs += a + bb;
+              w[c / 2] = pack_bf16(a, bb);
+            }
+            tmem_st16(tm_s + lane_off + c0 / 2, w);
           }
         }
         m_ref = m_use;
-        const float msub = (m_use == -INFINITY) ? 0.f : m_use;
-        // pass 2: P = exp2(s * scale - m), bf16 pairs over S's first 64 columns
-        // (columns already read: chunk c0 writes columns c0/2 .. c0/2 + 15)
-        float rs = 0.f;
-#pragma unroll
-        for (int c0 = 0; c0 < kTile; c0 += 32) {
-          uint32_t rr[32];
-          tmem_ld32(tm_s + lane_off + c0, rr);
-          tmem_wait_ld();
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float a = ex2(fmaf(__uint_as_float(rr[c]), p.qk_scale, -msub));
-            float bb = ex2(fmaf(__uint_as_float(rr[c + 1]), p.qk_scale, -msub));
-            if (!full) {
-              if (c0 + c >= bound) a = 0.f;
-              if (c0 + c + 1 >= bound) bb = 0.f;
-            }
-            rs += a + bb;
-            pk[c / 2] = pack_bf16(a, bb);
-          }
-          tmem_st16(tm_s + lane_off + c0 / 2, pk);
-        }
         l_sum = l_sum * alpha + rs;
         tmem_wait_st();
         tc_fence_before();
