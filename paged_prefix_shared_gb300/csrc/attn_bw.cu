@@ -300,6 +300,185 @@ struct Bw3Smem {
   static constexpr int total = comb + comb_bytes;
 };
 
+// Pointers a consumer warp needs besides its task (shared memory of the CTA).
+struct BwShared {
+  const uint8_t* ring;
+  uint64_t* full;
+  uint64_t* empty;
+  volatile int* abort_flag;
+  int32_t* err;
+  float* cm;
+  float* cl;
+  float* co;
+};
+
+// One consumer warp's share of one task: its sub-blocks (stream positions
+// g = gk + k with g % kBw2Consumers == warp), an online softmax over the
+// task's R rows, then its (max, sum, o) written to the combine buffer whose row
+// stride is RS >= R.  Returns false when a wait ran out.
+template <int D, int R, int RS>
+__device__ __forceinline__ bool bw_consume(const pps::Task& task, int nrows, int G, int n_sub,
+                                           int gk, const uint8_t* qs, float qk_scale, bool live,
+                                           const BwShared& sh, uint64_t* qempty) {
+  using C = Bw2<D, R>;
+  constexpr int EL = C::EL, LPT = C::LPT, TPW = C::TPW, ITERS = C::ITERS, CH = C::CH;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int grp = lane / LPT, sub = lane % LPT;
+  const int my_row = rs_row<R, LPT / 2>(lane);
+  float qr[R][EL];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      float f[8];
+      const int4 v = (live && r < nrows)
+                         ? *reinterpret_cast<const int4*>(qs + r * D * 2 + (sub + j * LPT) * 16)
+                         : make_int4(0, 0, 0, 0);
+      bf16x8_to_f32(v, f);
+#pragma unroll
+      for (int x = 0; x < 8; ++x) qr[r][j * 8 + x] = f[x] * qk_scale;
+    }
+  }
+  __syncwarp();
+  if (lane == 0) sm100::mbar_arrive(sm100::smem_u32(qempty));
+
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[R][EL];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int e = 0; e < EL; ++e) acc[r][e] = 0.f;
+  const int lim0 = task.causal;
+  const int my_lim = task.causal + my_row / G;
+  const int first = (warp - gk % kBw2Consumers + kBw2Consumers) % kBw2Consumers;
+  for (int k = first; live && k < n_sub; k += kBw2Consumers) {
+    const int g = gk + k;                                  // g % kBw2Consumers == warp
+    const int wi = g / kBw2Consumers;
+    const int s = warp * kStagesPerWarp + wi % kStagesPerWarp;
+    const bool got =
+        sm100::mbar_wait(sm100::smem_u32(&sh.full[s]), (wi / kStagesPerWarp) & 1) && !*sh.abort_flag;
+    if (!__all_sync(0xffffffffu, got)) {
+      if (lane == 0) {
+        atomicCAS(sh.err, 0, PPS_DEV_ERR_WAIT_TIMEOUT);
+        *sh.abort_flag = 1;
+      }
+      live = false;
+      break;
+    }
+    const int pos0 = task.kv_begin + k * kBw2Sub;
+    const bool fast = (pos0 + kBw2Sub <= task.kv_end) && (pos0 + kBw2Sub - 1 <= lim0);
+    const uint8_t* kb = sh.ring + s * (2 * kBw2Sub * D * 2);
+    const uint8_t* vb = kb + kBw2Sub * D * 2;
+    float sc[ITERS];
+#pragma unroll
+    for (int it = 0; it < ITERS; ++it) {
+      const int tt = it * TPW + grp;
+      float kf[EL];
+#pragma unroll
+      for (int j = 0; j < CH; ++j) {
+        const int4 v = *reinterpret_cast<const int4*>(kb + tt * D * 2 + (sub + j * LPT) * 16);
+        bf16x8_to_f32(v, kf + j * 8);
+      }
+      float d[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < EL; e += 2)
+          a = __ffma2_rn(make_float2(qr[r][e], qr[r][e + 1]), make_float2(kf[e], kf[e + 1]), a);
+        d[r] = a.x + a.y;
+      }
+      reduce_scatter<R, LPT / 2>(d, lane);
+      float sv = d[0];
+      if (!fast) {
+        const int pos = pos0 + tt;
+        if (pos >= task.kv_end || pos > my_lim) sv = -INFINITY;
+      }
+      sc[it] = sv;
+    }
+    float mx = sc[0];
+#pragma unroll
+    for (int it = 1; it < ITERS; ++it) mx = fmaxf(mx, sc[it]);
+#pragma unroll
+    for (int o = LPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const bool need = (mx > m_run + 8.f) || (m_run == -INFINITY && mx != -INFINITY);
+    if (__any_sync(0xffffffffu, need)) {
+      const float m_new = need ? fmaxf(mx, m_run) : m_run;
+      const float alpha = (m_run == -INFINITY) ? 0.f : fast_ex2(m_run - m_new);
+      m_run = m_new;
+      l_run *= alpha;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float a = __shfl_sync(0xffffffffu, alpha, rs_lane<R, LPT>(r));
+#pragma unroll
+        for (int e = 0; e < EL; ++e) acc[r][e] *= a;
+      }
+    }
+    const float msub = (m_run == -INFINITY) ? 0.f : m_run;
+    float ls = 0.f;
+#pragma unroll
+    for (int it = 0; it < ITERS; ++it) {
+      sc[it] = fast_ex2(sc[it] - msub);
+      ls += sc[it];
+    }
+#pragma unroll
+    for (int o = LPT; o < 32; o <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    l_run += ls;
+#pragma unroll
+    for (int it = 0; it < ITERS; ++it) {
+      const int tt = it * TPW + grp;
+      float vf[EL];
+#pragma unroll
+      for (int j = 0; j < CH; ++j) {
+        const int4 v = *reinterpret_cast<const int4*>(vb + tt * D * 2 + (sub + j * LPT) * 16);
+        bf16x8_to_f32(v, vf + j * 8);
+      }
+      if (!fast && pos0 + tt >= task.kv_end) {
+#pragma unroll
+        for (int e = 0; e < EL; ++e) vf[e] = 0.f;   // rows past the end may hold NaN
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float pr = __shfl_sync(0xffffffffu, sc[it], grp * LPT + rs_lane<R, LPT>(r));
+#pragma unroll
+        for (int e = 0; e < EL; e += 2) {
+          const float2 o2 = __ffma2_rn(make_float2(pr, pr), make_float2(vf[e], vf[e + 1]),
+                                       make_float2(acc[r][e], acc[r][e + 1]));
+          acc[r][e] = o2.x;
+          acc[r][e + 1] = o2.y;
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) sm100::mbar_arrive(sm100::smem_u32(&sh.empty[s]));
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int e = 0; e < EL; ++e)
+#pragma unroll
+      for (int o = LPT; o < 32; o <<= 1) acc[r][e] += __shfl_xor_sync(0xffffffffu, acc[r][e], o);
+
+  // The previous task's combine readers are done (consumer warps only; the
+  // producer keeps streaming the next task meanwhile), then write this warp's
+  // state.  Rows R..RS-1 of the buffer are unused for this task.
+  asm volatile("bar.sync 1, %0;" ::"r"(kBw2Consumers * 32) : "memory");
+  if (grp == 0) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int j = 0; j < CH; ++j)
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+          sh.co[(warp * RS + r) * D + (sub + j * LPT) * 8 + x] = acc[r][j * 8 + x];
+    if (lane == rs_lane<R, LPT>(my_row)) {
+      sh.cm[warp * RS + my_row] = m_run;
+      sh.cl[warp * RS + my_row] = l_run;
+    }
+  }
+  return live;
+}
+
 template <int D, int R>
 __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
     const pps::Task* __restrict__ tasks, int32_t num_tasks, const int32_t* __restrict__ rows,
@@ -310,7 +489,6 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
     int32_t page_size, float qk_scale) {
   using C = Bw2<D, R>;
   using S = Bw3Smem<D, R>;
-  constexpr int EL = C::EL, LPT = C::LPT, TPW = C::TPW, ITERS = C::ITERS, CH = C::CH;
   extern __shared__ __align__(128) uint8_t bw2_smem[];
   __shared__ uint64_t full[kBw2Stages], empty[kBw2Stages], qfull[2], qempty[2];
   __shared__ volatile int abort_flag;
@@ -418,11 +596,10 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
   }
 
   // ------------------------------------------------------------------ consumers
-  const int grp = lane / LPT, sub = lane % LPT;
-  const int my_row = rs_row<R, LPT / 2>(lane);
   float* cm = reinterpret_cast<float*>(bw2_smem + S::comb);   // [warps][R] max
   float* cl = cm + kBw2Consumers * R;                          // [warps][R] sum
   float* co = cl + kBw2Consumers * R;                          // [warps][R][D]
+  BwShared sh{bw2_smem + S::ring, full, empty, &abort_flag, err, cm, cl, co};
   int gk = 0, t;
   for (int ti = 0; (t = snake_task(ti, b, nctas)) < num_tasks; ++ti) {
     bool live = !abort_flag;
@@ -438,155 +615,15 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
     for (int i = 0; i < R; ++i) tok[i] = (live && i < task.n_tok) ? ttok[qb][i] : 0;
     const int nrows = task.n_tok * G;
     const int n_sub = (task.kv_end - task.kv_begin + kBw2Sub - 1) / kBw2Sub;
-    float qr[R][EL];
     const uint8_t* qs = bw2_smem + S::qbuf + qb * ((S::qbuf_bytes + 127) / 128 * 128);
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-#pragma unroll
-      for (int j = 0; j < CH; ++j) {
-        float f[8];
-        const int4 v = (live && r < nrows)
-                           ? *reinterpret_cast<const int4*>(qs + r * D * 2 + (sub + j * LPT) * 16)
-                           : make_int4(0, 0, 0, 0);
-        bf16x8_to_f32(v, f);
-#pragma unroll
-        for (int x = 0; x < 8; ++x) qr[r][j * 8 + x] = f[x] * qk_scale;
-      }
-    }
-    __syncwarp();
-    if (lane == 0) sm100::mbar_arrive(sm100::smem_u32(&qempty[qb]));
-
-    float m_run = -INFINITY, l_run = 0.f;
-    float acc[R][EL];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int e = 0; e < EL; ++e) acc[r][e] = 0.f;
-    const int lim0 = task.causal;
-    const int my_lim = task.causal + my_row / G;
-    const int first = (warp - gk % kBw2Consumers + kBw2Consumers) % kBw2Consumers;
-    for (int k = first; live && k < n_sub; k += kBw2Consumers) {
-      const int g = gk + k;                                  // g % kBw2Consumers == warp
-      const int wi = g / kBw2Consumers;
-      const int s = warp * kStagesPerWarp + wi % kStagesPerWarp;
-      const bool got =
-          sm100::mbar_wait(sm100::smem_u32(&full[s]), (wi / kStagesPerWarp) & 1) && !abort_flag;
-      if (!__all_sync(0xffffffffu, got)) {
-        if (lane == 0) fail();
-        live = false;
-        break;
-      }
-      const int pos0 = task.kv_begin + k * kBw2Sub;
-      const bool fast = (pos0 + kBw2Sub <= task.kv_end) && (pos0 + kBw2Sub - 1 <= lim0);
-      const uint8_t* kb = bw2_smem + S::ring + s * C::STAGE;
-      const uint8_t* vb = kb + kBw2Sub * D * 2;
-      float sc[ITERS];
-#pragma unroll
-      for (int it = 0; it < ITERS; ++it) {
-        const int tt = it * TPW + grp;
-        float kf[EL];
-#pragma unroll
-        for (int j = 0; j < CH; ++j) {
-          const int4 v = *reinterpret_cast<const int4*>(kb + tt * D * 2 + (sub + j * LPT) * 16);
-          bf16x8_to_f32(v, kf + j * 8);
-        }
-        float d[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int e = 0; e < EL; e += 2)
-            a = __ffma2_rn(make_float2(qr[r][e], qr[r][e + 1]), make_float2(kf[e], kf[e + 1]), a);
-          d[r] = a.x + a.y;
-        }
-        reduce_scatter<R, LPT / 2>(d, lane);
-        float sv = d[0];
-        if (!fast) {
-          const int pos = pos0 + tt;
-          if (pos >= task.kv_end || pos > my_lim) sv = -INFINITY;
-        }
-        sc[it] = sv;
-      }
-      float mx = sc[0];
-#pragma unroll
-      for (int it = 1; it < ITERS; ++it) mx = fmaxf(mx, sc[it]);
-#pragma unroll
-      for (int o = LPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const bool need = (mx > m_run + 8.f) || (m_run == -INFINITY && mx != -INFINITY);
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? fmaxf(mx, m_run) : m_run;
-        const float alpha = (m_run == -INFINITY) ? 0.f : fast_ex2(m_run - m_new);
-        m_run = m_new;
-        l_run *= alpha;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float a = __shfl_sync(0xffffffffu, alpha, rs_lane<R, LPT>(r));
-#pragma unroll
-          for (int e = 0; e < EL; ++e) acc[r][e] *= a;
-        }
-      }
-      const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-      float ls = 0.f;
-#pragma unroll
-      for (int it = 0; it < ITERS; ++it) {
-        sc[it] = fast_ex2(sc[it] - msub);
-        ls += sc[it];
-      }
-#pragma unroll
-      for (int o = LPT; o < 32; o <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-      l_run += ls;
-#pragma unroll
-      for (int it = 0; it < ITERS; ++it) {
-        const int tt = it * TPW + grp;
-        float vf[EL];
-#pragma unroll
-        for (int j = 0; j < CH; ++j) {
-          const int4 v = *reinterpret_cast<const int4*>(vb + tt * D * 2 + (sub + j * LPT) * 16);
-          bf16x8_to_f32(v, vf + j * 8);
-        }
-        if (!fast && pos0 + tt >= task.kv_end) {
-#pragma unroll
-          for (int e = 0; e < EL; ++e) vf[e] = 0.f;   // rows past the end may hold NaN
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float pr = __shfl_sync(0xffffffffu, sc[it], grp * LPT + rs_lane<R, LPT>(r));
-#pragma unroll
-          for (int e = 0; e < EL; e += 2) {
-            const float2 o2 = __ffma2_rn(make_float2(pr, pr), make_float2(vf[e], vf[e + 1]),
-                                         make_float2(acc[r][e], acc[r][e + 1]));
-            acc[r][e] = o2.x;
-            acc[r][e + 1] = o2.y;
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) sm100::mbar_arrive(sm100::smem_u32(&empty[s]));
-    }
+    // Tasks of up to 4 rows (one decode token at G = 4) take the 4-row inner
+    // loop even in the 8-row instance: half the arithmetic per K/V byte.
+    if (R == 8 && nrows <= 4)
+      live = bw_consume<D, (R == 8 ? 4 : R), R>(task, nrows, G, n_sub, gk, qs, qk_scale, live, sh,
+                                                 &qempty[qb]);
+    else
+      live = bw_consume<D, R, R>(task, nrows, G, n_sub, gk, qs, qk_scale, live, sh, &qempty[qb]);
     gk += n_sub;
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int e = 0; e < EL; ++e)
-#pragma unroll
-        for (int o = LPT; o < 32; o <<= 1) acc[r][e] += __shfl_xor_sync(0xffffffffu, acc[r][e], o);
-
-    // merge the consumer warps' states (named barrier: consumer warps only,
-    // the producer keeps streaming the next task meanwhile)
-    asm volatile("bar.sync 1, %0;" ::"r"(kBw2Consumers * 32) : "memory");
-    if (grp == 0) {
-#pragma unroll
-      for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int j = 0; j < CH; ++j)
-#pragma unroll
-          for (int x = 0; x < 8; ++x)
-            co[(warp * R + r) * D + (sub + j * LPT) * 8 + x] = acc[r][j * 8 + x];
-      if (lane == rs_lane<R, LPT>(my_row)) {
-        cm[warp * R + my_row] = m_run;
-        cl[warp * R + my_row] = l_run;
-      }
-    }
     asm volatile("bar.sync 1, %0;" ::"r"(kBw2Consumers * 32) : "memory");
     for (int idx = tid; idx < nrows * D; idx += kBw2Consumers * 32) {
       const int r = idx / D, c = idx - (idx / D) * D;
