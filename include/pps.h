@@ -176,11 +176,12 @@ pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_len,
  *  workspace  device, >= the plan's workspace bytes, 256-byte aligned; holds the
  *             uploaded task table and fp32 partials.  It must not be used by
  *             other work in flight on another stream.
- * Enqueues: one host-to-device copy of the task table (from the plan's host
- * memory; the call returns only after the source has been consumed, so the
- * plan may be destroyed right after), then up to three kernels (bandwidth
- * tasks, tensor-core tasks, partial merge).  A plan may be run any number of
- * times.
+ * Enqueues: one host-to-device copy of the task table (from the plan's
+ * page-locked host memory when a device is usable, so the call does not wait
+ * for earlier work), then up to three kernels (bandwidth tasks, tensor-core
+ * tasks, partial merge).  The plan may be destroyed as soon as the call
+ * returns: the library keeps the table's host memory until the upload has
+ * completed.  A plan may be run any number of times.
  */
 pps_status pps_attn_run(const pps_plan* plan, const void* q, const pps_pool* pool, void* out,
                         void* workspace, size_t workspace_bytes, void* stream);

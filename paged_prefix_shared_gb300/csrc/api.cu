@@ -6,7 +6,9 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <cstdlib>
 #include <mutex>
+#include <vector>
 
 #include "pps_internal.h"
 #include "sm100_ptx.cuh"
@@ -71,10 +73,11 @@ pps_status run_impl(const pps_plan* plan, const void* q, const pps_pool* pool, v
     return PPS_OK;
   }
   char* ws = (char*)workspace;
-  // The plan's table is pageable host memory: the copy returns once the
-  // source has been staged, so the plan may be freed as soon as we return.
-  e = cudaMemcpyAsync(ws, plan->image.data(), plan->image.size() * 4, cudaMemcpyHostToDevice, st);
+  // Asynchronous when the plan's table is page-locked; the buffer is not
+  // reused before this upload completes, so the plan may be destroyed at once.
+  e = cudaMemcpyAsync(ws, plan->image.data, (size_t)plan->image_ints * 4, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return PPS_ERR_CUDA;
+  if (pps::host_buf_mark_use(plan->image, stream) != 0) return PPS_ERR_CUDA;
   const int32_t* base = (const int32_t*)ws;
   const auto& L = plan->layout;
   pps::DeviceTables t;
@@ -119,6 +122,81 @@ __global__ void wait_timeout_selftest_kernel(int32_t* err, uint64_t limit_ns) {
 namespace pps {
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+// ---- host staging buffers for plan tables -------------------------------------------
+namespace {
+struct HostSlot {
+  int32_t* p = nullptr;
+  size_t ints = 0;
+  bool pinned = false;
+  bool in_use = false;
+  cudaEvent_t ev = nullptr;   // last upload recorded on this buffer
+  int ev_dev = -1;
+};
+std::mutex g_host_mu;
+std::vector<HostSlot> g_host;
+
+bool slot_idle(HostSlot& s) {
+  if (!s.ev) return true;
+  const cudaError_t q = cudaEventQuery(s.ev);
+  if (q == cudaErrorNotReady) return false;
+  if (q != cudaSuccess) cudaGetLastError();   // a failed context: the upload is over either way
+  return true;
+}
+}  // namespace
+
+HostBuf host_buf_acquire(size_t ints) {
+  std::lock_guard<std::mutex> lk(g_host_mu);
+  int best = -1;
+  for (int i = 0; i < (int)g_host.size(); ++i) {
+    HostSlot& s = g_host[i];
+    if (s.in_use || s.ints < ints || !slot_idle(s)) continue;
+    if (best < 0 || s.ints < g_host[best].ints) best = i;
+  }
+  if (best < 0) {
+    size_t cap = 1 << 14;                      // ints; power-of-two classes from 64 KB
+    while (cap < ints) cap <<= 1;
+    HostSlot s;
+    void* p = nullptr;
+    if (cudaHostAlloc(&p, cap * 4, cudaHostAllocPortable) == cudaSuccess && p) {
+      s.pinned = true;
+    } else {
+      cudaGetLastError();
+      p = std::malloc(cap * 4);
+      if (!p) return HostBuf{};
+    }
+    s.p = (int32_t*)p;
+    s.ints = cap;
+    g_host.push_back(s);
+    best = (int)g_host.size() - 1;
+  }
+  g_host[best].in_use = true;
+  return HostBuf{g_host[best].p, g_host[best].ints, best};
+}
+
+void host_buf_release(HostBuf& b) {
+  if (b.slot < 0) return;
+  std::lock_guard<std::mutex> lk(g_host_mu);
+  if (b.slot < (int)g_host.size()) g_host[b.slot].in_use = false;
+  b = HostBuf{};
+}
+
+int host_buf_mark_use(const HostBuf& b, void* stream) {
+  if (b.slot < 0) return 0;
+  std::lock_guard<std::mutex> lk(g_host_mu);
+  HostSlot& s = g_host[b.slot];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (s.ev && s.ev_dev != dev) {
+    cudaEventDestroy(s.ev);
+    s.ev = nullptr;
+  }
+  if (!s.ev) {
+    if (cudaEventCreateWithFlags(&s.ev, cudaEventDisableTiming) != cudaSuccess) return 1;
+    s.ev_dev = dev;
+  }
+  return cudaEventRecord(s.ev, (cudaStream_t)stream) == cudaSuccess ? 0 : 1;
+}
 
 int device_sm_count() {
   int dev = 0, n = 0;

@@ -358,8 +358,11 @@ extern "C" pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_l
     L.merge_pids = off;    off += al((int64_t)m_pid.size());
     L.total_ints = off;
     plan->layout = L;
-    plan->image.assign((size_t)std::max<int64_t>(off, 64), 0);
-    int32_t* img = plan->image.data();
+    plan->image_ints = std::max<int64_t>(off, 64);
+    plan->image = pps::host_buf_acquire((size_t)plan->image_ints);
+    if (!plan->image.data) throw std::bad_alloc();
+    int32_t* img = plan->image.data;
+    std::memset(img, 0, (size_t)plan->image_ints * 4);
     if (!bw.empty()) std::memcpy(img + L.bw_tasks, bw.data(), bw.size() * sizeof(Task));
     if (!mm.empty()) std::memcpy(img + L.mma_tasks, mm.data(), mm.size() * sizeof(Task));
     if (!rows.empty()) std::memcpy(img + L.rows, rows.data(), rows.size() * 4);
@@ -376,7 +379,7 @@ extern "C" pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_l
     plan->num_rows = (int64_t)rows.size();
     plan->num_pages_listed = nnz;
     auto al256 = [](size_t n) { return (n + 255) / 256 * 256; };
-    plan->table_bytes = al256(plan->image.size() * 4);
+    plan->table_bytes = al256((size_t)plan->image_ints * 4);
     plan->partial_o_bytes = al256((size_t)next_pid * num_q_heads * head_dim * 4);
     plan->partial_lse_bytes = al256((size_t)next_pid * num_q_heads * 4);
     plan->workspace_bytes = plan->table_bytes + plan->partial_o_bytes + plan->partial_lse_bytes;
@@ -420,7 +423,7 @@ extern "C" pps_status pps_plan_get_info(const pps_plan* p, pps_plan_info* info) 
 extern "C" pps_status pps_plan_get_array(const pps_plan* p, int32_t which, const int32_t** data,
                                          int64_t* count) {
   if (!p || !data || !count) return PPS_ERR_INVALID_ARGUMENT;
-  const int32_t* img = p->image.data();
+  const int32_t* img = p->image.data;
   const auto& L = p->layout;
   switch (which) {
     case PPS_ARRAY_BW_TASKS: *data = img + L.bw_tasks; *count = p->num_bw * PPS_TASK_INTS; break;

@@ -55,6 +55,20 @@ struct Shape {
   int32_t bw_rows_max;   // largest n_tok * G over bandwidth tasks
 };
 
+// Host memory for plan tables.  Page-locked when a CUDA device is usable, so
+// the upload in pps_attn_run is asynchronous and host planning of the next
+// batch overlaps the GPU work of this one; ordinary memory otherwise.  A
+// released buffer is handed out again only after the last upload recorded on
+// it (host_buf_mark_use) has completed.
+struct HostBuf {
+  int32_t* data = nullptr;
+  size_t ints = 0;
+  int slot = -1;
+};
+HostBuf host_buf_acquire(size_t ints);
+void host_buf_release(HostBuf& b);
+int host_buf_mark_use(const HostBuf& b, void* stream);
+
 }  // namespace pps
 
 struct pps_plan {
@@ -65,14 +79,16 @@ struct pps_plan {
   int64_t num_bw = 0, num_mma = 0, num_partials = 0, num_merge_tokens = 0, num_merge_pids = 0;
   int64_t num_rows = 0, num_pages_listed = 0;
   pps::TableLayout layout;
-  std::vector<int32_t> image;   // host copy of the device table
-  size_t table_bytes = 0;       // bytes of `image`, rounded to 256
+  pps::HostBuf image;           // host copy of the device table
+  int64_t image_ints = 0;       // ints of the table in `image`
+  size_t table_bytes = 0;       // bytes of the table, rounded to 256
   size_t partial_o_bytes = 0;
   size_t partial_lse_bytes = 0;
   size_t workspace_bytes = 0;
   int64_t kv_bytes_unique = 0, kv_bytes_read = 0;
   double flops_mma = 0, flops_total = 0;
   bool use_mma = false;
+  ~pps_plan() { pps::host_buf_release(image); }
 };
 
 namespace pps {
