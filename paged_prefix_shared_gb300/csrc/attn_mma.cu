@@ -132,6 +132,34 @@ __device__ __forceinline__ TileRange tile_range(const pps::Task& t, int X, int G
   return r;
 }
 
+// Rare path of the softmax (a row's reference max moved): scale the P chunks
+// 0..k-1 already stored over S's first columns and, when `o_cols` > 0, the
+// first `o_cols` columns of O by this thread's `alpha`.  Warp-collective.
+__device__ __noinline__ void rescale_row(uint32_t tm_s_lane, uint32_t tm_o_lane, int k, int o_cols,
+                                         float alpha) {
+  tmem_wait_st();
+  for (int q = 0; q < k; ++q) {
+    uint32_t w[16];
+    tmem_ld16(tm_s_lane + q * 16, w);
+    tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const float lo = __uint_as_float(w[c] << 16), hi = __uint_as_float(w[c] & 0xffff0000u);
+      w[c] = pack_bf16(lo * alpha, hi * alpha);
+    }
+    tmem_st16(tm_s_lane + q * 16, w);
+  }
+  for (int c1 = 0; c1 < o_cols; c1 += 32) {
+    uint32_t w[32];
+    tmem_ld32(tm_o_lane + c1, w);
+    tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < 32; ++c) w[c] = __float_as_uint(__uint_as_float(w[c]) * alpha);
+    tmem_st32(tm_o_lane + c1, w);
+  }
+  tmem_wait_st();
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     mma_attention_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -243,14 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // score exceeds it by kOverflowGuard (or the row has none yet), and then
         // the stored P chunks, O and the sums are rescaled in place.
         float rs = 0.f;
-        uint32_t ra[32], rb[32];
-        tmem_ld32(tm_s + lane_off, ra);
-        tmem_wait_ld_dep(ra);
-#pragma unroll
-        for (int k = 0; k < kTile / 32; ++k) {
-          uint32_t(&cur)[32] = (k & 1) ? rb : ra;
-          uint32_t(&nxt)[32] = (k & 1) ? ra : rb;
-          if (k + 1 < kTile / 32) tmem_ld32(tm_s + lane_off + (k + 1) * 32, nxt);
+        // One 32-column chunk: reference update (rare, out of line), then
+        // P = exp2(s * scale - m) packed to bf16 and stored over columns
+        // 16k .. 16k + 15, which earlier chunks have already read.
+        auto chunk = [&](const uint32_t(&cur)[32], int k) {
           const int c0 = k * 32;
           float cmx = -INFINITY;
 #pragma unroll
@@ -265,31 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             m_ref = m_new;
             l_sum *= alpha;
             rs *= alpha;
-            tmem_wait_st();
-            for (int q = 0; q < k; ++q) {                 // P chunks already stored
-              uint32_t w[16];
-              tmem_ld16(tm_s + lane_off + q * 16, w);
-              tmem_wait_ld();
-#pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                const float lo = __uint_as_float(w[c] << 16), hi = __uint_as_float(w[c] & 0xffff0000u);
-                w[c] = pack_bf16(lo * alpha, hi * alpha);
-              }
-              tmem_st16(tm_s + lane_off + q * 16, w);
-            }
-            if (j > 0) {
-              // O holds this tile's earlier KV tiles; their PV completed before
-              // this S was delivered (one in-order tcgen05 stream).
-#pragma unroll
-              for (int c1 = 0; c1 < D; c1 += 32) {
-                uint32_t w[32];
-                tmem_ld32(tm_o + lane_off + c1, w);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) w[c] = __float_as_uint(__uint_as_float(w[c]) * alpha);
-                tmem_st32(tm_o + lane_off + c1, w);
-              }
-            }
+            rescale_row(tm_s + lane_off, tm_o + lane_off, k, j > 0 ? D : 0, alpha);
           }
           const float msub = (m_ref == -INFINITY) ? 0.f : m_ref;
           uint32_t w[16];
@@ -305,8 +305,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             w[c / 2] = pack_bf16(a, bb);
           }
           tmem_st16(tm_s + lane_off + k * 16, w);
-          if (k + 1 < kTile / 32) tmem_wait_ld_dep(nxt);
-        }
+        };
+        // loads double-buffered: chunk k + 1 is in flight while chunk k is used
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tm_s + lane_off, ra);
+        tmem_wait_ld_dep(ra);
+        tmem_ld32(tm_s + lane_off + 32, rb);
+        chunk(ra, 0);
+        tmem_wait_ld_dep(rb);
+        tmem_ld32(tm_s + lane_off + 64, ra);
+        chunk(rb, 1);
+        tmem_wait_ld_dep(ra);
+        tmem_ld32(tm_s + lane_off + 96, rb);
+        chunk(ra, 2);
+        tmem_wait_ld_dep(rb);
+        chunk(rb, 3);
         l_sum += rs;
         tmem_wait_st();
         tc_fence_before();
