@@ -18,10 +18,10 @@
 //   warps 0-3  softmax A, warps 4-7 softmax B: thread m of a warpgroup owns
 //              query row m = TMEM lane m.  It loads its Q row into 128-byte
 //              swizzled shared memory, turns its S row into P in one pass over
-//              TMEM against its running reference max (moved, with P, O and
-//              the sums rescaled in place, only on a row's first visible key or
-//              when a score exceeds the reference by 2^64), writes P as bf16 over
-//              S's own columns, and writes the output row or the partial (o, lse).
+//              TMEM against its running reference max (two passes, and an O
+//              rescale in TMEM, only when a score exceeds that reference by more
+//              than 2^8), writes P as bf16 over S's own columns, and writes the
+//              output row or the partial (o, lse).
 //   warp 8     TMA producer: K and V tiles of 128 positions (one box per page
 //              and 64-column block, issued by one lane each) into a 2-stage ring.
 //   warp 9     MMA issuer: S_X = Q_X K^T (both K-major in shared memory) and
@@ -51,10 +51,7 @@ constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
 constexpr int kStages = 2;
 constexpr int kTile = 128;                    // KV positions per tile = query rows per tile
-// The reference max of a row moves only when a score exceeds it by this much
-// (log2 units): P = 2^(s - m) stays below 2^64 and O, l stay far inside the
-// fp32 range, while bf16 P keeps its relative precision at any magnitude.
-constexpr float kOverflowGuard = 64.f;
+constexpr float kRescaleThreshold = 8.f;      // log2 units
 
 struct MmaParams {
   const pps::Task* tasks;
@@ -130,34 +127,6 @@ __device__ __forceinline__ TileRange tile_range(const pps::Task& t, int X, int G
   if (t.causal != PPS_NO_CAUSAL) end = min(end, t.causal + last_tok + 1);
   r.n_tiles = (end - t.kv_begin + kTile - 1) / kTile;
   return r;
-}
-
-// Rare path of the softmax (a row's reference max moved): scale the P chunks
-// 0..k-1 already stored over S's first columns and, when `o_cols` > 0, the
-// first `o_cols` columns of O by this thread's `alpha`.  Warp-collective.
-__device__ __noinline__ void rescale_row(uint32_t tm_s_lane, uint32_t tm_o_lane, int k, int o_cols,
-                                         float alpha) {
-  tmem_wait_st();
-  for (int q = 0; q < k; ++q) {
-    uint32_t w[16];
-    tmem_ld16(tm_s_lane + q * 16, w);
-    tmem_wait_ld();
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const float lo = __uint_as_float(w[c] << 16), hi = __uint_as_float(w[c] & 0xffff0000u);
-      w[c] = pack_bf16(lo * alpha, hi * alpha);
-    }
-    tmem_st16(tm_s_lane + q * 16, w);
-  }
-  for (int c1 = 0; c1 < o_cols; c1 += 32) {
-    uint32_t w[32];
-    tmem_ld32(tm_o_lane + c1, w);
-    tmem_wait_ld();
-#pragma unroll
-    for (int c = 0; c < 32; ++c) w[c] = __float_as_uint(__uint_as_float(w[c]) * alpha);
-    tmem_st32(tm_o_lane + c1, w);
-  }
-  tmem_wait_st();
 }
 
 template <int D>
@@ -254,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tr.n_tiles == 0) continue;
 
       const int lim = real ? task.causal + i : -1;  // last visible position (inclusive)
-      // Padding rows see no key: a finite reference keeps them off the
-      // rescale path (their P is 0 either way).
+      // Padding rows see no key: any finite reference keeps their P at 0 and
+      // keeps them off the exact path below.
       float m_ref = real ? -INFINITY : 0.f, l_sum = 0.f;
       bool ok = true;
       for (int j = 0; j < tr.n_tiles; ++j, ++sx) {
@@ -264,63 +233,105 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int bound = min(task.kv_end - t0, lim - t0 + 1);     // columns c < bound visible
         const bool full = __all_sync(0xffffffffu, bound >= kTile);
-        // S -> P in 32-column chunks, loads double-buffered (chunk k + 1 is in
-        // flight while chunk k is turned into P), each chunk stored as bf16
-        // pairs over columns 16k .. 16k + 15 (already read).  P is taken
-        // against the row's reference max; the reference moves only when a
-        // score exceeds it by kOverflowGuard (or the row has none yet), and then
-        // the stored P chunks, O and the sums are rescaled in place.
-        float rs = 0.f;
-        // One 32-column chunk: reference update (rare, out of line), then
-        // P = exp2(s * scale - m) packed to bf16 and stored over columns
-        // 16k .. 16k + 15, which earlier chunks have already read.
-        auto chunk = [&](const uint32_t(&cur)[32], int k) {
-          const int c0 = k * 32;
-          float cmx = -INFINITY;
+        uint32_t pk[kTile / 2];                    // P row, bf16 pairs, stored once verified
+        float rs = 0.f, alpha = 1.f, m_use = m_ref;
+        // One pass against the running reference max: P = exp2(s * scale - m_ref).
+        // Valid unless some score exceeds the reference by the rescale threshold
+        // (rare once a row has seen a tile); then the exact two-pass path below.
+        bool exact = __any_sync(0xffffffffu, m_ref == -INFINITY);
+        if (!exact) {
+          float mx = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (full || c0 + c < bound) cmx = fmaxf(cmx, __uint_as_float(cur[c]));
-          const float cmxs = (cmx == -INFINITY) ? -INFINITY : cmx * p.qk_scale;
-          const bool need = (m_ref == -INFINITY) ? (cmxs != -INFINITY)
-                                                 : (cmxs > m_ref + kOverflowGuard);
-          if (__any_sync(0xffffffffu, need)) {
-            const float m_new = need ? fmaxf(cmxs, m_ref) : m_ref;
-            const float alpha = need ? ((m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new)) : 1.f;
-            m_ref = m_new;
-            l_sum *= alpha;
-            rs *= alpha;
-            rescale_row(tm_s + lane_off, tm_o + lane_off, k, j > 0 ? D : 0, alpha);
-          }
-          const float msub = (m_ref == -INFINITY) ? 0.f : m_ref;
-          uint32_t w[16];
+          for (int c0 = 0; c0 < kTile; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tm_s + lane_off + c0, rr);
+            tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float a = ex2(fmaf(__uint_as_float(cur[c]), p.qk_scale, -msub));
-            float bb = ex2(fmaf(__uint_as_float(cur[c + 1]), p.qk_scale, -msub));
-            if (!full) {
-              if (c0 + c >= bound) a = 0.f;
-              if (c0 + c + 1 >= bound) bb = 0.f;
+            for (int c = 0; c < 32; c += 2) {
+              float sa = __uint_as_float(rr[c]), sb = __uint_as_float(rr[c + 1]);
+              if (!full) {
+                if (c0 + c >= bound) sa = -INFINITY;
+                if (c0 + c + 1 >= bound) sb = -INFINITY;
+              }
+              mx = fmaxf(mx, fmaxf(sa, sb));
+              const float a = ex2(fmaf(sa, p.qk_scale, -m_ref));
+              const float bb = ex2(fmaf(sb, p.qk_scale, -m_ref));
+              rs += a + bb;
+              pk[(c0 + c) / 2] = pack_bf16(a, bb);
             }
-            rs += a + bb;
-            w[c / 2] = pack_bf16(a, bb);
           }
-          tmem_st16(tm_s + lane_off + k * 16, w);
-        };
-        // loads double-buffered: chunk k + 1 is in flight while chunk k is used
-        uint32_t ra[32], rb[32];
-        tmem_ld32(tm_s + lane_off, ra);
-        tmem_wait_ld_dep(ra);
-        tmem_ld32(tm_s + lane_off + 32, rb);
-        chunk(ra, 0);
-        tmem_wait_ld_dep(rb);
-        tmem_ld32(tm_s + lane_off + 64, ra);
-        chunk(rb, 1);
-        tmem_wait_ld_dep(ra);
-        tmem_ld32(tm_s + lane_off + 96, rb);
-        chunk(ra, 2);
-        tmem_wait_ld_dep(rb);
-        chunk(rb, 3);
-        l_sum += rs;
+          const float mxs = (mx == -INFINITY) ? -INFINITY : mx * p.qk_scale;
+          exact = __any_sync(0xffffffffu, mxs > m_ref + kRescaleThreshold);
+          if (!exact) {
+            // P over S's first 64 columns (S has been read in full above)
+#pragma unroll
+            for (int c0 = 0; c0 < kTile / 2; c0 += 16) {
+              uint32_t w[16];
+#pragma unroll
+              for (int c = 0; c < 16; ++c) w[c] = pk[c0 + c];
+              tmem_st16(tm_s + lane_off + c0, w);
+            }
+          }
+        }
+        if (exact) {
+          // pass 1: row max of the raw scores
+          float mx = -INFINITY;
+#pragma unroll
+          for (int c0 = 0; c0 < kTile; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tm_s + lane_off + c0, rr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (full || c0 + c < bound) mx = fmaxf(mx, __uint_as_float(rr[c]));
+          }
+          const float mxs = (mx == -INFINITY) ? -INFINITY : mx * p.qk_scale;
+          m_use = m_ref;
+          alpha = 1.f;
+          if (mxs > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mxs != -INFINITY)) {
+            m_use = fmaxf(mxs, m_ref);
+            alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_use);
+          }
+          // O rescale: the PV of this tile's previous KV tile completed before
+          // this S was delivered (one in-order tcgen05 stream; the commit behind
+          // s_full covers both).
+          if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t rr[32];
+              tmem_ld32(tm_o + lane_off + c0, rr);
+              tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
+              tmem_st32(tm_o + lane_off + c0, rr);
+            }
+          }
+          const float msub = (m_use == -INFINITY) ? 0.f : m_use;
+          // pass 2: P = exp2(s * scale - m); chunk c0 is stored over columns
+          // c0/2 .. c0/2 + 15, all of which this pass has already read
+          rs = 0.f;
+#pragma unroll
+          for (int c0 = 0; c0 < kTile; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tm_s + lane_off + c0, rr);
+            tmem_wait_ld();
+            uint32_t w[16];
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              float a = ex2(fmaf(__uint_as_float(rr[c]), p.qk_scale, -msub));
+              float bb = ex2(fmaf(__uint_as_float(rr[c + 1]), p.qk_scale, -msub));
+              if (!full) {
+                if (c0 + c >= bound) a = 0.f;
+                if (c0 + c + 1 >= bound) bb = 0.f;
+              }
+              rs += a + bb;
+              w[c / 2] = pack_bf16(a, bb);
+            }
+            tmem_st16(tm_s + lane_off + c0 / 2, w);
+          }
+        }
+        m_ref = m_use;
+        l_sum = l_sum * alpha + rs;
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
