@@ -224,13 +224,16 @@ extern "C" pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_l
         else bw_kv += sp.end - sp.a;
       }
     }
-    // The bandwidth kernel is persistent (one CTA per SM taking tasks in
-    // symmetric round-robin order), so chunks only need to be small enough to
-    // give every SM about eight tasks; larger chunks mean fewer partials.
+    // The bandwidth kernel is persistent (one CTA per SM taking the
+    // work-sorted tasks in symmetric round-robin order), so tasks only need to
+    // be small enough to give every SM about two of them: each task costs a
+    // query load and a cross-warp merge, and a split request costs partials
+    // and a merge.  Measured on GB300: 4096-token tasks beat 2048 (decode,
+    // 256 requests) and 1024+ beat 352 (radix subtrees, 64 requests).
     int32_t bw_chunk = o.bw_chunk_tokens;
     if (bw_chunk <= 0) {
-      const int64_t want = ceil_div(bw_kv * num_kv_heads, (int64_t)num_sms * 8);
-      bw_chunk = (int32_t)std::min<int64_t>(2048, std::max<int64_t>(128, want));
+      const int64_t want = ceil_div(bw_kv * num_kv_heads, (int64_t)num_sms * 2);
+      bw_chunk = (int32_t)std::min<int64_t>(4096, std::max<int64_t>(128, want));
     }
     bw_chunk = (int32_t)(ceil_div(bw_chunk, P) * P);
     int32_t mma_chunk = o.mma_chunk_tokens;

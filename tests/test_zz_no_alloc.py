@@ -59,10 +59,12 @@ def test_noalloc_matches_workspace_entry_point(pps, make):
 
 
 def test_noalloc_rejects_plans_larger_than_its_scratch(pps):
-    # The full mixed-budget layout needs ~364 MiB of partials: far above the cap.
+    # The full mixed-budget layout split into 128-token tasks needs over 1 GiB
+    # of partials: far above the cap.
     L = workloads.mixed_budget(values=False).layout
     plan = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices, L.num_q_heads,
-                         L.num_kv_heads, L.head_dim, L.page_size, L.num_pages)
+                         L.num_kv_heads, L.head_dim, L.page_size, L.num_pages,
+                         bw_chunk_tokens=128)
     assert plan.workspace_bytes > pps.NOALLOC_SCRATCH_BYTES
     dummy = torch.zeros((1, 1, 16, 128), dtype=torch.bfloat16, device="cuda")
     q = torch.zeros((L.num_tokens, 32, 128), dtype=torch.bfloat16, device="cuda")
