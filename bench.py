@@ -300,6 +300,7 @@ def run_pps(args):
     L0 = steps[0]["L"]
     qo_bytes = sum(2 * s["L"].num_tokens * L0.num_q_heads * L0.head_dim * 2 for s in steps)
     kv_unique = sum(i["kv_bytes_unique"] for i in infos)
+    kv_bw = sum(i["kv_bytes_bw"] for i in infos)            # K/V read by bandwidth tasks
     flops_mma = sum(i["flops_mma"] for i in infos)
     if dom == pps.KERNEL_TENSOR:
         ach = flops_mma / (kern_ms[dom] / 1e3) / 1e12
@@ -309,14 +310,15 @@ def run_pps(args):
                 "kernel": "tcgen05 attention tiles",
                 "algorithmic": f"{flops_mma:.4g} FLOP per step (4*d per visible (row,key) pair)"}
     else:
-        alg = kv_unique + qo_bytes
+        alg = kv_bw + qo_bytes
         ach = alg / (kern_ms[dom] / 1e3) / 1e9
         peak = peaks.get("hbm_gbs", 6800.0)
         roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
                 "frac": ach / peak,
                 "traffic": traffic_record("attn_bw.cu" if dom == 0 else "merge.cu", args.workload),
                 "kernel": ["split-KV bandwidth attention", "", "partial merge"][dom],
-                "algorithmic": f"{alg} B per step (unique K+V {kv_unique} + Q,O {qo_bytes})"}
+                "algorithmic": f"{alg} B per step (K+V read by the bandwidth tasks, each "
+                               f"once: {kv_bw}; Q and O rows: {qo_bytes})"}
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else \
         "fallback"
 
@@ -338,6 +340,8 @@ def run_pps(args):
         "roofline": roof,
         "clocks": clocks,
         "achieved": {"kv_unique_gbs": kv_unique / (ms_max / 1e3) / 1e9,
+                     "attention_unique_gbs": kv_unique / (max(kern_ms[0], kern_ms[1]) + kern_ms[2])
+                     * 1e3 / 1e9,
                      "tflops_total": sum(i["flops_total"] for i in infos) / (ms_max / 1e3) / 1e12},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

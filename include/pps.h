@@ -187,9 +187,12 @@ pps_status pps_attn_run(const pps_plan* plan, const void* q, const pps_pool* poo
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* Same as pps_attn_run, and records caller-created CUDA events (cudaEvent_t
- * passed as void*, any may be NULL) on `stream` immediately before and after
- * each kernel class: events[2*i] / events[2*i+1] for i = PPS_KERNEL_*.
- * A class that has no work this step records both events back to back. */
+ * passed as void*, any may be NULL) immediately before and after each kernel
+ * class: events[2*i] / events[2*i+1] for i = PPS_KERNEL_*.  A class that has
+ * no work this step records both events back to back.  When a batch has both
+ * bandwidth and tensor-core tasks the two kernels run concurrently on disjoint
+ * SMs: the tensor-core kernel on a library-owned stream forked from and joined
+ * back into `stream`, and its two events are recorded on that stream. */
 #define PPS_KERNEL_BANDWIDTH 0
 #define PPS_KERNEL_TENSOR 1
 #define PPS_KERNEL_MERGE 2
@@ -241,6 +244,8 @@ typedef struct pps_plan_info {
   int64_t kv_bytes_read;       /* K+V bytes the tasks read (shared runs counted once)    */
   double flops_mma;            /* 4*d per visible (query row, key) pair on tensor tasks  */
   double flops_total;          /* same over all tasks                                   */
+  int64_t kv_bytes_bw;         /* K+V bytes the bandwidth tasks read (each once)         */
+  double flops_mma_issued;     /* FLOP the tensor core executes: whole 128-row x 128-key tiles */
 } pps_plan_info;
 pps_status pps_plan_get_info(const pps_plan* plan, pps_plan_info* info);
 

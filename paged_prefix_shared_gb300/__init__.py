@@ -58,7 +58,8 @@ class _PlanInfo(ctypes.Structure):
         "num_groups")] + [(n, ctypes.c_int64) for n in (
             "num_bw_tasks", "num_mma_tasks", "num_partials", "num_merge_tokens", "table_bytes",
             "workspace_bytes", "kv_bytes_unique", "kv_bytes_read")] + [
-        ("flops_mma", ctypes.c_double), ("flops_total", ctypes.c_double)]
+        ("flops_mma", ctypes.c_double), ("flops_total", ctypes.c_double),
+        ("kv_bytes_bw", ctypes.c_int64), ("flops_mma_issued", ctypes.c_double)]
 
 
 _lib = None

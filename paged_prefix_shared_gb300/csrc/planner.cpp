@@ -332,7 +332,8 @@ extern "C" pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_l
       plan->kv_bytes_unique = slots * tok_bytes;
     }
     double fl_tot = 0, fl_mma = 0;
-    int64_t read = 0;
+    int64_t read = 0, read_bw = 0;
+    double issued = 0;
     for (const auto& ts : sets) {
       double pairs = 0;
       for (int32_t i = 0; i < ts.n_tok; ++i) {
@@ -343,10 +344,20 @@ extern "C" pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_l
       fl_tot += f;
       if (ts.mma) fl_mma += f;
       read += (int64_t)(ts.kv_end - ts.kv_begin) * tok_bytes;
+      if (!ts.mma) {
+        read_bw += (int64_t)(ts.kv_end - ts.kv_begin) * tok_bytes;
+      } else {
+        // whole tiles per kv head: ceil(rows / 128) x ceil(span / 128) of 128 x 128 x d
+        const int64_t tiles = ceil_div((int64_t)ts.n_tok * G, pps::kMmaRows) *
+                              ceil_div(ts.kv_end - ts.kv_begin, pps::kMmaKvTile);
+        issued += (double)tiles * num_kv_heads * 4.0 * pps::kMmaRows * pps::kMmaKvTile * head_dim;
+      }
     }
     plan->flops_total = fl_tot;
     plan->flops_mma = fl_mma;
     plan->kv_bytes_read = read;
+    plan->kv_bytes_bw = read_bw;
+    plan->flops_mma_issued = issued;
 
     // ---- 7. table image ----------------------------------------------------------------
     auto al = [](int64_t n) { return (n + 63) / 64 * 64; };
@@ -420,6 +431,8 @@ extern "C" pps_status pps_plan_get_info(const pps_plan* p, pps_plan_info* info) 
   info->kv_bytes_read = p->kv_bytes_read;
   info->flops_mma = p->flops_mma;
   info->flops_total = p->flops_total;
+  info->kv_bytes_bw = p->kv_bytes_bw;
+  info->flops_mma_issued = p->flops_mma_issued;
   return PPS_OK;
 }
 

@@ -85,7 +85,8 @@ struct pps_plan {
   size_t partial_o_bytes = 0;
   size_t partial_lse_bytes = 0;
   size_t workspace_bytes = 0;
-  int64_t kv_bytes_unique = 0, kv_bytes_read = 0;
+  int64_t kv_bytes_unique = 0, kv_bytes_read = 0, kv_bytes_bw = 0;
+  double flops_mma_issued = 0;
   double flops_mma = 0, flops_total = 0;
   bool use_mma = false;
   ~pps_plan() { pps::host_buf_release(image); }
@@ -100,11 +101,14 @@ int launch_kv_append(const pps_pool& pool, const void* k_new, const void* v_new,
                      const int32_t* page_indptr, const int32_t* page_indices,
                      int32_t num_requests, int32_t num_new_tokens, int32_t* err, void* stream);
 
+// `max_ctas` > 0 caps the persistent grid (to leave SMs to a concurrent kernel).
 int launch_bw_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
-                        const pps_pool& pool, void* out, int32_t* err, void* stream);
+                        const pps_pool& pool, void* out, int32_t* err, void* stream,
+                        int max_ctas = 0);
 
 int launch_mma_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
-                         const pps_pool& pool, void* out, int32_t* err, void* stream);
+                         const pps_pool& pool, void* out, int32_t* err, void* stream,
+                         int max_ctas = 0);
 
 int launch_merge(const Shape& s, const DeviceTables& t, int64_t num_merge_tokens, void* out,
                  void* stream);
