@@ -223,6 +223,11 @@ def run_pps(args):
     # per-kernel events (one set per step per chunk) -> average launch duration
     ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2 * nk)] for _ in steps]
           for _ in range(args.steps)]
+    for per_step in ev:                 # torch creates events on first record: do it now,
+        for per_chunk in per_step:      # outside the timed region
+            for e in per_chunk:
+                e.record(stream)
+    torch.cuda.synchronize()
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)

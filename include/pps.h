@@ -189,10 +189,7 @@ pps_status pps_attn_run(const pps_plan* plan, const void* q, const pps_pool* poo
 /* Same as pps_attn_run, and records caller-created CUDA events (cudaEvent_t
  * passed as void*, any may be NULL) immediately before and after each kernel
  * class: events[2*i] / events[2*i+1] for i = PPS_KERNEL_*.  A class that has
- * no work this step records both events back to back.  When a batch has both
- * bandwidth and tensor-core tasks the two kernels run concurrently on disjoint
- * SMs: the tensor-core kernel on a library-owned stream forked from and joined
- * back into `stream`, and its two events are recorded on that stream. */
+ * no work this step records both events back to back. */
 #define PPS_KERNEL_BANDWIDTH 0
 #define PPS_KERNEL_TENSOR 1
 #define PPS_KERNEL_MERGE 2

@@ -40,39 +40,6 @@ int32_t* error_word(cudaError_t* status) {
   return g_err_ptr[dev];
 }
 
-// Library-owned side stream (one per device) for the tensor-core kernel when
-// it runs alongside the bandwidth kernel, with the fork/join events.
-struct Side {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-  std::mutex mu;
-};
-Side g_side[kMaxDevices];
-std::mutex g_side_mu;
-
-Side* side_stream(cudaError_t* status) {
-  int dev = 0;
-  *status = cudaGetDevice(&dev);
-  if (*status != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lk(g_side_mu);
-  Side& s = g_side[dev];
-  if (!s.stream) {
-    if ((*status = cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking)) != cudaSuccess ||
-        (*status = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming)) != cudaSuccess ||
-        (*status = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming)) != cudaSuccess) {
-      s.stream = nullptr;
-      return nullptr;
-    }
-  }
-  return &s;
-}
-
-// Work-rate estimates used only to split SMs between the two concurrent
-// kernels (measured on GB300: ~6.5 TB/s and ~1.1 PFLOP/s of whole tiles over
-// 152 SMs).
-constexpr double kBwBytesPerSmSecond = 6.5e12 / 152;
-constexpr double kMmaFlopsPerSmSecond = 1.1e15 / 152;
-
 bool pool_ok(const pps_pool* p) {
   return p && p->k && p->v && p->num_pages > 0 && p->num_kv_heads > 0 &&
          (p->page_size == 16 || p->page_size == 32 || p->page_size == 64 || p->page_size == 128) &&
@@ -125,51 +92,15 @@ pps_status run_impl(const pps_plan* plan, const void* q, const pps_pool* pool, v
   t.o_part = (float*)(ws + plan->table_bytes);
   t.lse_part = (float*)(ws + plan->table_bytes + plan->partial_o_bytes);
 
-  if (plan->num_bw > 0 && plan->num_mma > 0) {
-    // Both kernels are persistent and independent until the merge: run them
-    // at once on disjoint SMs, the tensor-core kernel on a side stream forked
-    // from and joined back into `stream`, SMs split by estimated work.
-    Side* side = side_stream(&e);
-    if (!side) return PPS_ERR_CUDA;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return PPS_ERR_CUDA;
-    const double t_bw = (double)plan->kv_bytes_bw / kBwBytesPerSmSecond;
-    const double t_mma = plan->flops_mma_issued / kMmaFlopsPerSmSecond;
-    int g_mma = (int)(sms * t_mma / std::max(t_bw + t_mma, 1e-30) + 0.5);
-    g_mma = std::max(1, std::min(g_mma, sms - 1));
-    g_mma = (int)std::min<int64_t>(g_mma, plan->num_mma);
-    const int g_bw = sms - g_mma;
-    std::lock_guard<std::mutex> lk(side->mu);   // the fork/join events are shared
-    const auto rec_on = [&](int i, cudaStream_t where) {
-      if (events && events[i]) return cudaEventRecord((cudaEvent_t)events[i], where);
-      return cudaSuccess;
-    };
-    if (cudaEventRecord(side->fork, st) != cudaSuccess ||
-        cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
-      return PPS_ERR_CUDA;
-    if (rec_on(2 * PPS_KERNEL_TENSOR, side->stream) != cudaSuccess) return PPS_ERR_CUDA;
-    if (pps::launch_mma_attention(s, t, plan->num_mma, q, *pool, out, err, side->stream, g_mma))
-      return PPS_ERR_CUDA;
-    if (rec_on(2 * PPS_KERNEL_TENSOR + 1, side->stream) != cudaSuccess) return PPS_ERR_CUDA;
-    if (cudaEventRecord(side->join, side->stream) != cudaSuccess) return PPS_ERR_CUDA;
-    if (rec(2 * PPS_KERNEL_BANDWIDTH) != cudaSuccess) return PPS_ERR_CUDA;
-    if (pps::launch_bw_attention(s, t, plan->num_bw, q, *pool, out, err, stream, g_bw))
-      return PPS_ERR_CUDA;
-    if (rec(2 * PPS_KERNEL_BANDWIDTH + 1) != cudaSuccess) return PPS_ERR_CUDA;
-    if (cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess) return PPS_ERR_CUDA;
-  } else {
-    if (rec(2 * PPS_KERNEL_BANDWIDTH) != cudaSuccess) return PPS_ERR_CUDA;
-    if (pps::launch_bw_attention(s, t, plan->num_bw, q, *pool, out, err, stream))
-      return PPS_ERR_CUDA;
-    if (rec(2 * PPS_KERNEL_BANDWIDTH + 1) != cudaSuccess) return PPS_ERR_CUDA;
-    if (rec(2 * PPS_KERNEL_TENSOR) != cudaSuccess) return PPS_ERR_CUDA;
-    if (plan->num_mma &&
-        pps::launch_mma_attention(s, t, plan->num_mma, q, *pool, out, err, stream))
-      return PPS_ERR_CUDA;
-    if (rec(2 * PPS_KERNEL_TENSOR + 1) != cudaSuccess) return PPS_ERR_CUDA;
-  }
+  if (rec(2 * PPS_KERNEL_BANDWIDTH) != cudaSuccess) return PPS_ERR_CUDA;
+  if (pps::launch_bw_attention(s, t, plan->num_bw, q, *pool, out, err, stream))
+    return PPS_ERR_CUDA;
+  if (rec(2 * PPS_KERNEL_BANDWIDTH + 1) != cudaSuccess) return PPS_ERR_CUDA;
+  if (rec(2 * PPS_KERNEL_TENSOR) != cudaSuccess) return PPS_ERR_CUDA;
+  if (plan->num_mma &&
+      pps::launch_mma_attention(s, t, plan->num_mma, q, *pool, out, err, stream))
+    return PPS_ERR_CUDA;
+  if (rec(2 * PPS_KERNEL_TENSOR + 1) != cudaSuccess) return PPS_ERR_CUDA;
   if (rec(2 * PPS_KERNEL_MERGE) != cudaSuccess) return PPS_ERR_CUDA;
   if (pps::launch_merge(s, t, plan->num_merge_tokens, out, stream)) return PPS_ERR_CUDA;
   if (rec(2 * PPS_KERNEL_MERGE + 1) != cudaSuccess) return PPS_ERR_CUDA;
