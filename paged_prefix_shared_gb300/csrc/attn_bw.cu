@@ -657,7 +657,7 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
 
 template <int D, int R>
 int launch_v2(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const void* q,
-              const pps_pool& pool, void* out, int32_t* err, cudaStream_t st, int max_ctas) {
+              const pps_pool& pool, void* out, int32_t* err, cudaStream_t st) {
   auto kern = bw2_attention_kernel<D, R>;
   constexpr int smem = Bw3Smem<D, R>::total;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -669,8 +669,7 @@ int launch_v2(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const 
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBw2Threads, smem)) !=
       cudaSuccess)
     return (int)e;
-  int64_t grid = std::min<int64_t>(n, (int64_t)sms * std::max(per_sm, 1));
-  if (max_ctas > 0) grid = std::min<int64_t>(grid, max_ctas);
+  const int64_t grid = std::min<int64_t>(n, (int64_t)sms * std::max(per_sm, 1));
   kern<<<(unsigned)grid, kBw2Threads, smem, st>>>(
       t.bw_tasks, (int32_t)n, t.rows, t.pages, (const __nv_bfloat16*)q,
       (const __nv_bfloat16*)pool.k, (const __nv_bfloat16*)pool.v, (__nv_bfloat16*)out, t.o_part,
@@ -704,20 +703,19 @@ int launch_t(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const v
 namespace pps {
 
 int launch_bw_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
-                        const pps_pool& pool, void* out, int32_t* err, void* stream,
-                        int max_ctas) {
+                        const pps_pool& pool, void* out, int32_t* err, void* stream) {
   if (num_tasks == 0) return cudaSuccess;
   auto st = (cudaStream_t)stream;
   // The planner caps rows per task at kBwMaxRows; pick the smallest instance.
   // Up to 8 rows: the pipelined v2 kernel; 9..16 rows (CUDA-core-only plans): v1.
   const int rows = s.bw_rows_max;
   if (s.head_dim == 128) {
-    if (rows <= 4) return launch_v2<128, 4>(s, t, num_tasks, q, pool, out, err, st, max_ctas);
-    if (rows <= 8) return launch_v2<128, 8>(s, t, num_tasks, q, pool, out, err, st, max_ctas);
+    if (rows <= 4) return launch_v2<128, 4>(s, t, num_tasks, q, pool, out, err, st);
+    if (rows <= 8) return launch_v2<128, 8>(s, t, num_tasks, q, pool, out, err, st);
     return launch_t<128, 16>(s, t, num_tasks, q, pool, out, st);
   }
-  if (rows <= 4) return launch_v2<64, 4>(s, t, num_tasks, q, pool, out, err, st, max_ctas);
-  if (rows <= 8) return launch_v2<64, 8>(s, t, num_tasks, q, pool, out, err, st, max_ctas);
+  if (rows <= 4) return launch_v2<64, 4>(s, t, num_tasks, q, pool, out, err, st);
+  if (rows <= 8) return launch_v2<64, 8>(s, t, num_tasks, q, pool, out, err, st);
   return launch_t<64, 16>(s, t, num_tasks, q, pool, out, st);
 }
 

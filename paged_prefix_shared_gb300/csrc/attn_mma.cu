@@ -578,7 +578,7 @@ bool make_pool_map(CUtensorMap* map, const void* base, const pps_pool& pool) {
 
 template <int D>
 int launch_t(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const void* q,
-             const pps_pool& pool, void* out, int32_t* err, cudaStream_t st, int max_ctas) {
+             const pps_pool& pool, void* out, int32_t* err, cudaStream_t st) {
   CUtensorMap mk, mv;
   if (!make_pool_map(&mk, pool.k, pool) || !make_pool_map(&mv, pool.v, pool))
     return (int)cudaErrorInvalidValue;
@@ -590,8 +590,7 @@ int launch_t(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const v
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return (int)e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return (int)e;
-  int64_t grid = std::min<int64_t>(n, sms);
-  if (max_ctas > 0) grid = std::min<int64_t>(grid, max_ctas);
+  const int64_t grid = std::min<int64_t>(n, sms);
   MmaParams prm{t.mma_tasks, (int32_t)n, t.rows, t.pages, (const __nv_bfloat16*)q,
                 (__nv_bfloat16*)out, t.o_part, t.lse_part, err, s.num_q_heads, s.group,
                 s.page_size, s.sm_scale * 1.4426950408889634f};
@@ -607,12 +606,11 @@ namespace pps {
 bool mma_path_available() { return true; }
 
 int launch_mma_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
-                         const pps_pool& pool, void* out, int32_t* err, void* stream,
-                         int max_ctas) {
+                         const pps_pool& pool, void* out, int32_t* err, void* stream) {
   if (num_tasks == 0) return cudaSuccess;
   auto st = (cudaStream_t)stream;
-  if (s.head_dim == 128) return launch_t<128>(s, t, num_tasks, q, pool, out, err, st, max_ctas);
-  return launch_t<64>(s, t, num_tasks, q, pool, out, err, st, max_ctas);
+  if (s.head_dim == 128) return launch_t<128>(s, t, num_tasks, q, pool, out, err, st);
+  return launch_t<64>(s, t, num_tasks, q, pool, out, err, st);
 }
 
 }  // namespace pps

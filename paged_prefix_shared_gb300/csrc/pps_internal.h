@@ -101,14 +101,11 @@ int launch_kv_append(const pps_pool& pool, const void* k_new, const void* v_new,
                      const int32_t* page_indptr, const int32_t* page_indices,
                      int32_t num_requests, int32_t num_new_tokens, int32_t* err, void* stream);
 
-// `max_ctas` > 0 caps the persistent grid (to leave SMs to a concurrent kernel).
 int launch_bw_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
-                        const pps_pool& pool, void* out, int32_t* err, void* stream,
-                        int max_ctas = 0);
+                        const pps_pool& pool, void* out, int32_t* err, void* stream);
 
 int launch_mma_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
-                         const pps_pool& pool, void* out, int32_t* err, void* stream,
-                         int max_ctas = 0);
+                         const pps_pool& pool, void* out, int32_t* err, void* stream);
 
 int launch_merge(const Shape& s, const DeviceTables& t, int64_t num_merge_tokens, void* out,
                  void* stream);
