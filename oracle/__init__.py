@@ -12,11 +12,12 @@ token j and query head h (kv head g = h // G, G = Hq / Hkv):
     o[r, j, h] = sum_{p <= c_r + j} softmax_p(scale * q[r, j, h] . k[r, p, g]) v[r, p, g]
 
 with c_r the request's cached length and k[r, p, g] read through the paged
-block table.  Every function is pinned by ``tests/test_oracle_pins.py``
+block table.  With a draft tree (``tree_parent``) the new positions a token
+sees are restricted to its ancestors and itself.  Every function is pinned by ``tests/test_oracle_pins.py``
 against something other than itself (brute force on unpaged copies, closed
 forms, invariances); none is "parity unpinned".
 """
 from .attention import (  # noqa: F401
     reference_scatter, gather_request_kv, paged_attention, dense_attention_loops,
-    attention_partial, lse_merge, split_kv_attention,
+    attention_partial, lse_merge, split_kv_attention, tree_ancestors,
 )

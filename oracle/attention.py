@@ -30,6 +30,14 @@ design notes):
   use the same mask).
 * GQA: query head h reads kv head h // G.
 * scale = 1 / sqrt(head_dim).
+* Tree verify (attentionhub.org listing, the Medusa entry: several candidate
+  continuations verified in one step with tree-based attention; XY-Serve
+  review, Fig. 8: tree-based speculative algorithms organise their
+  predictions as a tree): the draft tokens of a request are
+  given in an order where every token's parent comes before it, each with a
+  parent index (-1: it hangs directly off the cached context).  Token j sees
+  every cached position and the new positions of its ancestors and itself,
+  and nothing else of the draft.  A chain (parent j - 1) is the causal mask.
 """
 from __future__ import annotations
 
@@ -94,8 +102,31 @@ def gather_request_kv(pool_k, pool_v, r, kv_len, page_indptr, page_indices, page
     return _f64(pool_k[pages, :, slots, :]), _f64(pool_v[pages, :, slots, :])
 
 
+def tree_ancestors(parent):
+    """Ancestor-or-self sets of the draft tokens of one request.
+
+    ``parent[j]`` is the index (within the request's new tokens) of token j's
+    parent, or -1 when token j hangs off the cached context; parents come
+    before their children.  Returns a list of sets, walking each token's
+    parent links up to the context."""
+    parent = [int(x) for x in parent]
+    for j, a in enumerate(parent):
+        if not -1 <= a < j:
+            raise ValueError(f"token {j}: parent {a} is not an earlier token or -1")
+    out = []
+    for j in range(len(parent)):
+        seen = set()
+        i = j
+        while i >= 0:
+            seen.add(i)
+            i = parent[i]
+        out.append(seen)
+    return out
+
+
 def paged_attention(q, pool_k, pool_v, q_indptr, kv_len, page_indptr, page_indices,
-                    page_size, sm_scale, num_kv_heads, tokens=None, block_bytes=128 << 20):
+                    page_size, sm_scale, num_kv_heads, tokens=None, block_bytes=128 << 20,
+                    tree_parent=None):
     """Exact causal GQA attention of every new token over its request's paged KV.
 
     ``q`` [T, Hq, d]; pools [num_pages, Hkv, P, d] holding every row the step
@@ -108,6 +139,11 @@ def paged_attention(q, pool_k, pool_v, q_indptr, kv_len, page_indptr, page_indic
     block stays under ``block_bytes``), masked causally (new token j sees
     positions <= c_r + j; XY-Serve review, Figs. 8 and 15), max-subtracted,
     exponentiated, normalised and multiplied by V.
+
+    ``tree_parent`` (optional, [T]): per new token its parent's index within
+    the request's new tokens, or -1.  New position c_r + i is then visible to
+    token j only when i is j or one of its ancestors (``tree_ancestors``);
+    cached positions stay visible.  Omitted, every request is a chain.
     """
     qf = q
     T = int(q_indptr[-1])
@@ -133,6 +169,9 @@ def paged_attention(q, pool_k, pool_v, q_indptr, kv_len, page_indptr, page_indic
                 continue
         n = int(kv_len[r])
         c = n - (t1 - t0)
+        anc = None
+        if tree_parent is not None:
+            anc = tree_ancestors(np.asarray(tree_parent)[t0:t1])
         k, v = gather_request_kv(pool_k, pool_v, r, kv_len, page_indptr, page_indices, page_size)
         qr = _f64(qf[t0 + js] if want is None else qf[[t0 + int(j) for j in js]])  # [m, Hq, d]
         rows_per_block = max(1, int(block_bytes // (8 * G * max(n, 1))))
@@ -145,6 +184,11 @@ def paged_attention(q, pool_k, pool_v, q_indptr, kv_len, page_indptr, page_indic
                 s = sm_scale * (qb.reshape(-1, d) @ kg.T)               # [m*G, n]
                 s = s.reshape(len(jb), G, n)
                 visible = np.arange(n)[None, :] <= (c + jb)[:, None]    # [m, n]
+                if anc is not None:
+                    for x, j in enumerate(jb):
+                        for i in range(int(j)):
+                            if i not in anc[int(j)]:
+                                visible[x, c + i] = False
                 s = np.where(visible[:, None, :], s, -np.inf)
                 s = s - s.max(axis=-1, keepdims=True)
                 p = np.exp(s)
@@ -158,11 +202,13 @@ def paged_attention(q, pool_k, pool_v, q_indptr, kv_len, page_indptr, page_indic
     return out
 
 
-def dense_attention_loops(q_rows, k, v, cached_len, sm_scale, num_kv_heads):
+def dense_attention_loops(q_rows, k, v, cached_len, sm_scale, num_kv_heads, keys=None):
     """Brute force, unvectorised: the definition written as plain loops over
     unpaged (contiguous) K/V of one request.
 
     ``q_rows`` [q, Hq, d], ``k``/``v`` [n, Hkv, d] with n = cached_len + q.
+    ``keys`` (optional): per row, the list of key positions it attends to;
+    default every position up to cached_len + j.
     Returns a nested list [q][Hq][d] of Python floats.
     """
     q_rows = _f64(q_rows).tolist()
@@ -172,12 +218,12 @@ def dense_attention_loops(q_rows, k, v, cached_len, sm_scale, num_kv_heads):
     G = Hq // int(num_kv_heads)
     out = []
     for j, qj in enumerate(q_rows):
-        last = cached_len + j
+        seen = list(range(cached_len + j + 1)) if keys is None else list(keys[j])
         row = []
         for h in range(Hq):
             g = h // G
             logits = []
-            for p in range(last + 1):
+            for p in seen:
                 acc = 0.0
                 for x, y in zip(qj[h], k[p][g]):
                     acc += x * y
@@ -186,9 +232,9 @@ def dense_attention_loops(q_rows, k, v, cached_len, sm_scale, num_kv_heads):
             w = [math.exp(a - m) for a in logits]
             z = sum(w)
             o = [0.0] * len(qj[h])
-            for p in range(last + 1):
+            for i, p in enumerate(seen):
                 for e in range(len(o)):
-                    o[e] += w[p] * v[p][g][e]
+                    o[e] += w[i] * v[p][g][e]
             row.append([x / z for x in o])
         out.append(row)
     return out

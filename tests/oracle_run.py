@@ -23,7 +23,7 @@ def oracle_steps(wl, pool_k=None, pool_v=None, upto=None):
                                           L.page_indptr, L.page_indices, L.page_size)
         outs.append(oracle.paged_attention(st.q, pk, pv, L.q_indptr, L.kv_len, L.page_indptr,
                                            L.page_indices, L.page_size, L.sm_scale,
-                                           L.num_kv_heads))
+                                           L.num_kv_heads, tree_parent=L.tree_parent))
     return outs, (pk, pv)
 
 
@@ -53,5 +53,5 @@ def oracle_steps_selected(sub, step, reqs, L, tokens, req_of):
     sub_tok = [int(SL.q_indptr[pos[int(r)]]) + int(t - L.q_indptr[r]) for t, r in zip(tokens, req_of)]
     out = oracle.paged_attention(sub.steps[step].q, pk, pv, SL.q_indptr, SL.kv_len, SL.page_indptr,
                                  SL.page_indices, SL.page_size, SL.sm_scale, SL.num_kv_heads,
-                                 tokens=sub_tok)
+                                 tokens=sub_tok, tree_parent=SL.tree_parent)
     return out, (pk, pv)

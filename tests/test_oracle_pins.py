@@ -9,6 +9,9 @@
   splitting the keys then merging by log-sum-exp gives plain softmax
   (online-softmax equivalence);
 * batch composition: a request's rows do not depend on the other requests;
+* draft trees: a token's output equals that of the last token of a plain
+  causal request made of its root-to-node path; a chain tree is the causal
+  mask; brute force with each token's key list built bottom-up;
 * planted mistakes: textual mutations of the oracle (a dropped scale, a
   shifted causal limit, a transposed head mapping, a wrong page slot, a
   missing max-subtraction guard) each make one of these pins fail.
@@ -43,6 +46,8 @@ def small_workloads():
                                                num_verify=2, verify_lo=2, verify_hi=4, mu=3.0,
                                                sigma=0.5, clip_lo=16, clip_hi=40, **kw),
         "long_prefill": workloads.long_prefill(num_requests=2, chunk=8, num_chunks=3, **kw),
+        "tree_verify": workloads.tree_verify(num_requests=3, tree_size=12, kv_lo=5, kv_hi=40,
+                                             **kw),
     }
 
 
@@ -68,9 +73,23 @@ def test_bruteforce_on_unpaged_copies(name):
                 continue
             k, v = workloads.contiguous_kv(wl, r, upto_step=s)
             assert k.shape[0] == int(L.kv_len[r])
+            keys = None
+            if L.tree_parent is not None:
+                keys = _tree_keys(L.tree_parent[a:b], int(L.cached_len[r]))
             bf = np.array(oracle.dense_attention_loops(st.q[a:b], k, v, int(L.cached_len[r]),
-                                                       L.sm_scale, L.num_kv_heads))
+                                                       L.sm_scale, L.num_kv_heads, keys=keys))
             np.testing.assert_allclose(outs[s][a:b], bf, rtol=0, atol=1e-12)
+
+
+def _tree_keys(parent, c):
+    """Key positions of each draft token, built bottom-up (a token sees what
+    its parent sees plus its own position), independently of the oracle's
+    upward walk."""
+    keys = []
+    for j, a in enumerate(parent):
+        base = list(range(c)) if a < 0 else keys[a]
+        keys.append(base + [c + j])
+    return keys
 
 
 @pytest.mark.parametrize("name", list(workloads.WORKLOADS))
@@ -167,6 +186,112 @@ def test_request_alone_equals_request_in_batch():
         sub = workloads.sub_workload(wl, 0, [r])
         got, _ = oracle_steps(sub)
         assert np.array_equal(got[0], ref[0][L.q_indptr[r]:L.q_indptr[r + 1]])
+
+
+# --- draft trees ------------------------------------------------------------
+
+def _tree_request(parent, n_cached, Hq=4, Hkv=2, d=16, P=4, seed=3):
+    wl = workloads.build_workload("tree", num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d,
+                                  page_size=P, shared_lens=[], requests=[([], n_cached, [len(parent)])],
+                                  seed=seed, keep_segments=True)
+    wl.steps[0].layout.tree_parent = np.asarray(parent, np.int32)
+    return wl
+
+
+def _chain_output(q_rows, k, v, P=4):
+    """Causal (chain) attention of ``q_rows`` [m, Hq, d] over contiguous K/V
+    [n, Hkv, d], run through the paged oracle with a fresh identity page table."""
+    n, Hkv, d = k.shape
+    npg = -(-n // P)
+    pk = torch.full((npg, Hkv, P, d), float("nan"), dtype=torch.bfloat16)
+    pv = pk.clone()
+    for p in range(n):
+        pk[p // P, :, p % P] = k[p]
+        pv[p // P, :, p % P] = v[p]
+    m = q_rows.shape[0]
+    return oracle.paged_attention(q_rows, pk, pv, np.array([0, m]), np.array([n]),
+                                  np.array([0, npg]), np.arange(npg), P, 1 / math.sqrt(d), Hkv)
+
+
+TREES = {
+    "random": workloads.draft_tree(np.random.default_rng(11), 14),
+    "star": np.full(9, -1, np.int32),                       # every token hangs off the context
+    "two_chains": np.array([-1, 0, 1, 2, -1, 4, 5], np.int32),
+    "binary": np.array([-1, 0, 0, 1, 1, 2, 2, 3, 3, 4], np.int32),
+}
+
+
+@pytest.mark.parametrize("tree", list(TREES))
+def test_tree_node_equals_its_path_as_a_chain(tree):
+    """A draft token's output is the output of the last token of a plain
+    causal request whose new tokens are the token's root-to-node path."""
+    parent = TREES[tree]
+    c = 10
+    wl = _tree_request(parent, c)
+    out, _ = oracle_steps(wl)
+    st = wl.steps[0]
+    k, v = workloads.contiguous_kv(wl, 0)
+    for j in range(len(parent)):
+        path = []
+        i = j
+        while i >= 0:
+            path.append(i)
+            i = int(parent[i])
+        path = path[::-1]
+        idx = list(range(c)) + [c + i for i in path]
+        ref = _chain_output(st.q[path], k[idx], v[idx])
+        np.testing.assert_allclose(out[0][j], ref[-1], rtol=0, atol=1e-12)
+
+
+def test_chain_tree_is_the_causal_mask():
+    wl = _small()["mixed_budget"]
+    ref, _ = oracle_steps(wl)
+    L = wl.steps[0].layout
+    L.tree_parent = np.concatenate([workloads.chain_parents(int(q)) for q in L.q_len])
+    try:
+        got, _ = oracle_steps(wl)
+    finally:
+        L.tree_parent = None
+    assert np.array_equal(ref[0], got[0])
+
+
+def test_tree_parent_must_precede_the_token():
+    with pytest.raises(ValueError):
+        oracle.tree_ancestors([-1, 1])
+    with pytest.raises(ValueError):
+        oracle.tree_ancestors([0])
+    assert oracle.tree_ancestors([-1, 0, 0, 2]) == [{0}, {0, 1}, {0, 2}, {0, 2, 3}]
+
+
+TREE_MUTATIONS = {
+    "parent_only": ("            i = parent[i]\n", "            i = parent[i] if i == j else -1\n"),
+    "mask_offset": ("visible[x, c + i] = False", "visible[x, c + i - 1] = False"),
+    "tree_ignored": ("        if tree_parent is not None:\n            anc =",
+                     "        if False:\n            anc ="),
+}
+
+
+@pytest.mark.parametrize("name", list(TREE_MUTATIONS))
+def test_planted_tree_mistake_is_caught(name):
+    src_path = os.path.join(os.path.dirname(oracle.__file__), "attention.py")
+    src = open(src_path).read()
+    old, new = TREE_MUTATIONS[name]
+    assert src.count(old) == 1, name
+    mod = types.ModuleType("oracle_tree_mutant_" + name)
+    exec(compile(src.replace(old, new), src_path, "exec"), mod.__dict__)
+    parent = TREES["binary"]
+    c = 10
+    wl = _tree_request(parent, c)
+    st = wl.steps[0]
+    L = st.layout
+    pk, pv = oracle.reference_scatter(wl.pool_k, wl.pool_v, st.k_new, st.v_new, L.q_indptr,
+                                      L.cached_len, L.page_indptr, L.page_indices, L.page_size)
+    out = mod.paged_attention(st.q, pk, pv, L.q_indptr, L.kv_len, L.page_indptr, L.page_indices,
+                              L.page_size, L.sm_scale, L.num_kv_heads, tree_parent=parent)
+    k, v = workloads.contiguous_kv(wl, 0)
+    bf = np.array(oracle.dense_attention_loops(st.q, k, v, c, L.sm_scale, L.num_kv_heads,
+                                               keys=_tree_keys(parent, c)))
+    assert not np.allclose(out, bf, rtol=0, atol=1e-12), f"tree mutation {name} slipped through"
 
 
 # --- closed forms -----------------------------------------------------------

@@ -36,7 +36,7 @@ import torch
 __all__ = [
     "Layout", "Step", "Workload", "build_workload", "tiny_mixed", "decode_heavy",
     "radix_sharing", "mixed_budget", "long_prefill", "WORKLOADS", "make",
-    "contiguous_kv", "sub_workload",
+    "contiguous_kv", "sub_workload", "draft_tree", "chain_parents", "tree_verify",
 ]
 
 
@@ -53,6 +53,9 @@ class Layout:
     kv_len: np.ndarray        # [R]   cached + new
     page_indptr: np.ndarray   # [R+1]
     page_indices: np.ndarray  # [nnz] physical page ids, in logical order
+    # [T] per new token: index of its parent among the request's new tokens, or
+    # -1 (hangs off the cached context); None = every request is a chain.
+    tree_parent: np.ndarray | None = None
 
     @property
     def num_requests(self) -> int:
@@ -333,12 +336,47 @@ def long_prefill(seed=4, device="cpu", num_requests=4, chunk=8192, num_chunks=4,
                           keep_segments=keep_segments, values=values)
 
 
+def chain_parents(n: int) -> np.ndarray:
+    """Parents of a linear chain of n draft tokens (token j's parent is j - 1)."""
+    return np.arange(-1, n - 1, dtype=np.int32)
+
+
+def draft_tree(rng: np.random.Generator, n: int) -> np.ndarray:
+    """A random draft tree of n tokens in parent-before-child order: token 0
+    hangs off the cached context, token j >= 1 picks its parent uniformly
+    among tokens 0..j-1 (a random recursive tree: branching near the root,
+    depth about ln n, the shape of top-k token trees)."""
+    par = np.full(n, -1, dtype=np.int32)
+    for j in range(1, n):
+        par[j] = rng.integers(0, j)
+    return par
+
+
+def tree_verify(seed=5, device="cpu", num_requests=128, tree_size=64, kv_lo=512, kv_hi=4096,
+                num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+                keep_segments=False, values=True):
+    """Speculative tree verification: every request verifies a ``tree_size``
+    token draft tree (``draft_tree``) on top of a cached context of uniform
+    length in [kv_lo, kv_hi]; no sharing, scattered pages."""
+    rng = np.random.default_rng(seed)
+    kv = rng.integers(kv_lo, kv_hi + 1, size=num_requests)
+    parents = np.concatenate([draft_tree(rng, tree_size) for _ in range(num_requests)])
+    reqs = [([], int(c), [tree_size]) for c in kv]
+    wl = build_workload("tree_verify", num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+                        head_dim=head_dim, page_size=page_size, shared_lens=[],
+                        requests=reqs, seed=seed + 1000, device=device,
+                        keep_segments=keep_segments, values=values)
+    wl.steps[0].layout.tree_parent = parents
+    return wl
+
+
 WORKLOADS = {
     "tiny_mixed": tiny_mixed,
     "decode_heavy": decode_heavy,
     "radix_sharing": radix_sharing,
     "mixed_budget": mixed_budget,
     "long_prefill": long_prefill,
+    "tree_verify": tree_verify,
 }
 
 
@@ -377,9 +415,13 @@ def sub_workload(wl: Workload, step: int, requests, device="cpu"):
         sel = [torch.arange(int(lay.q_indptr[r]), int(lay.q_indptr[r + 1])) for r in requests]
         sel = torch.cat(sel) if sel else torch.zeros(0, dtype=torch.long)
         sel = sel.to(wl.steps[s].q.device)
+        tp = None
+        if lay.tree_parent is not None:
+            tp = np.concatenate([lay.tree_parent[lay.q_indptr[r]:lay.q_indptr[r + 1]]
+                                 for r in requests] or [np.zeros(0, np.int32)]).astype(np.int32)
         nl = Layout(lay.num_q_heads, lay.num_kv_heads, lay.head_dim, lay.page_size, len(uniq),
                     q_indptr, lay.cached_len[requests].astype(np.int32),
-                    lay.kv_len[requests].astype(np.int32), page_indptr, page_indices)
+                    lay.kv_len[requests].astype(np.int32), page_indptr, page_indices, tp)
         steps.append(Step(nl, wl.steps[s].q.index_select(0, sel).to(device),
                           wl.steps[s].k_new.index_select(0, sel).to(device),
                           wl.steps[s].v_new.index_select(0, sel).to(device)))
