@@ -41,6 +41,8 @@ DESCRIPTIONS = {
     "long_prefill": "4 requests x 32768 tokens as 4 causal chunks of 8192, 32/8, d 128, P 64, seed 4",
     "tiny_mixed": "4 requests 8/2 heads d 64 P 16, cached {37,64,100,129} sharing a 32-token prefix, "
                   "q {1,1,4,16}, seed 0",
+    "tree_verify": "128 requests each verifying a 64-token random draft tree (parent of token j "
+                   "uniform in [0, j)), cached kv uniform [512,4096], 32/8, d 128, P 16, seed 5",
 }
 METRIC = "attention tokens/s and achieved HBM GB/s / tensor TFLOPS vs GB300 roofline"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -198,7 +200,8 @@ def run_pps(args):
                 for n in ("q_indptr", "cached_len", "page_indptr", "page_indices")}
         out = torch.empty_like(st.q)
         plan = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices, L.num_q_heads,
-                             L.num_kv_heads, L.head_dim, L.page_size, L.num_pages)
+                             L.num_kv_heads, L.head_dim, L.page_size, L.num_pages,
+                             tree_parent=L.tree_parent)
         info = plan.info()
         ws = torch.empty(info["workspace_bytes"], dtype=torch.uint8, device=dev)
         steps.append(dict(L=L, st=st, tabs=tabs, out=out, ws=ws, info=info))
@@ -212,7 +215,7 @@ def run_pps(args):
                           t["page_indptr"], t["page_indices"])
             plan = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices,
                                  L.num_q_heads, L.num_kv_heads, L.head_dim, L.page_size,
-                                 L.num_pages)
+                                 L.num_pages, tree_parent=L.tree_parent)
             pps.attn_run(plan, st.q, pk, pv, s["out"], s["ws"],
                          events=None if ev is None else ev[i])
 
@@ -301,7 +304,7 @@ def run_pps(args):
                           d["page_indptr"], d["page_indices"])
             plan = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices,
                                  L.num_q_heads, L.num_kv_heads, L.head_dim, L.page_size,
-                                 L.num_pages)
+                                 L.num_pages, tree_parent=L.tree_parent)
             pps.attn_run(plan, d["q"], pk, pv, s["out"], s["ws"])
             x["out_h"].copy_(s["out"], non_blocking=True)
 
@@ -329,13 +332,28 @@ def run_pps(args):
     kv_unique = sum(i["kv_bytes_unique"] for i in infos)
     kv_bw = sum(i["kv_bytes_bw"] for i in infos)            # K/V read by bandwidth tasks
     flops_mma = sum(i["flops_mma"] for i in infos)
-    if dom == pps.KERNEL_TENSOR:
-        ach = flops_mma / (roof_ms[dom] / 1e3) / 1e12
-        peak = peaks.get("bf16_tflops_sustained" if len(steps) > 1 else "bf16_tflops", 1900.0)
-        roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                "frac": ach / peak, "traffic": traffic_record("attn_mma.cu", args.workload),
+    # K/V the tensor-core tasks read, each byte once (a page several tiles
+    # re-read counts once): at most the unique bytes of the batch
+    kv_mma = min(sum(i["kv_bytes_read"] - i["kv_bytes_bw"] for i in infos), kv_unique)
+    mma_hbm = (kv_mma + qo_bytes) / (roof_ms[pps.KERNEL_TENSOR] / 1e3) / 1e9 \
+        if roof_ms[pps.KERNEL_TENSOR] > 0 else 0.0
+    mma_tf = flops_mma / (roof_ms[pps.KERNEL_TENSOR] / 1e3) / 1e12 \
+        if roof_ms[pps.KERNEL_TENSOR] > 0 else 0.0
+    tpeak = peaks.get("bf16_tflops_sustained" if len(steps) > 1 else "bf16_tflops", 1900.0)
+    hpeak = peaks.get("hbm_gbs", 6800.0)
+    if dom == pps.KERNEL_TENSOR and mma_tf / tpeak >= mma_hbm / hpeak:
+        roof = {"bound": "tensor", "achieved": mma_tf, "peak": tpeak, "unit": "TFLOP/s",
+                "frac": mma_tf / tpeak, "traffic": traffic_record("attn_mma.cu", args.workload),
                 "kernel": "tcgen05 attention tiles",
                 "algorithmic": f"{flops_mma:.4g} FLOP per step (4*d per visible (row,key) pair)"}
+    elif dom == pps.KERNEL_TENSOR:
+        # few query rows per K/V byte (verify trees): the tile kernel is bound by HBM
+        roof = {"bound": "hbm", "achieved": mma_hbm, "peak": hpeak, "unit": "GB/s",
+                "frac": mma_hbm / hpeak, "traffic": traffic_record("attn_mma.cu", args.workload),
+                "kernel": "tcgen05 attention tiles",
+                "algorithmic": f"{kv_mma + qo_bytes} B per step (K+V each tensor-core task "
+                               f"reads: {kv_mma}; Q and O rows: {qo_bytes}); "
+                               f"{mma_tf:.1f} TFLOP/s = {mma_tf / tpeak:.3f} of the tensor peak"}
     else:
         alg = kv_bw + qo_bytes
         ach = alg / (roof_ms[dom] / 1e3) / 1e9

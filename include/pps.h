@@ -166,6 +166,39 @@ pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_len,
                          size_t* out_workspace_bytes);
 
 /*
+ * pps_attn_plan_tree -- pps_attn_plan for batches whose verify rows are draft
+ * trees (tree-based speculative decoding).
+ *
+ * Sources: XY-Serve review, Fig. 8 (tree-based speculative algorithms keep
+ * their predictions for several continuations as one tree that the target
+ * model verifies in a single pass); attentionhub.org listing, the Medusa
+ * entry (several candidate continuations verified at once with tree-based
+ * attention).  The pages fix no mask format; this one is the plain reading:
+ *
+ *  tree_parent  host int32 [num_new_tokens], or NULL (= pps_attn_plan).
+ *               Entry q_indptr[r] + j is the index, among request r's new
+ *               tokens, of token j's parent, or -1 when token j hangs
+ *               directly off the cached context.  A parent precedes its child
+ *               (-1 <= parent < j).  New token j (absolute position c_r + j)
+ *               then sees every cached position and the new positions of its
+ *               ancestors and itself; other draft positions are masked out.
+ *               The chain parent = j - 1 is the ordinary causal mask.
+ * The draft tokens' K/V rows are appended at positions c_r + j as usual
+ * (pps_kv_append); the tree order is the row order.  A request whose parents
+ * are not a chain may have at most PPS_TREE_MAX_TOKENS new tokens.
+ * Errors: as pps_attn_plan; PPS_ERR_INVALID_ARGUMENT for a parent out of
+ * range, PPS_ERR_UNSUPPORTED for a tree request with too many new tokens.
+ */
+#define PPS_TREE_MAX_TOKENS 64
+pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t* kv_len,
+                              const int32_t* page_indptr, const int32_t* page_indices,
+                              const int32_t* tree_parent, int32_t num_requests,
+                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t page_size, int32_t num_pages, float sm_scale,
+                              const pps_plan_options* opts, pps_plan** out_plan,
+                              size_t* out_workspace_bytes);
+
+/*
  * pps_attn_run -- the mixed-batch attention.
  *
  *  q          device bf16 [num_new_tokens, num_q_heads, head_dim].
@@ -243,6 +276,7 @@ typedef struct pps_plan_info {
   double flops_total;          /* same over all tasks                                   */
   int64_t kv_bytes_bw;         /* K+V bytes the bandwidth tasks read (each once)         */
   double flops_mma_issued;     /* FLOP the tensor core executes: whole 128-row x 128-key tiles */
+  int32_t num_tree_requests;   /* requests whose draft is a tree (not a chain)           */
 } pps_plan_info;
 pps_status pps_plan_get_info(const pps_plan* plan, pps_plan_info* info);
 
@@ -260,6 +294,11 @@ pps_status pps_plan_get_info(const pps_plan* plan, pps_plan_info* info);
  *   [7] out_pid    -1: write final output rows; else token i writes partial
  *                  slot out_pid + i (rows (out_pid + i) * num_q_heads + h)
  * MERGE_INDPTR / MERGE_PIDS list, for each token in MERGE_TOKENS, its partials.
+ * TREE_MASK (plans made with a draft tree only; count 0 otherwise) holds one
+ * 64-bit word per new token, as int32 pairs (low word first): bit k is set
+ * when the key k positions before the token's own position is visible to it
+ * (keys 64 or more positions back are always visible).  Chain tokens hold
+ * all ones.  Tasks apply it only when their causal field is not PPS_NO_CAUSAL.
  */
 #define PPS_TASK_INTS 8
 #define PPS_NO_CAUSAL 0x3fffffff
@@ -270,6 +309,7 @@ pps_status pps_plan_get_info(const pps_plan* plan, pps_plan_info* info);
 #define PPS_ARRAY_MERGE_TOKENS 4
 #define PPS_ARRAY_MERGE_INDPTR 5
 #define PPS_ARRAY_MERGE_PIDS 6
+#define PPS_ARRAY_TREE_MASK 7
 pps_status pps_plan_get_array(const pps_plan* plan, int32_t which, const int32_t** data,
                               int64_t* count);
 

@@ -34,7 +34,8 @@ NUM_KERNEL_CLASSES = 3
 TASK_INTS = 8
 NO_CAUSAL = 0x3FFFFFFF
 ARRAYS = {"bw_tasks": 0, "mma_tasks": 1, "rows": 2, "pages": 3, "merge_tokens": 4,
-          "merge_indptr": 5, "merge_pids": 6}
+          "merge_indptr": 5, "merge_pids": 6, "tree_mask": 7}
+TREE_MAX_TOKENS = 64
 
 
 class PPSError(RuntimeError):
@@ -59,7 +60,8 @@ class _PlanInfo(ctypes.Structure):
             "num_bw_tasks", "num_mma_tasks", "num_partials", "num_merge_tokens", "table_bytes",
             "workspace_bytes", "kv_bytes_unique", "kv_bytes_read")] + [
         ("flops_mma", ctypes.c_double), ("flops_total", ctypes.c_double),
-        ("kv_bytes_bw", ctypes.c_int64), ("flops_mma_issued", ctypes.c_double)]
+        ("kv_bytes_bw", ctypes.c_int64), ("flops_mma_issued", ctypes.c_double),
+        ("num_tree_requests", ctypes.c_int32)]
 
 
 _lib = None
@@ -85,6 +87,9 @@ def lib():
     L.pps_attn_plan.argtypes = [_I32P, _I32P, _I32P, _I32P, i32, i32, i32, i32, i32, i32,
                                 ctypes.c_float, ctypes.POINTER(_PlanOptions),
                                 ctypes.POINTER(vp), ctypes.POINTER(sz)]
+    L.pps_attn_plan_tree.argtypes = [_I32P, _I32P, _I32P, _I32P, _I32P, i32, i32, i32, i32,
+                                     i32, i32, ctypes.c_float, ctypes.POINTER(_PlanOptions),
+                                     ctypes.POINTER(vp), ctypes.POINTER(sz)]
     L.pps_attn_run.argtypes = [vp, vp, ctypes.POINTER(_Pool), vp, vp, sz, vp]
     L.pps_attn_run_events.argtypes = [vp, vp, ctypes.POINTER(_Pool), vp, vp, sz, vp,
                                       ctypes.POINTER(vp)]
@@ -100,7 +105,8 @@ def lib():
     L.pps_status_string.restype = ctypes.c_char_p
     L.pps_status_string.argtypes = [i32]
     L.pps_version.restype = i32
-    for f in (L.pps_kv_append, L.pps_attn_plan, L.pps_attn_run, L.pps_attn_run_events,
+    for f in (L.pps_kv_append, L.pps_attn_plan, L.pps_attn_plan_tree, L.pps_attn_run,
+              L.pps_attn_run_events,
               L.pps_plan_destroy, L.pps_plan_get_info, L.pps_plan_get_array,
               L.pps_get_device_error):
         f.restype = i32
@@ -212,8 +218,10 @@ class Plan:
 
 def attn_plan(q_indptr, kv_len, page_indptr, page_indices, num_q_heads, num_kv_heads, head_dim,
               page_size, num_pages, sm_scale=None, num_sms=0, bw_chunk_tokens=0,
-              mma_chunk_tokens=0, flags=0) -> Plan:
-    """pps_attn_plan on host int32 arrays (numpy or lists)."""
+              mma_chunk_tokens=0, flags=0, tree_parent=None) -> Plan:
+    """pps_attn_plan on host int32 arrays (numpy or lists); with ``tree_parent``
+    (one parent index per new token, -1 = off the cached context) it calls
+    pps_attn_plan_tree."""
     qi, qi_p = _host_i32(q_indptr)
     kl, kl_p = _host_i32(kv_len)
     pi, pi_p = _host_i32(page_indptr)
@@ -223,10 +231,17 @@ def attn_plan(q_indptr, kv_len, page_indptr, page_indices, num_q_heads, num_kv_h
     opts = _PlanOptions(int(num_sms), int(bw_chunk_tokens), int(mma_chunk_tokens), int(flags))
     h = ctypes.c_void_p()
     ws = ctypes.c_size_t()
-    _check(lib().pps_attn_plan(qi_p, kl_p, pi_p, px_p, len(kl), int(num_q_heads),
-                               int(num_kv_heads), int(head_dim), int(page_size), int(num_pages),
-                               float(sm_scale), ctypes.byref(opts), ctypes.byref(h),
-                               ctypes.byref(ws)), "pps_attn_plan")
+    if tree_parent is None:
+        _check(lib().pps_attn_plan(qi_p, kl_p, pi_p, px_p, len(kl), int(num_q_heads),
+                                   int(num_kv_heads), int(head_dim), int(page_size),
+                                   int(num_pages), float(sm_scale), ctypes.byref(opts),
+                                   ctypes.byref(h), ctypes.byref(ws)), "pps_attn_plan")
+    else:
+        tp, tp_p = _host_i32(tree_parent if len(tree_parent) else np.zeros(1, np.int32))
+        _check(lib().pps_attn_plan_tree(qi_p, kl_p, pi_p, px_p, tp_p, len(kl), int(num_q_heads),
+                                        int(num_kv_heads), int(head_dim), int(page_size),
+                                        int(num_pages), float(sm_scale), ctypes.byref(opts),
+                                        ctypes.byref(h), ctypes.byref(ws)), "pps_attn_plan_tree")
     return Plan(h, ws.value)
 
 

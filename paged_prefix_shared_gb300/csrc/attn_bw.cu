@@ -41,7 +41,8 @@ __global__ void __launch_bounds__(kThreads) bw_attention_kernel(
     const int32_t* __restrict__ pages, const __nv_bfloat16* __restrict__ q,
     const __nv_bfloat16* __restrict__ pool_k, const __nv_bfloat16* __restrict__ pool_v,
     __nv_bfloat16* __restrict__ out, float* __restrict__ o_part, float* __restrict__ lse_part,
-    int32_t num_q_heads, int32_t num_kv_heads, int32_t G, int32_t page_size, float qk_scale) {
+    const unsigned long long* __restrict__ tree_mask, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t G, int32_t page_size, float qk_scale) {
   constexpr int LPT = D / 8;                  // lanes per KV row (8 bf16 = 16 B each)
   constexpr int TPI = kThreads / LPT;         // KV rows per CTA iteration
   extern __shared__ float smem[];
@@ -74,6 +75,12 @@ __global__ void __launch_bounds__(kThreads) bw_attention_kernel(
     }
   }
   if (tid < R) { m_run[tid] = -INFINITY; l_run[tid] = 0.f; }
+  // Draft-tree lookback masks of the task's tokens (all ones: plain causal).
+  __shared__ unsigned long long tmk[R];
+  if (tid < R)
+    tmk[tid] = (tree_mask && tid < task.n_tok && task.causal != PPS_NO_CAUSAL)
+                   ? tree_mask[rows[task.row_off + tid]] : ~0ull;
+  __syncthreads();
   float acc[R][8];
 #pragma unroll
   for (int r = 0; r < R; ++r)
@@ -104,7 +111,8 @@ __global__ void __launch_bounds__(kThreads) bw_attention_kernel(
 #pragma unroll
         for (int off = LPT / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
         if (in && dl == 0 && r < nrows) {
-          const bool vis = p <= task.causal + r / G;
+          const int back = task.causal + r / G - p;        // keys before the row's own one
+          const bool vis = back >= 0 && (back >= 64 || ((tmk[r / G] >> back) & 1ull));
           s[r * kKB + i] = vis ? d : -INFINITY;
         }
       }
@@ -316,10 +324,11 @@ struct BwShared {
 // g = gk + k with g % kBw2Consumers == warp), an online softmax over the
 // task's R rows, then its (max, sum, o) written to the combine buffer whose row
 // stride is RS >= R.  Returns false when a wait ran out.
-template <int D, int R, int RS>
+template <int D, int R, int RS, bool TREE>
 __device__ __forceinline__ bool bw_consume(const pps::Task& task, int nrows, int G, int n_sub,
-                                           int gk, const uint8_t* qs, float qk_scale, bool live,
-                                           const BwShared& sh, uint64_t* qempty) {
+                                           int gk, const uint8_t* qs,
+                                           const unsigned long long* tmk, float qk_scale,
+                                           bool live, const BwShared& sh, uint64_t* qempty) {
   using C = Bw2<D, R>;
   constexpr int EL = C::EL, LPT = C::LPT, TPW = C::TPW, ITERS = C::ITERS, CH = C::CH;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -348,8 +357,13 @@ __device__ __forceinline__ bool bw_consume(const pps::Task& task, int nrows, int
   for (int r = 0; r < R; ++r)
 #pragma unroll
     for (int e = 0; e < EL; ++e) acc[r][e] = 0.f;
-  const int lim0 = task.causal;
   const int my_lim = task.causal + my_row / G;
+  // Draft-tree tasks (TREE) mask non-ancestor keys among the 64 before each
+  // row's own one; a sub-block takes the fast (unmasked) path only if it ends
+  // before every row's window.
+  unsigned long long my_mask = ~0ull;
+  if constexpr (TREE) my_mask = (live && my_row < nrows) ? tmk[my_row / G] : ~0ull;
+  const int lim0 = task.causal - (TREE ? 64 : 0);
   const int first = (warp - gk % kBw2Consumers + kBw2Consumers) % kBw2Consumers;
   for (int k = first; live && k < n_sub; k += kBw2Consumers) {
     const int g = gk + k;                                  // g % kBw2Consumers == warp
@@ -395,6 +409,13 @@ __device__ __forceinline__ bool bw_consume(const pps::Task& task, int nrows, int
         if (pos >= task.kv_end || pos > my_lim) sv = -INFINITY;
       }
       sc[it] = sv;
+    }
+    if (TREE && !fast) {                       // warp-uniform; kept out of the loop above
+#pragma unroll
+      for (int it = 0; it < ITERS; ++it) {
+        const int back = my_lim - (pos0 + it * TPW + grp);
+        if (back >= 0 && back < 64 && !((my_mask >> back) & 1ull)) sc[it] = -INFINITY;
+      }
     }
     float mx = sc[0];
 #pragma unroll
@@ -479,14 +500,16 @@ __device__ __forceinline__ bool bw_consume(const pps::Task& task, int nrows, int
   return live;
 }
 
-template <int D, int R>
+// TREE: the batch holds draft-tree verify rows (per-token lookback masks);
+// batches without one run the TREE = false instance, which has no mask code.
+template <int D, int R, bool TREE>
 __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
     const pps::Task* __restrict__ tasks, int32_t num_tasks, const int32_t* __restrict__ rows,
     const int32_t* __restrict__ pages, const __nv_bfloat16* __restrict__ q,
     const __nv_bfloat16* __restrict__ pool_k, const __nv_bfloat16* __restrict__ pool_v,
     __nv_bfloat16* __restrict__ out, float* __restrict__ o_part, float* __restrict__ lse_part,
-    int32_t* __restrict__ err, int32_t num_q_heads, int32_t num_kv_heads, int32_t G,
-    int32_t page_size, float qk_scale) {
+    const unsigned long long* __restrict__ tree_mask, int32_t* __restrict__ err,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t G, int32_t page_size, float qk_scale) {
   using C = Bw2<D, R>;
   using S = Bw3Smem<D, R>;
   extern __shared__ __align__(128) uint8_t bw2_smem[];
@@ -496,6 +519,7 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
   // token ids, written by the producer so consumers never wait on global loads.
   __shared__ pps::Task tinfo[2];
   __shared__ int32_t ttok[2][R];
+  __shared__ unsigned long long tmsk[2][R];   // draft-tree lookback mask per token
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x, nctas = gridDim.x;
@@ -534,7 +558,11 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
              !abort_flag;
         if (ok) {
           tinfo[qb] = task;
-          for (int i = 0; i < task.n_tok; ++i) ttok[qb][i] = rows[task.row_off + i];
+          for (int i = 0; i < task.n_tok; ++i) {
+            ttok[qb][i] = rows[task.row_off + i];
+            if constexpr (TREE)
+              tmsk[qb][i] = task.causal != PPS_NO_CAUSAL ? tree_mask[ttok[qb][i]] : ~0ull;
+          }
           const uint32_t qbar = sm100::smem_u32(&qfull[qb]);
           const uint32_t tok_bytes = (uint32_t)G * D * 2;
           sm100::mbar_expect_tx(qbar, tok_bytes * task.n_tok);   // releases tinfo / ttok
@@ -619,10 +647,11 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
     // Tasks of up to 4 rows (one decode token at G = 4) take the 4-row inner
     // loop even in the 8-row instance: half the arithmetic per K/V byte.
     if (R == 8 && nrows <= 4)
-      live = bw_consume<D, (R == 8 ? 4 : R), R>(task, nrows, G, n_sub, gk, qs, qk_scale, live, sh,
-                                                 &qempty[qb]);
+      live = bw_consume<D, (R == 8 ? 4 : R), R, TREE>(task, nrows, G, n_sub, gk, qs, tmsk[qb],
+                                                       qk_scale, live, sh, &qempty[qb]);
     else
-      live = bw_consume<D, R, R>(task, nrows, G, n_sub, gk, qs, qk_scale, live, sh, &qempty[qb]);
+      live = bw_consume<D, R, R, TREE>(task, nrows, G, n_sub, gk, qs, tmsk[qb], qk_scale, live,
+                                       sh, &qempty[qb]);
     gk += n_sub;
     asm volatile("bar.sync 1, %0;" ::"r"(kBw2Consumers * 32) : "memory");
     for (int idx = tid; idx < nrows * D; idx += kBw2Consumers * 32) {
@@ -655,10 +684,10 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
   }
 }
 
-template <int D, int R>
+template <int D, int R, bool TREE>
 int launch_v2(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const void* q,
               const pps_pool& pool, void* out, int32_t* err, cudaStream_t st) {
-  auto kern = bw2_attention_kernel<D, R>;
+  auto kern = bw2_attention_kernel<D, R, TREE>;
   constexpr int smem = Bw3Smem<D, R>::total;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return (int)e;
@@ -673,7 +702,7 @@ int launch_v2(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const 
   kern<<<(unsigned)grid, kBw2Threads, smem, st>>>(
       t.bw_tasks, (int32_t)n, t.rows, t.pages, (const __nv_bfloat16*)q,
       (const __nv_bfloat16*)pool.k, (const __nv_bfloat16*)pool.v, (__nv_bfloat16*)out, t.o_part,
-      t.lse_part, err, s.num_q_heads, s.num_kv_heads, s.group, s.page_size,
+      t.lse_part, t.tree_mask, err, s.num_q_heads, s.num_kv_heads, s.group, s.page_size,
       s.sm_scale * kLog2e);
   pps::count_launch();
   return (int)cudaGetLastError();
@@ -692,8 +721,8 @@ int launch_t(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const v
   }
   kern<<<(unsigned)n, kThreads, smem, st>>>(
       t.bw_tasks, t.rows, t.pages, (const __nv_bfloat16*)q, (const __nv_bfloat16*)pool.k,
-      (const __nv_bfloat16*)pool.v, (__nv_bfloat16*)out, t.o_part, t.lse_part, s.num_q_heads,
-      s.num_kv_heads, s.group, s.page_size, s.sm_scale * kLog2e);
+      (const __nv_bfloat16*)pool.v, (__nv_bfloat16*)out, t.o_part, t.lse_part, t.tree_mask,
+      s.num_q_heads, s.num_kv_heads, s.group, s.page_size, s.sm_scale * kLog2e);
   pps::count_launch();
   return (int)cudaGetLastError();
 }
@@ -709,13 +738,18 @@ int launch_bw_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks
   // The planner caps rows per task at kBwMaxRows; pick the smallest instance.
   // Up to 8 rows: the pipelined v2 kernel; 9..16 rows (CUDA-core-only plans): v1.
   const int rows = s.bw_rows_max;
+  const bool tree = t.tree_mask != nullptr;
   if (s.head_dim == 128) {
-    if (rows <= 4) return launch_v2<128, 4>(s, t, num_tasks, q, pool, out, err, st);
-    if (rows <= 8) return launch_v2<128, 8>(s, t, num_tasks, q, pool, out, err, st);
+    if (rows <= 4) return tree ? launch_v2<128, 4, true>(s, t, num_tasks, q, pool, out, err, st)
+                               : launch_v2<128, 4, false>(s, t, num_tasks, q, pool, out, err, st);
+    if (rows <= 8) return tree ? launch_v2<128, 8, true>(s, t, num_tasks, q, pool, out, err, st)
+                               : launch_v2<128, 8, false>(s, t, num_tasks, q, pool, out, err, st);
     return launch_t<128, 16>(s, t, num_tasks, q, pool, out, st);
   }
-  if (rows <= 4) return launch_v2<64, 4>(s, t, num_tasks, q, pool, out, err, st);
-  if (rows <= 8) return launch_v2<64, 8>(s, t, num_tasks, q, pool, out, err, st);
+  if (rows <= 4) return tree ? launch_v2<64, 4, true>(s, t, num_tasks, q, pool, out, err, st)
+                             : launch_v2<64, 4, false>(s, t, num_tasks, q, pool, out, err, st);
+  if (rows <= 8) return tree ? launch_v2<64, 8, true>(s, t, num_tasks, q, pool, out, err, st)
+                             : launch_v2<64, 8, false>(s, t, num_tasks, q, pool, out, err, st);
   return launch_t<64, 16>(s, t, num_tasks, q, pool, out, st);
 }
 

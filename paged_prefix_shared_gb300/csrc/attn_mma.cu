@@ -11,7 +11,9 @@
 // warpgroup A turns S_A into P_A, the MMA warp runs PV_B and QK_B on tile B,
 // and the other way round.  Each tile skips the KV tiles past its own causal
 // limit, and fully masked tiles never exist (the planner stops each task's
-// range at its last token's limit; Fig. 11, mask-aware computation).
+// range at its last token's limit; Fig. 11, mask-aware computation).  Draft-
+// tree rows (Fig. 8, tree-based speculation) also mask the draft positions
+// that are not their ancestors, in the KV tiles their 64-key window reaches.
 //
 // Warp roles (320 threads, one persistent CTA per SM taking tasks in
 // symmetric round-robin order over the work-sorted list):
@@ -63,6 +65,7 @@ struct MmaParams {
   float* o_part;
   float* lse_part;
   int32_t* err;
+  const unsigned long long* tree_mask;        // per token lookback masks, or nullptr
   int32_t num_q_heads;
   int32_t G;
   int32_t page_size;
@@ -95,6 +98,18 @@ __device__ __forceinline__ bool softmax_barrier_or(bool pred) {
       : "r"((uint32_t)pred)
       : "memory");
   return r != 0;
+}
+
+// Bit c of the result is bit c + s of `rev` where 0 <= c + s < 64, else 1.
+__device__ __forceinline__ unsigned long long window64(unsigned long long rev, int s) {
+  if (s >= 64 || s <= -64) return ~0ull;
+  if (s >= 0) return (rev >> s) | (s ? (~0ull << (64 - s)) : 0ull);
+  return (rev << -s) | ((1ull << -s) - 1ull);
+}
+
+// Columns [0, n) of a 64-column word.
+__device__ __forceinline__ unsigned long long low_bits(int n) {
+  return n >= 64 ? ~0ull : (n <= 0 ? 0ull : ((1ull << n) - 1ull));
 }
 
 template <int D>
@@ -223,6 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tr.n_tiles == 0) continue;
 
       const int lim = real ? task.causal + i : -1;  // last visible position (inclusive)
+      // Draft-tree rows: bit k of the lookback mask = the key k positions
+      // before the row's own one is visible.  Kept bit-reversed so the
+      // visibility of a tile's columns is a shifted window of it.
+      const unsigned long long tmask =
+          (p.tree_mask && real && task.causal != PPS_NO_CAUSAL) ? p.tree_mask[tok] : ~0ull;
+      const bool trow = tmask != ~0ull;
+      const unsigned long long trev = __brevll(tmask);
       // Padding rows see no key: any finite reference keeps their P at 0 and
       // keeps them off the exact path below.
       float m_ref = real ? -INFINITY : 0.f, l_sum = 0.f;
@@ -232,7 +254,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(&bars.s_full[X], sx & 1)) { fail(); ok = false; break; }
         tc_fence_after();
         const int bound = min(task.kv_end - t0, lim - t0 + 1);     // columns c < bound visible
-        const bool full = __all_sync(0xffffffffu, bound >= kTile);
+        // the row's tree window [lim - 63, lim] reaches into this tile
+        const bool tree_here = trow && t0 + kTile - 1 >= lim - 63;
+        const bool full = __all_sync(0xffffffffu, bound >= kTile && !tree_here);
+        // Visible columns (when not full): bit c of vis[c / 64].
+        unsigned long long vis[2] = {~0ull, ~0ull};
+        if (!full) {
+          vis[0] = low_bits(bound);
+          vis[1] = low_bits(bound - 64);
+          if (tree_here) {
+            vis[0] &= window64(trev, 63 - (lim - t0));
+            vis[1] &= window64(trev, 127 - (lim - t0));
+          }
+        }
         uint32_t pk[kTile / 2];                    // P row, bf16 pairs, stored once verified
         float rs = 0.f, alpha = 1.f, m_use = m_ref;
         // One pass against the running reference max: P = exp2(s * scale - m_ref).
@@ -250,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 32; c += 2) {
               float sa = __uint_as_float(rr[c]), sb = __uint_as_float(rr[c + 1]);
               if (!full) {
-                if (c0 + c >= bound) sa = -INFINITY;
-                if (c0 + c + 1 >= bound) sb = -INFINITY;
+                if (!((vis[(c0 + c) >> 6] >> ((c0 + c) & 63)) & 1ull)) sa = -INFINITY;
+                if (!((vis[(c0 + c + 1) >> 6] >> ((c0 + c + 1) & 63)) & 1ull)) sb = -INFINITY;
               }
               mx = fmaxf(mx, fmaxf(sa, sb));
               const float a = ex2(fmaf(sa, p.qk_scale, -m_ref));
@@ -283,7 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 32; ++c)
-              if (full || c0 + c < bound) mx = fmaxf(mx, __uint_as_float(rr[c]));
+              if (full || ((vis[(c0 + c) >> 6] >> ((c0 + c) & 63)) & 1ull))
+                mx = fmaxf(mx, __uint_as_float(rr[c]));
           }
           const float mxs = (mx == -INFINITY) ? -INFINITY : mx * p.qk_scale;
           m_use = m_ref;
@@ -321,8 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               float a = ex2(fmaf(__uint_as_float(rr[c]), p.qk_scale, -msub));
               float bb = ex2(fmaf(__uint_as_float(rr[c + 1]), p.qk_scale, -msub));
               if (!full) {
-                if (c0 + c >= bound) a = 0.f;
-                if (c0 + c + 1 >= bound) bb = 0.f;
+                if (!((vis[(c0 + c) >> 6] >> ((c0 + c) & 63)) & 1ull)) a = 0.f;
+                if (!((vis[(c0 + c + 1) >> 6] >> ((c0 + c + 1) & 63)) & 1ull)) bb = 0.f;
               }
               rs += a + bb;
               w[c / 2] = pack_bf16(a, bb);
@@ -592,7 +627,7 @@ int launch_t(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const v
     return (int)e;
   const int64_t grid = std::min<int64_t>(n, sms);
   MmaParams prm{t.mma_tasks, (int32_t)n, t.rows, t.pages, (const __nv_bfloat16*)q,
-                (__nv_bfloat16*)out, t.o_part, t.lse_part, err, s.num_q_heads, s.group,
+                (__nv_bfloat16*)out, t.o_part, t.lse_part, err, t.tree_mask, s.num_q_heads, s.group,
                 s.page_size, s.sm_scale * 1.4426950408889634f};
   kern<<<(unsigned)grid, kThreads, Layout<D>::smem_alloc, st>>>(mk, mv, prm);
   pps::count_launch();

@@ -1,5 +1,5 @@
 // Host tile planner: turns one mixed prefill/decode/verify batch into a
-// work-sorted task table (pps_attn_plan).
+// work-sorted task table (pps_attn_plan, pps_attn_plan_tree).
 //
 // Follows the XY-Serve review (pith.science/paper/ABCKJ6RF): "Core claim"
 // (every stage's attention decomposed into tile tasks recorded in tables),
@@ -85,6 +85,18 @@ extern "C" pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_l
                                     int32_t num_pages, float sm_scale,
                                     const pps_plan_options* opts, pps_plan** out_plan,
                                     size_t* out_workspace_bytes) {
+  return pps_attn_plan_tree(q_indptr, kv_len, page_indptr, page_indices, nullptr, num_requests,
+                            num_q_heads, num_kv_heads, head_dim, page_size, num_pages, sm_scale,
+                            opts, out_plan, out_workspace_bytes);
+}
+
+extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t* kv_len,
+                                         const int32_t* page_indptr, const int32_t* page_indices,
+                                         const int32_t* tree_parent, int32_t num_requests,
+                                         int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t page_size, int32_t num_pages,
+                                         float sm_scale, const pps_plan_options* opts,
+                                         pps_plan** out_plan, size_t* out_workspace_bytes) {
   if (out_plan) *out_plan = nullptr;
   if (out_workspace_bytes) *out_workspace_bytes = 0;
   if (!out_plan || !out_workspace_bytes || num_requests < 0 || !q_indptr || !page_indptr ||
@@ -112,6 +124,24 @@ extern "C" pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_l
   }
   const int64_t nnz = page_indptr[R];
   if (nnz > 0 && !page_indices) return PPS_ERR_INVALID_ARGUMENT;
+  // Draft trees: parents precede their children; a request whose parents are
+  // not the chain j - 1 is a tree and must fit the 64-bit per-token mask.
+  int32_t num_tree = 0;
+  if (tree_parent) {
+    for (int32_t r = 0; r < R; ++r) {
+      const int32_t t0 = q_indptr[r], q = q_indptr[r + 1] - t0;
+      bool chain = true;
+      for (int32_t j = 0; j < q; ++j) {
+        const int32_t a = tree_parent[t0 + j];
+        if (a < -1 || a >= j) return PPS_ERR_INVALID_ARGUMENT;
+        chain &= (a == j - 1);
+      }
+      if (!chain) {
+        if (q > PPS_TREE_MAX_TOKENS) return PPS_ERR_UNSUPPORTED;
+        ++num_tree;
+      }
+    }
+  }
 
   pps_plan_options o{};
   if (opts) o = *opts;
@@ -129,6 +159,33 @@ extern "C" pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_l
     plan->num_tokens = q_indptr[R];
     plan->use_mma = use_mma;
     const int32_t T = q_indptr[R];
+    plan->num_tree_requests = num_tree;
+    plan->has_tree = num_tree > 0;
+
+    // ---- 0. per-token lookback masks of draft trees -----------------------------------
+    // anc = ancestor-or-self set over the request's new-token indices (bit i =
+    // token i); lookback bit k = visibility of the key k positions back, which
+    // for k <= j is new token j - k, and a cached position beyond that.
+    std::vector<uint64_t> tmask;
+    if (plan->has_tree) {
+      tmask.assign((size_t)T, ~0ull);
+      std::vector<uint64_t> anc;
+      for (int32_t r = 0; r < R; ++r) {
+        const int32_t t0 = q_indptr[r], q = q_indptr[r + 1] - t0;
+        bool chain = true;
+        for (int32_t j = 0; j < q; ++j) chain &= (tree_parent[t0 + j] == j - 1);
+        if (chain) continue;
+        anc.assign((size_t)q, 0);
+        for (int32_t j = 0; j < q; ++j) {
+          const int32_t a = tree_parent[t0 + j];
+          anc[j] = (1ull << j) | (a >= 0 ? anc[a] : 0ull);
+          uint64_t m = ~0ull;
+          for (int32_t k = 0; k <= j; ++k)
+            if (!((anc[j] >> (j - k)) & 1ull)) m &= ~(1ull << k);
+          tmask[t0 + j] = m;
+        }
+      }
+    }
 
     // ---- 1. radix grouping over fully cached pages --------------------------------
     std::vector<int32_t> group_end(R, 0);
@@ -339,6 +396,13 @@ extern "C" pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_l
       for (int32_t i = 0; i < ts.n_tok; ++i) {
         const int64_t lim = std::min<int64_t>(ts.kv_end, (int64_t)ts.causal + i + 1);
         pairs += (double)std::max<int64_t>(0, lim - ts.kv_begin);
+        if (plan->has_tree && ts.causal != PPS_NO_CAUSAL) {
+          const uint64_t m = tmask[rows[ts.row_off + i]];
+          for (int k = 0; k < 64 && m != ~0ull; ++k) {
+            const int64_t pos = (int64_t)ts.causal + i - k;
+            if (!((m >> k) & 1ull) && pos >= ts.kv_begin && pos < lim) pairs -= 1;
+          }
+        }
       }
       const double f = pairs * num_q_heads * 4.0 * head_dim;
       fl_tot += f;
@@ -370,6 +434,7 @@ extern "C" pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_l
     L.merge_tokens = off;  off += al((int64_t)m_tok.size());
     L.merge_indptr = off;  off += al((int64_t)m_ptr.size());
     L.merge_pids = off;    off += al((int64_t)m_pid.size());
+    L.tree_mask = off;     off += plan->has_tree ? al(2LL * T) : 0;
     L.total_ints = off;
     plan->layout = L;
     plan->image_ints = std::max<int64_t>(off, 64);
@@ -384,6 +449,7 @@ extern "C" pps_status pps_attn_plan(const int32_t* q_indptr, const int32_t* kv_l
     if (!m_tok.empty()) std::memcpy(img + L.merge_tokens, m_tok.data(), m_tok.size() * 4);
     std::memcpy(img + L.merge_indptr, m_ptr.data(), m_ptr.size() * 4);
     if (!m_pid.empty()) std::memcpy(img + L.merge_pids, m_pid.data(), m_pid.size() * 4);
+    if (plan->has_tree) std::memcpy(img + L.tree_mask, tmask.data(), tmask.size() * 8);
 
     plan->num_bw = (int64_t)bw.size();
     plan->num_mma = (int64_t)mm.size();
@@ -433,6 +499,7 @@ extern "C" pps_status pps_plan_get_info(const pps_plan* p, pps_plan_info* info) 
   info->flops_total = p->flops_total;
   info->kv_bytes_bw = p->kv_bytes_bw;
   info->flops_mma_issued = p->flops_mma_issued;
+  info->num_tree_requests = p->num_tree_requests;
   return PPS_OK;
 }
 
@@ -449,6 +516,10 @@ extern "C" pps_status pps_plan_get_array(const pps_plan* p, int32_t which, const
     case PPS_ARRAY_MERGE_TOKENS: *data = img + L.merge_tokens; *count = p->num_merge_tokens; break;
     case PPS_ARRAY_MERGE_INDPTR: *data = img + L.merge_indptr; *count = p->num_merge_tokens + 1; break;
     case PPS_ARRAY_MERGE_PIDS: *data = img + L.merge_pids; *count = p->num_merge_pids; break;
+    case PPS_ARRAY_TREE_MASK:
+      *data = img + L.tree_mask;
+      *count = p->has_tree ? 2LL * p->num_tokens : 0;
+      break;
     default: return PPS_ERR_INVALID_ARGUMENT;
   }
   return PPS_OK;

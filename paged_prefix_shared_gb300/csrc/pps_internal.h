@@ -32,6 +32,7 @@ constexpr int kMmaKvTile = 128;     // KV positions per tensor-core step
 struct TableLayout {
   int64_t bw_tasks = 0, mma_tasks = 0, rows = 0, pages = 0;
   int64_t merge_tokens = 0, merge_indptr = 0, merge_pids = 0;
+  int64_t tree_mask = 0;   // 2 ints per new token, only when the plan has a draft tree
   int64_t total_ints = 0;
 };
 
@@ -44,6 +45,9 @@ struct DeviceTables {
   const int32_t* merge_tokens;
   const int32_t* merge_indptr;
   const int32_t* merge_pids;
+  // Per new token, bit k: the key k positions before the token is visible
+  // (draft-tree verify); nullptr when the batch has no tree.
+  const unsigned long long* tree_mask;
   float* o_part;     // [num_partials, Hq, d]
   float* lse_part;   // [num_partials, Hq] (log2 domain)
 };
@@ -78,6 +82,8 @@ struct pps_plan {
   int32_t num_groups = 0;
   int64_t num_bw = 0, num_mma = 0, num_partials = 0, num_merge_tokens = 0, num_merge_pids = 0;
   int64_t num_rows = 0, num_pages_listed = 0;
+  int32_t num_tree_requests = 0;   // requests with a non-chain draft tree
+  bool has_tree = false;           // table holds the per-token tree masks
   pps::TableLayout layout;
   pps::HostBuf image;           // host copy of the device table
   int64_t image_ints = 0;       // ints of the table in `image`

@@ -39,7 +39,7 @@ def run_workload(wl, flags=0, device_inputs=None, keep_outputs=True, **plan_kw):
                       t["page_indptr"], t["page_indices"])
         plan = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices, L.num_q_heads,
                              L.num_kv_heads, L.head_dim, L.page_size, pk.shape[0], flags=flags,
-                             **plan_kw)
+                             tree_parent=L.tree_parent, **plan_kw)
         ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=pk.device)
         out = torch.full_like(st["q"], float("nan"))
         pps.attn_run(plan, st["q"], pk, pv, out, ws)

@@ -45,7 +45,38 @@ def small_cases():
                                                   num_verify=3, mu=4.0, sigma=1.0, clip_lo=1,
                                                   clip_hi=700, num_q_heads=4, num_kv_heads=4,
                                                   head_dim=128, page_size=128),
+        # draft trees: 40-token trees (tensor-core tiles of 160 rows), 64-token
+        # trees at G = 8 (two tasks per tree), 8-token trees at G = 1 (bandwidth
+        # kernel), and trees behind a shared prefix (group tasks + tree tasks)
+        "tree_verify": lambda: workloads.tree_verify(num_requests=6, tree_size=40, kv_lo=1,
+                                                     kv_hi=1500, **KW),
+        "tree_g8_d64": lambda: workloads.tree_verify(num_requests=3, tree_size=64, kv_lo=1,
+                                                     kv_hi=700, num_q_heads=16, num_kv_heads=2,
+                                                     head_dim=64, page_size=32),
+        "tree_g1_bw": lambda: _star_and_chains(),
+        "tree_shared": lambda: _tree_shared(),
     }
+
+
+def _star_and_chains():
+    """G = 1, 8-token drafts: every token off the context, two chains, random."""
+    wl = workloads.tree_verify(num_requests=5, tree_size=8, kv_lo=1, kv_hi=900, num_q_heads=4,
+                               num_kv_heads=4, head_dim=128, page_size=16, seed=8)
+    par = wl.steps[0].layout.tree_parent
+    par[0:8] = -1
+    par[8:16] = [-1, 0, 1, 2, -1, 4, 5, 6]
+    return wl
+
+
+def _tree_shared():
+    rng = np.random.default_rng(9)
+    tails = rng.integers(1, 400, size=6)
+    wl = workloads.build_workload("tree_shared", shared_lens=[256], requests=[([0], int(t), [24])
+                                                                             for t in tails],
+                                  seed=19, **{k: v for k, v in KW.items() if k != "keep_segments"})
+    wl.steps[0].layout.tree_parent = np.concatenate([workloads.draft_tree(rng, 24)
+                                                     for _ in tails])
+    return wl
 
 
 _CACHE = {}
@@ -176,7 +207,8 @@ def test_run_rejects_small_workspace(pps):
 
 # --- full sizes, sampled rows ------------------------------------------------
 
-FULL = ["tiny_mixed", "decode_heavy", "radix_sharing", "mixed_budget", "long_prefill"]
+FULL = ["tiny_mixed", "decode_heavy", "radix_sharing", "mixed_budget", "long_prefill",
+        "tree_verify"]
 
 
 def _sample_tokens(L, n, seed):

@@ -157,3 +157,87 @@ def test_full_size_plans_fast(pps, name):
         info = plan.info()
         assert info["workspace_bytes"] > 0
         assert dt < 3.0, f"planning {name} took {dt:.3f}s"
+
+
+# --- draft trees -------------------------------------------------------------
+
+def _lookback(parent):
+    """Expected lookback words: bit k set when the key k positions before the
+    token is visible (its ancestor-or-self among the draft, or cached)."""
+    anc = []
+    words = []
+    for j, a in enumerate(parent):
+        anc.append({j} | (anc[a] if a >= 0 else set()))
+        w = 0
+        for k in range(64):
+            if k > j or (j - k) in anc[j]:
+                w |= 1 << k
+        words.append(w)
+    return words
+
+
+def _tree_layout(n_tree=3, seed=0):
+    wl = workloads.tree_verify(num_requests=n_tree, tree_size=20, kv_lo=1, kv_hi=300, **SMALL)
+    L = wl.steps[0].layout
+    return L
+
+
+def test_tree_masks_in_the_plan(pps):
+    L = _tree_layout()
+    plan = _plan(pps, L, tree_parent=L.tree_parent)
+    info = plan.info()
+    assert info["num_tree_requests"] == L.num_requests
+    words = plan.array("tree_mask").view(np.uint64)
+    assert len(words) == L.num_tokens
+    for r in range(L.num_requests):
+        a, b = int(L.q_indptr[r]), int(L.q_indptr[r + 1])
+        assert [int(x) for x in words[a:b]] == _lookback(L.tree_parent[a:b].tolist())
+    check_plan(pps, L, plan)          # causal coverage is unchanged; masks apply in-kernel
+
+
+def test_chain_parents_make_no_tree(pps):
+    L = _tree_layout()
+    chain = np.concatenate([workloads.chain_parents(int(q)) for q in L.q_len])
+    plan = _plan(pps, L, tree_parent=chain)
+    assert plan.info()["num_tree_requests"] == 0
+    assert len(plan.array("tree_mask")) == 0
+    ref = _plan(pps, L)
+    for name in ("bw_tasks", "mma_tasks", "rows", "merge_pids"):
+        assert np.array_equal(plan.array(name), ref.array(name))
+
+
+def test_tree_flops_count_only_visible_pairs(pps):
+    L = _tree_layout()
+    plan = _plan(pps, L, tree_parent=L.tree_parent)
+    pairs = 0                       # cached keys plus the ancestor-or-self set
+
+    for r in range(L.num_requests):
+        a, b = int(L.q_indptr[r]), int(L.q_indptr[r + 1])
+        par = L.tree_parent[a:b].tolist()
+        anc = []
+        for j, p in enumerate(par):
+            anc.append({j} | (anc[p] if p >= 0 else set()))
+            pairs += int(L.cached_len[r]) + len(anc[j])
+    expect = pairs * L.num_q_heads * 4.0 * L.head_dim
+    assert plan.info()["flops_total"] == pytest.approx(expect, rel=1e-12)
+
+
+@pytest.mark.parametrize("bad,code", [
+    ([-1, 1], "invalid argument"),      # a token cannot be its own parent
+    ([0, -1], "invalid argument"),      # token 0 has no earlier token
+    ([-1, -2], "invalid argument"),
+])
+def test_tree_parent_validation(pps, bad, code):
+    with pytest.raises(pps.PPSError, match=code):
+        pps.attn_plan([0, 2], [10], [0, 1], [0], 8, 2, 64, 16, 1, tree_parent=bad)
+
+
+def test_tree_size_limit(pps):
+    q = pps.TREE_MAX_TOKENS + 1
+    star = [-1] * q
+    with pytest.raises(pps.PPSError, match="unsupported"):
+        pps.attn_plan([0, q], [q + 5], [0, 5], list(range(5)), 8, 2, 64, 16, 5, tree_parent=star)
+    # a chain of the same length is plain causal and has no limit
+    plan = pps.attn_plan([0, q], [q + 5], [0, 5], list(range(5)), 8, 2, 64, 16, 5,
+                         tree_parent=list(range(-1, q - 1)))
+    assert plan.info()["num_tree_requests"] == 0
