@@ -186,6 +186,8 @@ def run_pps(args):
                                     num_requests=args.requests or 256)
     elif args.workload == "long_prefill" and args.requests:
         wl = workloads.long_prefill(device=dev, num_requests=args.requests)
+    elif args.workload == "tree_verify" and args.requests:
+        wl = workloads.tree_verify(device=dev, num_requests=args.requests)
     else:
         wl = workloads.make(args.workload, device=dev)
     # device-resident inputs
