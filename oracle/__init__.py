@@ -13,7 +13,11 @@ token j and query head h (kv head g = h // G, G = Hq / Hkv):
 
 with c_r the request's cached length and k[r, p, g] read through the paged
 block table.  With a draft tree (``tree_parent``) the new positions a token
-sees are restricted to its ancestors and itself.  Every function is pinned by ``tests/test_oracle_pins.py``
+sees are restricted to its ancestors and itself.
+
+``radix_cache.RadixCacheOracle`` is the reference for the host prefix cache
+that produces those page tables (token-wise reuse with copy-on-write, page
+allocation, LRU/LFU eviction); ``tests/test_radix_cache_oracle.py`` pins it.  Every function is pinned by ``tests/test_oracle_pins.py``
 against something other than itself (brute force on unpaged copies, closed
 forms, invariances); none is "parity unpinned".
 """
