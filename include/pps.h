@@ -65,12 +65,14 @@ typedef int32_t pps_status;
 #define PPS_ERR_CUDA (-5)              /* a CUDA runtime/driver call failed                 */
 #define PPS_ERR_NO_MEMORY (-6)         /* host allocation failed                            */
 #define PPS_ERR_SCRATCH_LIMIT (-7)     /* plan needs more than the fixed no-alloc scratch    */
+#define PPS_ERR_CACHE_FULL (-8)        /* prefix cache: no free page and nothing evictable   */
 
 /* Device error word values (pps_get_device_error).  0 = no error. */
 #define PPS_DEV_ERR_APPEND_PAGE_ID 1     /* kv_append read a page id outside [0, num_pages)   */
 #define PPS_DEV_ERR_APPEND_PAGE_LIST 2   /* kv_append position beyond the request's page list */
 #define PPS_DEV_ERR_APPEND_REQUEST 3     /* kv_append token not inside q_indptr's range       */
 #define PPS_DEV_ERR_WAIT_TIMEOUT 4       /* a bounded pipeline wait in a kernel ran out       */
+#define PPS_DEV_ERR_COPY_ARGUMENT 5      /* copy_slots: page id or slot count out of range    */
 
 /*
  * The paged KV pool: two caller-owned device arrays, bf16,
@@ -113,6 +115,98 @@ pps_status pps_kv_append(const pps_pool* pool, const void* k_new, const void* v_
                          const int32_t* q_indptr, const int32_t* cached_len,
                          const int32_t* page_indptr, const int32_t* page_indices,
                          int32_t num_requests, int32_t num_new_tokens, void* stream);
+
+/*
+ * pps_copy_slots -- copy-on-write of partly reused pages: for each i < count,
+ * slots [0, num_slots[i]) of page src_pages[i] are copied to the same slots of
+ * page dst_pages[i], for every kv head, in both pool arrays (bit exact).
+ *
+ * This is the copy a prefix cache needs when a new request reuses only the
+ * first tokens of a cached page (XY-Serve review, "Assumptions & free
+ * parameters": copy-on-write under the block table; Fig. 7, token-wise K/V
+ * reuse): the request gets its own page, starting with those tokens' K/V.
+ *  src_pages, dst_pages, num_slots  device int32 [count].
+ * Enqueued on `stream`; a page id outside [0, num_pages) or a slot count outside
+ * [0, page_size] is skipped and recorded in the device error word
+ * (PPS_DEV_ERR_COPY_ARGUMENT).  src and dst must differ.
+ */
+pps_status pps_copy_slots(const pps_pool* pool, const int32_t* src_pages, const int32_t* dst_pages,
+                          const int32_t* num_slots, int32_t count, void* stream);
+
+/*
+ * Host radix-tree prefix cache with a page allocator (pps_cache_*): the step
+ * that produces the page lists pps_kv_append and pps_attn_plan consume.
+ *
+ * Sources: SGLang review, "Core claim" (RadixAttention: the KV of finished
+ * requests stays in a radix tree and later requests sharing a prefix reuse
+ * it); XY-Serve review, "Assumptions & free parameters" and Fig. 7 (block
+ * table plus radix tree under copy-on-write and eviction; token-wise reuse);
+ * attentionhub.org listing, cache-replacement entries (LRU and LFU eviction).
+ * The pages fix no algorithm; these rules are the plain reading:
+ *  - One tree node is one page of the pool: a chunk of up to page_size token
+ *    ids.  A chunk shorter than a page (a finished request's partly filled last
+ *    page) is always a leaf.
+ *  - pps_cache_begin walks the tree from the root: among the children, the one
+ *    whose chunk shares the longest prefix with the next tokens wins (ties: the
+ *    lower page id).  A whole full page matched is shared and the walk goes on;
+ *    a partly matched page is reused token-wise by copy-on-write into the
+ *    request's first new page (out_copy).  At most n - 1 tokens are reused, so
+ *    a request always computes its last token.
+ *  - Pages are handed out lowest id first.  With none free, one evictable node
+ *    (a leaf whose page no active request holds) is evicted and its page reused:
+ *    the smallest (last use, page id) with PPS_CACHE_LRU, the smallest (hits,
+ *    last use, page id) with PPS_CACHE_LFU.  Every call advances a tick; a
+ *    node's last use is the tick of the last call that matched, copied from or
+ *    walked it; its hits count the begin calls that reused it.
+ *  - pps_cache_finish inserts the request's pages below its matched path: a
+ *    chunk equal to an existing child's drops the request's page (freed unless
+ *    still held) and follows that child; otherwise the page becomes a new node.
+ *  - A call that needs pages when none are free and nothing is evictable
+ *    returns PPS_ERR_CACHE_FULL and gives back the pages it took (evictions it
+ *    already made stay made); the request is not started or not extended.
+ * Typical step: pps_cache_begin / pps_cache_extend per request, pps_copy_slots
+ * for the returned copies, pps_kv_append of positions [cached_len, n), then
+ * pps_attn_plan with kv_len = n over the pages from pps_cache_request_pages.
+ * Copies and appends must be enqueued (on one stream) before any later step's
+ * writes to the same pages: a page evicted by a later call can be handed out
+ * again at once.  A cache is not thread safe; it holds host memory only.
+ */
+#define PPS_CACHE_LRU 0
+#define PPS_CACHE_LFU 1
+typedef struct pps_cache pps_cache;
+typedef struct pps_cache_stats {
+  int32_t num_pages, page_size, free_pages, active_requests;
+  int64_t tree_nodes;      /* pages held by the tree                               */
+  int64_t evictions;       /* nodes evicted so far                                 */
+  int64_t reused_tokens;   /* sum of cached_len returned by pps_cache_begin         */
+  int64_t begun_tokens;    /* sum of n passed to pps_cache_begin                    */
+  int64_t tick;            /* calls so far                                         */
+} pps_cache_stats;
+
+/* A cache over pool pages [0, num_pages) of page_size slots. */
+pps_status pps_cache_create(int32_t num_pages, int32_t page_size, int32_t policy,
+                            pps_cache** out_cache);
+pps_status pps_cache_destroy(pps_cache* cache);
+/* Starts a request of n >= 1 tokens (host int32 ids).  Outputs: its id, the
+ * number of leading tokens whose K/V is already in its pages (cached_len), and
+ * out_copy[3] = {src page, dst page, slots} (slots 0: no copy needed). */
+pps_status pps_cache_begin(pps_cache* cache, const int32_t* tokens, int32_t n,
+                           int32_t* out_request, int32_t* out_cached_len, int32_t* out_copy);
+/* Appends m tokens (decode); *out_first_position (optional) = their first position. */
+pps_status pps_cache_extend(pps_cache* cache, int32_t request, const int32_t* tokens, int32_t m,
+                            int32_t* out_first_position);
+/* Ends a request; insert != 0 keeps its pages in the tree for reuse. */
+pps_status pps_cache_finish(pps_cache* cache, int32_t request, int32_t insert);
+/* The request's page list (valid until its next extend or finish). */
+pps_status pps_cache_request_pages(const pps_cache* cache, int32_t request,
+                                   const int32_t** pages, int32_t* num_pages,
+                                   int32_t* num_tokens);
+pps_status pps_cache_get_stats(const pps_cache* cache, pps_cache_stats* stats);
+/* Tree contents for inspection: per node (5 + page_size) int64 values {page,
+ * parent's page or -1, chunk length, last use, hits, chunk (padded with -1)}.
+ * *needed = values required; with capacity 0 only *needed is set. */
+pps_status pps_cache_dump(const pps_cache* cache, int64_t* out, int64_t capacity,
+                          int64_t* needed);
 
 /* Optional planner knobs; pass NULL for defaults.  Zero fields take defaults. */
 typedef struct pps_plan_options {

@@ -64,6 +64,13 @@ class _PlanInfo(ctypes.Structure):
         ("num_tree_requests", ctypes.c_int32)]
 
 
+class _CacheStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("num_pages", "page_size", "free_pages",
+                                              "active_requests")] + [
+        (n, ctypes.c_int64) for n in ("tree_nodes", "evictions", "reused_tokens", "begun_tokens",
+                                      "tick")]
+
+
 _lib = None
 _I32P = ctypes.POINTER(ctypes.c_int32)
 
@@ -91,6 +98,20 @@ def lib():
                                      i32, i32, ctypes.c_float, ctypes.POINTER(_PlanOptions),
                                      ctypes.POINTER(vp), ctypes.POINTER(sz)]
     L.pps_attn_run.argtypes = [vp, vp, ctypes.POINTER(_Pool), vp, vp, sz, vp]
+    L.pps_copy_slots.argtypes = [ctypes.POINTER(_Pool), vp, vp, vp, i32, vp]
+    L.pps_cache_create.argtypes = [i32, i32, i32, ctypes.POINTER(vp)]
+    L.pps_cache_destroy.argtypes = [vp]
+    L.pps_cache_begin.argtypes = [vp, _I32P, i32, _I32P, _I32P, _I32P]
+    L.pps_cache_extend.argtypes = [vp, i32, _I32P, i32, _I32P]
+    L.pps_cache_finish.argtypes = [vp, i32, i32]
+    L.pps_cache_request_pages.argtypes = [vp, i32, ctypes.POINTER(_I32P), _I32P, _I32P]
+    L.pps_cache_get_stats.argtypes = [vp, ctypes.POINTER(_CacheStats)]
+    L.pps_cache_dump.argtypes = [vp, ctypes.POINTER(ctypes.c_int64), ctypes.c_int64,
+                                 ctypes.POINTER(ctypes.c_int64)]
+    for f in (L.pps_copy_slots, L.pps_cache_create, L.pps_cache_destroy, L.pps_cache_begin,
+              L.pps_cache_extend, L.pps_cache_finish, L.pps_cache_request_pages,
+              L.pps_cache_get_stats, L.pps_cache_dump):
+        f.restype = i32
     L.pps_attn_run_events.argtypes = [vp, vp, ctypes.POINTER(_Pool), vp, vp, sz, vp,
                                       ctypes.POINTER(vp)]
     L.pps_attn_run_noalloc.argtypes = [vp, vp, ctypes.POINTER(_Pool), vp, vp]
@@ -297,3 +318,100 @@ def attn_run_noalloc(plan: Plan, q, pool_k, pool_v, out, stream=None):
     _check(lib().pps_attn_run_noalloc(plan.handle, _dev(q, torch.bfloat16), ctypes.byref(pool),
                                       _dev(out, torch.bfloat16), _stream(stream)),
            "pps_attn_run_noalloc")
+
+
+# ---- copy-on-write and the host prefix cache ------------------------------------------
+
+def copy_slots(pool_k, pool_v, src_pages, dst_pages, num_slots, stream=None):
+    """pps_copy_slots: int32 CUDA tensors [count] of source pages, destination
+    pages and slot counts."""
+    import torch
+    pool = _pool(pool_k, pool_v)
+    n = int(src_pages.shape[0])
+    _check(lib().pps_copy_slots(ctypes.byref(pool), _dev(src_pages, torch.int32),
+                                _dev(dst_pages, torch.int32), _dev(num_slots, torch.int32), n,
+                                _stream(stream)), "pps_copy_slots")
+
+
+class CacheFull(PPSError):
+    """pps_cache_*: no free page and nothing evictable."""
+
+
+CACHE_LRU, CACHE_LFU = 0, 1
+
+
+class Cache:
+    """Owner of a pps_cache (host radix-tree prefix cache + page allocator)."""
+
+    def __init__(self, num_pages, page_size, policy=CACHE_LRU):
+        h = ctypes.c_void_p()
+        _check(lib().pps_cache_create(int(num_pages), int(page_size), int(policy),
+                                      ctypes.byref(h)), "pps_cache_create")
+        self._h = h
+        self.page_size = int(page_size)
+
+    def _status(self, code, what):
+        if code == -8:
+            raise CacheFull(f"{what}: {status_string(code)}")
+        _check(code, what)
+
+    def begin(self, tokens):
+        """Returns (request id, cached_len, copy or None); copy = (src, dst, slots)."""
+        t, tp = _host_i32(tokens)
+        rid, cached = ctypes.c_int32(), ctypes.c_int32()
+        cp = (ctypes.c_int32 * 3)()
+        self._status(lib().pps_cache_begin(self._h, tp, len(t), ctypes.byref(rid),
+                                           ctypes.byref(cached), cp), "pps_cache_begin")
+        copy = (cp[0], cp[1], cp[2]) if cp[2] > 0 else None
+        return rid.value, cached.value, copy
+
+    def extend(self, request, tokens):
+        """Appends tokens; returns their first position."""
+        t, tp = _host_i32(tokens if len(tokens) else np.zeros(1, np.int32))
+        first = ctypes.c_int32()
+        self._status(lib().pps_cache_extend(self._h, int(request), tp, len(tokens),
+                                            ctypes.byref(first)), "pps_cache_extend")
+        return first.value
+
+    def finish(self, request, insert=True):
+        self._status(lib().pps_cache_finish(self._h, int(request), int(bool(insert))),
+                     "pps_cache_finish")
+
+    def pages(self, request):
+        ptr, n, nt = _I32P(), ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().pps_cache_request_pages(self._h, int(request), ctypes.byref(ptr),
+                                             ctypes.byref(n), ctypes.byref(nt)),
+               "pps_cache_request_pages")
+        return np.ctypeslib.as_array(ptr, shape=(n.value,)).copy() if n.value else \
+            np.zeros(0, np.int32)
+
+    def stats(self) -> dict:
+        st = _CacheStats()
+        _check(lib().pps_cache_get_stats(self._h, ctypes.byref(st)), "pps_cache_get_stats")
+        return {n: getattr(st, n) for n, _ in _CacheStats._fields_}
+
+    def dump(self):
+        """List of (page, parent page, chunk tuple, last use, hits)."""
+        need = ctypes.c_int64()
+        _check(lib().pps_cache_dump(self._h, None, 0, ctypes.byref(need)), "pps_cache_dump")
+        buf = np.zeros(max(need.value, 1), np.int64)
+        _check(lib().pps_cache_dump(self._h, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                    need.value, ctypes.byref(need)), "pps_cache_dump")
+        rec = 5 + self.page_size
+        out = []
+        for k in range(need.value // rec):
+            r = buf[k * rec:(k + 1) * rec]
+            out.append((int(r[0]), int(r[1]), tuple(int(x) for x in r[5:5 + int(r[2])]),
+                        int(r[3]), int(r[4])))
+        return out
+
+    def destroy(self):
+        if self._h is not None:
+            lib().pps_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass

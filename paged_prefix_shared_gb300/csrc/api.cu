@@ -237,6 +237,22 @@ pps_status pps_kv_append(const pps_pool* pool, const void* k_new, const void* v_
              ? PPS_ERR_CUDA : PPS_OK;
 }
 
+pps_status pps_copy_slots(const pps_pool* pool, const int32_t* src_pages, const int32_t* dst_pages,
+                          const int32_t* num_slots, int32_t count, void* stream) {
+  if (!pool || count < 0) return PPS_ERR_INVALID_ARGUMENT;
+  if (pool->head_dim != 64 && pool->head_dim != 128) return PPS_ERR_UNSUPPORTED;
+  if (!pool_ok(pool)) return PPS_ERR_INVALID_ARGUMENT;
+  if (count == 0) return PPS_OK;
+  if (!src_pages || !dst_pages || !num_slots || ((uintptr_t)pool->k & 15) ||
+      ((uintptr_t)pool->v & 15))
+    return PPS_ERR_INVALID_ARGUMENT;
+  cudaError_t e;
+  int32_t* err = error_word(&e);
+  if (!err) return PPS_ERR_CUDA;
+  return pps::launch_copy_slots(*pool, src_pages, dst_pages, num_slots, count, err, stream)
+             ? PPS_ERR_CUDA : PPS_OK;
+}
+
 pps_status pps_attn_run(const pps_plan* plan, const void* q, const pps_pool* pool, void* out,
                         void* workspace, size_t workspace_bytes, void* stream) {
   return run_impl(plan, q, pool, out, workspace, workspace_bytes, stream, nullptr);
@@ -284,6 +300,7 @@ const char* pps_status_string(pps_status s) {
     case PPS_ERR_CUDA: return "CUDA call failed";
     case PPS_ERR_NO_MEMORY: return "host allocation failed";
     case PPS_ERR_SCRATCH_LIMIT: return "plan needs more than the fixed no-alloc scratch";
+    case PPS_ERR_CACHE_FULL: return "cache full: no free page and nothing evictable";
     default: return "unknown status";
   }
 }

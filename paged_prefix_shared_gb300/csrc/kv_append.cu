@@ -65,9 +65,57 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
   }
 }
 
+// Copy-on-write of a partly reused page: slots [0, n) of every kv head of page
+// src go to the same slots of page dst (K and V), one warp per (copy, kv head,
+// slot).  A page id out of range or a slot count outside [0, page_size] is
+// skipped and recorded in the device error word.
+template <int D>
+__global__ void __launch_bounds__(256) copy_slots_kernel(
+    int4* __restrict__ pool_k, int4* __restrict__ pool_v, const int32_t* __restrict__ src_pages,
+    const int32_t* __restrict__ dst_pages, const int32_t* __restrict__ num_slots, int32_t count,
+    int32_t num_kv_heads, int32_t page_size, int32_t num_pages, int32_t* __restrict__ err) {
+  constexpr int kVec = D * 2 / 16;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t per_copy = (int64_t)num_kv_heads * page_size;
+  const int64_t c = warp / per_copy;
+  if (c >= count) return;
+  const int rem = (int)(warp - c * per_copy);
+  const int h = rem / page_size, slot = rem - h * page_size;
+  const int src = src_pages[c], dst = dst_pages[c], n = num_slots[c];
+  if (src < 0 || src >= num_pages || dst < 0 || dst >= num_pages || n < 0 || n > page_size) {
+    if (lane == 0 && h == 0 && slot == 0) set_error(err, PPS_DEV_ERR_COPY_ARGUMENT);
+    return;
+  }
+  if (slot >= n) return;
+  const size_t so = (((size_t)src * num_kv_heads + h) * page_size + slot) * kVec;
+  const size_t d0 = (((size_t)dst * num_kv_heads + h) * page_size + slot) * kVec;
+  if (lane < kVec) pool_k[d0 + lane] = pool_k[so + lane];
+  else if (lane < 2 * kVec) pool_v[d0 + lane - kVec] = pool_v[so + lane - kVec];
+}
+
 }  // namespace
 
 namespace pps {
+
+int launch_copy_slots(const pps_pool& pool, const int32_t* src_pages, const int32_t* dst_pages,
+                      const int32_t* num_slots, int32_t count, int32_t* err, void* stream) {
+  const int64_t warps = (int64_t)count * pool.num_kv_heads * pool.page_size;
+  if (warps == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (warps * 32 + threads - 1) / threads;
+  auto s = (cudaStream_t)stream;
+  if (pool.head_dim == 128)
+    copy_slots_kernel<128><<<(unsigned)blocks, threads, 0, s>>>(
+        (int4*)pool.k, (int4*)pool.v, src_pages, dst_pages, num_slots, count, pool.num_kv_heads,
+        pool.page_size, pool.num_pages, err);
+  else
+    copy_slots_kernel<64><<<(unsigned)blocks, threads, 0, s>>>(
+        (int4*)pool.k, (int4*)pool.v, src_pages, dst_pages, num_slots, count, pool.num_kv_heads,
+        pool.page_size, pool.num_pages, err);
+  count_launch();
+  return (int)cudaGetLastError();
+}
 
 int launch_kv_append(const pps_pool& pool, const void* k_new, const void* v_new,
                      const int32_t* q_indptr, const int32_t* cached_len,
