@@ -128,7 +128,9 @@ pps_status pps_kv_append(const pps_pool* pool, const void* k_new, const void* v_
  *  src_pages, dst_pages, num_slots  device int32 [count].
  * Enqueued on `stream`; a page id outside [0, num_pages) or a slot count outside
  * [0, page_size] is skipped and recorded in the device error word
- * (PPS_DEV_ERR_COPY_ARGUMENT).  src and dst must differ.
+ * (PPS_DEV_ERR_COPY_ARGUMENT).  The copies of one call run concurrently: no
+ * destination page may also be a source page of the same call (issue them in
+ * separate calls, in order, when that happens).
  */
 pps_status pps_copy_slots(const pps_pool* pool, const int32_t* src_pages, const int32_t* dst_pages,
                           const int32_t* num_slots, int32_t count, void* stream);
@@ -167,9 +169,10 @@ pps_status pps_copy_slots(const pps_pool* pool, const int32_t* src_pages, const 
  * Typical step: pps_cache_begin / pps_cache_extend per request, pps_copy_slots
  * for the returned copies, pps_kv_append of positions [cached_len, n), then
  * pps_attn_plan with kv_len = n over the pages from pps_cache_request_pages.
- * Copies and appends must be enqueued (on one stream) before any later step's
- * writes to the same pages: a page evicted by a later call can be handed out
- * again at once.  A cache is not thread safe; it holds host memory only.
+ * Enqueue each copy (on one stream) before making the next cache call, and the
+ * step's appends before the next step's: a page evicted by a later call can be
+ * handed out again at once.  A cache is not thread safe; it holds host memory
+ * only.
  */
 #define PPS_CACHE_LRU 0
 #define PPS_CACHE_LFU 1
