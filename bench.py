@@ -41,6 +41,10 @@ DESCRIPTIONS = {
     "long_prefill": "4 requests x 32768 tokens as 4 causal chunks of 8192, 32/8, d 128, P 64, seed 4",
     "tiny_mixed": "4 requests 8/2 heads d 64 P 16, cached {37,64,100,129} sharing a 32-token prefix, "
                   "q {1,1,4,16}, seed 0",
+    "cache_serving": "prefix cache + attention serving loop: 256 active requests over 32 shared "
+                     "system prompts (U[1024,4096] tokens) + private suffixes U[32,256], outputs "
+                     "U[16,128]; per step 8 admitted (cache begin, copy-on-write), the rest decode; "
+                     "32/8 heads, d 128, P 16, 131072-page pool, LRU, seed 6",
     "tree_verify": "128 requests each verifying a 64-token random draft tree (parent of token j "
                    "uniform in [0, j)), cached kv uniform [512,4096], 32/8, d 128, P 16, seed 5",
 }
@@ -160,6 +164,51 @@ def traffic_record(kernel_file: str, workload: str):
     src = os.path.join(ROOT, "paged_prefix_shared_gb300", "csrc", kernel_file)
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
     return rec["dram_bytes_per_launch"] if rec.get("source_sha256") == sha else None
+
+
+def roofline(pps, roof_ms, infos, qo_bytes, workload, sustained):
+    """Roofline object of the dominant kernel class.  ``roof_ms`` (per kernel
+    class), ``infos`` (plan info dicts) and ``qo_bytes`` cover the same work."""
+    import numpy as np
+    peaks, peak_src = load_peaks()
+    dom = int(np.argmax(roof_ms))
+    kv_unique = sum(i["kv_bytes_unique"] for i in infos)
+    kv_bw = sum(i["kv_bytes_bw"] for i in infos)            # K/V read by bandwidth tasks
+    flops_mma = sum(i["flops_mma"] for i in infos)
+    # K/V the tensor-core tasks read, each byte once (a page several tiles
+    # re-read counts once): at most the unique bytes of the batch
+    kv_mma = min(sum(i["kv_bytes_read"] - i["kv_bytes_bw"] for i in infos), kv_unique)
+    mma_hbm = (kv_mma + qo_bytes) / (roof_ms[pps.KERNEL_TENSOR] / 1e3) / 1e9 \
+        if roof_ms[pps.KERNEL_TENSOR] > 0 else 0.0
+    mma_tf = flops_mma / (roof_ms[pps.KERNEL_TENSOR] / 1e3) / 1e12 \
+        if roof_ms[pps.KERNEL_TENSOR] > 0 else 0.0
+    tpeak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops", 1900.0)
+    hpeak = peaks.get("hbm_gbs", 6800.0)
+    if dom == pps.KERNEL_TENSOR and mma_tf / tpeak >= mma_hbm / hpeak:
+        roof = {"bound": "tensor", "achieved": mma_tf, "peak": tpeak, "unit": "TFLOP/s",
+                "frac": mma_tf / tpeak, "traffic": traffic_record("attn_mma.cu", workload),
+                "kernel": "tcgen05 attention tiles",
+                "algorithmic": f"{flops_mma:.4g} FLOP per step (4*d per visible (row,key) pair)"}
+    elif dom == pps.KERNEL_TENSOR:
+        # few query rows per K/V byte (verify trees): the tile kernel is bound by HBM
+        roof = {"bound": "hbm", "achieved": mma_hbm, "peak": hpeak, "unit": "GB/s",
+                "frac": mma_hbm / hpeak, "traffic": traffic_record("attn_mma.cu", workload),
+                "kernel": "tcgen05 attention tiles",
+                "algorithmic": f"{kv_mma + qo_bytes:.0f} B per step (K+V each tensor-core task "
+                               f"reads: {kv_mma:.0f}; Q and O rows: {qo_bytes:.0f}); "
+                               f"{mma_tf:.1f} TFLOP/s = {mma_tf / tpeak:.3f} of the tensor peak"}
+    else:
+        alg = kv_bw + qo_bytes
+        ach = alg / (roof_ms[dom] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": hpeak, "unit": "GB/s",
+                "frac": ach / hpeak,
+                "traffic": traffic_record("attn_bw.cu" if dom == 0 else "merge.cu", workload),
+                "kernel": ["split-KV bandwidth attention", "", "partial merge"][dom],
+                "algorithmic": f"{alg:.0f} B per step (K+V read by the bandwidth tasks, each "
+                               f"once: {kv_bw:.0f}; Q and O rows: {qo_bytes:.0f})"}
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else \
+        "fallback"
+    return roof
 
 
 # ---------------------------------------------------------------------------
@@ -326,48 +375,11 @@ def run_pps(args):
     e2e_value = total_tokens / (ms_e2e / 1e3)
 
     # ---- roofline of the dominant kernel ------------------------------------------------
-    peaks, peak_src = load_peaks()
     infos = [s["info"] for s in steps]
-    dom = int(np.argmax(roof_ms))
     L0 = steps[0]["L"]
     qo_bytes = sum(2 * s["L"].num_tokens * L0.num_q_heads * L0.head_dim * 2 for s in steps)
     kv_unique = sum(i["kv_bytes_unique"] for i in infos)
-    kv_bw = sum(i["kv_bytes_bw"] for i in infos)            # K/V read by bandwidth tasks
-    flops_mma = sum(i["flops_mma"] for i in infos)
-    # K/V the tensor-core tasks read, each byte once (a page several tiles
-    # re-read counts once): at most the unique bytes of the batch
-    kv_mma = min(sum(i["kv_bytes_read"] - i["kv_bytes_bw"] for i in infos), kv_unique)
-    mma_hbm = (kv_mma + qo_bytes) / (roof_ms[pps.KERNEL_TENSOR] / 1e3) / 1e9 \
-        if roof_ms[pps.KERNEL_TENSOR] > 0 else 0.0
-    mma_tf = flops_mma / (roof_ms[pps.KERNEL_TENSOR] / 1e3) / 1e12 \
-        if roof_ms[pps.KERNEL_TENSOR] > 0 else 0.0
-    tpeak = peaks.get("bf16_tflops_sustained" if len(steps) > 1 else "bf16_tflops", 1900.0)
-    hpeak = peaks.get("hbm_gbs", 6800.0)
-    if dom == pps.KERNEL_TENSOR and mma_tf / tpeak >= mma_hbm / hpeak:
-        roof = {"bound": "tensor", "achieved": mma_tf, "peak": tpeak, "unit": "TFLOP/s",
-                "frac": mma_tf / tpeak, "traffic": traffic_record("attn_mma.cu", args.workload),
-                "kernel": "tcgen05 attention tiles",
-                "algorithmic": f"{flops_mma:.4g} FLOP per step (4*d per visible (row,key) pair)"}
-    elif dom == pps.KERNEL_TENSOR:
-        # few query rows per K/V byte (verify trees): the tile kernel is bound by HBM
-        roof = {"bound": "hbm", "achieved": mma_hbm, "peak": hpeak, "unit": "GB/s",
-                "frac": mma_hbm / hpeak, "traffic": traffic_record("attn_mma.cu", args.workload),
-                "kernel": "tcgen05 attention tiles",
-                "algorithmic": f"{kv_mma + qo_bytes} B per step (K+V each tensor-core task "
-                               f"reads: {kv_mma}; Q and O rows: {qo_bytes}); "
-                               f"{mma_tf:.1f} TFLOP/s = {mma_tf / tpeak:.3f} of the tensor peak"}
-    else:
-        alg = kv_bw + qo_bytes
-        ach = alg / (roof_ms[dom] / 1e3) / 1e9
-        peak = peaks.get("hbm_gbs", 6800.0)
-        roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
-                "frac": ach / peak,
-                "traffic": traffic_record("attn_bw.cu" if dom == 0 else "merge.cu", args.workload),
-                "kernel": ["split-KV bandwidth attention", "", "partial merge"][dom],
-                "algorithmic": f"{alg} B per step (K+V read by the bandwidth tasks, each "
-                               f"once: {kv_bw}; Q and O rows: {qo_bytes})"}
-    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else \
-        "fallback"
+    roof = roofline(pps, roof_ms, infos, qo_bytes, args.workload, sustained=len(steps) > 1)
 
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -404,6 +416,324 @@ def run_pps(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+class CacheServer:
+    """A serving loop over the prefix cache: every step retires finished
+    requests (their pages go into the radix tree), decodes one token for each
+    active request, admits new ones (pps_cache_begin: shared system-prompt
+    pages reused, copy-on-write of a partly matched page), then runs the step's
+    copy-on-write copies, kv_append, attn_plan and attn_run over the page lists
+    the cache produced.  New K/V/Q rows are slices of seeded device buffers."""
+
+    def __init__(self, pps, torch, dev, trace, num_pages=131072, page_size=16, num_q_heads=32,
+                 num_kv_heads=8, head_dim=128, active=256, max_rows=65536, seed=6):
+        self.pps, self.torch, self.dev = pps, torch, dev
+        self.prompts, self.reqs = trace
+        self.P, self.Hq, self.Hkv, self.D = page_size, num_q_heads, num_kv_heads, head_dim
+        self.num_pages, self.target, self.max_rows = num_pages, active, max_rows
+        self.cache = pps.Cache(num_pages, page_size)
+        bf = torch.bfloat16
+        self.pk = torch.zeros((num_pages, num_kv_heads, page_size, head_dim), dtype=bf, device=dev)
+        self.pv = torch.zeros_like(self.pk)
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.rows_k = torch.randn((max_rows, num_kv_heads, head_dim), generator=g, device=dev).to(bf)
+        self.rows_v = torch.randn((max_rows, num_kv_heads, head_dim), generator=g, device=dev).to(bf)
+        self.q = torch.randn((max_rows, num_q_heads, head_dim), generator=g, device=dev).to(bf)
+        self.out = torch.empty_like(self.q)
+        self.ws = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        # two page-locked staging buffers for the step's tables, each reused
+        # only after the upload that last read it has completed
+        self.h_tab = [torch.empty(1 << 22, dtype=torch.int32).pin_memory() for _ in range(2)]
+        self.h_ev = [None, None]
+        self.d_tab = torch.empty(1 << 22, dtype=torch.int32, device=dev)
+        self.nstep = 0
+        self.next_req = 0
+        # active requests: cache id, trace index, outputs produced so far
+        import numpy as np
+        self.a_rid = np.zeros(0, np.int32)
+        self.a_idx = np.zeros(0, np.int32)
+        self.a_k = np.zeros(0, np.int32)
+        self.new_idx = []
+        self.out_len = np.array([len(r[2]) for r in self.reqs], np.int32)
+        self.out_tok = np.zeros((len(self.reqs), int(self.out_len.max()) + 1), np.int32)
+        for i, r in enumerate(self.reqs):
+            self.out_tok[i, :len(r[2])] = r[2]
+        self.host_s = 0.0                     # host time inside cache calls
+        self.cache_calls = 0
+        self.io = None                        # (pinned q/k/v rows, pinned out) for the e2e run
+
+    def step(self, admit, events=None):
+        import numpy as np
+        torch, pps = self.torch, self.pps
+        t0 = time.perf_counter()
+        # retire requests that produced all their tokens (pages go into the tree)
+        if len(self.a_rid):
+            done = self.a_k >= self.out_len[self.a_idx]
+            for rid in self.a_rid[done]:
+                self.cache.finish(int(rid))
+            self.cache_calls += int(done.sum())
+            keep = ~done
+            self.a_rid, self.a_idx, self.a_k = self.a_rid[keep], self.a_idx[keep], self.a_k[keep]
+        # one decode token for every active request, in one native call
+        n_dec = len(self.a_rid)
+        first = np.zeros(0, np.int32)
+        if n_dec:
+            toks = self.out_tok[self.a_idx, self.a_k]
+            first = self.cache.extend_batch(self.a_rid, np.arange(n_dec + 1, dtype=np.int32), toks)
+            self.a_k += 1
+            self.cache_calls += n_dec
+        # admissions
+        new_rid, new_cached, copies = [], [], []
+        while admit > 0 and len(self.a_rid) + len(new_rid) < self.target and \
+                self.next_req < len(self.reqs):
+            i = self.next_req
+            self.next_req += 1
+            rid, cached, copy = self.cache.begin(self.reqs[i][1])
+            if copy is not None:
+                copies.append(copy)
+            new_rid.append(rid)
+            new_cached.append(cached)
+            self.new_idx.append(i)
+            admit -= 1
+            self.cache_calls += 1
+        rids = np.concatenate([self.a_rid, np.array(new_rid, np.int32)]).astype(np.int32)
+        kv_len, page_indptr, page_indices = self.cache.tables(rids)
+        cached = np.concatenate([first, np.array(new_cached, np.int32)]).astype(np.int32)
+        self.a_rid = rids
+        self.a_idx = np.concatenate([self.a_idx, np.array(self.new_idx, np.int32)]).astype(np.int32)
+        self.a_k = np.concatenate([self.a_k, np.zeros(len(new_rid), np.int32)]).astype(np.int32)
+        self.new_idx = []
+        self.host_s += time.perf_counter() - t0
+        R = len(rids)
+        q_len = kv_len.astype(np.int64) - cached
+        q_indptr = np.concatenate([[0], np.cumsum(q_len)]).astype(np.int32)
+        T = int(q_indptr[-1])
+        if T > self.max_rows:
+            raise RuntimeError("step larger than the row buffers")
+        # copy-on-write copies, split into calls whose copies do not touch each
+        # other's pages (a later call may hand a source page out again)
+        waves, cur, used = [], [], set()
+        for c in copies:
+            if c[0] in used or c[1] in used:
+                waves.append(cur)
+                cur, used = [], set()
+            cur.append(c)
+            used |= {c[0], c[1]}
+        if cur:
+            waves.append(cur)
+        # one upload of every table of the step
+        parts = [q_indptr, cached, page_indptr, page_indices] + \
+            [np.array(w, np.int32).T.reshape(-1) for w in waves]
+        sizes = [len(a) for a in parts]
+        flat = np.concatenate(parts).astype(np.int32)
+        hb = self.nstep & 1
+        self.nstep += 1
+        if self.h_ev[hb] is not None:
+            self.h_ev[hb].synchronize()
+        self.h_tab[hb][:len(flat)].copy_(torch.from_numpy(flat))
+        self.d_tab[:len(flat)].copy_(self.h_tab[hb][:len(flat)], non_blocking=True)
+        self.h_ev[hb] = torch.cuda.Event()
+        self.h_ev[hb].record()
+        views, off = [], 0
+        for n in sizes:
+            views.append(self.d_tab[off:off + n])
+            off += n
+        d_qi, d_cached, d_pi, d_px = views[:4]
+        for w, v in zip(waves, views[4:]):
+            n = len(w)
+            pps.copy_slots(self.pk, self.pv, v[:n], v[n:2 * n], v[2 * n:3 * n])
+        if self.io is not None:
+            hq, hk, hv, ho = self.io
+            self.q[:T].copy_(hq[:T], non_blocking=True)
+            self.rows_k[:T].copy_(hk[:T], non_blocking=True)
+            self.rows_v[:T].copy_(hv[:T], non_blocking=True)
+        pps.kv_append(self.pk, self.pv, self.rows_k[:T], self.rows_v[:T], d_qi, d_cached, d_pi,
+                      d_px)
+        t1 = time.perf_counter()
+        plan = pps.attn_plan(q_indptr, kv_len, page_indptr, page_indices, self.Hq, self.Hkv,
+                             self.D, self.P, self.num_pages)
+        self.host_s += time.perf_counter() - t1
+        if plan.workspace_bytes > self.ws.numel():
+            raise RuntimeError("workspace buffer too small")
+        pps.attn_run(plan, self.q[:T], self.pk, self.pv, self.out[:T], self.ws, events=events)
+        if self.io is not None:
+            self.io[3][:T].copy_(self.out[:T], non_blocking=True)
+        return T, R, plan.info(), len(copies)
+
+
+def run_cache_serving(args):
+    """The cache_serving workload: prefix cache + attention, step by step."""
+    import numpy as np
+    import torch
+
+    import paged_prefix_shared_gb300 as pps
+    import workloads
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pps.build()
+    trace = workloads.cache_trace(seed=6 + 1000 * rank)
+    srv = CacheServer(pps, torch, dev, trace)
+    stream = torch.cuda.current_stream()
+    # warm up: every system prompt once, then fill the active set
+    for k in range(len(trace[0])):
+        rid, _, _ = srv.cache.begin(trace[0][k])
+        srv.cache.finish(rid)
+    while len(srv.a_rid) < srv.target:
+        srv.step(admit=64)
+    for _ in range(args.warmup):
+        srv.step(admit=8)
+    torch.cuda.synchronize()
+    nk = pps.NUM_KERNEL_CLASSES
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nk)] for _ in range(args.steps)]
+    for per in ev:
+        for e in per:
+            e.record(stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    n0 = pps.launch_count()
+    srv.host_s, srv.cache_calls = 0.0, 0
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.mark("t0")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    tokens, infos, reqs, ncopy = 0, [], 0, 0
+    for k in range(args.steps):
+        T, R, info, nc = srv.step(admit=8, events=ev[k])
+        tokens += T
+        reqs += R
+        ncopy += nc
+        infos.append(info)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("t1")
+    barrier(world)
+    launches = pps.launch_count() - n0
+    clocks = sampler.stop()
+    host_ms = srv.host_s / args.steps * 1e3
+    calls = srv.cache_calls
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    total_tokens = sum_over_ranks(tokens, world, dev)
+    value = total_tokens / (ms * args.steps / 1e3)
+    kern_ms = [sum(ev[k][2 * c].elapsed_time(ev[k][2 * c + 1]) for k in range(args.steps))
+               / args.steps for c in range(nk)]
+
+    # e2e: the step's Q/K/V rows come from pinned host memory, outputs go back
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype).pin_memory().copy_(t.cpu())
+    srv.io = (pin(srv.q), pin(srv.rows_k), pin(srv.rows_v),
+              torch.empty(srv.out.shape, dtype=srv.out.dtype).pin_memory())
+    k_e2e = max(3, args.steps // 2)
+    for _ in range(3):
+        srv.step(admit=8)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    tok_e2e, h2d, d2h = 0, 0, 0
+    row_b = srv.Hkv * srv.D * 2
+    for _ in range(k_e2e):
+        T, R, info, nc = srv.step(admit=8)
+        tok_e2e += T
+        h2d += T * (srv.Hq * srv.D * 2 + 2 * row_b)
+        d2h += T * srv.Hq * srv.D * 2
+    f1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(f0.elapsed_time(f1) / k_e2e, world, dev)
+    e2e_value = sum_over_ranks(tok_e2e, world, dev) / (ms_e2e * k_e2e / 1e3)
+
+    avg = lambda key: sum(i[key] for i in infos) / len(infos)
+    avg_infos = [{k: avg(k) for k in ("kv_bytes_unique", "kv_bytes_bw", "flops_mma",
+                                      "kv_bytes_read", "flops_total")}]
+    qo = tokens / args.steps * 2 * srv.Hq * srv.D * 2
+    roof = roofline(pps, kern_ms, avg_infos, qo, args.workload, sustained=False)
+    st = srv.cache.stats()
+    result = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded token ids and N(0,1) bf16 Q/K/V rows; no dataset)",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                   "tokens_per_step": tokens / args.steps, "requests_per_step": reqs / args.steps,
+                   "kv_bytes_unique_per_step": avg("kv_bytes_unique"),
+                   "l2": "inputs larger than L2 (system-prompt KV ~0.3 GB plus private KV), "
+                         "no flush",
+                   "parallelism": f"dp{world} (independent server per GPU, no collective)"},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d / k_e2e,
+                "d2h_bytes_per_step": d2h / k_e2e, "ms_per_step": ms_e2e},
+        "gpu_launches": launches,
+        "kernel_ms_per_step": {"bandwidth": kern_ms[0], "tensor": kern_ms[1], "merge": kern_ms[2]},
+        "roofline": roof,
+        "clocks": clocks,
+        "host_cache": {"host_ms_per_step": host_ms, "cache_calls_per_step": calls / args.steps,
+                       "us_per_cache_call_incl_plan": srv.host_s / max(calls, 1) * 1e6,
+                       "copies_per_step": ncopy / args.steps,
+                       "reused_token_fraction": st["reused_tokens"] / max(st["begun_tokens"], 1),
+                       "tree_pages": st["tree_nodes"], "evictions": st["evictions"]},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cache_serving_cpu_baseline(trace, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def cache_serving_cpu_baseline(trace, budget_s=15.0, steps=None):
+    """The oracles on the host: the reference radix cache replays the serving
+    trace's cache calls and the fp64 attention oracle attends every decode
+    token of a sample of requests (their K/V rows drawn on the host), until
+    about ``budget_s`` seconds are spent.  tokens/s = attended tokens / time."""
+    import math as _m
+    import numpy as np
+    import torch
+    import oracle
+    from oracle import radix_cache as rc
+    P, Hq, Hkv, D = 16, 32, 8, 128
+    prompts, reqs = trace
+    cores = len(os.sched_getaffinity(0))
+    o = rc.RadixCacheOracle(8192, P)          # the reference scans every page per call
+    for k in range(len(prompts)):              # the system prompts, not timed
+        rid, _, _ = o.begin(prompts[k].tolist())
+        o.finish(rid)
+    t0 = time.perf_counter()
+    tok, i = 0, 0
+    g = torch.Generator().manual_seed(6)
+    while time.perf_counter() - t0 < budget_s and i < len(reqs):
+        toks = reqs[i][1].tolist()
+        rid, cached, copy = o.begin(toks)
+        n = len(toks)
+        k = torch.randn((n + 1, Hkv, D), generator=g).to(torch.bfloat16)
+        v = torch.randn((n + 1, Hkv, D), generator=g).to(torch.bfloat16)
+        q = torch.randn((1, Hq, D), generator=g).to(torch.bfloat16)
+        o.extend(rid, reqs[i][2][:1].tolist())
+        npg = -(-(n + 1) // P)
+        pk = torch.zeros((npg * P, Hkv, D), dtype=torch.bfloat16)
+        pv = torch.zeros_like(pk)
+        pk[:n + 1] = k
+        pv[:n + 1] = v
+        pk = pk.view(npg, P, Hkv, D).permute(0, 2, 1, 3).contiguous()
+        pv = pv.view(npg, P, Hkv, D).permute(0, 2, 1, 3).contiguous()
+        oracle.paged_attention(q, pk, pv, np.array([0, 1]), np.array([n + 1]), np.array([0, npg]),
+                               np.arange(npg), P, 1 / _m.sqrt(D), Hkv)
+        o.finish(rid)
+        tok += 1
+        i += 1
+    secs = time.perf_counter() - t0
+    return {"value": tok / secs, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{i} requests of the trace after the system prompts were cached "
+                      f"(untimed): reference radix cache (8192-page pool) begin/extend/finish "
+                      f"and the fp64 attention oracle for one decode token each (K/V drawn on "
+                      f"the host), {secs:.1f} s; numpy fp64 with BLAS threads = "
+                      f"{os.environ.get('OPENBLAS_NUM_THREADS', 'all')} of {cores} cores"}
 
 
 def _oracle_sample_time(wl, reqs, step):
@@ -447,6 +777,26 @@ def run_reference(args):
         return
     import torch
     import workloads
+    if args.workload == "cache_serving":
+        cores = len(os.sched_getaffinity(0))
+        trace = workloads.cache_trace(seed=6)
+        cache_serving_cpu_baseline(trace, budget_s=min(2.0, args.cpu_seconds))   # warm-up
+        t0 = time.perf_counter()
+        base = cache_serving_cpu_baseline(trace, budget_s=args.cpu_seconds)
+        wall = time.perf_counter() - t0
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": base["value"], "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": wall / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded token ids and N(0,1) bf16 Q/K/V rows; no dataset)",
+            "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                       "parallelism": "host cores, rank 0 only"},
+            "cpu_baseline": base,
+            "e2e": {"value": base["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     wl = workloads.make(args.workload, device=dev)
     L = wl.steps[-1].layout
@@ -503,6 +853,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "cache_serving":
+        run_cache_serving(args)
     else:
         run_pps(args)
 

@@ -204,6 +204,20 @@ pps_status pps_cache_finish(pps_cache* cache, int32_t request, int32_t insert);
 pps_status pps_cache_request_pages(const pps_cache* cache, int32_t request,
                                    const int32_t** pages, int32_t* num_pages,
                                    int32_t* num_tokens);
+/* pps_cache_extend for many requests in one call: request requests[i] gets
+ * tokens [token_indptr[i], token_indptr[i + 1]).  out_first_positions
+ * (optional) receives each request's first new position.  Stops at the first
+ * failure (PPS_ERR_CACHE_FULL, or an unknown request) with *out_done = the
+ * number of requests already extended. */
+pps_status pps_cache_extend_batch(pps_cache* cache, const int32_t* requests,
+                                  const int32_t* token_indptr, const int32_t* tokens,
+                                  int32_t count, int32_t* out_first_positions, int32_t* out_done);
+/* The batch's CSR page table for pps_kv_append / pps_attn_plan: kv_len[count]
+ * (tokens each request holds), page_indptr[count + 1] and page_indices (room
+ * for `capacity` entries), for requests[0..count) in that order. */
+pps_status pps_cache_tables(const pps_cache* cache, const int32_t* requests, int32_t count,
+                            int32_t* kv_len, int32_t* page_indptr, int32_t* page_indices,
+                            int64_t capacity);
 pps_status pps_cache_get_stats(const pps_cache* cache, pps_cache_stats* stats);
 /* Tree contents for inspection: per node (5 + page_size) int64 values {page,
  * parent's page or -1, chunk length, last use, hits, chunk (padded with -1)}.

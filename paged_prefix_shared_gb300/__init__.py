@@ -108,6 +108,10 @@ def lib():
     L.pps_cache_get_stats.argtypes = [vp, ctypes.POINTER(_CacheStats)]
     L.pps_cache_dump.argtypes = [vp, ctypes.POINTER(ctypes.c_int64), ctypes.c_int64,
                                  ctypes.POINTER(ctypes.c_int64)]
+    L.pps_cache_extend_batch.argtypes = [vp, _I32P, _I32P, _I32P, i32, _I32P, _I32P]
+    L.pps_cache_tables.argtypes = [vp, _I32P, i32, _I32P, _I32P, _I32P, ctypes.c_int64]
+    for f in (L.pps_cache_extend_batch, L.pps_cache_tables):
+        f.restype = i32
     for f in (L.pps_copy_slots, L.pps_cache_create, L.pps_cache_destroy, L.pps_cache_begin,
               L.pps_cache_extend, L.pps_cache_finish, L.pps_cache_request_pages,
               L.pps_cache_get_stats, L.pps_cache_dump):
@@ -372,6 +376,39 @@ class Cache:
         self._status(lib().pps_cache_extend(self._h, int(request), tp, len(tokens),
                                             ctypes.byref(first)), "pps_cache_extend")
         return first.value
+
+    def extend_batch(self, requests, token_indptr, tokens):
+        """pps_cache_extend_batch; returns the first new position of each request.
+        On CacheFull the requests before the failing one stay extended."""
+        r, rp = _host_i32(requests)
+        ti, tip = _host_i32(token_indptr)
+        t, tp = _host_i32(tokens if len(tokens) else np.zeros(1, np.int32))
+        first = np.zeros(max(len(r), 1), np.int32)
+        done = ctypes.c_int32()
+        self._status(lib().pps_cache_extend_batch(self._h, rp, tip, tp, len(r),
+                                                  first.ctypes.data_as(_I32P),
+                                                  ctypes.byref(done)), "pps_cache_extend_batch")
+        return first[:len(r)]
+
+    def tables(self, requests):
+        """(kv_len, page_indptr, page_indices) of the given requests, in order."""
+        r, rp = _host_i32(requests)
+        n = len(r)
+        kv = np.zeros(max(n, 1), np.int32)
+        ip = np.zeros(n + 1, np.int32)
+        if getattr(self, "_px", None) is None:
+            self._px = np.zeros(1 << 16, np.int32)
+        while True:
+            code = lib().pps_cache_tables(self._h, rp, n, kv.ctypes.data_as(_I32P),
+                                          ip.ctypes.data_as(_I32P),
+                                          self._px.ctypes.data_as(_I32P), len(self._px))
+            if code == 0:
+                break
+            need = sum(len(self.pages(x)) for x in r)              # raises on an unknown id
+            if need <= len(self._px):
+                _check(code, "pps_cache_tables")
+            self._px = np.zeros(2 * need, np.int32)
+        return kv[:n], ip, self._px[:ip[-1]].copy()
 
     def finish(self, request, insert=True):
         self._status(lib().pps_cache_finish(self._h, int(request), int(bool(insert))),

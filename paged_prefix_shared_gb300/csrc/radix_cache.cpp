@@ -388,3 +388,44 @@ extern "C" pps_status pps_cache_dump(const pps_cache* c, int64_t* out, int64_t c
   }
   return PPS_OK;
 }
+
+extern "C" pps_status pps_cache_extend_batch(pps_cache* c, const int32_t* requests,
+                                             const int32_t* token_indptr, const int32_t* tokens,
+                                             int32_t count, int32_t* out_first_positions,
+                                             int32_t* out_done) {
+  if (!c || count < 0 || (count > 0 && (!requests || !token_indptr || !tokens)) || !out_done)
+    return PPS_ERR_INVALID_ARGUMENT;
+  *out_done = 0;
+  for (int32_t i = 0; i < count; ++i) {
+    const int32_t m = token_indptr[i + 1] - token_indptr[i];
+    if (m < 0) return PPS_ERR_INVALID_ARGUMENT;
+    int32_t first = 0;
+    const pps_status st = pps_cache_extend(c, requests[i], tokens + token_indptr[i], m, &first);
+    if (st != PPS_OK) return st;
+    if (out_first_positions) out_first_positions[i] = first;
+    *out_done = i + 1;
+  }
+  return PPS_OK;
+}
+
+extern "C" pps_status pps_cache_tables(const pps_cache* c, const int32_t* requests, int32_t count,
+                                       int32_t* kv_len, int32_t* page_indptr,
+                                       int32_t* page_indices, int64_t capacity) {
+  if (!c || count < 0 || !page_indptr || (count > 0 && (!requests || !kv_len)))
+    return PPS_ERR_INVALID_ARGUMENT;
+  int64_t off = 0;
+  page_indptr[0] = 0;
+  for (int32_t i = 0; i < count; ++i) {
+    auto it = c->requests.find(requests[i]);
+    if (it == c->requests.end()) return PPS_ERR_INVALID_ARGUMENT;
+    const auto& pg = it->second.pages;
+    if (off + (int64_t)pg.size() > capacity || (!page_indices && !pg.empty()))
+      return PPS_ERR_INVALID_ARGUMENT;
+    if (!pg.empty()) std::memcpy(page_indices + off, pg.data(), pg.size() * 4);
+    off += (int64_t)pg.size();
+    if (off > INT32_MAX) return PPS_ERR_INVALID_ARGUMENT;
+    page_indptr[i + 1] = (int32_t)off;
+    kv_len[i] = (int32_t)it->second.tokens.size();
+  }
+  return PPS_OK;
+}

@@ -123,3 +123,38 @@ def test_cache_is_fast_on_a_serving_trace(pps):
     st = c.stats()
     assert st["reused_tokens"] > 0.7 * st["begun_tokens"]
     assert dt < 5.0, dt
+
+
+def test_batch_calls_equal_single_calls(pps):
+    rng = np.random.default_rng(7)
+    a, b = pps.Cache(64, 4), pps.Cache(64, 4)
+    prompts = [list(rng.integers(0, 9, size=12)) for _ in range(3)]
+    rids = []
+    for k in range(6):
+        toks = prompts[k % 3] + list(rng.integers(0, 9, size=3))
+        ra, rb = a.begin(toks), b.begin(toks)
+        assert ra == rb
+        rids.append(ra[0])
+    for step in range(5):
+        lens = rng.integers(0, 3, size=len(rids))
+        indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        toks = rng.integers(0, 9, size=int(indptr[-1])).astype(np.int32)
+        first_b = b.extend_batch(rids, indptr, toks)
+        first_a = [a.extend(r, toks[indptr[i]:indptr[i + 1]]) for i, r in enumerate(rids)]
+        assert list(first_b) == first_a
+        assert sorted(a.dump()) == sorted(b.dump()) and a.stats() == b.stats()
+    order = rids[::-1]
+    kv, ip, px = b.tables(order)
+    for i, r in enumerate(order):
+        assert list(px[ip[i]:ip[i + 1]]) == list(b.pages(r))
+        assert len(b.pages(r)) == -(-int(kv[i]) // 4)      # pages cover exactly kv_len tokens
+
+
+def test_extend_batch_stops_at_the_first_failure(pps):
+    c = pps.Cache(3, 4)
+    r0, _, _ = c.begin([1, 2, 3, 4])                 # one page
+    r1, _, _ = c.begin([5, 6, 7, 8])                 # one page
+    with pytest.raises(pps.CacheFull):               # r0 takes the last page, r1 finds none
+        c.extend_batch([r0, r1], np.array([0, 1, 2], np.int32), np.array([9, 9], np.int32))
+    kv, ip, px = c.tables([r0, r1])
+    assert list(kv) == [5, 4] and c.stats()["free_pages"] == 0

@@ -36,7 +36,7 @@ import torch
 __all__ = [
     "Layout", "Step", "Workload", "build_workload", "tiny_mixed", "decode_heavy",
     "radix_sharing", "mixed_budget", "long_prefill", "WORKLOADS", "make",
-    "contiguous_kv", "sub_workload", "draft_tree", "chain_parents", "tree_verify",
+    "contiguous_kv", "sub_workload", "draft_tree", "chain_parents", "tree_verify", "cache_trace",
 ]
 
 
@@ -368,6 +368,28 @@ def tree_verify(seed=5, device="cpu", num_requests=128, tree_size=64, kv_lo=512,
                         keep_segments=keep_segments, values=values)
     wl.steps[0].layout.tree_parent = parents
     return wl
+
+
+def cache_trace(seed=6, num_prompts=32, prompt_lo=1024, prompt_hi=4096, suffix_lo=32,
+                suffix_hi=256, out_lo=16, out_hi=128, num_requests=4096, vocab=32000):
+    """A serving trace for the prefix cache: ``num_prompts`` shared system
+    prompts (lengths uniform in [prompt_lo, prompt_hi]); each request is one
+    of them (uniform) followed by a private user suffix (uniform in
+    [suffix_lo, suffix_hi] tokens) and then generates ``out`` tokens (uniform
+    in [out_lo, out_hi]), one per decode step.  Token ids uniform in
+    [0, vocab).  Returns (prompts, requests) with requests a list of
+    (prompt index, input token ids, output token ids) as int32 arrays."""
+    rng = np.random.default_rng(seed)
+    prompts = [rng.integers(0, vocab, size=int(rng.integers(prompt_lo, prompt_hi + 1)))
+               .astype(np.int32) for _ in range(num_prompts)]
+    reqs = []
+    for _ in range(num_requests):
+        k = int(rng.integers(num_prompts))
+        suffix = rng.integers(0, vocab, size=int(rng.integers(suffix_lo, suffix_hi + 1)))
+        out = rng.integers(0, vocab, size=int(rng.integers(out_lo, out_hi + 1)))
+        reqs.append((k, np.concatenate([prompts[k], suffix]).astype(np.int32),
+                     out.astype(np.int32)))
+    return prompts, reqs
 
 
 WORKLOADS = {
