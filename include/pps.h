@@ -225,6 +225,46 @@ pps_status pps_cache_get_stats(const pps_cache* cache, pps_cache_stats* stats);
 pps_status pps_cache_dump(const pps_cache* cache, int64_t* out, int64_t capacity,
                           int64_t* needed);
 
+/*
+ * Host token-wise budget scheduler (pps_sched_*): forms each step's mixed
+ * batch from the prefill, decode and verify queues.
+ *
+ * Sources: XY-Serve review, "Core claim" (a token-wise scheduler selects a
+ * budgeted chunk of tokens from mixed prefill, decode and verify queues, with
+ * SplitFuse-style chunking) and Fig. 6 (prefills are split so every scheduled
+ * chunk stays within the budget; some slots are reserved for decode and
+ * speculative tokens to keep the time between tokens stable).  Plain reading:
+ *  - A step holds at most `budget` tokens; prefill never uses the last
+ *    `reserved` of them.
+ *  - Generation requests (decode: 1 token per step; verify: its draft length)
+ *    come first, in the order they started generating, each whole; one that
+ *    does not fit in what is left waits (later ones may still fit).
+ *  - Then prefill requests, first come first served: each takes
+ *    min(its remaining prompt tokens, the prefill room left, the step left);
+ *    when either runs out the rest wait (chunked prefill).
+ *  - A request whose prompt is done starts generating at the next step.
+ * The caller feeds each step's batch to the prefix cache and the attention
+ * path (q = the tokens the scheduler gave the request) and removes finished
+ * requests.  Host memory only; not thread safe.
+ */
+typedef struct pps_sched pps_sched;
+pps_status pps_sched_create(int32_t budget, int32_t reserved, pps_sched** out_sched);
+pps_status pps_sched_destroy(pps_sched* sched);
+/* Queues a request id (not already queued) with prompt_tokens still to compute
+ * (0: it generates from the next step) and gen_tokens >= 1 per generation step. */
+pps_status pps_sched_add(pps_sched* sched, int32_t request, int32_t prompt_tokens,
+                         int32_t gen_tokens);
+pps_status pps_sched_remove(pps_sched* sched, int32_t request);
+/* Changes the tokens per generation step (e.g. a new draft length). */
+pps_status pps_sched_set_gen_tokens(pps_sched* sched, int32_t request, int32_t gen_tokens);
+/* Forms the next batch: entries (request, tokens, is_prefill), generation
+ * entries first.  Fails with PPS_ERR_INVALID_ARGUMENT, changing nothing, if it
+ * has more than `capacity` entries. */
+pps_status pps_sched_step(pps_sched* sched, int32_t* out_requests, int32_t* out_tokens,
+                          int32_t* out_is_prefill, int32_t capacity, int32_t* out_count);
+pps_status pps_sched_counts(const pps_sched* sched, int32_t* prefill_requests,
+                            int64_t* prefill_tokens, int32_t* gen_requests);
+
 /* Optional planner knobs; pass NULL for defaults.  Zero fields take defaults. */
 typedef struct pps_plan_options {
   int32_t num_sms;          /* SMs to balance over; 0 = query the current device (152 if none) */

@@ -112,6 +112,16 @@ def lib():
     L.pps_cache_tables.argtypes = [vp, _I32P, i32, _I32P, _I32P, _I32P, ctypes.c_int64]
     for f in (L.pps_cache_extend_batch, L.pps_cache_tables):
         f.restype = i32
+    L.pps_sched_create.argtypes = [i32, i32, ctypes.POINTER(vp)]
+    L.pps_sched_destroy.argtypes = [vp]
+    L.pps_sched_add.argtypes = [vp, i32, i32, i32]
+    L.pps_sched_remove.argtypes = [vp, i32]
+    L.pps_sched_set_gen_tokens.argtypes = [vp, i32, i32]
+    L.pps_sched_step.argtypes = [vp, _I32P, _I32P, _I32P, i32, _I32P]
+    L.pps_sched_counts.argtypes = [vp, _I32P, ctypes.POINTER(ctypes.c_int64), _I32P]
+    for f in (L.pps_sched_create, L.pps_sched_destroy, L.pps_sched_add, L.pps_sched_remove,
+              L.pps_sched_set_gen_tokens, L.pps_sched_step, L.pps_sched_counts):
+        f.restype = i32
     for f in (L.pps_copy_slots, L.pps_cache_create, L.pps_cache_destroy, L.pps_cache_begin,
               L.pps_cache_extend, L.pps_cache_finish, L.pps_cache_request_pages,
               L.pps_cache_get_stats, L.pps_cache_dump):
@@ -445,6 +455,63 @@ class Cache:
     def destroy(self):
         if self._h is not None:
             lib().pps_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+class Scheduler:
+    """Owner of a pps_sched (token-wise budget scheduler)."""
+
+    def __init__(self, budget, reserved=0):
+        h = ctypes.c_void_p()
+        _check(lib().pps_sched_create(int(budget), int(reserved), ctypes.byref(h)),
+               "pps_sched_create")
+        self._h = h
+        self._cap = 1024
+        self._buf = [np.zeros(self._cap, np.int32) for _ in range(3)]
+
+    def add(self, request, prompt_tokens, gen_tokens=1):
+        _check(lib().pps_sched_add(self._h, int(request), int(prompt_tokens), int(gen_tokens)),
+               "pps_sched_add")
+
+    def remove(self, request):
+        _check(lib().pps_sched_remove(self._h, int(request)), "pps_sched_remove")
+
+    def set_gen_tokens(self, request, gen_tokens):
+        _check(lib().pps_sched_set_gen_tokens(self._h, int(request), int(gen_tokens)),
+               "pps_sched_set_gen_tokens")
+
+    def counts(self):
+        a, b, c = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int32()
+        _check(lib().pps_sched_counts(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+               "pps_sched_counts")
+        return a.value, b.value, c.value
+
+    def step(self):
+        """(requests, tokens, is_prefill) int32 arrays of the next batch."""
+        n = ctypes.c_int32()
+        while True:
+            r, t, p = self._buf
+            code = lib().pps_sched_step(self._h, r.ctypes.data_as(_I32P), t.ctypes.data_as(_I32P),
+                                        p.ctypes.data_as(_I32P), self._cap, ctypes.byref(n))
+            if code == 0:
+                break
+            pr, _, gr = self.counts()
+            if pr + gr <= self._cap:
+                _check(code, "pps_sched_step")
+            self._cap = 2 * (pr + gr)
+            self._buf = [np.zeros(self._cap, np.int32) for _ in range(3)]
+        k = n.value
+        return self._buf[0][:k].copy(), self._buf[1][:k].copy(), self._buf[2][:k].copy()
+
+    def destroy(self):
+        if self._h is not None:
+            lib().pps_sched_destroy(self._h)
             self._h = None
 
     def __del__(self):

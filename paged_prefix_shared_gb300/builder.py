@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpps.so")
 
 CUDA_SOURCES = ["api.cu", "kv_append.cu", "attn_bw.cu", "attn_mma.cu", "merge.cu", "noalloc.cu"]
-CXX_SOURCES = ["planner.cpp", "radix_cache.cpp"]
+CXX_SOURCES = ["planner.cpp", "radix_cache.cpp", "scheduler.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
