@@ -45,6 +45,12 @@ DESCRIPTIONS = {
                      "system prompts (U[1024,4096] tokens) + private suffixes U[32,256], outputs "
                      "U[16,128]; per step 8 admitted (cache begin, copy-on-write), the rest decode; "
                      "32/8 heads, d 128, P 16, 131072-page pool, LRU, seed 6",
+    "engine_serving": "token-wise scheduler + prefix cache + attention: 8192-token budget (512 "
+                      "reserved for generation), up to 256 requests in the system, 32 shared "
+                      "system prompts U[1024,4096], 25% with a private document U[2048,8192], "
+                      "suffix U[32,256], outputs U[16,128]; 25% verify 4-token drafts, the rest "
+                      "decode; chunked prefill; 32/8 heads, d 128, P 16, 262144-page pool, LRU, "
+                      "seed 7",
     "tree_verify": "128 requests each verifying a 64-token random draft tree (parent of token j "
                    "uniform in [0, j)), cached kv uniform [512,4096], 32/8, d 128, P 16, seed 5",
 }
@@ -506,7 +512,14 @@ class CacheServer:
         self.a_k = np.concatenate([self.a_k, np.zeros(len(new_rid), np.int32)]).astype(np.int32)
         self.new_idx = []
         self.host_s += time.perf_counter() - t0
-        R = len(rids)
+        return self._run_batch(kv_len, cached, page_indptr, page_indices, copies, events)
+
+    def _run_batch(self, kv_len, cached, page_indptr, page_indices, copies, events=None):
+        """Device side of a step: copy-on-write copies, kv_append of positions
+        [cached, kv_len) of every request, attn_plan and attn_run."""
+        import numpy as np
+        torch, pps = self.torch, self.pps
+        R = len(kv_len)
         q_len = kv_len.astype(np.int64) - cached
         q_indptr = np.concatenate([[0], np.cumsum(q_len)]).astype(np.int32)
         T = int(q_indptr[-1])
@@ -563,6 +576,79 @@ class CacheServer:
         return T, R, plan.info(), len(copies)
 
 
+class EngineServer(CacheServer):
+    """Scheduler + prefix cache + attention: every step the token-wise
+    scheduler (pps_sched_*) picks the batch within a token budget: the
+    generation requests (decode: 1 token; speculative verify: a draft of
+    ``draft`` tokens, all accepted), then chunks of pending prompts (the part
+    the prefix cache did not already hold).  Requests are admitted (cache
+    begin + scheduler add) while fewer than ``active`` are in the system."""
+
+    def __init__(self, pps, torch, dev, trace, budget=8192, reserved=512, draft=4,
+                 verify_frac=0.25, admit_max=32, **kw):
+        import numpy as np
+        super().__init__(pps, torch, dev, trace, **kw)
+        self.sched = pps.Scheduler(budget, reserved)
+        self.draft, self.admit_max = draft, admit_max
+        rng = np.random.default_rng(17)
+        self.gen_k = np.where(rng.random(len(self.reqs)) < verify_frac, draft, 1).astype(np.int32)
+        pad = np.zeros((len(self.reqs), draft), np.int32)
+        self.out_tok = np.concatenate([self.out_tok, pad], axis=1)
+        self.info = {}                       # rid -> [trace index, cached0, prompt done, produced]
+        self.in_system = 0
+
+    def step(self, admit=None, events=None):
+        import numpy as np
+        t0 = time.perf_counter()
+        cache, sched = self.cache, self.sched
+        # retire requests that produced all their outputs
+        for rid in [r for r, v in self.info.items() if v[3] >= self.out_len[v[0]]]:
+            cache.finish(rid)
+            sched.remove(rid)
+            del self.info[rid]
+            self.cache_calls += 1
+        copies = []
+        n_adm = 0
+        while len(self.info) < self.target and n_adm < self.admit_max and \
+                self.next_req < len(self.reqs):
+            i = self.next_req
+            self.next_req += 1
+            rid, cached, copy = cache.begin(self.reqs[i][1])
+            if copy is not None:
+                copies.append(copy)
+            sched.add(rid, len(self.reqs[i][1]) - cached, int(self.gen_k[i]))
+            self.info[rid] = [i, cached, 0, 0]
+            n_adm += 1
+            self.cache_calls += 1
+        req, tok, pre = sched.step()
+        gen = ~pre.astype(bool)
+        g_rid = req[gen]
+        first = np.zeros(0, np.int32)
+        if len(g_rid):
+            idx = np.array([self.info[r][0] for r in g_rid], np.int32)
+            prod = np.array([self.info[r][3] for r in g_rid], np.int32)
+            k = tok[gen]
+            cols = prod[:, None] + np.arange(self.draft)[None, :]
+            mat = self.out_tok[idx[:, None], np.minimum(cols, self.out_tok.shape[1] - 1)]
+            keep = np.arange(self.draft)[None, :] < k[:, None]
+            toks = mat[keep].astype(np.int32)
+            indptr = np.concatenate([[0], np.cumsum(k)]).astype(np.int32)
+            first = cache.extend_batch(g_rid, indptr, toks)
+            for r, kk in zip(g_rid, k):
+                self.info[r][3] += int(kk)
+            self.cache_calls += len(g_rid)
+        kv_len, page_indptr, page_indices = cache.tables(req)
+        cached = np.zeros(len(req), np.int32)
+        cached[gen] = first
+        for j in np.nonzero(pre)[0]:
+            v = self.info[int(req[j])]
+            cached[j] = v[1] + v[2]
+            v[2] += int(tok[j])
+            kv_len[j] = cached[j] + tok[j]
+        self.host_s += time.perf_counter() - t0
+        return self._run_batch(kv_len, cached, page_indptr, page_indices, copies, events)
+
+
 def run_cache_serving(args):
     """The cache_serving workload: prefix cache + attention, step by step."""
     import numpy as np
@@ -578,15 +664,24 @@ def run_cache_serving(args):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     pps.build()
-    trace = workloads.cache_trace(seed=6 + 1000 * rank)
-    srv = CacheServer(pps, torch, dev, trace)
+    engine = args.workload == "engine_serving"
+    if engine:
+        trace = workloads.cache_trace(seed=7 + 1000 * rank, doc_frac=0.25)
+        srv = EngineServer(pps, torch, dev, trace, num_pages=262144)
+    else:
+        trace = workloads.cache_trace(seed=6 + 1000 * rank)
+        srv = CacheServer(pps, torch, dev, trace)
     stream = torch.cuda.current_stream()
-    # warm up: every system prompt once, then fill the active set
+    # warm up: every system prompt once, then fill the system
     for k in range(len(trace[0])):
         rid, _, _ = srv.cache.begin(trace[0][k])
         srv.cache.finish(rid)
-    while len(srv.a_rid) < srv.target:
-        srv.step(admit=64)
+    if engine:
+        for _ in range(60):
+            srv.step()
+    else:
+        while len(srv.a_rid) < srv.target:
+            srv.step(admit=64)
     for _ in range(args.warmup):
         srv.step(admit=8)
     torch.cuda.synchronize()
@@ -680,6 +775,8 @@ def run_cache_serving(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cache_serving_cpu_baseline(trace, budget_s=args.cpu_seconds)
+    if engine:
+        result["host_cache"]["scheduler"] = "pps_sched_* (budget 8192, reserved 512)"
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -777,9 +874,10 @@ def run_reference(args):
         return
     import torch
     import workloads
-    if args.workload == "cache_serving":
+    if args.workload in ("cache_serving", "engine_serving"):
         cores = len(os.sched_getaffinity(0))
-        trace = workloads.cache_trace(seed=6)
+        trace = workloads.cache_trace(seed=6) if args.workload == "cache_serving" else \
+            workloads.cache_trace(seed=7, doc_frac=0.25)
         cache_serving_cpu_baseline(trace, budget_s=min(2.0, args.cpu_seconds))   # warm-up
         t0 = time.perf_counter()
         base = cache_serving_cpu_baseline(trace, budget_s=args.cpu_seconds)
@@ -853,7 +951,7 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload == "cache_serving":
+    elif args.workload in ("cache_serving", "engine_serving"):
         run_cache_serving(args)
     else:
         run_pps(args)

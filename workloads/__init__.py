@@ -371,12 +371,15 @@ def tree_verify(seed=5, device="cpu", num_requests=128, tree_size=64, kv_lo=512,
 
 
 def cache_trace(seed=6, num_prompts=32, prompt_lo=1024, prompt_hi=4096, suffix_lo=32,
-                suffix_hi=256, out_lo=16, out_hi=128, num_requests=4096, vocab=32000):
+                suffix_hi=256, out_lo=16, out_hi=128, num_requests=4096, vocab=32000,
+                doc_frac=0.0, doc_lo=2048, doc_hi=8192):
     """A serving trace for the prefix cache: ``num_prompts`` shared system
     prompts (lengths uniform in [prompt_lo, prompt_hi]); each request is one
     of them (uniform) followed by a private user suffix (uniform in
     [suffix_lo, suffix_hi] tokens) and then generates ``out`` tokens (uniform
-    in [out_lo, out_hi]), one per decode step.  Token ids uniform in
+    in [out_lo, out_hi]), one per decode step.  With probability
+    ``doc_frac`` a request also carries a private document (uniform in
+    [doc_lo, doc_hi] tokens) between prompt and suffix.  Token ids uniform in
     [0, vocab).  Returns (prompts, requests) with requests a list of
     (prompt index, input token ids, output token ids) as int32 arrays."""
     rng = np.random.default_rng(seed)
@@ -387,6 +390,9 @@ def cache_trace(seed=6, num_prompts=32, prompt_lo=1024, prompt_hi=4096, suffix_l
         k = int(rng.integers(num_prompts))
         suffix = rng.integers(0, vocab, size=int(rng.integers(suffix_lo, suffix_hi + 1)))
         out = rng.integers(0, vocab, size=int(rng.integers(out_lo, out_hi + 1)))
+        if doc_frac > 0 and rng.random() < doc_frac:
+            doc = rng.integers(0, vocab, size=int(rng.integers(doc_lo, doc_hi + 1)))
+            suffix = np.concatenate([doc, suffix])
         reqs.append((k, np.concatenate([prompts[k], suffix]).astype(np.int32),
                      out.astype(np.int32)))
     return prompts, reqs
