@@ -17,7 +17,9 @@ sees are restricted to its ancestors and itself.
 
 ``radix_cache.RadixCacheOracle`` is the reference for the host prefix cache
 that produces those page tables (token-wise reuse with copy-on-write, page
-allocation, LRU/LFU eviction); ``tests/test_radix_cache_oracle.py`` pins it.  Every function is pinned by ``tests/test_oracle_pins.py``
+allocation, LRU/LFU eviction); ``tests/test_radix_cache_oracle.py`` pins it.
+``scheduler.SchedulerOracle`` is the reference token-wise budget scheduler and
+``gemm.linear`` the definition of the projection GEMM; each has its own pins.  Every function is pinned by ``tests/test_oracle_pins.py``
 against something other than itself (brute force on unpaged copies, closed
 forms, invariances); none is "parity unpinned".
 """
