@@ -265,6 +265,24 @@ pps_status pps_sched_step(pps_sched* sched, int32_t* out_requests, int32_t* out_
 pps_status pps_sched_counts(const pps_sched* sched, int32_t* prefill_requests,
                             int64_t* prefill_tokens, int32_t* gen_requests);
 
+/*
+ * pps_gemm_bf16 -- the projection GEMM of a mixed batch: C = A W^T.
+ *
+ * XY-Serve review, "Core claim": SmoothGEMM serves arbitrary shapes with the
+ * efficiency of a fixed-shape kernel by padding virtually in on-chip buffers
+ * and reading / writing only real data.  Here the fixed shape is a 128 x 256
+ * output tile on the tensor cores (tcgen05); a tile that runs past M, N or K is
+ * zero-padded in shared memory only, and only rows < M, columns < N are stored.
+ *  a  device bf16 [M, K] row-major (token rows; M may be any value >= 0)
+ *  w  device bf16 [N, K] row-major (one weight row per output column)
+ *  c  device bf16 [M, N] row-major, written (fp32 accumulation, RNE to bf16)
+ * N and K must be multiples of 8 (16-byte rows); pointers 16-byte aligned.
+ * Enqueued on `stream`.  A pipeline wait that runs out is recorded in the
+ * device error word (PPS_DEV_ERR_WAIT_TIMEOUT).
+ */
+pps_status pps_gemm_bf16(const void* a, const void* w, void* c, int32_t M, int32_t N, int32_t K,
+                         void* stream);
+
 /* Optional planner knobs; pass NULL for defaults.  Zero fields take defaults. */
 typedef struct pps_plan_options {
   int32_t num_sms;          /* SMs to balance over; 0 = query the current device (152 if none) */

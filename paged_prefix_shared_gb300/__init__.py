@@ -99,6 +99,8 @@ def lib():
                                      ctypes.POINTER(vp), ctypes.POINTER(sz)]
     L.pps_attn_run.argtypes = [vp, vp, ctypes.POINTER(_Pool), vp, vp, sz, vp]
     L.pps_copy_slots.argtypes = [ctypes.POINTER(_Pool), vp, vp, vp, i32, vp]
+    L.pps_gemm_bf16.argtypes = [vp, vp, vp, i32, i32, i32, vp]
+    L.pps_gemm_bf16.restype = i32
     L.pps_cache_create.argtypes = [i32, i32, i32, ctypes.POINTER(vp)]
     L.pps_cache_destroy.argtypes = [vp]
     L.pps_cache_begin.argtypes = [vp, _I32P, i32, _I32P, _I32P, _I32P]
@@ -519,3 +521,15 @@ class Scheduler:
             self.destroy()
         except Exception:
             pass
+
+
+def gemm_bf16(a, w, c, stream=None):
+    """pps_gemm_bf16: c[M, N] = a[M, K] @ w[N, K]^T (bf16 CUDA tensors)."""
+    import torch
+    M, K = a.shape
+    N = w.shape[0]
+    if w.shape[1] != K or tuple(c.shape) != (M, N):
+        raise PPSError("shapes: a [M, K], w [N, K], c [M, N]")
+    _check(lib().pps_gemm_bf16(_dev(a, torch.bfloat16), _dev(w, torch.bfloat16),
+                               _dev(c, torch.bfloat16), int(M), int(N), int(K), _stream(stream)),
+           "pps_gemm_bf16")

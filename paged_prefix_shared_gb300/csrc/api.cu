@@ -253,6 +253,18 @@ pps_status pps_copy_slots(const pps_pool* pool, const int32_t* src_pages, const 
              ? PPS_ERR_CUDA : PPS_OK;
 }
 
+pps_status pps_gemm_bf16(const void* a, const void* w, void* c, int32_t M, int32_t N, int32_t K,
+                         void* stream) {
+  if (M < 0 || N <= 0 || K <= 0 || (N % 8) || (K % 8)) return PPS_ERR_INVALID_ARGUMENT;
+  if (M == 0) return PPS_OK;
+  if (!a || !w || !c || ((uintptr_t)a & 15) || ((uintptr_t)w & 15) || ((uintptr_t)c & 15))
+    return PPS_ERR_INVALID_ARGUMENT;
+  cudaError_t e;
+  int32_t* err = error_word(&e);
+  if (!err) return PPS_ERR_CUDA;
+  return pps::launch_gemm_bf16(a, w, c, M, N, K, err, stream) ? PPS_ERR_CUDA : PPS_OK;
+}
+
 pps_status pps_attn_run(const pps_plan* plan, const void* q, const pps_pool* pool, void* out,
                         void* workspace, size_t workspace_bytes, void* stream) {
   return run_impl(plan, q, pool, out, workspace, workspace_bytes, stream, nullptr);

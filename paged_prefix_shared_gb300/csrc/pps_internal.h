@@ -110,6 +110,9 @@ int launch_kv_append(const pps_pool& pool, const void* k_new, const void* v_new,
 int launch_copy_slots(const pps_pool& pool, const int32_t* src_pages, const int32_t* dst_pages,
                       const int32_t* num_slots, int32_t count, int32_t* err, void* stream);
 
+int launch_gemm_bf16(const void* a, const void* w, void* c, int32_t M, int32_t N, int32_t K,
+                     int32_t* err, void* stream);
+
 int launch_bw_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
                         const pps_pool& pool, void* out, int32_t* err, void* stream);
 
