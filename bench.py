@@ -51,6 +51,8 @@ DESCRIPTIONS = {
                       "suffix U[32,256], outputs U[16,128]; 25% verify 4-token drafts, the rest "
                       "decode; chunked prefill; 32/8 heads, d 128, P 16, 262144-page pool, LRU, "
                       "seed 7",
+    "projections": "QKV (N 6144) and O (N 4096) projection GEMMs of a mixed batch of 8229 tokens, "
+                   "hidden 4096, bf16, virtual padding of the ragged last tile, seed 8",
     "tree_verify": "128 requests each verifying a 64-token random draft tree (parent of token j "
                    "uniform in [0, j)), cached kv uniform [512,4096], 32/8, d 128, P 16, seed 5",
 }
@@ -833,6 +835,138 @@ def cache_serving_cpu_baseline(trace, budget_s=15.0, steps=None):
                       f"{os.environ.get('OPENBLAS_NUM_THREADS', 'all')} of {cores} cores"}
 
 
+def run_projections(args):
+    """The projections workload: the QKV (6144 outputs) and O (4096 outputs)
+    GEMMs of a mixed batch of 8192 + 37 tokens, hidden 4096, through
+    pps_gemm_bf16.  One step = both GEMMs."""
+    import numpy as np
+    import torch
+
+    import paged_prefix_shared_gb300 as pps
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pps.build()
+    M, K, shapes = 8229, 4096, (6144, 4096)
+    g = torch.Generator(device=dev)
+    g.manual_seed(8 + 1000 * rank)
+    a = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+    ws = [(torch.randn((N, K), generator=g, device=dev) / K ** 0.5).to(torch.bfloat16)
+          for N in shapes]
+    cs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for N in shapes]
+    stream = torch.cuda.current_stream()
+    flops = sum(2.0 * M * N * K for N in shapes)
+
+    def step():
+        for w, c in zip(ws, cs):
+            pps.gemm_bf16(a, w, c)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    n0 = pps.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.mark("t0")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("t1")
+    barrier(world)
+    launches = pps.launch_count() - n0
+    clocks = sampler.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    value = sum_over_ranks(M, world, dev) / (ms / 1e3)
+    tf = flops / (ms / 1e3) / 1e12
+    # e2e: activations in from pinned host memory, outputs back
+    ha = a.cpu().pin_memory()
+    hc = [torch.empty(c.shape, dtype=c.dtype).pin_memory() for c in cs]
+    k_e2e = max(3, args.steps // 2)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(k_e2e):
+        a.copy_(ha, non_blocking=True)
+        step()
+        for c, h in zip(cs, hc):
+            h.copy_(c, non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(f0.elapsed_time(f1) / k_e2e, world, dev)
+    # library GEMM on the same shapes, for context only
+    cub = []
+    for w in ws:
+        torch.matmul(a, w.t())
+        torch.cuda.synchronize()
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        for _ in range(10):
+            torch.matmul(a, w.t())
+        x1.record(stream)
+        torch.cuda.synchronize()
+        cub.append(x0.elapsed_time(x1) / 10)
+    peaks, peak_src = load_peaks()
+    peak = peaks.get("bf16_tflops", 1900.0)
+    result = {
+        "metric": "projection GEMM tokens/s and achieved tensor TFLOPS vs GB300 roofline",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, "
+        "N(0,1/K) weights; no trained weights)",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                   "tokens_per_step": M, "flop_per_step": flops,
+                   "l2": "inputs (67 MB activations + 88 MB weights) about L2-sized; no flush: "
+                         "warm-L2 figure, as the projections of one step are",
+                   "parallelism": f"dp{world} (independent batch per GPU, no collective)"},
+        "e2e": {"value": sum_over_ranks(M, world, dev) / (ms_e2e / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": M * K * 2,
+                "d2h_bytes_per_step": sum(M * N * 2 for N in shapes), "ms_per_step": ms_e2e},
+        "gpu_launches": launches,
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tf / peak, "traffic": None, "kernel": "tcgen05 projection GEMM",
+                     "algorithmic": f"{flops:.4g} FLOP per step (2*M*N*K, QKV and O)",
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json, burst)"},
+        "library_gemm_ms": {"qkv": cub[0], "o": cub[1],
+                            "tflops": flops / (sum(cub) / 1e3) / 1e12},
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = projections_cpu_baseline(a, ws, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def projections_cpu_baseline(a, ws, budget_s=15.0):
+    """The fp64 oracle (oracle.gemm.linear) on row blocks of the same batch
+    until about budget_s seconds; tokens/s = rows through both GEMMs / time."""
+    from oracle import gemm as og
+    cores = len(os.sched_getaffinity(0))
+    wc = [w.cpu() for w in ws]
+    rows, t0, blk = 0, time.perf_counter(), 64
+    while time.perf_counter() - t0 < budget_s and rows < a.shape[0]:
+        ab = a[rows:rows + blk].cpu()
+        for w in wc:
+            og.linear(ab, w)
+        rows += ab.shape[0]
+    secs = time.perf_counter() - t0
+    return {"value": rows / secs, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows} of {a.shape[0]} rows through both GEMMs in {secs:.1f} s; numpy "
+                      f"fp64 matmul with BLAS threads = "
+                      f"{os.environ.get('OPENBLAS_NUM_THREADS', 'all')} of {cores} cores"}
+
+
 def _oracle_sample_time(wl, reqs, step):
     """Oracle wall time (s) and tokens for a subset of requests of one step."""
     from oracle_run import oracle_steps
@@ -888,6 +1022,28 @@ def run_reference(args):
             "ms_per_step": wall / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded token ids and N(0,1) bf16 Q/K/V rows; no dataset)",
+            "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                       "parallelism": "host cores, rank 0 only"},
+            "cpu_baseline": base,
+            "e2e": {"value": base["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
+    if args.workload == "projections":
+        cores = len(os.sched_getaffinity(0))
+        g = torch.Generator().manual_seed(8)
+        M, K = 8229, 4096
+        a = torch.randn((M, K), generator=g).to(torch.bfloat16)
+        ws = [(torch.randn((N, K), generator=g) / K ** 0.5).to(torch.bfloat16) for N in (6144, 4096)]
+        t0 = time.perf_counter()
+        base = projections_cpu_baseline(a, ws, budget_s=args.cpu_seconds)
+        wall = time.perf_counter() - t0
+        print(json.dumps({
+            "impl": "reference", "metric": "projection GEMM tokens/s and achieved tensor TFLOPS "
+            "vs GB300 roofline", "value": base["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) activations, N(0,1/K) weights)",
             "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
                        "parallelism": "host cores, rank 0 only"},
             "cpu_baseline": base,
@@ -953,6 +1109,8 @@ def main():
         run_reference(args)
     elif args.workload in ("cache_serving", "engine_serving"):
         run_cache_serving(args)
+    elif args.workload == "projections":
+        run_projections(args)
     else:
         run_pps(args)
 
