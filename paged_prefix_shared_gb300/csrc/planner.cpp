@@ -21,6 +21,23 @@ namespace {
 
 using pps::Task;
 
+// Per-thread page stamps reused across calls (no per-plan allocation of a
+// pool-sized array): entry p is "set in this pass" when it equals the pass's
+// epoch.
+thread_local std::vector<uint32_t> g_page_stamp;
+thread_local uint32_t g_epoch = 0;
+uint32_t next_epoch(int32_t num_pages) {
+  if (g_page_stamp.size() < (size_t)num_pages) {
+    g_page_stamp.assign((size_t)num_pages, 0);
+    g_epoch = 0;
+  }
+  if (++g_epoch == 0) {                       // wrapped: start over
+    std::fill(g_page_stamp.begin(), g_page_stamp.end(), 0);
+    g_epoch = 1;
+  }
+  return g_epoch;
+}
+
 struct Segment {       // KV positions [kv_begin, kv_end) of one page list, with query tokens
   int32_t row_off;     // first token in the rows array
   int32_t n_tok;
@@ -199,6 +216,19 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
         if (q > 0 && full[r] > 0) cand.push_back(r);
       }
       auto seq = [&](int32_t r) { return page_indices + page_indptr[r]; };
+      // A group needs two requests whose first cached pages are the same; with
+      // none, the sort below has nothing to find.
+      {
+        uint32_t ep = next_epoch(num_pages);
+        uint32_t* stamp = g_page_stamp.data();     // thread-local lookups hoisted
+        bool any = false;
+        for (int32_t r : cand) {
+          uint32_t& m = stamp[seq(r)[0]];
+          if (m == ep) { any = true; break; }
+          m = ep;
+        }
+        if (!any) cand.clear();
+      }
       std::sort(cand.begin(), cand.end(), [&](int32_t a, int32_t b) {
         const int32_t n = std::min(full[a], full[b]);
         const int32_t* pa = seq(a);
@@ -335,35 +365,69 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
     }
 
     // ---- 4. partial slots and merge lists ------------------------------------------
+    // A task set writes its rows directly when each of its tokens is covered by
+    // this set alone; otherwise every token of the set gets a partial slot, and
+    // the merge lists (CSR over the tokens in increasing order, slots in task
+    // order) name them.  Built in three passes over flat arrays.
     std::vector<int32_t> pieces(T, 0);
     for (const auto& ts : sets)
       for (int32_t i = 0; i < ts.n_tok; ++i) ++pieces[rows[ts.row_off + i]];
-    std::vector<std::vector<int32_t>> tok_pids(T);
-    int64_t next_pid = 0;
-    for (auto& ts : sets) {
-      bool direct = true;
-      for (int32_t i = 0; i < ts.n_tok; ++i) direct &= pieces[rows[ts.row_off + i]] == 1;
-      if (direct) continue;
-      ts.out_pid = (int32_t)next_pid;
-      for (int32_t i = 0; i < ts.n_tok; ++i) tok_pids[rows[ts.row_off + i]].push_back((int32_t)(next_pid + i));
-      next_pid += ts.n_tok;
+    std::vector<uint8_t> direct(sets.size(), 1);
+    std::vector<int32_t> slots(T + 1, 0);             // partial slots per token, then offsets
+    for (size_t k = 0; k < sets.size(); ++k) {
+      const auto& ts = sets[k];
+      for (int32_t i = 0; i < ts.n_tok; ++i)
+        if (pieces[rows[ts.row_off + i]] != 1) { direct[k] = 0; break; }
+      if (!direct[k])
+        for (int32_t i = 0; i < ts.n_tok; ++i) ++slots[rows[ts.row_off + i] + 1];
     }
     std::vector<int32_t> m_tok, m_ptr{0}, m_pid;
+    std::vector<int32_t> first(T, 0);                 // token -> first slot in m_pid
     for (int32_t t = 0; t < T; ++t) {
-      if (tok_pids[t].empty()) continue;
+      if (!slots[t + 1]) continue;
+      first[t] = m_ptr.back();
       m_tok.push_back(t);
-      m_pid.insert(m_pid.end(), tok_pids[t].begin(), tok_pids[t].end());
-      m_ptr.push_back((int32_t)m_pid.size());
+      m_ptr.push_back(m_ptr.back() + slots[t + 1]);
+    }
+    m_pid.resize((size_t)m_ptr.back());
+    std::fill(slots.begin(), slots.end(), 0);         // now: slots filled per token
+    int64_t next_pid = 0;
+    for (size_t k = 0; k < sets.size(); ++k) {
+      auto& ts = sets[k];
+      if (direct[k]) continue;
+      ts.out_pid = (int32_t)next_pid;
+      for (int32_t i = 0; i < ts.n_tok; ++i) {
+        const int32_t t = rows[ts.row_off + i];
+        m_pid[first[t] + slots[t]++] = (int32_t)(next_pid + i);
+      }
+      next_pid += ts.n_tok;
     }
 
     // ---- 5. sort by work (descending), deterministic ties ---------------------------
-    std::stable_sort(sets.begin(), sets.end(), [](const TaskSet& a, const TaskSet& b) {
-      if (a.mma != b.mma) return a.mma < b.mma;
-      if (a.work != b.work) return a.work > b.work;
-      if (a.key != b.key) return a.key < b.key;
-      if (a.tile != b.tile) return a.tile < b.tile;
-      return a.chunk < b.chunk;
-    });
+    // Order: bandwidth before tensor-core sets, then work descending, then
+    // (key, tile, chunk), which identify a set, so the order is total.
+    {
+      struct SortKey {
+        uint64_t a, b;
+        uint32_t c, idx;
+      };
+      std::vector<SortKey> keys(sets.size());
+      for (size_t k = 0; k < sets.size(); ++k) {
+        const TaskSet& t = sets[k];
+        keys[k].a = ((uint64_t)t.mma << 63) | (((uint64_t)1 << 62) - 1 - (uint64_t)t.work);
+        keys[k].b = ((uint64_t)(uint32_t)t.key << 32) | (uint32_t)t.tile;
+        keys[k].c = (uint32_t)t.chunk;
+        keys[k].idx = (uint32_t)k;
+      }
+      std::sort(keys.begin(), keys.end(), [](const SortKey& x, const SortKey& y) {
+        if (x.a != y.a) return x.a < y.a;
+        if (x.b != y.b) return x.b < y.b;
+        return x.c < y.c;
+      });
+      std::vector<TaskSet> sorted(sets.size());
+      for (size_t k = 0; k < sets.size(); ++k) sorted[k] = sets[keys[k].idx];
+      sets.swap(sorted);
+    }
     std::vector<Task> bw, mm;
     for (const auto& ts : sets) {
       if (!ts.mma) plan->shape.bw_rows_max = std::max(plan->shape.bw_rows_max, ts.n_tok * G);
@@ -376,7 +440,7 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
     // ---- 6. statistics ---------------------------------------------------------------
     const int64_t tok_bytes = 2LL * num_kv_heads * head_dim * 2;   // K+V, all kv heads
     {
-      std::vector<uint8_t> seen((size_t)num_pages, 0);
+      std::vector<uint8_t> seen((size_t)num_pages, 0);   // valid slots counted per page
       int64_t slots = 0;
       for (int32_t r = 0; r < R; ++r) {
         const int64_t need = ceil_div(kv_len[r], P);
@@ -441,15 +505,19 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
     plan->image = pps::host_buf_acquire((size_t)plan->image_ints);
     if (!plan->image.data) throw std::bad_alloc();
     int32_t* img = plan->image.data;
-    std::memset(img, 0, (size_t)plan->image_ints * 4);
-    if (!bw.empty()) std::memcpy(img + L.bw_tasks, bw.data(), bw.size() * sizeof(Task));
-    if (!mm.empty()) std::memcpy(img + L.mma_tasks, mm.data(), mm.size() * sizeof(Task));
-    if (!rows.empty()) std::memcpy(img + L.rows, rows.data(), rows.size() * 4);
-    if (nnz) std::memcpy(img + L.pages, page_indices, (size_t)nnz * 4);
-    if (!m_tok.empty()) std::memcpy(img + L.merge_tokens, m_tok.data(), m_tok.size() * 4);
-    std::memcpy(img + L.merge_indptr, m_ptr.data(), m_ptr.size() * 4);
-    if (!m_pid.empty()) std::memcpy(img + L.merge_pids, m_pid.data(), m_pid.size() * 4);
-    if (plan->has_tree) std::memcpy(img + L.tree_mask, tmask.data(), tmask.size() * 8);
+    // Each section is copied in and the alignment gap after it zeroed.
+    auto put = [&](int64_t at, const void* src, int64_t ints, int64_t end) {
+      if (ints) std::memcpy(img + at, src, (size_t)ints * 4);
+      if (end > at + ints) std::memset(img + at + ints, 0, (size_t)(end - at - ints) * 4);
+    };
+    put(L.bw_tasks, bw.data(), (int64_t)bw.size() * PPS_TASK_INTS, L.mma_tasks);
+    put(L.mma_tasks, mm.data(), (int64_t)mm.size() * PPS_TASK_INTS, L.rows);
+    put(L.rows, rows.data(), (int64_t)rows.size(), L.pages);
+    put(L.pages, page_indices, nnz, L.merge_tokens);
+    put(L.merge_tokens, m_tok.data(), (int64_t)m_tok.size(), L.merge_indptr);
+    put(L.merge_indptr, m_ptr.data(), (int64_t)m_ptr.size(), L.merge_pids);
+    put(L.merge_pids, m_pid.data(), (int64_t)m_pid.size(), L.tree_mask);
+    put(L.tree_mask, tmask.data(), plan->has_tree ? 2LL * T : 0, plan->image_ints);
 
     plan->num_bw = (int64_t)bw.size();
     plan->num_mma = (int64_t)mm.size();
