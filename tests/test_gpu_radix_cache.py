@@ -170,3 +170,100 @@ def test_copy_slots_is_bit_exact_and_checks_ids(pps):
     torch.cuda.synchronize()
     assert pps.get_device_error(clear=True) == 5                # PPS_DEV_ERR_COPY_ARGUMENT
     assert torch.equal(pk.view(torch.int16), before.view(torch.int16))
+
+
+@pytest.mark.parametrize("budget,reserved", [(96, 16), (40, 8)])
+def test_scheduler_and_cache_drive_chunked_steps(pps, budget, reserved):
+    """The engine loop: the token-wise scheduler picks each step's tokens
+    (whole generation steps, including 3-token verify drafts, then chunks of
+    pending prompts within the budget), the prefix cache holds the pages
+    (copy-on-write at admission), and every scheduled token's output is
+    checked against the oracle on the request's contiguous K/V."""
+    rng = np.random.default_rng(21)
+    tabs = _tables(3, max_pos=1024)
+    num_pages = 96
+    cache = pps.Cache(num_pages, P)
+    sched = pps.Scheduler(budget, reserved)
+    pool_k = torch.full((num_pages, Hkv, P, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pool_v = torch.full_like(pool_k, float("nan"))
+    prompts = [list(rng.integers(0, VOCAB, size=int(rng.integers(30, 120)))) for _ in range(3)]
+    state = {}                      # rid -> dict(tokens, cached0, done, gen_k, produced, goal)
+    pps.get_device_error(clear=True)
+    checked = 0
+    for step in range(40):
+        for _ in range(int(rng.integers(0, 3))):
+            if len(state) >= 6:
+                break
+            base = prompts[int(rng.integers(len(prompts)))]
+            toks = base[:int(rng.integers(1, len(base) + 1))] + \
+                list(rng.integers(0, VOCAB, size=int(rng.integers(1, 70))))
+            try:
+                rid, cached, copy = cache.begin(toks)
+            except pps.CacheFull:
+                continue
+            if copy is not None:
+                c3 = torch.tensor([copy], dtype=torch.int32, device="cuda")
+                pps.copy_slots(pool_k, pool_v, c3[:, 0].contiguous(), c3[:, 1].contiguous(),
+                               c3[:, 2].contiguous())
+            k = int(rng.choice([1, 3]))
+            sched.add(rid, len(toks) - cached, k)
+            state[rid] = dict(tokens=list(toks), cached0=cached, done=0, gen_k=k, produced=0,
+                              goal=int(rng.integers(2, 12)))
+        req, tok, pre = sched.step()
+        if len(req) == 0:
+            continue
+        batch = []                  # (rid, first position, tokens this step)
+        for r, k, p in zip(req.tolist(), tok.tolist(), pre.tolist()):
+            s = state[r]
+            if p:
+                first = s["cached0"] + s["done"]
+                s["done"] += k
+            else:
+                new = list(rng.integers(0, VOCAB, size=k))
+                try:
+                    first = cache.extend(r, new)
+                except pps.CacheFull:
+                    continue
+                s["tokens"] += new
+                s["produced"] += k
+            batch.append((r, first, k))
+        if not batch:
+            continue
+        q_len = [k for _, _, k in batch]
+        q_indptr = np.concatenate([[0], np.cumsum(q_len)]).astype(np.int32)
+        cached = np.array([f for _, f, _ in batch], np.int32)
+        kv_len = cached + np.array(q_len, np.int32)
+        plists = [cache.pages(r) for r, _, _ in batch]
+        page_indptr = np.concatenate([[0], np.cumsum([len(p) for p in plists])]).astype(np.int32)
+        page_indices = np.concatenate(plists).astype(np.int32)
+        ks, vs = [], []
+        for (r, f, k) in batch:
+            kk, vv = _kv(tabs, state[r]["tokens"][f:f + k], range(f, f + k))
+            ks.append(kk)
+            vs.append(vv)
+        T = int(q_indptr[-1])
+        dev = lambda a: torch.as_tensor(a, dtype=torch.int32, device="cuda")
+        pps.kv_append(pool_k, pool_v, torch.cat(ks).cuda(), torch.cat(vs).cuda(), dev(q_indptr),
+                      dev(cached), dev(page_indptr), dev(page_indices))
+        q = torch.randn((T, Hq, D), generator=torch.Generator().manual_seed(100 + step)) \
+            .to(torch.bfloat16)
+        plan = pps.attn_plan(q_indptr, kv_len, page_indptr, page_indices, Hq, Hkv, D, P, num_pages)
+        ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+        out = torch.full((T, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        pps.attn_run(plan, q.cuda(), pool_k, pool_v, out, ws)
+        torch.cuda.synchronize()
+        assert pps.get_device_error(clear=True) == 0
+        for i, (r, f, k) in enumerate(batch):
+            a, b = int(q_indptr[i]), int(q_indptr[i + 1])
+            ref = _reference(q[a:b], state[r]["tokens"][:f + k], f, tabs)
+            mx, mean = errors(out[a:b], ref)
+            assert mx <= MAX_ABS and mean <= MEAN_ABS, (step, r, mx, mean)
+            checked += 1
+        for r in list(state):
+            s = state[r]
+            if s["done"] == len(s["tokens"]) - s["cached0"] - s["produced"] and \
+                    s["produced"] >= s["goal"]:
+                sched.remove(r)
+                cache.finish(r)
+                del state[r]
+    assert checked > 20
