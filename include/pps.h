@@ -11,6 +11,16 @@
  *
  * for every request r, new token j (absolute position c_r + j, c_r = tokens
  * cached before the step) and query head h, G = num_q_heads / num_kv_heads.
+ * Verify rows may also form a draft tree (pps_attn_plan_tree): a draft token
+ * then sees the cached positions, its ancestors and itself.
+ *
+ * Around that path the library also provides the steps that feed it and the
+ * GEMMs of the same batch:
+ *  - pps_cache_*   host radix-tree prefix cache + page allocator producing the
+ *                  page tables (token-wise reuse, copy-on-write via
+ *                  pps_copy_slots, LRU / LFU eviction);
+ *  - pps_sched_*   token-wise budget scheduler forming each step's batch;
+ *  - pps_gemm_bf16 virtual-padded projection GEMM for the batch's token rows.
  *
  * Sources (page title and section):
  *  - XY-Serve review, "Tackling the Dynamicity in a Production LLM Serving

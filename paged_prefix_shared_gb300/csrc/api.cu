@@ -317,6 +317,6 @@ const char* pps_status_string(pps_status s) {
   }
 }
 
-int32_t pps_version(void) { return 100; }
+int32_t pps_version(void) { return 200; }
 
 }  // extern "C"
