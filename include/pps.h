@@ -293,6 +293,27 @@ pps_status pps_sched_counts(const pps_sched* sched, int32_t* prefill_requests,
 pps_status pps_gemm_bf16(const void* a, const void* w, void* c, int32_t M, int32_t N, int32_t K,
                          void* stream);
 
+/*
+ * pps_partition -- split one batch over num_parts GPUs so that no data has to
+ * move between them: every radix subtree (the requests whose first whole
+ * cached page is the same page, i.e. that share a cached prefix) stays on one
+ * GPU, where its shared pages are still read once, and the subtrees are
+ * balanced by work.  XY-Serve review, "What carries the argument" (work sorted
+ * by area and spread so every core gets a fair share); SGLang review, "Core
+ * claim" (prefix reuse).  Rules:
+ *  - a request with no whole cached page is a subtree of its own;
+ *  - work of a request = max(1, new tokens) x kv_len; of a subtree, the sum;
+ *  - subtrees by work, largest first (ties: lowest request id in it), each to
+ *    the part with the least work so far (ties: lowest part).
+ * Host arrays as in pps_attn_plan; out_part [num_requests] receives the part
+ * of each request, out_load [num_parts] (optional) the work of each part.
+ * Each GPU then plans and runs its own requests (no collective).
+ */
+pps_status pps_partition(const int32_t* q_indptr, const int32_t* kv_len,
+                         const int32_t* page_indptr, const int32_t* page_indices,
+                         int32_t num_requests, int32_t page_size, int32_t num_parts,
+                         int32_t* out_part, int64_t* out_load);
+
 /* Optional planner knobs; pass NULL for defaults.  Zero fields take defaults. */
 typedef struct pps_plan_options {
   int32_t num_sms;          /* SMs to balance over; 0 = query the current device (152 if none) */

@@ -100,6 +100,9 @@ def lib():
     L.pps_attn_run.argtypes = [vp, vp, ctypes.POINTER(_Pool), vp, vp, sz, vp]
     L.pps_copy_slots.argtypes = [ctypes.POINTER(_Pool), vp, vp, vp, i32, vp]
     L.pps_gemm_bf16.argtypes = [vp, vp, vp, i32, i32, i32, vp]
+    L.pps_partition.argtypes = [_I32P, _I32P, _I32P, _I32P, i32, i32, i32, _I32P,
+                                ctypes.POINTER(ctypes.c_int64)]
+    L.pps_partition.restype = i32
     L.pps_gemm_bf16.restype = i32
     L.pps_cache_create.argtypes = [i32, i32, i32, ctypes.POINTER(vp)]
     L.pps_cache_destroy.argtypes = [vp]
@@ -533,3 +536,18 @@ def gemm_bf16(a, w, c, stream=None):
     _check(lib().pps_gemm_bf16(_dev(a, torch.bfloat16), _dev(w, torch.bfloat16),
                                _dev(c, torch.bfloat16), int(M), int(N), int(K), _stream(stream)),
            "pps_gemm_bf16")
+
+
+def partition(q_indptr, kv_len, page_indptr, page_indices, page_size, num_parts):
+    """pps_partition: (part of each request, work of each part)."""
+    qi, qi_p = _host_i32(q_indptr)
+    kl, kl_p = _host_i32(kv_len)
+    pi, pi_p = _host_i32(page_indptr)
+    px, px_p = _host_i32(page_indices if len(page_indices) else np.zeros(1, np.int32))
+    part = np.zeros(max(len(kl), 1), np.int32)
+    load = np.zeros(int(num_parts), np.int64)
+    _check(lib().pps_partition(qi_p, kl_p, pi_p, px_p, len(kl), int(page_size), int(num_parts),
+                               part.ctypes.data_as(_I32P),
+                               load.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))),
+           "pps_partition")
+    return part[:len(kl)], load

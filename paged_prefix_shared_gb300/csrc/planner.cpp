@@ -14,6 +14,7 @@
 #include <cstring>
 #include <new>
 #include <numeric>
+#include <unordered_map>
 
 #include "pps_internal.h"
 
@@ -589,6 +590,66 @@ extern "C" pps_status pps_plan_get_array(const pps_plan* p, int32_t which, const
       *count = p->has_tree ? 2LL * p->num_tokens : 0;
       break;
     default: return PPS_ERR_INVALID_ARGUMENT;
+  }
+  return PPS_OK;
+}
+
+// Batch partition over GPUs (pps_partition): radix subtrees whole, greedy by
+// work, largest first.  Rules in pps.h.
+extern "C" pps_status pps_partition(const int32_t* q_indptr, const int32_t* kv_len,
+                                    const int32_t* page_indptr, const int32_t* page_indices,
+                                    int32_t num_requests, int32_t page_size, int32_t num_parts,
+                                    int32_t* out_part, int64_t* out_load) {
+  if (num_requests < 0 || num_parts <= 0 || page_size <= 0 || !out_part ||
+      (num_requests > 0 && (!q_indptr || !kv_len || !page_indptr)))
+    return PPS_ERR_INVALID_ARGUMENT;
+  try {
+    const int32_t R = num_requests;
+    struct Sub {
+      int64_t work = 0;
+      int32_t first_req = 0;
+      std::vector<int32_t> members;
+    };
+    std::vector<Sub> subs;
+    std::unordered_map<int32_t, int32_t> by_page;          // first cached page -> subtree
+    for (int32_t r = 0; r < R; ++r) {
+      const int32_t q = q_indptr[r + 1] - q_indptr[r];
+      if (q < 0 || kv_len[r] < q) return PPS_ERR_INVALID_ARGUMENT;
+      const int32_t cached = kv_len[r] - q;
+      int32_t id = -1;
+      if (cached >= page_size) {
+        if (!page_indices || page_indptr[r + 1] <= page_indptr[r]) return PPS_ERR_PAGE_TABLE;
+        const int32_t pg = page_indices[page_indptr[r]];
+        auto it = by_page.find(pg);
+        if (it != by_page.end()) id = it->second;
+        else by_page.emplace(pg, id = (int32_t)subs.size());
+      }
+      if (id < 0 || id == (int32_t)subs.size()) {
+        id = (int32_t)subs.size();
+        subs.emplace_back();
+        subs.back().first_req = r;
+      }
+      subs[id].work += (int64_t)std::max(1, q) * kv_len[r];
+      subs[id].members.push_back(r);
+    }
+    std::vector<int32_t> order(subs.size());
+    std::iota(order.begin(), order.end(), 0);
+    std::sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
+      if (subs[a].work != subs[b].work) return subs[a].work > subs[b].work;
+      return subs[a].first_req < subs[b].first_req;
+    });
+    std::vector<int64_t> load((size_t)num_parts, 0);
+    for (int32_t k : order) {
+      int32_t best = 0;
+      for (int32_t p = 1; p < num_parts; ++p)
+        if (load[p] < load[best]) best = p;
+      load[best] += subs[k].work;
+      for (int32_t r : subs[k].members) out_part[r] = best;
+    }
+    if (out_load)
+      for (int32_t p = 0; p < num_parts; ++p) out_load[p] = load[p];
+  } catch (const std::bad_alloc&) {
+    return PPS_ERR_NO_MEMORY;
   }
   return PPS_OK;
 }
