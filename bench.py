@@ -435,12 +435,13 @@ class CacheServer:
     the cache produced.  New K/V/Q rows are slices of seeded device buffers."""
 
     def __init__(self, pps, torch, dev, trace, num_pages=131072, page_size=16, num_q_heads=32,
-                 num_kv_heads=8, head_dim=128, active=256, max_rows=65536, seed=6):
+                 num_kv_heads=8, head_dim=128, active=256, max_rows=65536, seed=6,
+                 make_cache=True):
         self.pps, self.torch, self.dev = pps, torch, dev
         self.prompts, self.reqs = trace
         self.P, self.Hq, self.Hkv, self.D = page_size, num_q_heads, num_kv_heads, head_dim
         self.num_pages, self.target, self.max_rows = num_pages, active, max_rows
-        self.cache = pps.Cache(num_pages, page_size)
+        self.cache = pps.Cache(num_pages, page_size) if make_cache else None
         bf = torch.bfloat16
         self.pk = torch.zeros((num_pages, num_kv_heads, page_size, head_dim), dtype=bf, device=dev)
         self.pv = torch.zeros_like(self.pk)
@@ -471,6 +472,13 @@ class CacheServer:
         self.host_s = 0.0                     # host time inside cache calls
         self.cache_calls = 0
         self.io = None                        # (pinned q/k/v rows, pinned out) for the e2e run
+
+    def warm_prefix(self, tokens):
+        rid, _, _ = self.cache.begin(tokens)
+        self.cache.finish(rid)
+
+    def stats(self):
+        return self.cache.stats()
 
     def step(self, admit, events=None):
         import numpy as np
@@ -579,76 +587,78 @@ class CacheServer:
 
 
 class EngineServer(CacheServer):
-    """Scheduler + prefix cache + attention: every step the token-wise
-    scheduler (pps_sched_*) picks the batch within a token budget: the
-    generation requests (decode: 1 token; speculative verify: a draft of
-    ``draft`` tokens, all accepted), then chunks of pending prompts (the part
-    the prefix cache did not already hold).  Requests are admitted (cache
-    begin + scheduler add) while fewer than ``active`` are in the system."""
+    """Scheduler + prefix cache + attention through the native serving-step
+    runtime (pps_engine_*): every step pps_engine_schedule picks the batch
+    within a token budget (the generation requests, decode: 1 token,
+    speculative verify: a draft of ``draft`` tokens, all accepted; then chunks
+    of pending prompts, the part the prefix cache did not already hold), and
+    pps_engine_commit appends the generated tokens and writes the batch's
+    tables.  Requests are admitted (pps_engine_add) while fewer than
+    ``active`` are in the system."""
 
     def __init__(self, pps, torch, dev, trace, budget=8192, reserved=512, draft=4,
                  verify_frac=0.25, admit_max=32, **kw):
         import numpy as np
-        super().__init__(pps, torch, dev, trace, **kw)
-        self.sched = pps.Scheduler(budget, reserved)
+        super().__init__(pps, torch, dev, trace, make_cache=False, **kw)
+        self.eng = pps.Engine(self.num_pages, self.P, budget, reserved)
         self.draft, self.admit_max = draft, admit_max
         rng = np.random.default_rng(17)
         self.gen_k = np.where(rng.random(len(self.reqs)) < verify_frac, draft, 1).astype(np.int32)
         pad = np.zeros((len(self.reqs), draft), np.int32)
         self.out_tok = np.concatenate([self.out_tok, pad], axis=1)
-        self.info = {}                       # rid -> [trace index, cached0, prompt done, produced]
-        self.in_system = 0
+        # per request id (ids are handed out in admission order): trace index,
+        # generated tokens so far; ids of the requests in the system
+        n = len(self.reqs) + len(self.prompts) + 1
+        self.r_idx = np.zeros(n, np.int32)
+        self.r_prod = np.zeros(n, np.int32)
+        self.live = np.zeros(0, np.int32)
+
+    def warm_prefix(self, tokens):
+        rid, _, _ = self.eng.add(tokens)
+        self.eng.finish(rid)
+
+    def stats(self):
+        return self.eng.stats()
 
     def step(self, admit=None, events=None):
         import numpy as np
         t0 = time.perf_counter()
-        cache, sched = self.cache, self.sched
+        eng = self.eng
         # retire requests that produced all their outputs
-        for rid in [r for r, v in self.info.items() if v[3] >= self.out_len[v[0]]]:
-            cache.finish(rid)
-            sched.remove(rid)
-            del self.info[rid]
-            self.cache_calls += 1
-        copies = []
-        n_adm = 0
-        while len(self.info) < self.target and n_adm < self.admit_max and \
+        if len(self.live):
+            done = self.r_prod[self.live] >= self.out_len[self.r_idx[self.live]]
+            for rid in self.live[done].tolist():
+                eng.finish(rid)
+            self.cache_calls += int(done.sum())
+            self.live = self.live[~done]
+        copies, new = [], []
+        while len(self.live) + len(new) < self.target and len(new) < self.admit_max and \
                 self.next_req < len(self.reqs):
             i = self.next_req
             self.next_req += 1
-            rid, cached, copy = cache.begin(self.reqs[i][1])
+            rid, cached, copy = eng.add(self.reqs[i][1], int(self.gen_k[i]))
             if copy is not None:
                 copies.append(copy)
-            sched.add(rid, len(self.reqs[i][1]) - cached, int(self.gen_k[i]))
-            self.info[rid] = [i, cached, 0, 0]
-            n_adm += 1
-            self.cache_calls += 1
-        req, tok, pre = sched.step()
-        gen = ~pre.astype(bool)
-        g_rid = req[gen]
-        first = np.zeros(0, np.int32)
-        if len(g_rid):
-            idx = np.array([self.info[r][0] for r in g_rid], np.int32)
-            prod = np.array([self.info[r][3] for r in g_rid], np.int32)
-            k = tok[gen]
-            cols = prod[:, None] + np.arange(self.draft)[None, :]
-            mat = self.out_tok[idx[:, None], np.minimum(cols, self.out_tok.shape[1] - 1)]
-            keep = np.arange(self.draft)[None, :] < k[:, None]
-            toks = mat[keep].astype(np.int32)
-            indptr = np.concatenate([[0], np.cumsum(k)]).astype(np.int32)
-            first = cache.extend_batch(g_rid, indptr, toks)
-            for r, kk in zip(g_rid, k):
-                self.info[r][3] += int(kk)
-            self.cache_calls += len(g_rid)
-        kv_len, page_indptr, page_indices = cache.tables(req)
-        cached = np.zeros(len(req), np.int32)
-        cached[gen] = first
-        for j in np.nonzero(pre)[0]:
-            v = self.info[int(req[j])]
-            cached[j] = v[1] + v[2]
-            v[2] += int(tok[j])
-            kv_len[j] = cached[j] + tok[j]
+            self.r_idx[rid], self.r_prod[rid] = i, 0
+            new.append(rid)
+        if new:
+            self.live = np.concatenate([self.live, np.array(new, np.int32)])
+            self.cache_calls += len(new)
+        req, tok, pre = eng.schedule()
+        gen = pre == 0
+        g_rid, k = req[gen], tok[gen]
+        cols = self.r_prod[g_rid][:, None] + np.arange(self.draft)[None, :]
+        mat = self.out_tok[self.r_idx[g_rid][:, None], np.minimum(cols, self.out_tok.shape[1] - 1)]
+        toks = mat[np.arange(self.draft)[None, :] < k[:, None]].astype(np.int32)
+        rq, qi, cl, kl, pi, px = eng.commit(toks)
+        if len(rq) == len(req):
+            self.r_prod[g_rid] += k
+        else:                                  # some generation entries found no page
+            kept = np.isin(g_rid, rq)
+            self.r_prod[g_rid[kept]] += k[kept]
+        self.cache_calls += len(g_rid)
         self.host_s += time.perf_counter() - t0
-        return self._run_batch(kv_len, cached, page_indptr, page_indices, copies, events)
+        return self._run_batch(kl, cl, pi, px, copies, events)
 
 
 def run_cache_serving(args):
@@ -676,8 +686,7 @@ def run_cache_serving(args):
     stream = torch.cuda.current_stream()
     # warm up: every system prompt once, then fill the system
     for k in range(len(trace[0])):
-        rid, _, _ = srv.cache.begin(trace[0][k])
-        srv.cache.finish(rid)
+        srv.warm_prefix(trace[0][k])
     if engine:
         for _ in range(60):
             srv.step()
@@ -751,7 +760,7 @@ def run_cache_serving(args):
                                       "kv_bytes_read", "flops_total")}]
     qo = tokens / args.steps * 2 * srv.Hq * srv.D * 2
     roof = roofline(pps, kern_ms, avg_infos, qo, args.workload, sustained=False)
-    st = srv.cache.stats()
+    st = srv.stats()
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -778,7 +787,7 @@ def run_cache_serving(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cache_serving_cpu_baseline(trace, budget_s=args.cpu_seconds)
     if engine:
-        result["host_cache"]["scheduler"] = "pps_sched_* (budget 8192, reserved 512)"
+        result["host_cache"]["scheduler"] = "pps_engine_* (budget 8192, reserved 512)"
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:

@@ -314,6 +314,45 @@ pps_status pps_partition(const int32_t* q_indptr, const int32_t* kv_len,
                          int32_t num_requests, int32_t page_size, int32_t num_parts,
                          int32_t* out_part, int64_t* out_load);
 
+/*
+ * Serving-step runtime (pps_engine_*): a prefix cache (pps_cache_*) and a
+ * token-wise scheduler (pps_sched_*) kept together, so that one step of a
+ * serving loop is two native calls instead of a call per request:
+ *  1. pps_engine_schedule picks the batch: entries (request, tokens,
+ *     is_prefill), generation entries first (pps_sched_step).
+ *  2. pps_engine_commit takes the new token ids of the batch's generation
+ *     entries (concatenated in batch order: gen_tokens), appends them to the
+ *     cache, moves the prefill entries forward, and writes the tables of the
+ *     entries it kept, ready for pps_kv_append (cached_len) and pps_attn_plan
+ *     (kv_len, page CSR): out_requests[k], q_indptr[k + 1], cached_len[k],
+ *     kv_len[k], page_indptr[k + 1], page_indices.  A generation entry the cache
+ *     has no page for is left out (the scheduler picks it again next step).
+ *     page_capacity (entries of page_indices) must cover every entry's pages
+ *     plus 1 + tokens / page_size per generation entry; that bound is written
+ *     to *out_pages_needed (may be NULL) and checked before anything changes:
+ *     PPS_ERR_INVALID_ARGUMENT if it is short, the batch still pending.
+ * pps_engine_add admits a request (pps_cache_begin + pps_sched_add; copy as
+ * pps_cache_begin), pps_engine_finish retires one (pps_sched_remove +
+ * pps_cache_finish).  Neither may be called between schedule and commit.
+ * pps_engine_parts exposes the cache and the scheduler (owned by the engine)
+ * for their stats.  Host memory only; not thread safe.
+ */
+typedef struct pps_engine pps_engine;
+pps_status pps_engine_create(int32_t num_pages, int32_t page_size, int32_t cache_policy,
+                             int32_t budget, int32_t reserved, pps_engine** out_engine);
+pps_status pps_engine_destroy(pps_engine* engine);
+pps_status pps_engine_parts(pps_engine* engine, pps_cache** cache, pps_sched** sched);
+pps_status pps_engine_add(pps_engine* engine, const int32_t* tokens, int32_t n, int32_t gen_tokens,
+                          int32_t* out_request, int32_t* out_cached_len, int32_t* out_copy);
+pps_status pps_engine_finish(pps_engine* engine, int32_t request, int32_t insert);
+pps_status pps_engine_schedule(pps_engine* engine, int32_t* out_requests, int32_t* out_tokens,
+                               int32_t* out_is_prefill, int32_t capacity, int32_t* out_count);
+pps_status pps_engine_commit(pps_engine* engine, const int32_t* gen_tokens,
+                             int32_t* out_requests, int32_t* q_indptr, int32_t* cached_len,
+                             int32_t* kv_len, int32_t* page_indptr, int32_t* page_indices,
+                             int64_t page_capacity, int64_t* out_pages_needed,
+                             int32_t* out_count);
+
 /* Optional planner knobs; pass NULL for defaults.  Zero fields take defaults. */
 typedef struct pps_plan_options {
   int32_t num_sms;          /* SMs to balance over; 0 = query the current device (152 if none) */

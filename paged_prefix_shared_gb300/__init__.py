@@ -117,6 +117,17 @@ def lib():
     L.pps_cache_tables.argtypes = [vp, _I32P, i32, _I32P, _I32P, _I32P, ctypes.c_int64]
     for f in (L.pps_cache_extend_batch, L.pps_cache_tables):
         f.restype = i32
+    L.pps_engine_create.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(vp)]
+    L.pps_engine_destroy.argtypes = [vp]
+    L.pps_engine_parts.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp)]
+    L.pps_engine_add.argtypes = [vp, _I32P, i32, i32, _I32P, _I32P, _I32P]
+    L.pps_engine_finish.argtypes = [vp, i32, i32]
+    L.pps_engine_schedule.argtypes = [vp, _I32P, _I32P, _I32P, i32, _I32P]
+    L.pps_engine_commit.argtypes = [vp, _I32P, _I32P, _I32P, _I32P, _I32P, _I32P, _I32P,
+                                    ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), _I32P]
+    for f in (L.pps_engine_create, L.pps_engine_destroy, L.pps_engine_parts, L.pps_engine_add,
+              L.pps_engine_finish, L.pps_engine_schedule, L.pps_engine_commit):
+        f.restype = i32
     L.pps_sched_create.argtypes = [i32, i32, ctypes.POINTER(vp)]
     L.pps_sched_destroy.argtypes = [vp]
     L.pps_sched_add.argtypes = [vp, i32, i32, i32]
@@ -517,6 +528,114 @@ class Scheduler:
     def destroy(self):
         if self._h is not None:
             lib().pps_sched_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+class Engine:
+    """Owner of a pps_engine: a prefix cache and a token-wise scheduler driven
+    by two calls per serving step (schedule, then commit)."""
+
+    def __init__(self, num_pages, page_size, budget, reserved=0, policy=CACHE_LRU):
+        h = ctypes.c_void_p()
+        _check(lib().pps_engine_create(int(num_pages), int(page_size), int(policy), int(budget),
+                                       int(reserved), ctypes.byref(h)), "pps_engine_create")
+        self._h = h
+        self.page_size = int(page_size)
+        c, s = ctypes.c_void_p(), ctypes.c_void_p()
+        _check(lib().pps_engine_parts(h, ctypes.byref(c), ctypes.byref(s)), "pps_engine_parts")
+        self._cache, self._sched = c, s
+        self._cap = 1024
+        self._sb = [np.zeros(self._cap, np.int32) for _ in range(3)]
+        self._tb = [np.zeros(self._cap + 1, np.int32) for _ in range(5)]
+        self._px = np.zeros(1 << 16, np.int32)
+
+    def add(self, tokens, gen_tokens=1):
+        """Admits a prompt; returns (request id, cached_len, copy or None) as Cache.begin."""
+        t, tp = _host_i32(tokens)
+        rid, cached = ctypes.c_int32(), ctypes.c_int32()
+        cp = (ctypes.c_int32 * 3)()
+        code = lib().pps_engine_add(self._h, tp, len(t), int(gen_tokens), ctypes.byref(rid),
+                                    ctypes.byref(cached), cp)
+        if code == -8:
+            raise CacheFull(f"pps_engine_add: {status_string(code)}")
+        _check(code, "pps_engine_add")
+        return rid.value, cached.value, ((cp[0], cp[1], cp[2]) if cp[2] > 0 else None)
+
+    def finish(self, request, insert=True):
+        _check(lib().pps_engine_finish(self._h, int(request), int(bool(insert))),
+               "pps_engine_finish")
+
+    def counts(self):
+        a, b, c = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int32()
+        _check(lib().pps_sched_counts(self._sched, ctypes.byref(a), ctypes.byref(b),
+                                      ctypes.byref(c)), "pps_sched_counts")
+        return a.value, b.value, c.value
+
+    def stats(self) -> dict:
+        st = _CacheStats()
+        _check(lib().pps_cache_get_stats(self._cache, ctypes.byref(st)), "pps_cache_get_stats")
+        return {n: getattr(st, n) for n, _ in _CacheStats._fields_}
+
+    def pages(self, request):
+        ptr, n, nt = _I32P(), ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().pps_cache_request_pages(self._cache, int(request), ctypes.byref(ptr),
+                                             ctypes.byref(n), ctypes.byref(nt)),
+               "pps_cache_request_pages")
+        return np.ctypeslib.as_array(ptr, shape=(n.value,)).copy() if n.value else \
+            np.zeros(0, np.int32)
+
+    def schedule(self):
+        """(requests, tokens, is_prefill) of the next batch (views, valid until
+        the next call)."""
+        n = ctypes.c_int32()
+        while True:
+            r, t, p = self._sb
+            code = lib().pps_engine_schedule(self._h, r.ctypes.data_as(_I32P),
+                                             t.ctypes.data_as(_I32P), p.ctypes.data_as(_I32P),
+                                             self._cap, ctypes.byref(n))
+            if code == 0:
+                break
+            pr, _, gr = self.counts()
+            if pr + gr <= self._cap:
+                _check(code, "pps_engine_schedule")
+            self._cap = 2 * (pr + gr)
+            self._sb = [np.zeros(self._cap, np.int32) for _ in range(3)]
+            self._tb = [np.zeros(self._cap + 1, np.int32) for _ in range(5)]
+        k = n.value
+        return self._sb[0][:k], self._sb[1][:k], self._sb[2][:k]
+
+    def commit(self, gen_tokens):
+        """Appends the batch's generated tokens (int32, generation entries'
+        tokens concatenated in batch order) and returns the tables of the
+        entries kept: (requests, q_indptr, cached_len, kv_len, page_indptr,
+        page_indices), views valid until the next call."""
+        g, gp = _host_i32(gen_tokens if len(gen_tokens) else np.zeros(1, np.int32))
+        need, n = ctypes.c_int64(), ctypes.c_int32()
+        while True:
+            rq, qi, cl, kl, pi = self._tb
+            code = lib().pps_engine_commit(self._h, gp, rq.ctypes.data_as(_I32P),
+                                           qi.ctypes.data_as(_I32P), cl.ctypes.data_as(_I32P),
+                                           kl.ctypes.data_as(_I32P), pi.ctypes.data_as(_I32P),
+                                           self._px.ctypes.data_as(_I32P), len(self._px),
+                                           ctypes.byref(need), ctypes.byref(n))
+            if code == 0:
+                break
+            if code != -1 or need.value <= len(self._px):
+                _check(code, "pps_engine_commit")
+            self._px = np.zeros(2 * need.value, np.int32)
+        k = n.value
+        rq, qi, cl, kl, pi = self._tb
+        return rq[:k], qi[:k + 1], cl[:k], kl[:k], pi[:k + 1], self._px[:pi[k]]
+
+    def destroy(self):
+        if self._h is not None:
+            lib().pps_engine_destroy(self._h)
             self._h = None
 
     def __del__(self):

@@ -267,3 +267,73 @@ def test_scheduler_and_cache_drive_chunked_steps(pps, budget, reserved):
                 cache.finish(r)
                 del state[r]
     assert checked > 20
+
+
+def test_engine_drives_chunked_steps(pps):
+    """The same loop through the native serving-step runtime: pps_engine_add
+    admits, pps_engine_schedule picks the batch, pps_engine_commit appends the
+    generated tokens and hands back the tables that kv_append and attn_plan
+    take; every scheduled token's output is checked against the oracle."""
+    rng = np.random.default_rng(22)
+    tabs = _tables(4, max_pos=1024)
+    num_pages = 80
+    eng = pps.Engine(num_pages, P, budget=72, reserved=12)
+    pool_k = torch.full((num_pages, Hkv, P, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pool_v = torch.full_like(pool_k, float("nan"))
+    prompts = [list(rng.integers(0, VOCAB, size=int(rng.integers(30, 120)))) for _ in range(3)]
+    tokens, goal, produced = {}, {}, {}
+    pps.get_device_error(clear=True)
+    dev = lambda a: torch.as_tensor(np.asarray(a), dtype=torch.int32, device="cuda")
+    checked = 0
+    for step in range(40):
+        for _ in range(int(rng.integers(0, 3))):
+            if len(tokens) >= 6:
+                break
+            base = prompts[int(rng.integers(len(prompts)))]
+            toks = base[:int(rng.integers(1, len(base) + 1))] + \
+                list(rng.integers(0, VOCAB, size=int(rng.integers(1, 70))))
+            try:
+                rid, cached, copy = eng.add(toks, int(rng.choice([1, 3])))
+            except pps.CacheFull:
+                continue
+            if copy is not None:
+                pps.copy_slots(pool_k, pool_v, dev([copy[0]]), dev([copy[1]]), dev([copy[2]]))
+            tokens[rid], goal[rid], produced[rid] = list(toks), int(rng.integers(2, 12)), 0
+        req, tok, pre = eng.schedule()
+        gen = {int(r): int(k) for r, k, p in zip(req, tok, pre) if not p}
+        new = {r: list(rng.integers(0, VOCAB, size=k)) for r, k in gen.items()}
+        flat = np.array([t for r in req.tolist() if r in new for t in new[r]], np.int32)
+        rq, qi, cl, kl, pi, px = [a.copy() for a in eng.commit(flat)]
+        for r in rq.tolist():
+            if r in new:
+                tokens[r] += new[r]
+                produced[r] += 1
+        if len(rq) == 0:
+            continue
+        ks, vs = [], []
+        for r, f, e in zip(rq.tolist(), cl.tolist(), kl.tolist()):
+            kk, vv = _kv(tabs, tokens[r][f:e], range(f, e))
+            ks.append(kk)
+            vs.append(vv)
+        T = int(qi[-1])
+        pps.kv_append(pool_k, pool_v, torch.cat(ks).cuda(), torch.cat(vs).cuda(), dev(qi),
+                      dev(cl), dev(pi), dev(px))
+        q = torch.randn((T, Hq, D), generator=torch.Generator().manual_seed(200 + step)) \
+            .to(torch.bfloat16)
+        plan = pps.attn_plan(qi, kl, pi, px, Hq, Hkv, D, P, num_pages)
+        ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+        out = torch.full((T, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        pps.attn_run(plan, q.cuda(), pool_k, pool_v, out, ws)
+        torch.cuda.synchronize()
+        assert pps.get_device_error(clear=True) == 0
+        for i, (r, f, e) in enumerate(zip(rq.tolist(), cl.tolist(), kl.tolist())):
+            a, b = int(qi[i]), int(qi[i + 1])
+            ref = _reference(q[a:b], tokens[r][:e], f, tabs)
+            mx, mean = errors(out[a:b], ref)
+            assert mx <= MAX_ABS and mean <= MEAN_ABS, (step, r, mx, mean)
+            checked += 1
+        for r in list(tokens):
+            if produced[r] >= goal[r]:
+                eng.finish(r)
+                del tokens[r], goal[r], produced[r]
+    assert checked > 20
