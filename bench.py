@@ -208,10 +208,16 @@ def roofline(pps, roof_ms, infos, qo_bytes, workload, sustained):
     else:
         alg = kv_bw + qo_bytes
         ach = alg / (roof_ms[dom] / 1e3) / 1e9
+        # small-row tasks run on the key-tile tcgen05 kernel (attn_tt.cu) when
+        # the plan says so, else on the CUDA-core split-KV kernel (attn_bw.cu)
+        tt = any(i.get("small_rows_on_tensor") for i in infos)
+        src = ("attn_tt.cu" if tt else "attn_bw.cu") if dom == 0 else "merge.cu"
+        name = ("key-tile tcgen05 attention (small-row tasks)" if tt else
+                "split-KV bandwidth attention (CUDA cores)") if dom == 0 else "partial merge"
         roof = {"bound": "hbm", "achieved": ach, "peak": hpeak, "unit": "GB/s",
                 "frac": ach / hpeak,
-                "traffic": traffic_record("attn_bw.cu" if dom == 0 else "merge.cu", workload),
-                "kernel": ["split-KV bandwidth attention", "", "partial merge"][dom],
+                "traffic": traffic_record(src, workload),
+                "kernel": name,
                 "algorithmic": f"{alg:.0f} B per step (K+V read by the bandwidth tasks, each "
                                f"once: {kv_bw:.0f}; Q and O rows: {qo_bytes:.0f})"}
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else \
@@ -756,7 +762,7 @@ def run_cache_serving(args):
     e2e_value = sum_over_ranks(tok_e2e, world, dev) / (ms_e2e * k_e2e / 1e3)
 
     avg = lambda key: sum(i[key] for i in infos) / len(infos)
-    avg_infos = [{k: avg(k) for k in ("kv_bytes_unique", "kv_bytes_bw", "flops_mma",
+    avg_infos = [{k: avg(k) for k in ("kv_bytes_unique", "kv_bytes_bw", "flops_mma", "small_rows_on_tensor",
                                       "kv_bytes_read", "flops_total")}]
     qo = tokens / args.steps * 2 * srv.Hq * srv.D * 2
     roof = roofline(pps, kern_ms, avg_infos, qo, args.workload, sustained=False)

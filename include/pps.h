@@ -363,6 +363,7 @@ typedef struct pps_plan_options {
 
 #define PPS_PLAN_NO_GROUPS 1      /* do not merge shared-prefix pages into group tasks            */
 #define PPS_PLAN_CUDA_CORES_ONLY 2 /* route every task to the CUDA-core kernel (no tcgen05 tiles) */
+#define PPS_PLAN_SMALL_ROWS_CUDA_CORES 4 /* tasks of few rows on the CUDA-core kernel, not the key-tile one */
 
 typedef struct pps_plan pps_plan;
 
@@ -516,6 +517,8 @@ typedef struct pps_plan_info {
   int64_t kv_bytes_bw;         /* K+V bytes the bandwidth tasks read (each once)         */
   double flops_mma_issued;     /* FLOP the tensor core executes: whole 128-row x 128-key tiles */
   int32_t num_tree_requests;   /* requests whose draft is a tree (not a chain)           */
+  int32_t small_rows_on_tensor; /* 1: the small-row (bandwidth) tasks run on the key-tile
+                                   tcgen05 kernel; 0: on the CUDA-core kernel              */
 } pps_plan_info;
 pps_status pps_plan_get_info(const pps_plan* plan, pps_plan_info* info);
 

@@ -22,13 +22,14 @@ import numpy as np
 __all__ = [
     "PPSError", "Plan", "lib", "build", "kv_append", "attn_plan", "attn_run", "plan_destroy",
     "get_device_error", "launch_count", "status_string", "version", "LIB_PATH",
-    "PLAN_NO_GROUPS", "PLAN_CUDA_CORES_ONLY", "KERNEL_BANDWIDTH", "KERNEL_TENSOR", "KERNEL_MERGE",
+    "PLAN_NO_GROUPS", "PLAN_CUDA_CORES_ONLY", "PLAN_SMALL_ROWS_CUDA_CORES", "KERNEL_BANDWIDTH", "KERNEL_TENSOR", "KERNEL_MERGE",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpps.so")
 
 PLAN_NO_GROUPS = 1
 PLAN_CUDA_CORES_ONLY = 2
+PLAN_SMALL_ROWS_CUDA_CORES = 4
 KERNEL_BANDWIDTH, KERNEL_TENSOR, KERNEL_MERGE = 0, 1, 2
 NUM_KERNEL_CLASSES = 3
 TASK_INTS = 8
@@ -61,7 +62,7 @@ class _PlanInfo(ctypes.Structure):
             "workspace_bytes", "kv_bytes_unique", "kv_bytes_read")] + [
         ("flops_mma", ctypes.c_double), ("flops_total", ctypes.c_double),
         ("kv_bytes_bw", ctypes.c_int64), ("flops_mma_issued", ctypes.c_double),
-        ("num_tree_requests", ctypes.c_int32)]
+        ("num_tree_requests", ctypes.c_int32), ("small_rows_on_tensor", ctypes.c_int32)]
 
 
 class _CacheStats(ctypes.Structure):
@@ -91,10 +92,11 @@ def lib():
     L = ctypes.CDLL(LIB_PATH)
     vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
     L.pps_kv_append.argtypes = [ctypes.POINTER(_Pool), vp, vp, vp, vp, vp, vp, i32, i32, vp]
-    L.pps_attn_plan.argtypes = [_I32P, _I32P, _I32P, _I32P, i32, i32, i32, i32, i32, i32,
+    # host int32 arrays by address (see _host_addr)
+    L.pps_attn_plan.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                 ctypes.c_float, ctypes.POINTER(_PlanOptions),
                                 ctypes.POINTER(vp), ctypes.POINTER(sz)]
-    L.pps_attn_plan_tree.argtypes = [_I32P, _I32P, _I32P, _I32P, _I32P, i32, i32, i32, i32,
+    L.pps_attn_plan_tree.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                      i32, i32, ctypes.c_float, ctypes.POINTER(_PlanOptions),
                                      ctypes.POINTER(vp), ctypes.POINTER(sz)]
     L.pps_attn_run.argtypes = [vp, vp, ctypes.POINTER(_Pool), vp, vp, sz, vp]
@@ -188,6 +190,13 @@ def _host_i32(a):
     return a, a.ctypes.data_as(_I32P)
 
 
+def _host_addr(a):
+    """(contiguous int32 array, its address as an int): for the per-step calls,
+    where building a ctypes pointer object costs more than the call itself."""
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return a, a.__array_interface__["data"][0]
+
+
 def _dev(t, dtype=None):
     if t is None:
         return None
@@ -273,10 +282,10 @@ def attn_plan(q_indptr, kv_len, page_indptr, page_indices, num_q_heads, num_kv_h
     """pps_attn_plan on host int32 arrays (numpy or lists); with ``tree_parent``
     (one parent index per new token, -1 = off the cached context) it calls
     pps_attn_plan_tree."""
-    qi, qi_p = _host_i32(q_indptr)
-    kl, kl_p = _host_i32(kv_len)
-    pi, pi_p = _host_i32(page_indptr)
-    px, px_p = _host_i32(page_indices if len(page_indices) else np.zeros(1, np.int32))
+    qi, qi_p = _host_addr(q_indptr)
+    kl, kl_p = _host_addr(kv_len)
+    pi, pi_p = _host_addr(page_indptr)
+    px, px_p = _host_addr(page_indices if len(page_indices) else np.zeros(1, np.int32))
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(head_dim)
     opts = _PlanOptions(int(num_sms), int(bw_chunk_tokens), int(mma_chunk_tokens), int(flags))
@@ -288,7 +297,7 @@ def attn_plan(q_indptr, kv_len, page_indptr, page_indices, num_q_heads, num_kv_h
                                    int(num_pages), float(sm_scale), ctypes.byref(opts),
                                    ctypes.byref(h), ctypes.byref(ws)), "pps_attn_plan")
     else:
-        tp, tp_p = _host_i32(tree_parent if len(tree_parent) else np.zeros(1, np.int32))
+        tp, tp_p = _host_addr(tree_parent if len(tree_parent) else np.zeros(1, np.int32))
         _check(lib().pps_attn_plan_tree(qi_p, kl_p, pi_p, px_p, tp_p, len(kl), int(num_q_heads),
                                         int(num_kv_heads), int(head_dim), int(page_size),
                                         int(num_pages), float(sm_scale), ctypes.byref(opts),

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpps.so")
 
-CUDA_SOURCES = ["api.cu", "kv_append.cu", "attn_bw.cu", "attn_mma.cu", "merge.cu", "noalloc.cu",
+CUDA_SOURCES = ["api.cu", "kv_append.cu", "attn_bw.cu", "attn_mma.cu", "attn_tt.cu", "merge.cu", "noalloc.cu",
                 "gemm.cu"]
 CXX_SOURCES = ["planner.cpp", "radix_cache.cpp", "scheduler.cpp", "engine.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

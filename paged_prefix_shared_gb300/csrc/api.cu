@@ -317,6 +317,6 @@ const char* pps_status_string(pps_status s) {
   }
 }
 
-int32_t pps_version(void) { return 200; }
+int32_t pps_version(void) { return 210; }
 
 }  // extern "C"

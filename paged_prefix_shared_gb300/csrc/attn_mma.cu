@@ -580,42 +580,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ---- host: tensor maps over the pool ------------------------------------------------
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaDriverEntryPointQueryResult q;
-    void* f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
-  });
-  return fn;
-}
-
-// 4-D view [num_pages][Hkv][P][D] of one pool array; box = 64 columns x P slots
-// of one page and kv head, 128-byte swizzle (matches the UMMA K-major layout).
-bool make_pool_map(CUtensorMap* map, const void* base, const pps_pool& pool) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const int D = pool.head_dim, P = pool.page_size, H = pool.num_kv_heads;
-  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)P, (cuuint64_t)H, (cuuint64_t)pool.num_pages};
-  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)P * D * 2, (cuuint64_t)H * P * D * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)P, 1, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 int launch_t(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const void* q,
              const pps_pool& pool, void* out, int32_t* err, cudaStream_t st) {
   CUtensorMap mk, mv;
-  if (!make_pool_map(&mk, pool.k, pool) || !make_pool_map(&mv, pool.v, pool))
+  if (!pps::make_pool_map(&mk, pool.k, pool) || !pps::make_pool_map(&mv, pool.v, pool))
     return (int)cudaErrorInvalidValue;
   auto kern = mma_attention_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -637,6 +606,64 @@ int launch_t(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const v
 }  // namespace
 
 namespace pps {
+
+// ---- host: tensor maps over the pool ------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+  });
+  return fn;
+}
+
+// 4-D view [num_pages][Hkv][P][D] of one pool array; box = 64 columns x P slots
+// of one page and kv head, 128-byte swizzle (matches the UMMA K-major layout).
+bool make_pool_map(CUtensorMap* map, const void* base, const pps_pool& pool) {
+  // Encoding a map is host work on every launch; a serving loop reuses the
+  // same pool arrays, so the last few maps are kept (keyed by every field the
+  // encoding reads).
+  struct Entry {
+    const void* base;
+    int32_t D, P, H, pages;
+    CUtensorMap map;
+  };
+  static std::mutex mu;
+  static Entry cache[8];
+  static int used = 0, next = 0;
+  const int D = pool.head_dim, P = pool.page_size, H = pool.num_kv_heads;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i) {
+      const Entry& e = cache[i];
+      if (e.base == base && e.D == D && e.P == P && e.H == H && e.pages == pool.num_pages) {
+        *map = e.map;
+        return true;
+      }
+    }
+  }
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)P, (cuuint64_t)H, (cuuint64_t)pool.num_pages};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)P * D * 2, (cuuint64_t)H * P * D * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)P, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  if (fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lk(mu);
+  cache[next] = Entry{base, D, P, H, pool.num_pages, *map};
+  next = (next + 1) % 8;
+  used = used < 8 ? used + 1 : 8;
+  return true;
+}
 
 bool mma_path_available() { return true; }
 

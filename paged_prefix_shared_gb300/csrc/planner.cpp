@@ -59,6 +59,15 @@ struct TaskSet {       // emitted once per kv head
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Pages two sequences share from the start (first n at most), compared in
+// 32-byte blocks.
+inline int32_t common_pages(const int32_t* a, const int32_t* b, int32_t n) {
+  int32_t k = 0;
+  while (k + 8 <= n && std::memcmp(a + k, b + k, 32) == 0) k += 8;
+  while (k < n && a[k] == b[k]) ++k;
+  return k;
+}
+
 bool pow2_in(int32_t v, std::initializer_list<int32_t> set) {
   for (int32_t s : set) if (v == s) return true;
   return false;
@@ -135,10 +144,12 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
     if (kv_len[r] < q) return PPS_ERR_INVALID_ARGUMENT;
     const int64_t need = ceil_div(kv_len[r], P);
     if (page_indptr[r + 1] - page_indptr[r] < need) return PPS_ERR_PAGE_TABLE;
-    for (int64_t i = 0; i < need; ++i) {
-      const int32_t pg = page_indices[page_indptr[r] + i];
-      if (pg < 0 || pg >= num_pages) return PPS_ERR_PAGE_TABLE;
-    }
+    // ids in [0, num_pages): one unsigned compare per id, OR-ed without
+    // branches so the loop vectorizes
+    const int32_t* pl = page_indices + page_indptr[r];
+    uint32_t bad = 0;
+    for (int64_t i = 0; i < need; ++i) bad |= (uint32_t)((uint32_t)pl[i] >= (uint32_t)num_pages);
+    if (bad) return PPS_ERR_PAGE_TABLE;
   }
   const int64_t nnz = page_indptr[R];
   if (nnz > 0 && !page_indices) return PPS_ERR_INVALID_ARGUMENT;
@@ -172,7 +183,7 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
   pps_plan* plan = new (std::nothrow) pps_plan;
   if (!plan) return PPS_ERR_NO_MEMORY;
   try {
-    plan->shape = {num_q_heads, num_kv_heads, head_dim, page_size, G, num_pages, sm_scale, 0};
+    plan->shape = {num_q_heads, num_kv_heads, head_dim, page_size, G, num_pages, sm_scale, 0, 0};
     plan->num_requests = R;
     plan->num_tokens = q_indptr[R];
     plan->use_mma = use_mma;
@@ -230,22 +241,21 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
         }
         if (!any) cand.clear();
       }
+      // Lexicographic order of the page lists (by their first differing page
+      // id): every set of lists sharing a prefix is then one contiguous run.
       std::sort(cand.begin(), cand.end(), [&](int32_t a, int32_t b) {
         const int32_t n = std::min(full[a], full[b]);
         const int32_t* pa = seq(a);
         const int32_t* pb = seq(b);
-        for (int32_t i = 0; i < n; ++i)
-          if (pa[i] != pb[i]) return pa[i] < pb[i];
+        const int32_t k = common_pages(pa, pb, n);
+        if (k < n) return pa[k] < pb[k];
         if (full[a] != full[b]) return full[a] < full[b];
         return a < b;
       });
       std::vector<int32_t> lcp(cand.size(), 0);
       for (size_t i = 1; i < cand.size(); ++i) {
         const int32_t a = cand[i - 1], b = cand[i];
-        const int32_t n = std::min(full[a], full[b]);
-        int32_t k = 0;
-        while (k < n && seq(a)[k] == seq(b)[k]) ++k;
-        lcp[i] = k;
+        lcp[i] = common_pages(seq(a), seq(b), std::min(full[a], full[b]));
       }
       RadixBuilder rb{cand, lcp, {}, group_end};
       rb.build(0, (int32_t)cand.size(), 0);
@@ -289,7 +299,13 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
     }
 
     // ---- 3. tiles and split-KV chunks ----------------------------------------------
-    const int32_t bw_max_tok = std::max(1, 8 / G);          // decode-like rows stay on CUDA cores
+    // Small-row tasks (decode tokens, short drafts, narrow shared-prefix
+    // groups): up to 32 rows on the key-tile tensor kernel (head_dim 128, no
+    // draft tree), else up to 8 rows on the CUDA-core kernel.
+    const bool use_tt = use_mma && head_dim == 128 && !plan->has_tree && G <= pps::kTtRows &&
+                        !(o.flags & PPS_PLAN_SMALL_ROWS_CUDA_CORES);
+    plan->shape.small_tt = use_tt ? 1 : 0;
+    const int32_t bw_max_tok = use_tt ? pps::kTtRows / G : std::max(1, 8 / G);
     const int32_t bw_tile_tok = std::max(1, pps::kBwMaxRows / G);
     const int32_t mma_tile_tok = pps::kMmaTaskRows / G;
     auto is_mma = [&](const Segment& s) { return use_mma && s.n_tok > bw_max_tok; };
@@ -323,7 +339,10 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
       const int64_t want = ceil_div(bw_kv * num_kv_heads, (int64_t)num_sms * 2);
       bw_chunk = (int32_t)std::min<int64_t>(4096, std::max<int64_t>(128, want));
     }
-    bw_chunk = (int32_t)(ceil_div(bw_chunk, P) * P);
+    {
+      const int32_t unit = use_tt ? pps::kMmaKvTile : P;   // whole 128-key tiles on tensor cores
+      bw_chunk = (int32_t)(ceil_div(bw_chunk, unit) * unit);
+    }
     int32_t mma_chunk = o.mma_chunk_tokens;
     if (mma_chunk <= 0) {
       mma_chunk = 1 << 30;
@@ -344,21 +363,36 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
       for (int32_t i0 = 0; i0 < s.n_tok; i0 += tt, ++tile) {
         const int32_t i1 = std::min(s.n_tok, i0 + tt);
         const Span sp = span_of(s, i0, i1);
-        const int64_t nch = std::max<int64_t>(1, ceil_div(sp.b - sp.a, chunk));
+        int64_t step = chunk;
+        int64_t nch = std::max<int64_t>(1, ceil_div(sp.b - sp.a, chunk));
+        if (!mma && use_tt && o.bw_chunk_tokens <= 0) {
+          // key-tile tasks: no split within a quarter over the chunk, else
+          // equal whole-tile pieces (no one-tile remainder task)
+          const int64_t span = sp.b - sp.a;
+          nch = span <= chunk + chunk / 4 ? 1 : ceil_div(span, chunk);
+          step = ceil_div(ceil_div(span, nch), pps::kMmaKvTile) * pps::kMmaKvTile;
+          nch = std::max<int64_t>(1, ceil_div(span, step));
+        }
         for (int64_t k = 0; k < nch; ++k) {
           TaskSet ts{};
           ts.row_off = s.row_off + i0;
           ts.n_tok = i1 - i0;
           ts.page_off = s.page_off;
-          ts.kv_begin = sp.a + (int32_t)(k * chunk);
-          ts.kv_end = (k == nch - 1) ? sp.end : ts.kv_begin + chunk;
+          ts.kv_begin = sp.a + (int32_t)(k * step);
+          ts.kv_end = (k == nch - 1) ? sp.end : ts.kv_begin + (int32_t)step;
           ts.causal = s.causal ? s.c + i0 : PPS_NO_CAUSAL;
           ts.key = s.key;
           ts.tile = tile;
           ts.chunk = (int32_t)k;
           ts.mma = mma;
-          const int64_t rows_eff = mma ? pps::kMmaTaskRows : (int64_t)ts.n_tok * G;
-          ts.work = rows_eff * (ts.kv_end - ts.kv_begin);
+          if (!mma && use_tt) {
+            // key-tile tasks stream K/V at the memory rate whatever their rows:
+            // time ~ 128-key tiles, plus about two tiles of per-task work
+            ts.work = (ceil_div(ts.kv_end - ts.kv_begin, pps::kMmaKvTile) + 2) * pps::kMmaKvTile;
+          } else {
+            const int64_t rows_eff = mma ? pps::kMmaTaskRows : (int64_t)ts.n_tok * G;
+            ts.work = rows_eff * (ts.kv_end - ts.kv_begin);
+          }
           ts.out_pid = -1;
           sets.push_back(ts);
         }
@@ -441,17 +475,11 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
     // ---- 6. statistics ---------------------------------------------------------------
     const int64_t tok_bytes = 2LL * num_kv_heads * head_dim * 2;   // K+V, all kv heads
     {
-      std::vector<uint8_t> seen((size_t)num_pages, 0);   // valid slots counted per page
-      int64_t slots = 0;
-      for (int32_t r = 0; r < R; ++r) {
-        const int64_t need = ceil_div(kv_len[r], P);
-        for (int64_t i = 0; i < need; ++i) {
-          const int32_t pg = page_indices[page_indptr[r] + i];
-          const int32_t valid = (int32_t)std::min<int64_t>(P, kv_len[r] - i * P);
-          if (valid > seen[pg]) { slots += valid - seen[pg]; seen[pg] = (uint8_t)std::min(valid, 255); }
-        }
-      }
-      plan->kv_bytes_unique = slots * tok_bytes;
+      // the unique-slot count runs on demand (pps_plan_get_info) from these
+      plan->kv_len_copy.assign(kv_len, kv_len + R);
+      plan->page_indptr_copy.assign(page_indptr, page_indptr + R + 1);
+      plan->tok_bytes = tok_bytes;
+
     }
     double fl_tot = 0, fl_mma = 0;
     int64_t read = 0, read_bw = 0;
@@ -475,6 +503,9 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
       read += (int64_t)(ts.kv_end - ts.kv_begin) * tok_bytes;
       if (!ts.mma) {
         read_bw += (int64_t)(ts.kv_end - ts.kv_begin) * tok_bytes;
+        if (use_tt)   // 128 keys x 32 rows x d per tile and kv head
+          issued += (double)ceil_div(ts.kv_end - ts.kv_begin, pps::kMmaKvTile) * num_kv_heads *
+                    4.0 * pps::kMmaKvTile * pps::kTtRows * head_dim;
       } else {
         // whole tiles per kv head: ceil(rows / 128) x ceil(span / 128) of 128 x 128 x d
         const int64_t tiles = ceil_div((int64_t)ts.n_tok * G, pps::kMmaRows) *
@@ -546,8 +577,45 @@ extern "C" pps_status pps_plan_destroy(pps_plan* plan) {
   return PPS_OK;
 }
 
+namespace {
+// K+V bytes of the distinct (page, kv head, valid slot) triples of a plan's
+// requests: valid slots counted per page (P <= 128 fits a byte); every page of
+// a request is full but its last, and the update is branch-free.
+int64_t unique_kv_bytes(const pps_plan* p) {
+  const int32_t P = p->shape.page_size, R = p->num_requests;
+  const int32_t* pages = p->image.data + p->layout.pages;
+  std::vector<uint8_t> seen((size_t)p->shape.num_pages, 0);
+  int64_t slots = 0;
+  for (int32_t r = 0; r < R; ++r) {
+    const int32_t kv = p->kv_len_copy[r];
+    const int32_t need = (int32_t)ceil_div(kv, P);
+    const int32_t* pl = pages + p->page_indptr_copy[r];
+    for (int32_t i = 0; i + 1 < need; ++i) {
+      const int32_t old = seen[pl[i]];
+      slots += P - old;
+      seen[pl[i]] = (uint8_t)P;
+    }
+    if (need > 0) {
+      const int32_t last = kv - (need - 1) * P;
+      const int32_t old = seen[pl[need - 1]];
+      const int32_t nv = std::max(old, last);
+      slots += nv - old;
+      seen[pl[need - 1]] = (uint8_t)nv;
+    }
+  }
+  return slots * p->tok_bytes;
+}
+}  // namespace
+
 extern "C" pps_status pps_plan_get_info(const pps_plan* p, pps_plan_info* info) {
   if (!p || !info) return PPS_ERR_INVALID_ARGUMENT;
+  if (p->kv_bytes_unique < 0) {
+    try {
+      p->kv_bytes_unique = unique_kv_bytes(p);
+    } catch (const std::bad_alloc&) {
+      return PPS_ERR_NO_MEMORY;
+    }
+  }
   std::memset(info, 0, sizeof(*info));
   info->num_requests = p->num_requests;
   info->num_tokens = p->num_tokens;
@@ -569,6 +637,7 @@ extern "C" pps_status pps_plan_get_info(const pps_plan* p, pps_plan_info* info) 
   info->kv_bytes_bw = p->kv_bytes_bw;
   info->flops_mma_issued = p->flops_mma_issued;
   info->num_tree_requests = p->num_tree_requests;
+  info->small_rows_on_tensor = p->shape.small_tt;
   return PPS_OK;
 }
 

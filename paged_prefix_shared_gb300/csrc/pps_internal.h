@@ -27,6 +27,7 @@ constexpr int kBwMaxRows = 16;      // query rows (tokens x G) per bandwidth tas
 constexpr int kMmaRows = 128;       // query rows per tensor-core tile (TMEM lanes)
 constexpr int kMmaTaskRows = 256;   // query rows per tensor-core task (two tiles sharing K/V)
 constexpr int kMmaKvTile = 128;     // KV positions per tensor-core step
+constexpr int kTtRows = 32;         // query rows per key-tile tensor task (head_dim 128)
 
 // Offsets (in int32 units) of the sections of the uploaded task table.
 struct TableLayout {
@@ -57,6 +58,7 @@ struct Shape {
   int32_t num_pages;
   float sm_scale;
   int32_t bw_rows_max;   // largest n_tok * G over bandwidth tasks
+  int32_t small_tt;      // 1: the small-row tasks run on the key-tile tensor kernel
 };
 
 // Host memory for plan tables.  Page-locked when a CUDA device is usable, so
@@ -91,7 +93,10 @@ struct pps_plan {
   size_t partial_o_bytes = 0;
   size_t partial_lse_bytes = 0;
   size_t workspace_bytes = 0;
-  int64_t kv_bytes_unique = 0, kv_bytes_read = 0, kv_bytes_bw = 0;
+  mutable int64_t kv_bytes_unique = -1;   // computed on the first pps_plan_get_info
+  int64_t kv_bytes_read = 0, kv_bytes_bw = 0;
+  std::vector<int32_t> kv_len_copy, page_indptr_copy;   // inputs of that count
+  int64_t tok_bytes = 0;
   double flops_mma_issued = 0;
   double flops_mma = 0, flops_total = 0;
   bool use_mma = false;
@@ -119,10 +124,23 @@ int launch_bw_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks
 int launch_mma_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
                          const pps_pool& pool, void* out, int32_t* err, void* stream);
 
+// Small-row tasks (the bandwidth task list) on the key-tile tensor kernel.
+int launch_tt_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
+                        const pps_pool& pool, void* out, int32_t* err, void* stream);
+
 int launch_merge(const Shape& s, const DeviceTables& t, int64_t num_merge_tokens, void* out,
                  void* stream);
 
 bool mma_path_available();
+
+#if defined(__CUDACC__)
+}  // namespace pps
+#include <cuda.h>
+namespace pps {
+// 4-D TMA view [num_pages][Hkv][P][D] of one pool array, box = 64 columns x P
+// slots of one page and kv head, 128-byte swizzle (attn_mma.cu).
+bool make_pool_map(CUtensorMap* map, const void* base, const pps_pool& pool);
+#endif
 
 // SM count of the current device, or 0 when no device is usable.
 int device_sm_count();

@@ -103,7 +103,10 @@ def test_kv_append_bit_exact(name):
     assert torch.equal(gv.cpu().view(torch.int16), ov.view(torch.int16))
 
 
-@pytest.mark.parametrize("flags", [0, 1, 2])
+# 0: default routing (small-row tasks on the key-tile tensor kernel where it
+# applies), 1: no shared-prefix groups, 2: CUDA cores only, 4: small-row tasks
+# on the CUDA-core kernel with the tensor-core tiles for wide tasks
+@pytest.mark.parametrize("flags", [0, 1, 2, 4])
 @pytest.mark.parametrize("name", list(small_cases()))
 def test_parity_small(pps, name, flags):
     wl, (ref, _) = _small(name)
@@ -116,13 +119,15 @@ def test_parity_small(pps, name, flags):
         assert mx <= MAX_ABS and mean <= MEAN_ABS, (s, mx, mean, plans[s].info())
 
 
+@pytest.mark.parametrize("flags", [0, 4])
 @pytest.mark.parametrize("chunk", [512, 2048])
-def test_parity_long_tasks(pps, chunk):
-    """Tasks of hundreds of sub-blocks per CTA (consumer warps drift apart)."""
+def test_parity_long_tasks(pps, chunk, flags):
+    """Tasks of hundreds of sub-blocks or tiles per CTA (consumer warps drift
+    apart; the key-tile ring wraps many times)."""
     wl = workloads.decode_heavy(num_requests=16, kv_lo=3000, kv_hi=6000, seed=5, **KW)
     ref, _ = oracle_steps(wl)
     pps.get_device_error(clear=True)
-    outs, _, plans = run_workload(wl, bw_chunk_tokens=chunk, num_sms=4)
+    outs, _, plans = run_workload(wl, bw_chunk_tokens=chunk, num_sms=4, flags=flags)
     assert pps.get_device_error(clear=True) == 0
     mx, mean = errors(outs[0], ref[0])
     assert mx <= MAX_ABS and mean <= MEAN_ABS, (mx, mean)

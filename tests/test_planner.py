@@ -122,12 +122,27 @@ def test_unique_bytes_of_full_radix_workload(pps):
     # 8 roots of 2048 + 32 branches of 512 + private tails (+1 new token each)
     tails = int((L.kv_len - 2048 - 512).sum())
     assert info["kv_bytes_unique"] == (8 * 2048 + 32 * 512 + tails) * tok_bytes
-    if info["num_mma_tasks"]:
-        # wide groups run as one 128-row tensor-core tile: every shared page read once
+    if info["num_mma_tasks"] or info["small_rows_on_tensor"]:
+        # a root group of 8 decode rows x G=4 runs as one 32-row key-tile task
+        # (or one 128-row tile): every shared page read once
         assert info["kv_bytes_read"] == info["kv_bytes_unique"]
+        assert info["num_mma_tasks"] == 0 and info["num_bw_tasks"] > 0
     else:
         # CUDA cores only: a root group of 8 decode rows x G=4 needs two 16-row tiles
         assert info["kv_bytes_read"] == info["kv_bytes_unique"] + 8 * 2048 * tok_bytes
+
+
+def test_small_row_routing(pps):
+    """Tasks of up to 32 rows go to the key-tile tensor kernel (head_dim 128,
+    no draft tree); the CUDA-core kernel takes them under the flag, with head_dim
+    64, or in draft-tree batches."""
+    wl = workloads.radix_sharing(values=False)
+    L = wl.layout
+    on = _plan(pps, L).info()
+    off = _plan(pps, L, flags=pps.PLAN_SMALL_ROWS_CUDA_CORES).info()
+    assert on["small_rows_on_tensor"] == 1 and off["small_rows_on_tensor"] == 0
+    assert on["num_mma_tasks"] == 0 and off["num_mma_tasks"] > 0   # 32-row roots move over
+    assert _plan(pps, workloads.tiny_mixed(values=False).layout).info()["small_rows_on_tensor"] == 0
 
 
 def test_plan_is_deterministic(pps):
