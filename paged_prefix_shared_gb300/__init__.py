@@ -209,8 +209,14 @@ def _dev(t, dtype=None):
 
 def _stream(stream):
     import torch
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    # the current stream's handle without building a Stream object (a few
+    # microseconds per call, paid on every launch of a serving loop)
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return ctypes.c_void_p(raw(torch._C._cuda_getDevice()))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def _pool(pool_k, pool_v):
