@@ -75,6 +75,7 @@ struct TtParams {
   float* o_part;
   float* lse_part;
   int32_t* err;
+  const unsigned long long* tree_mask;       // per new token (draft trees), or nullptr
   int32_t num_q_heads;
   int32_t G;
   int32_t page_size;
@@ -96,12 +97,15 @@ struct TtLayout {
   static constexpr int v_off = k_off + kStages * kv_tile;
   static constexpr int q_off = v_off + kStages * kv_tile;
   static constexpr int p_off = q_off + 2 * q_tile;
-  static constexpr int red_off = p_off + 2 * p_tile;    // max and sum scratch: [2][kRows][4] fp32
-  static constexpr int m_off = red_off + 2 * kRows * 4 * 4;     // reference max per row
+  // per-row scratch: the tile maxima and (at a task's end) the row sums, one
+  // use at a time: [kRows][4 warps] fp32
+  static constexpr int red_off = p_off + 2 * p_tile;
+  static constexpr int m_off = red_off + kRows * 4 * 4;         // reference max per row
   static constexpr int a_off = m_off + kRows * 4;               // rescale factor per row
   static constexpr int inv_off = a_off + kRows * 4;             // 1 / l per row of a finished task
   static constexpr int tok_off = inv_off + kRows * 4;           // its token ids: [kRows]
-  static constexpr int bytes = tok_off + 2 * kRows * 4;
+  static constexpr int msk_off = tok_off + kRows * 4;           // draft-tree masks per token
+  static constexpr int bytes = msk_off + kRows * 8;
   static constexpr int smem_alloc = bytes + 1024;       // slack for the 1024-byte alignment
 };
 static_assert(TtLayout::smem_alloc + (int)sizeof(TtBars) + 64 <= 232448, "shared memory");
@@ -212,6 +216,7 @@ struct SmCtx {
   float* m_s;                      // [kRows] reference max of every row
   float* a_s;                      // [kRows] rescale factor of every row
   float* inv_s;                    // [kRows] 1 / l of every row of the last finished task
+  unsigned long long* msk_s;       // [kRows] draft-tree lookback masks of the task's tokens
   volatile int* abort_flag;
   uint32_t tm, lane_off;
   int t, warp, lane;
@@ -244,7 +249,7 @@ __device__ __forceinline__ void lds_rows(const float* src, float (&dst)[NR]) {
 // registers; the rare paths (a task's first tile, a rescale, the statistics)
 // work one row per lane and through shared memory, so they stay short in code
 // as well as in time.
-template <int NR, class AfterFirst>
+template <int NR, bool TREE, class AfterFirst>
 __device__ __forceinline__ bool softmax_tiles(const SmCtx& c, const pps::Task& task, int n, int ti,
                                               int& gt, AfterFirst&& after_first) {
   const TtParams& p = *c.p;
@@ -255,6 +260,10 @@ __device__ __forceinline__ bool softmax_tiles(const SmCtx& c, const pps::Task& t
   if (t < kRows) c.m_s[t] = t < nrows ? -INFINITY : 0.f;   // padding rows: P stays 0
   // token ids for the statistics step (loaded now, stored there)
   const int32_t my_tok = t < task.n_tok ? p.rows[task.row_off + t] : 0;
+  // Draft trees: bit k of a token's mask = the key k positions before its own
+  // one is visible (only new-token keys can be hidden; cached ones never are).
+  if (TREE && t < task.n_tok) c.msk_s[t] = causal ? p.tree_mask[my_tok] : ~0ull;
+  const int lg = __ffs(G) - 1;                           // G is a power of two
   float m_ref[NR], l_sum[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
@@ -277,7 +286,10 @@ __device__ __forceinline__ bool softmax_tiles(const SmCtx& c, const pps::Task& t
     tm_ld<NR>(c.tm + c.lane_off + sb * kRows, s);
     tmem_wait_ld();
     const int pos = t0 + t;
-    const bool full = t0 + kTile <= task.kv_end && (!causal || t0 + kTile - 1 <= task.causal);
+    // no masking: every key valid and before every row's limit (before the first
+    // new token for draft trees, whose own keys may be hidden)
+    const int last_free = TREE ? task.causal - 1 : task.causal;
+    const bool full = t0 + kTile <= task.kv_end && (!causal || t0 + kTile - 1 <= last_free);
     // row r (token r / G) sees key `pos` when r >= G * (pos - causal)
     const int first_vis = (full || !causal) ? 0 : G * (pos - task.causal);
     const bool key_ok = full || pos < task.kv_end;
@@ -285,7 +297,11 @@ __device__ __forceinline__ bool softmax_tiles(const SmCtx& c, const pps::Task& t
     bool need = j == 0;
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
-      const bool vis = r < nrows && key_ok && r >= first_vis;
+      bool vis = r < nrows && key_ok && r >= first_vis;
+      if (TREE && !full && causal && pos >= task.causal) {
+        const int back = task.causal + (r >> lg) - pos;     // key `back` positions before row r's token
+        if (back >= 0 && back < 64 && !((c.msk_s[r >> lg] >> back) & 1ull)) vis = false;
+      }
       x[r] = vis ? __uint_as_float(s[r]) * p.qk_scale : -INFINITY;
       need |= x[r] > m_ref[r] + kRescaleThreshold;
     }
@@ -431,6 +447,9 @@ __device__ __forceinline__ bool softmax_output(const SmCtx& c, const pps::Task& 
   return true;
 }
 
+// TREE: the batch holds draft-tree verify rows; batches without one run the
+// TREE = false instance, which has no mask code.
+template <bool TREE>
 __global__ void __launch_bounds__(kThreads, 1)
     tt_attention_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const TtParams p) {
@@ -449,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t q_base = smem_u32(smem + L::q_off);
   const uint32_t p_base = smem_u32(smem + L::p_off);
   float* red_max = reinterpret_cast<float*>(smem + L::red_off);   // [kRows][4 warps]
-  float* red_sum = red_max + kRows * 4;
+  float* red_sum = red_max;                                       // (not live at once)
   int32_t* tok_s = reinterpret_cast<int32_t*>(smem + L::tok_off); // [2][kRows]
 
   if (tid == 0) {
@@ -496,8 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     SmCtx ctx{&p,      &bars,         smem,     red_max, red_sum, tok_s,
               reinterpret_cast<float*>(smem + L::m_off), reinterpret_cast<float*>(smem + L::a_off),
-              reinterpret_cast<float*>(smem + L::inv_off), &abort_flag, tm, lane_off, t, warp,
-              lane};
+              reinterpret_cast<float*>(smem + L::inv_off),
+              reinterpret_cast<unsigned long long*>(smem + L::msk_off), &abort_flag, tm, lane_off,
+              t, warp, lane};
     TaskCursor cur(p.tasks, p.num_tasks, b, nctas);
     pps::Task task, prev;
     int prev_ti = -1;                                    // finished task whose output is pending
@@ -513,9 +533,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         return softmax_output(ctx, prev, pt);
       };
       // rows padded to 8, 16 or 32 (uniform over the CTA: one task at a time)
-      if (nrows <= 8) ok = softmax_tiles<8>(ctx, task, n, ti, gt, flush);
-      else if (nrows <= 16) ok = softmax_tiles<16>(ctx, task, n, ti, gt, flush);
-      else ok = softmax_tiles<32>(ctx, task, n, ti, gt, flush);
+      if (nrows <= 8) ok = softmax_tiles<8, TREE>(ctx, task, n, ti, gt, flush);
+      else if (nrows <= 16) ok = softmax_tiles<16, TREE>(ctx, task, n, ti, gt, flush);
+      else ok = softmax_tiles<32, TREE>(ctx, task, n, ti, gt, flush);
       if (!ok) break;
       prev = task;
       prev_ti = ti;
@@ -706,21 +726,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace pps {
 
-int launch_tt_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
-                        const pps_pool& pool, void* out, int32_t* err, void* stream) {
-  if (num_tasks == 0) return cudaSuccess;
-  if (s.head_dim != D) return (int)cudaErrorInvalidValue;
+namespace {
+template <bool TREE>
+int launch_tt(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
+              const pps_pool& pool, void* out, int32_t* err, void* stream) {
   CUtensorMap mk, mv;
   if (!make_pool_map(&mk, pool.k, pool) || !make_pool_map(&mv, pool.v, pool))
     return (int)cudaErrorInvalidValue;
-  // once per device: the shared-memory opt-in and the SM count
+  // once per device and instance: the shared-memory opt-in and the SM count
   static std::atomic<int> ready_sms[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return (int)e;
   int sms = (dev >= 0 && dev < 64) ? ready_sms[dev].load(std::memory_order_relaxed) : 0;
   if (sms == 0) {
-    if ((e = cudaFuncSetAttribute(tt_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(tt_attention_kernel<TREE>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   TtLayout::smem_alloc)) != cudaSuccess)
       return (int)e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
@@ -729,12 +750,21 @@ int launch_tt_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks
   }
   const int64_t grid = std::min<int64_t>(num_tasks, sms);
   TtParams prm{t.bw_tasks, (int32_t)num_tasks, t.rows, t.pages, (const __nv_bfloat16*)q,
-               (__nv_bfloat16*)out, t.o_part, t.lse_part, err, s.num_q_heads, s.group,
-               s.page_size, s.sm_scale * 1.4426950408889634f};
-  tt_attention_kernel<<<(unsigned)grid, kThreads, TtLayout::smem_alloc, (cudaStream_t)stream>>>(
-      mk, mv, prm);
+               (__nv_bfloat16*)out, t.o_part, t.lse_part, err, t.tree_mask, s.num_q_heads,
+               s.group, s.page_size, s.sm_scale * 1.4426950408889634f};
+  tt_attention_kernel<TREE>
+      <<<(unsigned)grid, kThreads, TtLayout::smem_alloc, (cudaStream_t)stream>>>(mk, mv, prm);
   count_launch();
   return (int)cudaGetLastError();
+}
+}  // namespace
+
+int launch_tt_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
+                        const pps_pool& pool, void* out, int32_t* err, void* stream) {
+  if (num_tasks == 0) return cudaSuccess;
+  if (s.head_dim != D) return (int)cudaErrorInvalidValue;
+  return t.tree_mask ? launch_tt<true>(s, t, num_tasks, q, pool, out, err, stream)
+                     : launch_tt<false>(s, t, num_tasks, q, pool, out, err, stream);
 }
 
 }  // namespace pps

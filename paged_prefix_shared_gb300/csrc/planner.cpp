@@ -299,10 +299,10 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
     }
 
     // ---- 3. tiles and split-KV chunks ----------------------------------------------
-    // Small-row tasks (decode tokens, short drafts, narrow shared-prefix
-    // groups): up to 32 rows on the key-tile tensor kernel (head_dim 128, no
-    // draft tree), else up to 8 rows on the CUDA-core kernel.
-    const bool use_tt = use_mma && head_dim == 128 && !plan->has_tree && G <= pps::kTtRows &&
+    // Small-row tasks (decode tokens, short drafts and draft trees, narrow
+    // shared-prefix groups): up to 32 rows on the key-tile tensor kernel
+    // (head_dim 128), else up to 8 rows on the CUDA-core kernel.
+    const bool use_tt = use_mma && head_dim == 128 && G <= pps::kTtRows &&
                         !(o.flags & PPS_PLAN_SMALL_ROWS_CUDA_CORES);
     plan->shape.small_tt = use_tt ? 1 : 0;
     const int32_t bw_max_tok = use_tt ? pps::kTtRows / G : std::max(1, 8 / G);

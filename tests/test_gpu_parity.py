@@ -54,6 +54,9 @@ def small_cases():
                                                      kv_hi=700, num_q_heads=16, num_kv_heads=2,
                                                      head_dim=64, page_size=32),
         "tree_g1_bw": lambda: _star_and_chains(),
+        # small trees at G = 4 (8 and 5 tokens: 32 and 20 rows, one key-tile task
+        # each, masks inside the last KV tile, short contexts too)
+        "tree_small_g4": lambda: _small_trees(),
         "tree_shared": lambda: _tree_shared(),
     }
 
@@ -65,6 +68,17 @@ def _star_and_chains():
     par = wl.steps[0].layout.tree_parent
     par[0:8] = -1
     par[8:16] = [-1, 0, 1, 2, -1, 4, 5, 6]
+    return wl
+
+
+def _small_trees():
+    rng = np.random.default_rng(12)
+    sizes = [8, 5, 8, 5, 8, 3]
+    kv = [1, 40, 130, 700, 1300, 2]
+    reqs = [([], int(c), [q]) for c, q in zip(kv, sizes)]
+    wl = workloads.build_workload("tree_small", shared_lens=[], requests=reqs, seed=21,
+                                  **{k: v for k, v in KW.items() if k != "keep_segments"})
+    wl.steps[0].layout.tree_parent = np.concatenate([workloads.draft_tree(rng, q) for q in sizes])
     return wl
 
 
