@@ -30,8 +30,9 @@
 //              swizzle.  K frees early (after QK) and V late (after PV), so each
 //              ring refills on its own; page ids come from a 32-page window
 //              prefetched one window ahead.
-//   warp 6     MMA issuer: QK of tiles j and j+1 ahead of the softmax, PV of
-//              tile j once its P^T is written.
+//   warp 6     MMA issuer: QK two tiles ahead of the softmax over the CTA's
+//              whole tile stream (across tasks), PV of tile j once its P^T is
+//              written.
 //   warp 7     query rows of each task (cp.async, zero-filled past its rows)
 //              into one of two 128-byte swizzled buffers, a task ahead.
 // TMEM (128 columns): S^T_0 | S^T_1 | O^T_0 | O^T_1 (32 columns each); task i
@@ -103,8 +104,8 @@ struct TtLayout {
   static constexpr int m_off = red_off + kRows * 4 * 4;         // reference max per row
   static constexpr int a_off = m_off + kRows * 4;               // rescale factor per row
   static constexpr int inv_off = a_off + kRows * 4;             // 1 / l per row of a finished task
-  static constexpr int tok_off = inv_off + kRows * 4;           // its token ids: [kRows]
-  static constexpr int msk_off = tok_off + kRows * 4;           // draft-tree masks per token
+  static constexpr int base_off = inv_off + kRows * 4;          // its output offset per row
+  static constexpr int msk_off = base_off + kRows * 8;          // draft-tree masks per token
   static constexpr int bytes = msk_off + kRows * 8;
   static constexpr int smem_alloc = bytes + 1024;       // slack for the 1024-byte alignment
 };
@@ -212,7 +213,7 @@ struct SmCtx {
   uint8_t* smem;
   float* red_max;                  // [kRows][4 warps]
   float* red_sum;
-  int32_t* tok_s;                  // [kRows] token ids of the task (epilogue)
+  int64_t* base_s;                 // [kRows] element offset of every output row of that task
   float* m_s;                      // [kRows] reference max of every row
   float* a_s;                      // [kRows] rescale factor of every row
   float* inv_s;                    // [kRows] 1 / l of every row of the last finished task
@@ -244,7 +245,7 @@ __device__ __forceinline__ void lds_rows(const float* src, float (&dst)[NR]) {
 // every tile's S^T -> P^T; `after_first()` runs once the first tile's P^T is
 // handed over (the previous task's output then overlaps this task's MMAs);
 // then the task's row statistics: 1 / l per row (inv_s), lse of partial rows,
-// token ids (tok_s).  gt counts tiles.  Returns false when a wait ran out
+// output offsets (base_s).  gt counts tiles.  Returns false when a wait ran out
 // (decided by all 128 threads together).  The per-tile path keeps its rows in
 // registers; the rare paths (a task's first tile, a rescale, the statistics)
 // work one row per lane and through shared memory, so they stay short in code
@@ -257,7 +258,12 @@ __device__ __forceinline__ bool softmax_tiles(const SmCtx& c, const pps::Task& t
   const int nrows = task.n_tok * G;
   const bool causal = task.causal != PPS_NO_CAUSAL;
   const uint32_t tm_o = c.tm + 2 * kRows + (ti & 1) * kRows;
-  if (t < kRows) c.m_s[t] = t < nrows ? -INFINITY : 0.f;   // padding rows: P stays 0
+  // Every row starts from a reference of 0 (log2 units): P = exp2(x) is exact
+  // up to the bf16 rounding whatever the reference, as long as no score is
+  // above it by more than 2^8 (overflow side) or below -64 (underflow side,
+  // far from fp32's limit); a first tile outside that range takes the exact
+  // per-row maxima below.  Padding rows see no key, so their P stays 0.
+  if (t < kRows) c.m_s[t] = 0.f;
   // token ids for the statistics step (loaded now, stored there)
   const int32_t my_tok = t < task.n_tok ? p.rows[task.row_off + t] : 0;
   // Draft trees: bit k of a token's mask = the key k positions before its own
@@ -267,7 +273,7 @@ __device__ __forceinline__ bool softmax_tiles(const SmCtx& c, const pps::Task& t
   float m_ref[NR], l_sum[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
-    m_ref[r] = r < nrows ? -INFINITY : 0.f;
+    m_ref[r] = 0.f;
     l_sum[r] = 0.f;
   }
   if (n == 0 && !after_first()) return false;
@@ -294,7 +300,7 @@ __device__ __forceinline__ bool softmax_tiles(const SmCtx& c, const pps::Task& t
     const int first_vis = (full || !causal) ? 0 : G * (pos - task.causal);
     const bool key_ok = full || pos < task.kv_end;
     float x[NR];
-    bool need = j == 0;
+    bool need = false;
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
       bool vis = r < nrows && key_ok && r >= first_vis;
@@ -304,6 +310,7 @@ __device__ __forceinline__ bool softmax_tiles(const SmCtx& c, const pps::Task& t
       }
       x[r] = vis ? __uint_as_float(s[r]) * p.qk_scale : -INFINITY;
       need |= x[r] > m_ref[r] + kRescaleThreshold;
+      if (j == 0) need |= vis && x[r] < -64.f;
     }
     if (softmax_or(need)) {
       // exact per-row maxima of this tile over its 128 keys; lane r of warp 0
@@ -321,8 +328,12 @@ __device__ __forceinline__ bool softmax_tiles(const SmCtx& c, const pps::Task& t
         const float mt = fmaxf(fmaxf(mm.x, mm.y), fmaxf(mm.z, mm.w));
         const float mo = c.m_s[lane];
         float mn = mo;
-        if (mt > mo + kRescaleThreshold || (mo == -INFINITY && mt != -INFINITY)) mn = fmaxf(mt, mo);
-        c.a_s[lane] = (mo == -INFINITY) ? 0.f : ex2(mo - mn);
+        if (j == 0) {
+          if (mt != -INFINITY) mn = mt;      // first tile: the row's own maximum
+        } else if (mt > mo + kRescaleThreshold) {
+          mn = fmaxf(mt, mo);
+        }
+        c.a_s[lane] = j == 0 ? 1.f : ex2(mo - mn);   // nothing accumulated before the first tile
         c.m_s[lane] = mn;
       }
       softmax_sync();
@@ -360,8 +371,8 @@ __device__ __forceinline__ bool softmax_tiles(const SmCtx& c, const pps::Task& t
     uint32_t pk[NR / 2];
 #pragma unroll
     for (int r = 0; r < NR; r += 2) {
-      const float a = (m_ref[r] == -INFINITY) ? 0.f : ex2(x[r] - m_ref[r]);
-      const float b = (m_ref[r + 1] == -INFINITY) ? 0.f : ex2(x[r + 1] - m_ref[r + 1]);
+      const float a = ex2(x[r] - m_ref[r]);          // references are always finite
+      const float b = ex2(x[r + 1] - m_ref[r + 1]);
       l_sum[r] += a;
       l_sum[r + 1] += b;
       pk[r / 2] = pack_bf16(a, b);
@@ -386,31 +397,33 @@ __device__ __forceinline__ bool softmax_tiles(const SmCtx& c, const pps::Task& t
     reduce_scatter<NR, 16, false>(v, lane);
     c.red_sum[rs_row<NR, 16>(lane) * 4 + warp] = v[0];
   }
-  softmax_sync();             // also: the previous task's output is done with inv_s, tok_s
+  softmax_sync();             // also: the previous task's output is done with inv_s, base_s
+  // lane l of warp 0 holds token l: row r's token is lane r >> lg's
+  const int row_tok = __shfl_sync(0xffffffffu, my_tok, (lane >> lg) & 31);
   if (warp == 0 && lane < NR) {
+    // lane r: row r's 1 / l, its output offset (token or partial slot, head),
+    // and its lse when the row is a partial
     const float4 ss = *reinterpret_cast<const float4*>(c.red_sum + lane * 4);
     const float lsum = (ss.x + ss.y) + (ss.z + ss.w);
     c.inv_s[lane] = lsum > 0.f ? 1.f / lsum : 0.f;
-    if (task.out_pid >= 0 && lane < nrows) {
-      const int i = lane / G, h = task.kv_head * G + (lane - i * G);
-      p.lse_part[(size_t)(task.out_pid + i) * p.num_q_heads + h] =
-          lsum > 0.f ? c.m_s[lane] + __log2f(lsum) : -INFINITY;
-    }
+    const int i = lane >> lg, h = task.kv_head * G + (lane & (G - 1));
+    const int64_t slot = task.out_pid < 0 ? (int64_t)row_tok : (int64_t)task.out_pid + i;
+    c.base_s[lane] = (slot * p.num_q_heads + h) * D;
+    if (task.out_pid >= 0 && lane < nrows)
+      p.lse_part[slot * p.num_q_heads + h] = lsum > 0.f ? c.m_s[lane] + __log2f(lsum) : -INFINITY;
   }
-  if (t < task.n_tok) c.tok_s[t] = my_tok;
   softmax_sync();
   return true;
 }
 
-// The output of a finished task (statistics in inv_s / tok_s): once its last
+// The output of a finished task (statistics in inv_s / base_s): once its last
 // PV has completed, thread t writes element t of every row, O^T / l, as bf16
 // (or the fp32 partial).  Rows in groups of 8 TMEM columns, so the code is the
 // same for every row count.
 __device__ __forceinline__ bool softmax_output(const SmCtx& c, const pps::Task& task, int ti) {
   const TtParams& p = *c.p;
-  const int t = c.t, G = p.G;
-  const int lg = __ffs(G) - 1;                           // G is a power of two
-  const int n = n_tiles_of(task), nrows = task.n_tok * G;
+  const int t = c.t;
+  const int n = n_tiles_of(task), nrows = task.n_tok * p.G;
   bool got = true;
   if (n > 0) got = mbar_wait(smem_u32(&c.bars->o_done[ti & 1]), (ti >> 1) & 1) && !*c.abort_flag;
   if (softmax_or(!got)) {
@@ -435,11 +448,10 @@ __device__ __forceinline__ bool softmax_output(const SmCtx& c, const pps::Task& 
       const int r = c0 + r8;
       if (r < nrows) {
         const float val = __uint_as_float(o[r8]) * c.inv_s[r];
-        const int i = r >> lg, h = task.kv_head * G + (r & (G - 1));
         if (direct)
-          p.out[((size_t)c.tok_s[i] * p.num_q_heads + h) * D + t] = __float2bfloat16_rn(val);
+          p.out[c.base_s[r] + t] = __float2bfloat16_rn(val);
         else
-          p.o_part[((size_t)(task.out_pid + i) * p.num_q_heads + h) * D + t] = val;
+          p.o_part[c.base_s[r] + t] = val;
       }
     }
   }
@@ -469,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t p_base = smem_u32(smem + L::p_off);
   float* red_max = reinterpret_cast<float*>(smem + L::red_off);   // [kRows][4 warps]
   float* red_sum = red_max;                                       // (not live at once)
-  int32_t* tok_s = reinterpret_cast<int32_t*>(smem + L::tok_off); // [2][kRows]
+  int64_t* base_s = reinterpret_cast<int64_t*>(smem + L::base_off);  // [kRows]
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -513,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- softmax warps
     const int t = tid;                                   // TMEM lane: key t / element t
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    SmCtx ctx{&p,      &bars,         smem,     red_max, red_sum, tok_s,
+    SmCtx ctx{&p,      &bars,         smem,     red_max, red_sum, base_s,
               reinterpret_cast<float*>(smem + L::m_off), reinterpret_cast<float*>(smem + L::a_off),
               reinterpret_cast<float*>(smem + L::inv_off),
               reinterpret_cast<unsigned long long*>(smem + L::msk_off), &abort_flag, tm, lane_off,
@@ -664,21 +676,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
     };
-    TaskCursor cur(p.tasks, p.num_tasks, b, nctas);
-    pps::Task task;
-    for (int ti = 0; ok && cur.next(task); ++ti) {
-      const int n = n_tiles_of(task);
-      const int qb = ti & 1;
-      if (!warp_wait(&bars.q_full[qb], (ti >> 1) & 1)) { fail(); ok = false; break; }
-      if (n == 0) {
-        if (lane == 0) {                      // no QK read the buffer, no PV wrote O
-          mbar_arrive(smem_u32(&bars.q_empty[qb]));
-          mbar_arrive(smem_u32(&bars.o_done[qb]));
+    // QK runs two tiles ahead of PV over the CTA's whole tile stream, across
+    // task boundaries: the next task's first S is ready when the softmax
+    // finishes the current task.  `qc` walks the tasks for QK (waiting for
+    // each task's query rows), `pc` for PV.
+    TaskCursor qc(p.tasks, p.num_tasks, b, nctas);
+    pps::Task qtask{};
+    int q_ti = -1, q_n = 0, q_j = 0;                // task, its tiles, next tile to QK
+    int gq = 0;                                     // next global tile to QK
+    // QK of global tile gq; false when the stream has ended or a wait ran out
+    // (ok says which).
+    auto qk_next = [&]() -> bool {
+      while (q_j >= q_n) {
+        if (!qc.next(qtask)) return false;
+        ++q_ti;
+        q_n = n_tiles_of(qtask);
+        q_j = 0;
+        if (!warp_wait(&bars.q_full[q_ti & 1], (q_ti >> 1) & 1)) {
+          fail();
+          ok = false;
+          return false;
         }
+        if (q_n == 0) {                             // no QK reads the buffer
+          if (lane == 0) umma_commit(smem_u32(&bars.q_empty[q_ti & 1]));
+          __syncwarp();
+        }
+      }
+      if (!qk(gq, q_ti & 1)) {
+        fail();
+        ok = false;
+        return false;
+      }
+      if (q_j == q_n - 1) {                         // the task's last QK: its buffer frees
+        if (lane == 0) umma_commit(smem_u32(&bars.q_empty[q_ti & 1]));
+        __syncwarp();
+      }
+      ++q_j;
+      ++gq;
+      return true;
+    };
+    while (gq < 2 && qk_next()) {
+    }
+    TaskCursor pc(p.tasks, p.num_tasks, b, nctas);
+    pps::Task task;
+    for (int ti = 0; ok && pc.next(task); ++ti) {
+      const int n = n_tiles_of(task);
+      const int ob = ti & 1;
+      if (n == 0) {                                 // nothing accumulated: O is ready now
+        if (lane == 0) umma_commit(smem_u32(&bars.o_done[ob]));
         __syncwarp();
         continue;
       }
-      if (!qk(gt, qb) || (n > 1 && !qk(gt + 1, qb))) { fail(); ok = false; break; }
       for (int j = 0; j < n; ++j) {
         const int g = gt + j, sb = g & 1, st = g % kStages;
         if (!warp_wait(&bars.p_full[sb], (g >> 1) & 1)) { fail(); ok = false; break; }
@@ -691,18 +739,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t pt = p_base + sb * L::p_tile;
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
-            umma_ss(tm_o + qb * kRows, smem_desc(vt + ks * 2048, 16384, 1024),
+            umma_ss(tm_o + ob * kRows, smem_desc(vt + ks * 2048, 16384, 1024),
                     smem_desc(pt + ks * 1024, 1024, 512, kLayoutSwizzle64), id_pv,
                     (j > 0 || ks > 0) ? 1u : 0u);
           umma_commit(smem_u32(&bars.v_empty[st]));
           umma_commit(smem_u32(&bars.p_empty[sb]));
-          if (j == n - 1) {
-            umma_commit(smem_u32(&bars.o_done[qb]));
-            umma_commit(smem_u32(&bars.q_empty[qb]));    // every QK of the task has run
-          }
+          if (j == n - 1) umma_commit(smem_u32(&bars.o_done[ob]));
         }
         __syncwarp();
-        if (j + 2 < n && !qk(g + 2, qb)) { fail(); ok = false; break; }
+        // S buffer (g & 1) is free again: QK of tile g + 2, whichever task
+        while (ok && gq <= g + 2 && qk_next()) {
+        }
+        if (!ok) break;
       }
       gt += n;
     }

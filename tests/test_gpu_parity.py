@@ -147,6 +147,26 @@ def test_parity_long_tasks(pps, chunk, flags):
     assert mx <= MAX_ABS and mean <= MEAN_ABS, (mx, mean)
 
 
+@pytest.mark.parametrize("flags", [0, 4])
+@pytest.mark.parametrize("name", ["decode_heavy", "radix_sharing", "mixed_budget", "tree_small_g4"])
+def test_parity_wide_scores(pps, name, flags):
+    """Query rows scaled by 32 (exact in bf16): scores spread over hundreds of
+    log2 units, so first tiles fall outside the one-pass window (exact maxima),
+    references rise mid-task (O rescaled in TMEM), and softmax rows are sharply
+    peaked."""
+    wl = small_cases()[name]()
+    for st in wl.steps:
+        st.q = (st.q.float() * 32.0).to(torch.bfloat16)
+    ref, _ = oracle_steps(wl)
+    pps.get_device_error(clear=True)
+    outs, _, plans = run_workload(wl, flags=flags)
+    assert pps.get_device_error(clear=True) == 0
+    for s, (o, r) in enumerate(zip(outs, ref)):
+        assert torch.isfinite(o).all()
+        mx, mean = errors(o, r)
+        assert mx <= MAX_ABS and mean <= MEAN_ABS, (s, mx, mean)
+
+
 @pytest.mark.parametrize("chunk", [16, 64, 200])
 def test_parity_forced_split(chunk):
     wl, (ref, _) = _small("mixed_budget")
