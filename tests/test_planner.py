@@ -256,3 +256,34 @@ def test_tree_size_limit(pps):
     plan = pps.attn_plan([0, q], [q + 5], [0, 5], list(range(5)), 8, 2, 64, 16, 5,
                          tree_parent=list(range(-1, q - 1)))
     assert plan.info()["num_tree_requests"] == 0
+
+
+def test_key_tile_splits_are_even_whole_tiles(pps):
+    """Adaptive chunking for key-tile tasks: a span within a quarter over the
+    chunk stays whole; longer spans split into pieces of whole 128-key tiles
+    that differ by at most one tile; no piece is a one-tile remainder unless
+    its span is that short; tasks are ordered by tiles (work), largest first."""
+    for L in (workloads.radix_sharing(values=False).layout,
+              workloads.decode_heavy(values=False).layout):
+        plan = _plan(pps, L)
+        assert plan.info()["small_rows_on_tensor"] == 1
+        t = plan.array("bw_tasks")
+        Hkv = L.num_kv_heads
+        heads0 = t[t[:, 2] == 0]                       # one record per task set
+        by_span = {}
+        for rec in heads0:
+            by_span.setdefault((int(rec[0]), int(rec[6])), []).append(rec)
+        for pieces in by_span.values():
+            pieces.sort(key=lambda r: r[4])
+            lens = [int(r[5] - r[4]) for r in pieces]
+            for r in pieces[:-1]:
+                assert (r[5] - r[4]) % 128 == 0       # whole tiles before the last piece
+            if len(pieces) > 1:
+                assert max(lens[:-1]) - min(lens[:-1]) <= 128
+                assert lens[-1] > 128 or sum(lens) <= 2 * 128
+        tiles = -(-(t[:, 5] - t[:, 4]) // 128)
+        work = (tiles + 2) * 128
+        assert (np.diff(work[::Hkv]) <= 0).all()      # sorted by work, descending
+    # the radix roots (2048 keys) stay whole: 8 subtrees x 8 kv heads of 16 tiles
+    t = _plan(pps, workloads.radix_sharing(values=False).layout).array("bw_tasks")
+    assert int(((t[:, 5] - t[:, 4]) == 2048).sum()) == 64
