@@ -10,7 +10,9 @@ larger than the 129 MB L2, so no flush is needed between steps).
 
 Prints one JSON line.  ``value`` is tokens/s with inputs resident in HBM;
 ``e2e`` is the same metric with every step's inputs copied from pinned host
-memory and the output copied back inside the timed region.  Under torchrun
+memory and the output copied back inside the timed region: one
+``pps_attn_step_host`` call per step (host rows and tables in, host rows out;
+for the serving loops, the same copies around the device calls).  Under torchrun
 each rank runs its own batch (weak scaling, no data-path collective).
 ``--impl reference`` times the fp64 CPU oracle on a bounded sample instead.
 """
@@ -349,29 +351,25 @@ def run_pps(args):
     value = total_tokens / (ms_max / 1e3)
 
     # ---- e2e: host buffers in, host result out, through the public API -------------------
+    # One pps_attn_step_host call per step: the step's rows and tables go from
+    # page-locked host memory to the device, through append, plan and attention,
+    # and the output rows come back, all enqueued by the library.
     h = []
     for s in steps:
-        st = s["st"]
+        st, L = s["st"], s["L"]
         host = {n: st.__dict__[n].cpu().pin_memory() for n in ("q", "k_new", "v_new")}
-        host.update({n: v.cpu().pin_memory() for n, v in s["tabs"].items()})
-        dv = {n: torch.empty_like(v, device=dev) for n, v in host.items()}
-        h.append(dict(host=host, dev=dv, out_h=torch.empty_like(s["out"], device="cpu").pin_memory()))
-    bi = sum(v.numel() * v.element_size() for x in h for v in x["host"].values())
+        h.append(dict(host=host, out_h=torch.empty_like(s["out"], device="cpu").pin_memory()))
+    tab_bytes = sum(4 * (3 * s["L"].num_requests + 2 + len(s["L"].page_indices)) for s in steps)
+    bi = sum(v.numel() * v.element_size() for x in h for v in x["host"].values()) + tab_bytes
     bo = sum(x["out_h"].numel() * x["out_h"].element_size() for x in h)
 
     def e2e_step():
         for s, x in zip(steps, h):
             L = s["L"]
-            for n, v in x["host"].items():
-                x["dev"][n].copy_(v, non_blocking=True)
-            d = x["dev"]
-            pps.kv_append(pk, pv, d["k_new"], d["v_new"], d["q_indptr"], d["cached_len"],
-                          d["page_indptr"], d["page_indices"])
-            plan = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices,
-                                 L.num_q_heads, L.num_kv_heads, L.head_dim, L.page_size,
-                                 L.num_pages, tree_parent=L.tree_parent)
-            pps.attn_run(plan, d["q"], pk, pv, s["out"], s["ws"])
-            x["out_h"].copy_(s["out"], non_blocking=True)
+            hq = x["host"]
+            pps.attn_step_host(pk, pv, hq["q"], hq["k_new"], hq["v_new"], L.q_indptr, L.kv_len,
+                               L.page_indptr, L.page_indices, x["out_h"],
+                               tree_parent=L.tree_parent)
 
     for _ in range(max(3, args.warmup // 4)):
         e2e_step()

@@ -555,6 +555,42 @@ pps_status pps_plan_get_info(const pps_plan* plan, pps_plan_info* info);
 pps_status pps_plan_get_array(const pps_plan* plan, int32_t which, const int32_t** data,
                               int64_t* count);
 
+/*
+ * pps_attn_step_host -- one whole step from host memory: the step's new K/V
+ * rows, query rows and tables are copied to device scratch, the K/V rows are
+ * appended to the pool (pps_kv_append), the batch is planned (pps_attn_plan_tree
+ * on the host tables) and attended (pps_attn_run), and the output rows are
+ * copied back.  The same operations as the device-side calls, in one native
+ * call, for a caller that keeps its batch on the host (the XY-Serve review's
+ * serving step, "Core claim": each step's mixed batch through one attention).
+ *
+ *  pool                  host pointer to the pool descriptor (k, v device).
+ *  h_q                   host bf16 [T, num_q_heads, head_dim], T = h_q_indptr[R].
+ *  h_k_new, h_v_new      host bf16 [T, num_kv_heads, head_dim].
+ *  h_q_indptr, h_kv_len, h_page_indptr, h_page_indices, h_tree_parent
+ *                        host int32 tables as for pps_attn_plan_tree (tree may be
+ *                        NULL); each request's new tokens are its last q_len
+ *                        positions (cached_len = kv_len - q_len).
+ *  h_out                 host bf16 [T, num_q_heads, head_dim], written when the
+ *                        stream reaches the end of this step.
+ *  d_scratch             device, 256-byte aligned, scratch_bytes long; the size
+ *                        it needs is written to *out_scratch_bytes (may be NULL).
+ * Everything is enqueued on `stream`; page-locked host rows make the copies
+ * asynchronous, and every host buffer must stay valid until the stream has
+ * passed this step.  The host tables are read before the call returns.
+ * The row copies start before the host plans, so on PPS_ERR_WORKSPACE (scratch
+ * missing, misaligned or smaller than needed) or a planning error only the
+ * scratch may have been written; the pool is untouched.
+ * Errors: as pps_attn_plan_tree and pps_attn_run, and PPS_ERR_WORKSPACE.
+ */
+pps_status pps_attn_step_host(const pps_pool* pool, const void* h_q, const void* h_k_new,
+                              const void* h_v_new, const int32_t* h_q_indptr,
+                              const int32_t* h_kv_len, const int32_t* h_page_indptr,
+                              const int32_t* h_page_indices, const int32_t* h_tree_parent,
+                              int32_t num_requests, int32_t num_q_heads, float sm_scale,
+                              const pps_plan_options* opts, void* h_out, void* d_scratch,
+                              size_t scratch_bytes, size_t* out_scratch_bytes, void* stream);
+
 /* Reads the current device's error word into *code (0 = none); if `clear`
  * is nonzero, resets it to 0.  Synchronous (waits for the device). */
 pps_status pps_get_device_error(int32_t* code, int32_t clear);

@@ -276,6 +276,101 @@ pps_status pps_attn_run_events(const pps_plan* plan, const void* q, const pps_po
   return run_impl(plan, q, pool, out, workspace, workspace_bytes, stream, events);
 }
 
+pps_status pps_attn_step_host(const pps_pool* pool, const void* h_q, const void* h_k_new,
+                              const void* h_v_new, const int32_t* h_q_indptr,
+                              const int32_t* h_kv_len, const int32_t* h_page_indptr,
+                              const int32_t* h_page_indices, const int32_t* h_tree_parent,
+                              int32_t num_requests, int32_t num_q_heads, float sm_scale,
+                              const pps_plan_options* opts, void* h_out, void* d_scratch,
+                              size_t scratch_bytes, size_t* out_scratch_bytes, void* stream) {
+  if (out_scratch_bytes) *out_scratch_bytes = 0;
+  if (!pool_ok(pool) || num_requests < 0 || num_q_heads <= 0 || !h_q_indptr ||
+      (num_requests > 0 && (!h_kv_len || !h_page_indptr)))
+    return pool && (pool->head_dim != 64 && pool->head_dim != 128) ? PPS_ERR_UNSUPPORTED
+                                                                     : PPS_ERR_INVALID_ARGUMENT;
+  const int32_t R = num_requests;
+  const int32_t T = h_q_indptr[R];
+  if (T < 0 || (T > 0 && (!h_q || !h_k_new || !h_v_new || !h_out)))
+    return PPS_ERR_INVALID_ARGUMENT;
+  // Device scratch: rows in and out, the step's tables, then the plan's
+  // workspace.  Everything before the workspace is sized by the batch alone,
+  // so the copies in start before the host plans (the GPU moves rows while the
+  // planner runs) and only the workspace check waits for the plan.
+  if (!h_page_indptr && R > 0) return PPS_ERR_INVALID_ARGUMENT;
+  auto al = [](size_t n) { return (n + 255) / 256 * 256; };
+  const size_t D = (size_t)pool->head_dim;
+  const size_t q_bytes = (size_t)T * num_q_heads * D * 2;
+  const size_t kv_bytes = (size_t)T * pool->num_kv_heads * D * 2;
+  const int64_t nnz = R > 0 ? h_page_indptr[R] : 0;
+  if (nnz < 0 || (nnz > 0 && !h_page_indices)) return PPS_ERR_INVALID_ARGUMENT;
+  const size_t tab_ints = (size_t)(R + 1) + R + (R + 1) + (size_t)nnz;
+  const size_t off_q = 0, off_k = al(q_bytes), off_v = off_k + al(kv_bytes),
+               off_out = off_v + al(kv_bytes), off_tab = off_out + al(q_bytes),
+               off_ws = off_tab + al(tab_ints * 4);
+  if (!d_scratch || scratch_bytes < off_ws || ((uintptr_t)d_scratch & 255)) {
+    // report the whole size (rows, tables and the plan's workspace); nothing enqueued
+    pps_plan* probe = nullptr;
+    size_t ws = 0;
+    const pps_status ps = pps_attn_plan_tree(h_q_indptr, h_kv_len, h_page_indptr, h_page_indices,
+                                             h_tree_parent, R, num_q_heads, pool->num_kv_heads,
+                                             pool->head_dim, pool->page_size, pool->num_pages,
+                                             sm_scale, opts, &probe, &ws);
+    if (ps != PPS_OK) return ps;
+    pps_plan_destroy(probe);
+    if (out_scratch_bytes) *out_scratch_bytes = off_ws + al(ws);
+    return PPS_ERR_WORKSPACE;
+  }
+  char* sc = (char*)d_scratch;
+  auto stm = (cudaStream_t)stream;
+  // 1. rows in (only the scratch is written until the plan is known)
+  if (T > 0 &&
+      (cudaMemcpyAsync(sc + off_q, h_q, q_bytes, cudaMemcpyHostToDevice, stm) != cudaSuccess ||
+       cudaMemcpyAsync(sc + off_k, h_k_new, kv_bytes, cudaMemcpyHostToDevice, stm) != cudaSuccess ||
+       cudaMemcpyAsync(sc + off_v, h_v_new, kv_bytes, cudaMemcpyHostToDevice, stm) != cudaSuccess))
+    return PPS_ERR_CUDA;
+  // 2. the plan, from the host tables (checks them all)
+  pps_plan* plan = nullptr;
+  size_t ws_bytes = 0;
+  pps_status st = pps_attn_plan_tree(h_q_indptr, h_kv_len, h_page_indptr, h_page_indices,
+                                     h_tree_parent, R, num_q_heads, pool->num_kv_heads,
+                                     pool->head_dim, pool->page_size, pool->num_pages, sm_scale,
+                                     opts, &plan, &ws_bytes);
+  if (st != PPS_OK) return st;
+  const size_t need = off_ws + al(ws_bytes);
+  if (out_scratch_bytes) *out_scratch_bytes = need;
+  if (scratch_bytes < need) {
+    pps_plan_destroy(plan);
+    return PPS_ERR_WORKSPACE;
+  }
+  // 3. tables (q_indptr, cached_len = kv_len - q_len, page CSR) through one
+  // page-locked staging buffer, reused only after this upload completes
+  pps::HostBuf tb = pps::host_buf_acquire(std::max<size_t>(tab_ints, 1));
+  if (!tb.data) {
+    pps_plan_destroy(plan);
+    return PPS_ERR_NO_MEMORY;
+  }
+  int32_t* t = tb.data;
+  std::memcpy(t, h_q_indptr, (size_t)(R + 1) * 4);
+  for (int32_t r = 0; r < R; ++r) t[R + 1 + r] = h_kv_len[r] - (h_q_indptr[r + 1] - h_q_indptr[r]);
+  if (R > 0) std::memcpy(t + 2 * R + 1, h_page_indptr, (size_t)(R + 1) * 4);
+  if (nnz) std::memcpy(t + 3 * R + 2, h_page_indices, (size_t)nnz * 4);
+  bool ok = cudaMemcpyAsync(sc + off_tab, t, tab_ints * 4, cudaMemcpyHostToDevice, stm) ==
+            cudaSuccess;
+  ok = ok && pps::host_buf_mark_use(tb, stream) == 0;
+  pps::host_buf_release(tb);
+  // 4. append, attend, rows out
+  const int32_t* d_tab = (const int32_t*)(sc + off_tab);
+  if (ok) st = pps_kv_append(pool, sc + off_k, sc + off_v, d_tab, d_tab + R + 1, d_tab + 2 * R + 1,
+                             d_tab + 3 * R + 2, R, T, stream);
+  if (ok && st == PPS_OK)
+    st = run_impl(plan, sc + off_q, pool, sc + off_out, sc + off_ws, al(ws_bytes), stream, nullptr);
+  if (ok && st == PPS_OK && T > 0)
+    ok = cudaMemcpyAsync(h_out, sc + off_out, q_bytes, cudaMemcpyDeviceToHost, stm) == cudaSuccess;
+  pps_plan_destroy(plan);
+  if (!ok) return PPS_ERR_CUDA;
+  return st;
+}
+
 pps_status pps_get_device_error(int32_t* code, int32_t clear) {
   if (!code) return PPS_ERR_INVALID_ARGUMENT;
   *code = 0;
@@ -317,6 +412,6 @@ const char* pps_status_string(pps_status s) {
   }
 }
 
-int32_t pps_version(void) { return 210; }
+int32_t pps_version(void) { return 220; }
 
 }  // extern "C"

@@ -1,0 +1,63 @@
+"""GPU: pps_attn_step_host (host rows and tables in, host output out) against
+the device-side calls (pps_kv_append + pps_attn_plan + pps_attn_run) on the same
+batch: the same kernels and plan, so the output rows and the pool must match
+bit for bit; and both within the oracle tolerance (the device path is checked
+against the oracle in test_gpu_parity)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_run import run_workload, to_device
+from test_gpu_parity import small_cases
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(pps):
+    assert torch.cuda.is_available()
+    return pps
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("name", ["decode_heavy", "radix_sharing", "mixed_budget", "tree_small_g4",
+                                  "d64_g8"])
+def test_step_host_matches_device_calls(pps, name, pinned):
+    wl = small_cases()[name]()
+    dev_in = to_device(wl)
+    outs, (pk, pv), _ = run_workload(wl, device_inputs=dev_in)
+    pk2, pv2 = wl.pool_k.to("cuda", copy=True), wl.pool_v.to("cuda", copy=True)
+    for s, st in enumerate(wl.steps):
+        L = st.layout
+        host = lambda t: t.cpu().contiguous().pin_memory() if pinned else t.cpu().contiguous()
+        q, k, v = host(st.q), host(st.k_new), host(st.v_new)
+        out = torch.full(tuple(st.q.shape), float("nan"), dtype=torch.bfloat16)
+        out = out.pin_memory() if pinned else out
+        pps.get_device_error(clear=True)
+        pps.attn_step_host(pk2, pv2, q, k, v, L.q_indptr, L.kv_len, L.page_indptr, L.page_indices,
+                           out, tree_parent=L.tree_parent)
+        torch.cuda.synchronize()
+        assert pps.get_device_error(clear=True) == 0
+        assert torch.equal(out.view(torch.int16), outs[s].cpu().view(torch.int16)), s
+    assert torch.equal(pk2.view(torch.int16), pk.view(torch.int16))
+    assert torch.equal(pv2.view(torch.int16), pv.view(torch.int16))
+
+
+def test_step_host_scratch_checks(pps):
+    wl = small_cases()["decode_heavy"]()
+    st = wl.steps[0]
+    L = st.layout
+    pk, pv = wl.pool_k.to("cuda", copy=True), wl.pool_v.to("cuda", copy=True)
+    before = pk.clone()
+    out = torch.empty(tuple(st.q.shape), dtype=torch.bfloat16)
+    tiny = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pps.PPSError, match="workspace"):
+        pps.attn_step_host(pk, pv, st.q.cpu(), st.k_new.cpu(), st.v_new.cpu(), L.q_indptr,
+                           L.kv_len, L.page_indptr, L.page_indices, out, scratch=tiny)
+    torch.cuda.synchronize()
+    assert torch.equal(pk.view(torch.int16), before.view(torch.int16))   # nothing enqueued
+    with pytest.raises(pps.PPSError):
+        pps.attn_step_host(pk, pv, st.q.cuda(), st.k_new.cpu(), st.v_new.cpu(), L.q_indptr,
+                           L.kv_len, L.page_indptr, L.page_indices, out)
