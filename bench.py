@@ -276,6 +276,7 @@ def run_pps(args):
     nk = pps.NUM_KERNEL_CLASSES
 
     def one_step(ev=None):
+        # append (device tables resident), plan (host, every step), attention
         for i, s in enumerate(steps):
             L, st, t = s["L"], s["st"], s["tabs"]
             pps.kv_append(pk, pv, st.k_new, st.v_new, t["q_indptr"], t["cached_len"],

@@ -556,6 +556,26 @@ pps_status pps_plan_get_array(const pps_plan* plan, int32_t which, const int32_t
                               int64_t* count);
 
 /*
+ * pps_attn_step -- one whole step with the rows already on the device and the
+ * tables on the host: the tables are uploaded (through a page-locked staging
+ * buffer) into d_scratch, the new K/V rows appended (pps_kv_append), the batch
+ * planned (pps_attn_plan_tree) and attended (pps_attn_run, or
+ * pps_attn_run_events when `events` is not NULL).  The same operations as the
+ * three device-side calls, in one native call per step.
+ *
+ *  q, k_new, v_new, out  device bf16 rows as for pps_kv_append / pps_attn_run.
+ *  host tables, scratch, errors: as pps_attn_step_host (its scratch holds only
+ *  the tables and the plan's workspace here).
+ */
+pps_status pps_attn_step(const pps_pool* pool, const void* q, const void* k_new, const void* v_new,
+                         const int32_t* h_q_indptr, const int32_t* h_kv_len,
+                         const int32_t* h_page_indptr, const int32_t* h_page_indices,
+                         const int32_t* h_tree_parent, int32_t num_requests, int32_t num_q_heads,
+                         float sm_scale, const pps_plan_options* opts, void* out, void* d_scratch,
+                         size_t scratch_bytes, size_t* out_scratch_bytes, void* stream,
+                         void* const* events);
+
+/*
  * pps_attn_step_host -- one whole step from host memory: the step's new K/V
  * rows, query rows and tables are copied to device scratch, the K/V rows are
  * appended to the pool (pps_kv_append), the batch is planned (pps_attn_plan_tree

@@ -21,7 +21,7 @@ import numpy as np
 
 __all__ = [
     "PPSError", "Plan", "lib", "build", "kv_append", "attn_plan", "attn_run", "plan_destroy",
-    "attn_step_host",
+    "attn_step_host", "attn_step",
     "get_device_error", "launch_count", "status_string", "version", "LIB_PATH",
     "PLAN_NO_GROUPS", "PLAN_CUDA_CORES_ONLY", "PLAN_SMALL_ROWS_CUDA_CORES", "KERNEL_BANDWIDTH", "KERNEL_TENSOR", "KERNEL_MERGE",
 ]
@@ -151,6 +151,10 @@ def lib():
                                      i32, ctypes.c_float, ctypes.POINTER(_PlanOptions), vp, vp,
                                      sz, ctypes.POINTER(sz), vp]
     L.pps_attn_step_host.restype = i32
+    L.pps_attn_step.argtypes = [ctypes.POINTER(_Pool), vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                ctypes.c_float, ctypes.POINTER(_PlanOptions), vp, vp, sz,
+                                ctypes.POINTER(sz), vp, vp]
+    L.pps_attn_step.restype = i32
     L.pps_attn_run_noalloc.argtypes = [vp, vp, ctypes.POINTER(_Pool), vp, vp]
     L.pps_attn_run_noalloc.restype = i32
     L.pps_plan_destroy.argtypes = [vp]
@@ -709,6 +713,47 @@ def attn_step_host(pool_k, pool_v, q, k_new, v_new, q_indptr, kv_len, page_indpt
             break
         _step_scratch[dev] = torch.empty(int(need.value * 1.25) + 256, dtype=torch.uint8, device=dev)
     _check(code, "pps_attn_step_host")
+
+
+def attn_step(pool_k, pool_v, q, k_new, v_new, q_indptr, kv_len, page_indptr, page_indices, out,
+              tree_parent=None, sm_scale=None, num_sms=0, bw_chunk_tokens=0, mma_chunk_tokens=0,
+              flags=0, scratch=None, stream=None, events=None):
+    """pps_attn_step: q, k_new, v_new, out are bf16 CUDA tensors, the tables host
+    int32 arrays.  Scratch as attn_step_host; `events` as attn_run."""
+    import torch
+    pool = _pool(pool_k, pool_v)
+    qi, qi_p = _host_addr(q_indptr)
+    kl, kl_p = _host_addr(kv_len)
+    pi, pi_p = _host_addr(page_indptr)
+    px, px_p = _host_addr(page_indices if len(page_indices) else np.zeros(1, np.int32))
+    tp, tp_p = (None, None) if tree_parent is None else \
+        _host_addr(tree_parent if len(tree_parent) else np.zeros(1, np.int32))
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(pool_k.shape[3])
+    opts = _PlanOptions(int(num_sms), int(bw_chunk_tokens), int(mma_chunk_tokens), int(flags))
+    bf = torch.bfloat16
+    ev = None
+    if events is not None:
+        handles = []
+        for e in events:
+            if e is not None and not e.cuda_event:
+                e.record()          # torch creates the CUDA event on first record
+            handles.append(ctypes.c_void_p(e.cuda_event) if e is not None else None)
+        ev = (ctypes.c_void_p * (2 * NUM_KERNEL_CLASSES))(*handles)
+    args = [ctypes.byref(pool), _dev(q, bf), _dev(k_new, bf), _dev(v_new, bf), qi_p, kl_p, pi_p,
+            px_p, tp_p, len(kl), int(q.shape[1]), float(sm_scale), ctypes.byref(opts),
+            _dev(out, bf)]
+    need = ctypes.c_size_t()
+    dev = pool_k.device
+    for _ in range(2):
+        sc = scratch if scratch is not None else _step_scratch.get(dev)
+        ptr = _dev(sc) if sc is not None else None
+        n = sc.numel() if sc is not None else 0
+        code = lib().pps_attn_step(*args, ptr, n, ctypes.byref(need), _stream(stream), ev)
+        if code != -4 or scratch is not None:
+            break
+        _step_scratch[dev] = torch.empty(int(need.value * 1.25) + 256, dtype=torch.uint8, device=dev)
+    _check(code, "pps_attn_step")
 
 
 def gemm_bf16(a, w, c, stream=None):

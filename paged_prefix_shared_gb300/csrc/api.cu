@@ -276,13 +276,21 @@ pps_status pps_attn_run_events(const pps_plan* plan, const void* q, const pps_po
   return run_impl(plan, q, pool, out, workspace, workspace_bytes, stream, events);
 }
 
-pps_status pps_attn_step_host(const pps_pool* pool, const void* h_q, const void* h_k_new,
-                              const void* h_v_new, const int32_t* h_q_indptr,
-                              const int32_t* h_kv_len, const int32_t* h_page_indptr,
-                              const int32_t* h_page_indices, const int32_t* h_tree_parent,
-                              int32_t num_requests, int32_t num_q_heads, float sm_scale,
-                              const pps_plan_options* opts, void* h_out, void* d_scratch,
-                              size_t scratch_bytes, size_t* out_scratch_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// One step: rows on the host (copied into scratch first) or already on the
+// device; host tables uploaded through a page-locked staging buffer; append,
+// plan, attention; rows out (to the host, or left in the caller's device
+// output).  The row copies start before the host plans.
+pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, const void* v_new,
+                     bool rows_on_host, const int32_t* h_q_indptr, const int32_t* h_kv_len,
+                     const int32_t* h_page_indptr, const int32_t* h_page_indices,
+                     const int32_t* h_tree_parent, int32_t num_requests, int32_t num_q_heads,
+                     float sm_scale, const pps_plan_options* opts, void* out, void* d_scratch,
+                     size_t scratch_bytes, size_t* out_scratch_bytes, void* stream,
+                     void* const* events) {
   if (out_scratch_bytes) *out_scratch_bytes = 0;
   if (!pool_ok(pool) || num_requests < 0 || num_q_heads <= 0 || !h_q_indptr ||
       (num_requests > 0 && (!h_kv_len || !h_page_indptr)))
@@ -290,13 +298,9 @@ pps_status pps_attn_step_host(const pps_pool* pool, const void* h_q, const void*
                                                                      : PPS_ERR_INVALID_ARGUMENT;
   const int32_t R = num_requests;
   const int32_t T = h_q_indptr[R];
-  if (T < 0 || (T > 0 && (!h_q || !h_k_new || !h_v_new || !h_out)))
-    return PPS_ERR_INVALID_ARGUMENT;
-  // Device scratch: rows in and out, the step's tables, then the plan's
-  // workspace.  Everything before the workspace is sized by the batch alone,
-  // so the copies in start before the host plans (the GPU moves rows while the
-  // planner runs) and only the workspace check waits for the plan.
-  if (!h_page_indptr && R > 0) return PPS_ERR_INVALID_ARGUMENT;
+  if (T < 0 || (T > 0 && (!q || !k_new || !v_new || !out))) return PPS_ERR_INVALID_ARGUMENT;
+  // Device scratch: [rows in and out, host rows only] tables, then the plan's
+  // workspace.  Everything before the workspace is sized by the batch alone.
   auto al = [](size_t n) { return (n + 255) / 256 * 256; };
   const size_t D = (size_t)pool->head_dim;
   const size_t q_bytes = (size_t)T * num_q_heads * D * 2;
@@ -304,17 +308,19 @@ pps_status pps_attn_step_host(const pps_pool* pool, const void* h_q, const void*
   const int64_t nnz = R > 0 ? h_page_indptr[R] : 0;
   if (nnz < 0 || (nnz > 0 && !h_page_indices)) return PPS_ERR_INVALID_ARGUMENT;
   const size_t tab_ints = (size_t)(R + 1) + R + (R + 1) + (size_t)nnz;
+  const size_t rows = rows_on_host ? al(q_bytes) * 2 + al(kv_bytes) * 2 : 0;
   const size_t off_q = 0, off_k = al(q_bytes), off_v = off_k + al(kv_bytes),
-               off_out = off_v + al(kv_bytes), off_tab = off_out + al(q_bytes),
-               off_ws = off_tab + al(tab_ints * 4);
+               off_out = off_v + al(kv_bytes), off_tab = rows, off_ws = off_tab + al(tab_ints * 4);
+  auto plan_for = [&](pps_plan** pl, size_t* ws) {
+    return pps_attn_plan_tree(h_q_indptr, h_kv_len, h_page_indptr, h_page_indices, h_tree_parent,
+                              R, num_q_heads, pool->num_kv_heads, pool->head_dim, pool->page_size,
+                              pool->num_pages, sm_scale, opts, pl, ws);
+  };
   if (!d_scratch || scratch_bytes < off_ws || ((uintptr_t)d_scratch & 255)) {
     // report the whole size (rows, tables and the plan's workspace); nothing enqueued
     pps_plan* probe = nullptr;
     size_t ws = 0;
-    const pps_status ps = pps_attn_plan_tree(h_q_indptr, h_kv_len, h_page_indptr, h_page_indices,
-                                             h_tree_parent, R, num_q_heads, pool->num_kv_heads,
-                                             pool->head_dim, pool->page_size, pool->num_pages,
-                                             sm_scale, opts, &probe, &ws);
+    const pps_status ps = plan_for(&probe, &ws);
     if (ps != PPS_OK) return ps;
     pps_plan_destroy(probe);
     if (out_scratch_bytes) *out_scratch_bytes = off_ws + al(ws);
@@ -322,19 +328,26 @@ pps_status pps_attn_step_host(const pps_pool* pool, const void* h_q, const void*
   }
   char* sc = (char*)d_scratch;
   auto stm = (cudaStream_t)stream;
-  // 1. rows in (only the scratch is written until the plan is known)
-  if (T > 0 &&
-      (cudaMemcpyAsync(sc + off_q, h_q, q_bytes, cudaMemcpyHostToDevice, stm) != cudaSuccess ||
-       cudaMemcpyAsync(sc + off_k, h_k_new, kv_bytes, cudaMemcpyHostToDevice, stm) != cudaSuccess ||
-       cudaMemcpyAsync(sc + off_v, h_v_new, kv_bytes, cudaMemcpyHostToDevice, stm) != cudaSuccess))
-    return PPS_ERR_CUDA;
-  // 2. the plan, from the host tables (checks them all)
+  const void* dq = q;
+  const void* dk = k_new;
+  const void* dv = v_new;
+  void* dout = out;
+  if (rows_on_host) {
+    // rows in (only the scratch is written until the plan is known)
+    if (T > 0 &&
+        (cudaMemcpyAsync(sc + off_q, q, q_bytes, cudaMemcpyHostToDevice, stm) != cudaSuccess ||
+         cudaMemcpyAsync(sc + off_k, k_new, kv_bytes, cudaMemcpyHostToDevice, stm) != cudaSuccess ||
+         cudaMemcpyAsync(sc + off_v, v_new, kv_bytes, cudaMemcpyHostToDevice, stm) != cudaSuccess))
+      return PPS_ERR_CUDA;
+    dq = sc + off_q;
+    dk = sc + off_k;
+    dv = sc + off_v;
+    dout = sc + off_out;
+  }
+  // the plan, from the host tables (checks them all)
   pps_plan* plan = nullptr;
   size_t ws_bytes = 0;
-  pps_status st = pps_attn_plan_tree(h_q_indptr, h_kv_len, h_page_indptr, h_page_indices,
-                                     h_tree_parent, R, num_q_heads, pool->num_kv_heads,
-                                     pool->head_dim, pool->page_size, pool->num_pages, sm_scale,
-                                     opts, &plan, &ws_bytes);
+  pps_status st = plan_for(&plan, &ws_bytes);
   if (st != PPS_OK) return st;
   const size_t need = off_ws + al(ws_bytes);
   if (out_scratch_bytes) *out_scratch_bytes = need;
@@ -342,7 +355,7 @@ pps_status pps_attn_step_host(const pps_pool* pool, const void* h_q, const void*
     pps_plan_destroy(plan);
     return PPS_ERR_WORKSPACE;
   }
-  // 3. tables (q_indptr, cached_len = kv_len - q_len, page CSR) through one
+  // tables (q_indptr, cached_len = kv_len - q_len, page CSR) through one
   // page-locked staging buffer, reused only after this upload completes
   pps::HostBuf tb = pps::host_buf_acquire(std::max<size_t>(tab_ints, 1));
   if (!tb.data) {
@@ -358,17 +371,46 @@ pps_status pps_attn_step_host(const pps_pool* pool, const void* h_q, const void*
             cudaSuccess;
   ok = ok && pps::host_buf_mark_use(tb, stream) == 0;
   pps::host_buf_release(tb);
-  // 4. append, attend, rows out
+  // append, attend, rows out
   const int32_t* d_tab = (const int32_t*)(sc + off_tab);
-  if (ok) st = pps_kv_append(pool, sc + off_k, sc + off_v, d_tab, d_tab + R + 1, d_tab + 2 * R + 1,
+  if (ok) st = pps_kv_append(pool, dk, dv, d_tab, d_tab + R + 1, d_tab + 2 * R + 1,
                              d_tab + 3 * R + 2, R, T, stream);
   if (ok && st == PPS_OK)
-    st = run_impl(plan, sc + off_q, pool, sc + off_out, sc + off_ws, al(ws_bytes), stream, nullptr);
-  if (ok && st == PPS_OK && T > 0)
-    ok = cudaMemcpyAsync(h_out, sc + off_out, q_bytes, cudaMemcpyDeviceToHost, stm) == cudaSuccess;
+    st = run_impl(plan, dq, pool, dout, sc + off_ws, al(ws_bytes), stream, events);
+  if (ok && st == PPS_OK && rows_on_host && T > 0)
+    ok = cudaMemcpyAsync(out, sc + off_out, q_bytes, cudaMemcpyDeviceToHost, stm) == cudaSuccess;
   pps_plan_destroy(plan);
   if (!ok) return PPS_ERR_CUDA;
   return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+pps_status pps_attn_step_host(const pps_pool* pool, const void* h_q, const void* h_k_new,
+                              const void* h_v_new, const int32_t* h_q_indptr,
+                              const int32_t* h_kv_len, const int32_t* h_page_indptr,
+                              const int32_t* h_page_indices, const int32_t* h_tree_parent,
+                              int32_t num_requests, int32_t num_q_heads, float sm_scale,
+                              const pps_plan_options* opts, void* h_out, void* d_scratch,
+                              size_t scratch_bytes, size_t* out_scratch_bytes, void* stream) {
+  return step_impl(pool, h_q, h_k_new, h_v_new, true, h_q_indptr, h_kv_len, h_page_indptr,
+                   h_page_indices, h_tree_parent, num_requests, num_q_heads, sm_scale, opts, h_out,
+                   d_scratch, scratch_bytes, out_scratch_bytes, stream, nullptr);
+}
+
+pps_status pps_attn_step(const pps_pool* pool, const void* q, const void* k_new, const void* v_new,
+                         const int32_t* h_q_indptr, const int32_t* h_kv_len,
+                         const int32_t* h_page_indptr, const int32_t* h_page_indices,
+                         const int32_t* h_tree_parent, int32_t num_requests, int32_t num_q_heads,
+                         float sm_scale, const pps_plan_options* opts, void* out, void* d_scratch,
+                         size_t scratch_bytes, size_t* out_scratch_bytes, void* stream,
+                         void* const* events) {
+  if (((uintptr_t)k_new & 15) || ((uintptr_t)v_new & 15)) return PPS_ERR_INVALID_ARGUMENT;
+  return step_impl(pool, q, k_new, v_new, false, h_q_indptr, h_kv_len, h_page_indptr,
+                   h_page_indices, h_tree_parent, num_requests, num_q_heads, sm_scale, opts, out,
+                   d_scratch, scratch_bytes, out_scratch_bytes, stream, events);
 }
 
 pps_status pps_get_device_error(int32_t* code, int32_t clear) {

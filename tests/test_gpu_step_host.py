@@ -1,8 +1,8 @@
-"""GPU: pps_attn_step_host (host rows and tables in, host output out) against
-the device-side calls (pps_kv_append + pps_attn_plan + pps_attn_run) on the same
+"""GPU: the one-call steps -- pps_attn_step_host (host rows and tables in, host
+output out) and pps_attn_step (device rows, host tables) -- against the
+device-side calls (pps_kv_append + pps_attn_plan + pps_attn_run) on the same
 batch: the same kernels and plan, so the output rows and the pool must match
-bit for bit; and both within the oracle tolerance (the device path is checked
-against the oracle in test_gpu_parity)."""
+bit for bit (the device path is checked against the oracle in test_gpu_parity)."""
 from __future__ import annotations
 
 import numpy as np
@@ -41,6 +41,31 @@ def test_step_host_matches_device_calls(pps, name, pinned):
         torch.cuda.synchronize()
         assert pps.get_device_error(clear=True) == 0
         assert torch.equal(out.view(torch.int16), outs[s].cpu().view(torch.int16)), s
+    assert torch.equal(pk2.view(torch.int16), pk.view(torch.int16))
+    assert torch.equal(pv2.view(torch.int16), pv.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["decode_heavy", "radix_sharing", "mixed_budget", "tree_small_g4",
+                                  "d64_g8", "long_prefill"])
+def test_step_device_matches_device_calls(pps, name):
+    wl = small_cases()[name]()
+    dev_in = to_device(wl)
+    outs, (pk, pv), _ = run_workload(wl, device_inputs=dev_in)
+    pk2, pv2 = wl.pool_k.to("cuda", copy=True), wl.pool_v.to("cuda", copy=True)
+    nk = pps.NUM_KERNEL_CLASSES
+    for s, st in enumerate(dev_in[2]):
+        L = st["layout"]
+        out = torch.full_like(st["q"], float("nan"))
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nk)]
+        pps.get_device_error(clear=True)
+        pps.attn_step(pk2, pv2, st["q"], st["k_new"], st["v_new"], L.q_indptr, L.kv_len,
+                      L.page_indptr, L.page_indices, out, tree_parent=L.tree_parent,
+                      events=ev if s == 0 else None)
+        torch.cuda.synchronize()
+        assert pps.get_device_error(clear=True) == 0
+        assert torch.equal(out.view(torch.int16), outs[s].view(torch.int16)), s
+        if s == 0:
+            assert all(ev[2 * c].elapsed_time(ev[2 * c + 1]) >= 0 for c in range(nk))
     assert torch.equal(pk2.view(torch.int16), pk.view(torch.int16))
     assert torch.equal(pv2.view(torch.int16), pv.view(torch.int16))
 
