@@ -258,11 +258,9 @@ __device__ __forceinline__ bool softmax_tiles(const SmCtx& c, const pps::Task& t
   const int nrows = task.n_tok * G;
   const bool causal = task.causal != PPS_NO_CAUSAL;
   const uint32_t tm_o = c.tm + 2 * kRows + (ti & 1) * kRows;
-  // Every row starts from a reference of 0 (log2 units): P = exp2(x) is exact
-  // up to the bf16 rounding whatever the reference, as long as no score is
-  // above it by more than 2^8 (overflow side) or below -64 (underflow side,
-  // far from fp32's limit); a first tile outside that range takes the exact
-  // per-row maxima below.  Padding rows see no key, so their P stays 0.
+  // The first tile takes the exact per-row maxima below, which set each row's
+  // reference to its maximum (its largest P is then exactly 1); padding rows
+  // see no key and keep a reference of 0, so their P stays 0.
   if (t < kRows) c.m_s[t] = 0.f;
   // token ids for the statistics step (loaded now, stored there)
   const int32_t my_tok = t < task.n_tok ? p.rows[task.row_off + t] : 0;
@@ -300,7 +298,7 @@ __device__ __forceinline__ bool softmax_tiles(const SmCtx& c, const pps::Task& t
     const int first_vis = (full || !causal) ? 0 : G * (pos - task.causal);
     const bool key_ok = full || pos < task.kv_end;
     float x[NR];
-    bool need = false;
+    bool need = j == 0;
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
       bool vis = r < nrows && key_ok && r >= first_vis;
@@ -310,7 +308,6 @@ __device__ __forceinline__ bool softmax_tiles(const SmCtx& c, const pps::Task& t
       }
       x[r] = vis ? __uint_as_float(s[r]) * p.qk_scale : -INFINITY;
       need |= x[r] > m_ref[r] + kRescaleThreshold;
-      if (j == 0) need |= vis && x[r] < -64.f;
     }
     if (softmax_or(need)) {
       // exact per-row maxima of this tile over its 128 keys; lane r of warp 0
@@ -563,7 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     pps::Task task;
     for (int ti = 0; ok && cur.next(task); ++ti) {
       const int qb = ti & 1;
-      if (!warp_wait(&bars.q_empty[qb], ((ti >> 1) - 1) & 1, ti >= 2)) { fail(); ok = false; break; }
+      const bool freed = ti < 2 || mbar_wait_idle(smem_u32(&bars.q_empty[qb]), ((ti >> 1) - 1) & 1);
+      if (!__all_sync(0xffffffffu, freed && !abort_flag)) { fail(); ok = false; break; }
       const int nrows = task.n_tok * G;
       const int my_tok = lane < task.n_tok ? p.rows[task.row_off + lane] : 0;
       const uint32_t qt = q_base + qb * L::q_tile;

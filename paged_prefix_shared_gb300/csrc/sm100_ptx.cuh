@@ -51,6 +51,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// The same wait for a warp with nothing else to do meanwhile (a loader that
+// runs a task ahead): it sleeps between polls instead of spinning, leaving the
+// issue slots of its scheduler to the warps on the critical path.
+__device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity,
+                                               uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  while (true) {
+    __nanosleep(200);
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > limit_ns) return false;
+  }
+}
+
 // ---- proxies / fences ------------------------------------------------------------
 // Generic-proxy writes to shared memory become visible to the async proxy
 // (TMA, tensor core) after this fence.
