@@ -127,7 +127,13 @@ namespace pps {
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 // ---- host staging buffers for plan tables -------------------------------------------
+// A slot is reused once the upload recorded on it has completed.  A caller
+// that enqueues steps faster than the GPU runs them would otherwise pin a new
+// buffer every step (and scan an ever longer list); after kRunAhead busy
+// slots large enough for a request, the request waits for the oldest upload
+// among them instead, so the host runs at most that many steps ahead.
 namespace {
+constexpr int kRunAhead = 4;
 struct HostSlot {
   int32_t* p = nullptr;
   size_t ints = 0;
@@ -135,9 +141,11 @@ struct HostSlot {
   bool in_use = false;
   cudaEvent_t ev = nullptr;   // last upload recorded on this buffer
   int ev_dev = -1;
+  uint64_t seq = 0;           // order of that upload
 };
 std::mutex g_host_mu;
 std::vector<HostSlot> g_host;
+uint64_t g_host_seq = 0;
 
 bool slot_idle(HostSlot& s) {
   if (!s.ev) return true;
@@ -149,12 +157,27 @@ bool slot_idle(HostSlot& s) {
 }  // namespace
 
 HostBuf host_buf_acquire(size_t ints) {
-  std::lock_guard<std::mutex> lk(g_host_mu);
-  int best = -1;
+  std::unique_lock<std::mutex> lk(g_host_mu);
+  int best = -1, oldest = -1, busy = 0;
   for (int i = 0; i < (int)g_host.size(); ++i) {
     HostSlot& s = g_host[i];
-    if (s.in_use || s.ints < ints || !slot_idle(s)) continue;
+    if (s.in_use || s.ints < ints) continue;
+    if (!slot_idle(s)) {
+      ++busy;
+      if (oldest < 0 || s.seq < g_host[oldest].seq) oldest = i;
+      continue;
+    }
     if (best < 0 || s.ints < g_host[best].ints) best = i;
+  }
+  if (best < 0 && busy >= kRunAhead) {
+    // wait for the oldest upload outside the lock; the slot is ours meanwhile
+    HostSlot& s = g_host[oldest];
+    s.in_use = true;
+    const HostBuf b{s.p, s.ints, oldest};
+    const cudaEvent_t ev = s.ev;
+    lk.unlock();
+    if (cudaEventSynchronize(ev) != cudaSuccess) cudaGetLastError();
+    return b;
   }
   if (best < 0) {
     size_t cap = 1 << 14;                      // ints; power-of-two classes from 64 KB
@@ -198,6 +221,7 @@ int host_buf_mark_use(const HostBuf& b, void* stream) {
     if (cudaEventCreateWithFlags(&s.ev, cudaEventDisableTiming) != cudaSuccess) return 1;
     s.ev_dev = dev;
   }
+  s.seq = ++g_host_seq;
   return cudaEventRecord(s.ev, (cudaStream_t)stream) == cudaSuccess ? 0 : 1;
 }
 
