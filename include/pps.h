@@ -541,6 +541,14 @@ pps_status pps_plan_get_info(const pps_plan* plan, pps_plan_info* info);
  * when the key k positions before the token's own position is visible to it
  * (keys 64 or more positions back are always visible).  Chain tokens hold
  * all ones.  Tasks apply it only when their causal field is not PPS_NO_CAUSAL.
+ * TT_CTA (plans whose small-row tasks run on the key-tile tensor kernel only;
+ * count 0 otherwise) holds C + 1 offsets for that kernel's C persistent CTAs:
+ * CTA b runs BW_TASKS records [TT_CTA[b], TT_CTA[b + 1]) in order.  The
+ * planner fills the ranges longest task first, each task to the CTA with the
+ * least work so far (whole 128-key tiles plus two per task; ties to the lowest
+ * CTA), so within a range the tasks keep descending work; C = min(tasks, SMs).
+ * Without TT_CTA, BW_TASKS is in descending work order and persistent CTA b of
+ * C takes records b, 2C-1-b, 2C+b, ... (the tensor-core and CUDA-core kernels).
  */
 #define PPS_TASK_INTS 8
 #define PPS_NO_CAUSAL 0x3fffffff
@@ -552,6 +560,7 @@ pps_status pps_plan_get_info(const pps_plan* plan, pps_plan_info* info);
 #define PPS_ARRAY_MERGE_INDPTR 5
 #define PPS_ARRAY_MERGE_PIDS 6
 #define PPS_ARRAY_TREE_MASK 7
+#define PPS_ARRAY_TT_CTA 8
 pps_status pps_plan_get_array(const pps_plan* plan, int32_t which, const int32_t** data,
                               int64_t* count);
 

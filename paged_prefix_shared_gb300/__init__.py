@@ -36,7 +36,7 @@ NUM_KERNEL_CLASSES = 3
 TASK_INTS = 8
 NO_CAUSAL = 0x3FFFFFFF
 ARRAYS = {"bw_tasks": 0, "mma_tasks": 1, "rows": 2, "pages": 3, "merge_tokens": 4,
-          "merge_indptr": 5, "merge_pids": 6, "tree_mask": 7}
+          "merge_indptr": 5, "merge_pids": 6, "tree_mask": 7, "tt_cta": 8}
 TREE_MAX_TOKENS = 64
 
 

@@ -90,6 +90,7 @@ pps_status run_impl(const pps_plan* plan, const void* q, const pps_pool* pool, v
   t.merge_indptr = base + L.merge_indptr;
   t.merge_pids = base + L.merge_pids;
   t.tree_mask = plan->has_tree ? (const unsigned long long*)(base + L.tree_mask) : nullptr;
+  t.tt_cta = plan->shape.tt_ctas > 0 ? base + L.tt_cta : nullptr;
   t.o_part = (float*)(ws + plan->table_bytes);
   t.lse_part = (float*)(ws + plan->table_bytes + plan->partial_o_bytes);
 

@@ -14,8 +14,9 @@
 // describes, and the SGLang review's grouped shared-prefix rows ("Core claim")
 // entering as up to 32 rows of one task.
 //
-// Warp roles (256 threads, one persistent CTA per SM taking the work-sorted
-// tasks in symmetric round-robin order):
+// Warp roles (256 threads, one persistent CTA per SM running its own
+// contiguous range of the task table, which the planner filled longest task
+// first onto the least-loaded CTA):
 //   warps 0-3  softmax: thread t owns TMEM lane t, i.e. key t of S^T and
 //              element t of head_dim in O^T.  Per tile it reads its S^T lane
 //              (32 rows), takes P = exp2(s * scale - m_ref[row]) against the
@@ -68,7 +69,7 @@ constexpr uint64_t kLayoutSwizzle64 = 4;     // smem descriptor layout: 64-byte 
 
 struct TtParams {
   const pps::Task* tasks;
-  int32_t num_tasks;
+  const int32_t* cta_tasks;                  // CTA b runs tasks [cta_tasks[b], cta_tasks[b + 1])
   const int32_t* rows;
   const int32_t* pages;
   const __nv_bfloat16* q;
@@ -117,27 +118,21 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ int snake_task(int ti, int b, int C) {
-  return ti * C + ((ti & 1) ? (C - 1 - b) : b);
-}
-
-// The CTA's tasks in order, each record loaded one task ahead so that its
-// global-memory latency overlaps the task before it.
+// The CTA's tasks (a contiguous range of the table, filled by the planner
+// longest first onto the least-loaded CTA) in order, each record loaded one
+// task ahead so that its global-memory latency overlaps the task before it.
 struct TaskCursor {
   const pps::Task* tasks;
-  int num, b, C, ti;
+  int k, end;
   pps::Task nxt;
-  __device__ __forceinline__ TaskCursor(const pps::Task* t, int n, int b_, int C_)
-      : tasks(t), num(n), b(b_), C(C_), ti(0) {
-    const int k = snake_task(0, b, C);
-    if (k < num) nxt = tasks[k];
+  __device__ __forceinline__ TaskCursor(const pps::Task* t, int lo, int hi)
+      : tasks(t), k(lo), end(hi) {
+    if (k < end) nxt = tasks[k];
   }
   __device__ __forceinline__ bool next(pps::Task& out) {
-    if (snake_task(ti, b, C) >= num) return false;
+    if (k >= end) return false;
     out = nxt;
-    const int k = snake_task(ti + 1, b, C);
-    if (k < num) nxt = tasks[k];
-    ++ti;
+    if (++k < end) nxt = tasks[k];
     return true;
   }
 };
@@ -468,9 +463,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ TtBars bars;
   __shared__ uint32_t tmem_base;
   __shared__ volatile int abort_flag;
+  __shared__ int task_range[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.x, nctas = gridDim.x;
+  const int b = blockIdx.x;
   const int G = p.G;
   const uint32_t k_base = smem_u32(smem + L::k_off);
   const uint32_t v_base = smem_u32(smem + L::v_off);
@@ -481,6 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int64_t* base_s = reinterpret_cast<int64_t*>(smem + L::base_off);  // [kRows]
 
   if (tid == 0) {
+    const int lo = p.cta_tasks[b], hi = p.cta_tasks[b + 1];   // latency hidden by the set-up
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars.k_full[s]), 1);
       mbar_init(smem_u32(&bars.k_empty[s]), 1);
@@ -497,6 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int x = 0; x < 2; ++x) mbar_init(smem_u32(&bars.o_done[x]), 1);
     mbar_init(smem_u32(&bars.drain), 1);
     abort_flag = 0;
+    task_range[0] = lo;
+    task_range[1] = hi;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -527,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               reinterpret_cast<float*>(smem + L::inv_off),
               reinterpret_cast<unsigned long long*>(smem + L::msk_off), &abort_flag, tm, lane_off,
               t, warp, lane};
-    TaskCursor cur(p.tasks, p.num_tasks, b, nctas);
+    TaskCursor cur(p.tasks, task_range[0], task_range[1]);
     pps::Task task, prev;
     int prev_ti = -1;                                    // finished task whose output is pending
     int gt = 0;                                          // tiles seen
@@ -556,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // buffer's previous user) have completed: 32 rows x 256 bytes, 16 bytes
     // per copy, 128-byte swizzled K-major, zeros past the task's rows.
     bool ok = true;
-    TaskCursor cur(p.tasks, p.num_tasks, b, nctas);
+    TaskCursor cur(p.tasks, task_range[0], task_range[1]);
     pps::Task task;
     for (int ti = 0; ok && cur.next(task); ++ti) {
       const int qb = ti & 1;
@@ -594,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t box_bytes = (uint32_t)P * 128u;
     int it = 0;
     bool ok = true;
-    TaskCursor cur(p.tasks, p.num_tasks, b, nctas);
+    TaskCursor cur(p.tasks, task_range[0], task_range[1]);
     pps::Task task;
     for (int ti = 0; ok && cur.next(task); ++ti) {
       const int n = n_tiles_of(task);
@@ -678,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // task boundaries: the next task's first S is ready when the softmax
     // finishes the current task.  `qc` walks the tasks for QK (waiting for
     // each task's query rows), `pc` for PV.
-    TaskCursor qc(p.tasks, p.num_tasks, b, nctas);
+    TaskCursor qc(p.tasks, task_range[0], task_range[1]);
     pps::Task qtask{};
     int q_ti = -1, q_n = 0, q_j = 0;                // task, its tiles, next tile to QK
     int gq = 0;                                     // next global tile to QK
@@ -715,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     while (gq < 2 && qk_next()) {
     }
-    TaskCursor pc(p.tasks, p.num_tasks, b, nctas);
+    TaskCursor pc(p.tasks, task_range[0], task_range[1]);
     pps::Task task;
     for (int ti = 0; ok && pc.next(task); ++ti) {
       const int n = n_tiles_of(task);
@@ -774,28 +773,27 @@ namespace pps {
 
 namespace {
 template <bool TREE>
-int launch_tt(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
-              const pps_pool& pool, void* out, int32_t* err, void* stream) {
+int launch_tt(const Shape& s, const DeviceTables& t, const void* q, const pps_pool& pool,
+              void* out, int32_t* err, void* stream) {
   CUtensorMap mk, mv;
   if (!make_pool_map(&mk, pool.k, pool) || !make_pool_map(&mv, pool.v, pool))
     return (int)cudaErrorInvalidValue;
-  // once per device and instance: the shared-memory opt-in and the SM count
-  static std::atomic<int> ready_sms[64];
+  // once per device and instance: the shared-memory opt-in
+  static std::atomic<int> ready[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return (int)e;
-  int sms = (dev >= 0 && dev < 64) ? ready_sms[dev].load(std::memory_order_relaxed) : 0;
-  if (sms == 0) {
+  if (dev < 0 || dev >= 64 || !ready[dev].load(std::memory_order_relaxed)) {
     if ((e = cudaFuncSetAttribute(tt_attention_kernel<TREE>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   TtLayout::smem_alloc)) != cudaSuccess)
       return (int)e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-      return (int)e;
-    if (dev >= 0 && dev < 64) ready_sms[dev].store(sms, std::memory_order_relaxed);
+    if (dev >= 0 && dev < 64) ready[dev].store(1, std::memory_order_relaxed);
   }
-  const int64_t grid = std::min<int64_t>(num_tasks, sms);
-  TtParams prm{t.bw_tasks, (int32_t)num_tasks, t.rows, t.pages, (const __nv_bfloat16*)q,
+  // one CTA per range of the plan's table (the planner sized them for the SMs)
+  const int64_t grid = s.tt_ctas;
+  if (grid <= 0 || !t.tt_cta) return (int)cudaErrorInvalidValue;
+  TtParams prm{t.bw_tasks, t.tt_cta, t.rows, t.pages, (const __nv_bfloat16*)q,
                (__nv_bfloat16*)out, t.o_part, t.lse_part, err, t.tree_mask, s.num_q_heads,
                s.group, s.page_size, s.sm_scale * 1.4426950408889634f};
   tt_attention_kernel<TREE>
@@ -809,8 +807,8 @@ int launch_tt_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks
                         const pps_pool& pool, void* out, int32_t* err, void* stream) {
   if (num_tasks == 0) return cudaSuccess;
   if (s.head_dim != D) return (int)cudaErrorInvalidValue;
-  return t.tree_mask ? launch_tt<true>(s, t, num_tasks, q, pool, out, err, stream)
-                     : launch_tt<false>(s, t, num_tasks, q, pool, out, err, stream);
+  return t.tree_mask ? launch_tt<true>(s, t, q, pool, out, err, stream)
+                     : launch_tt<false>(s, t, q, pool, out, err, stream);
 }
 
 }  // namespace pps

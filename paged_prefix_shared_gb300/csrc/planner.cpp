@@ -10,6 +10,8 @@
 // here from the lexicographically sorted page lists and their longest common
 // prefixes.
 #include <algorithm>
+#include <functional>
+#include <queue>
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -183,7 +185,7 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
   pps_plan* plan = new (std::nothrow) pps_plan;
   if (!plan) return PPS_ERR_NO_MEMORY;
   try {
-    plan->shape = {num_q_heads, num_kv_heads, head_dim, page_size, G, num_pages, sm_scale, 0, 0};
+    plan->shape = {num_q_heads, num_kv_heads, head_dim, page_size, G, num_pages, sm_scale, 0, 0, 0};
     plan->num_requests = R;
     plan->num_tokens = q_indptr[R];
     plan->use_mma = use_mma;
@@ -471,6 +473,34 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
         (ts.mma ? mm : bw).push_back(t);
       }
     }
+    // Key-tile plans: the persistent kernel's CTAs take contiguous ranges of
+    // the table.  Each task, largest first, goes to the CTA with the least
+    // work so far (ties: the lowest CTA), and keeps that order inside its
+    // range: tt_cta[b] .. tt_cta[b + 1] for CTA b.  The work unit is the
+    // key-tile kernel's: whole 128-key tiles plus two for the task's own work.
+    std::vector<int32_t> tt_cta;
+    if (use_tt && !bw.empty()) {
+      const int32_t C = (int32_t)std::min<int64_t>((int64_t)bw.size(), num_sms);
+      using Load = std::pair<int64_t, int32_t>;
+      std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
+      for (int32_t b = 0; b < C; ++b) least.push({0, b});
+      std::vector<int32_t> owner(bw.size());
+      tt_cta.assign((size_t)C + 1, 0);
+      for (size_t k = 0; k < bw.size(); ++k) {
+        const Load l = least.top();
+        least.pop();
+        owner[k] = l.second;
+        ++tt_cta[(size_t)l.second + 1];
+        least.push({l.first + ceil_div(bw[k].kv_end - bw[k].kv_begin, pps::kMmaKvTile) + 2,
+                    l.second});
+      }
+      for (int32_t b = 0; b < C; ++b) tt_cta[(size_t)b + 1] += tt_cta[b];
+      std::vector<int32_t> at(tt_cta.begin(), tt_cta.end() - 1);
+      std::vector<Task> grouped(bw.size());
+      for (size_t k = 0; k < bw.size(); ++k) grouped[(size_t)at[owner[k]]++] = bw[k];
+      bw.swap(grouped);
+    }
+    plan->shape.tt_ctas = tt_cta.empty() ? 0 : (int32_t)tt_cta.size() - 1;
 
     // ---- 6. statistics ---------------------------------------------------------------
     const int64_t tok_bytes = 2LL * num_kv_heads * head_dim * 2;   // K+V, all kv heads
@@ -531,6 +561,7 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
     L.merge_indptr = off;  off += al((int64_t)m_ptr.size());
     L.merge_pids = off;    off += al((int64_t)m_pid.size());
     L.tree_mask = off;     off += plan->has_tree ? al(2LL * T) : 0;
+    L.tt_cta = off;        off += al((int64_t)tt_cta.size());
     L.total_ints = off;
     plan->layout = L;
     plan->image_ints = std::max<int64_t>(off, 64);
@@ -549,7 +580,8 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
     put(L.merge_tokens, m_tok.data(), (int64_t)m_tok.size(), L.merge_indptr);
     put(L.merge_indptr, m_ptr.data(), (int64_t)m_ptr.size(), L.merge_pids);
     put(L.merge_pids, m_pid.data(), (int64_t)m_pid.size(), L.tree_mask);
-    put(L.tree_mask, tmask.data(), plan->has_tree ? 2LL * T : 0, plan->image_ints);
+    put(L.tree_mask, tmask.data(), plan->has_tree ? 2LL * T : 0, L.tt_cta);
+    put(L.tt_cta, tt_cta.data(), (int64_t)tt_cta.size(), plan->image_ints);
 
     plan->num_bw = (int64_t)bw.size();
     plan->num_mma = (int64_t)mm.size();
@@ -657,6 +689,10 @@ extern "C" pps_status pps_plan_get_array(const pps_plan* p, int32_t which, const
     case PPS_ARRAY_TREE_MASK:
       *data = img + L.tree_mask;
       *count = p->has_tree ? 2LL * p->num_tokens : 0;
+      break;
+    case PPS_ARRAY_TT_CTA:
+      *data = img + L.tt_cta;
+      *count = p->shape.tt_ctas > 0 ? p->shape.tt_ctas + 1 : 0;
       break;
     default: return PPS_ERR_INVALID_ARGUMENT;
   }

@@ -34,6 +34,7 @@ struct TableLayout {
   int64_t bw_tasks = 0, mma_tasks = 0, rows = 0, pages = 0;
   int64_t merge_tokens = 0, merge_indptr = 0, merge_pids = 0;
   int64_t tree_mask = 0;   // 2 ints per new token, only when the plan has a draft tree
+  int64_t tt_cta = 0;      // key-tile plans: per-CTA task ranges, CTAs + 1 offsets
   int64_t total_ints = 0;
 };
 
@@ -49,6 +50,8 @@ struct DeviceTables {
   // Per new token, bit k: the key k positions before the token is visible
   // (draft-tree verify); nullptr when the batch has no tree.
   const unsigned long long* tree_mask;
+  // Key-tile plans: CTA b runs bw_tasks[tt_cta[b] .. tt_cta[b + 1]).
+  const int32_t* tt_cta;
   float* o_part;     // [num_partials, Hq, d]
   float* lse_part;   // [num_partials, Hq] (log2 domain)
 };
@@ -59,6 +62,7 @@ struct Shape {
   float sm_scale;
   int32_t bw_rows_max;   // largest n_tok * G over bandwidth tasks
   int32_t small_tt;      // 1: the small-row tasks run on the key-tile tensor kernel
+  int32_t tt_ctas;       // CTAs of the key-tile kernel (its task table's ranges)
 };
 
 // Host memory for plan tables.  Page-locked when a CUDA device is usable, so

@@ -262,7 +262,7 @@ def test_key_tile_splits_are_even_whole_tiles(pps):
     """Adaptive chunking for key-tile tasks: a span within a quarter over the
     chunk stays whole; longer spans split into pieces of whole 128-key tiles
     that differ by at most one tile; no piece is a one-tile remainder unless
-    its span is that short; tasks are ordered by tiles (work), largest first."""
+    its span is that short."""
     for L in (workloads.radix_sharing(values=False).layout,
               workloads.decode_heavy(values=False).layout):
         plan = _plan(pps, L)
@@ -281,9 +281,48 @@ def test_key_tile_splits_are_even_whole_tiles(pps):
             if len(pieces) > 1:
                 assert max(lens[:-1]) - min(lens[:-1]) <= 128
                 assert lens[-1] > 128 or sum(lens) <= 2 * 128
-        tiles = -(-(t[:, 5] - t[:, 4]) // 128)
-        work = (tiles + 2) * 128
-        assert (np.diff(work[::Hkv]) <= 0).all()      # sorted by work, descending
     # the radix roots (2048 keys) stay whole: 8 subtrees x 8 kv heads of 16 tiles
     t = _plan(pps, workloads.radix_sharing(values=False).layout).array("bw_tasks")
     assert int(((t[:, 5] - t[:, 4]) == 2048).sum()) == 64
+
+
+@pytest.mark.parametrize("num_sms", [152, 37, 5])
+def test_key_tile_ranges_are_filled_least_loaded(pps, num_sms):
+    """Key-tile plans give each persistent CTA a contiguous range of the task
+    table (TT_CTA offsets), filled longest task first onto the CTA with the
+    least work (whole 128-key tiles + 2 per task): every range is non-empty
+    and in descending work order, and the most loaded CTA exceeds the least
+    loaded by at most one task's work (the list-scheduling bound: the last
+    task placed on the fullest CTA went to the least loaded CTA of its time)."""
+    for L in (workloads.radix_sharing(values=False).layout,
+              workloads.decode_heavy(values=False).layout,
+              workloads.decode_heavy(num_requests=3, values=False).layout):
+        plan = _plan(pps, L, num_sms=num_sms)
+        assert plan.info()["small_rows_on_tensor"] == 1
+        t = plan.array("bw_tasks")
+        off = plan.array("tt_cta")
+        C = min(len(t), num_sms)
+        assert len(off) == C + 1 and off[0] == 0 and off[-1] == len(t)
+        assert (np.diff(off) >= 1).all()
+        work = -(-(t[:, 5] - t[:, 4]) // 128) + 2
+        load = np.array([work[off[b]:off[b + 1]].sum() for b in range(C)])
+        for b in range(C):
+            assert (np.diff(work[off[b]:off[b + 1]]) <= 0).all()
+        assert load.max() - load.min() <= work.max()
+        assert load.sum() == work.sum()
+    # the radix batch: the snake order this replaced left one CTA 35 tiles
+    # (30.3 on average); balancing tiles + 2 per task leaves at most 32
+    t = _plan(pps, workloads.radix_sharing(values=False).layout).array("bw_tasks")
+    off = _plan(pps, workloads.radix_sharing(values=False).layout).array("tt_cta")
+    tiles = -(-(t[:, 5] - t[:, 4]) // 128)
+    per = np.array([tiles[off[b]:off[b + 1]].sum() for b in range(len(off) - 1)])
+    assert per.max() <= 32
+
+
+def test_plans_without_the_key_tile_kernel_have_no_ranges(pps):
+    L = workloads.decode_heavy(num_requests=6, **SMALL).layout       # head_dim 64
+    plan = _plan(pps, L)
+    assert plan.info()["small_rows_on_tensor"] == 0 and len(plan.array("tt_cta")) == 0
+    L = workloads.decode_heavy(num_requests=6, values=False).layout
+    plan = _plan(pps, L, flags=pps.PLAN_SMALL_ROWS_CUDA_CORES)
+    assert plan.info()["small_rows_on_tensor"] == 0 and len(plan.array("tt_cta")) == 0
