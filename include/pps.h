@@ -544,9 +544,10 @@ pps_status pps_plan_get_info(const pps_plan* plan, pps_plan_info* info);
  * TT_CTA (plans whose small-row tasks run on the key-tile tensor kernel only;
  * count 0 otherwise) holds C + 1 offsets for that kernel's C persistent CTAs:
  * CTA b runs BW_TASKS records [TT_CTA[b], TT_CTA[b + 1]) in order.  The
- * planner fills the ranges longest task first, each task to the CTA with the
- * least work so far (whole 128-key tiles plus two per task; ties to the lowest
- * CTA), so within a range the tasks keep descending work; C = min(tasks, SMs).
+ * planner fills the ranges longest task first, each task to a CTA with the
+ * least work so far (whole 128-key tiles plus two per task; ties to the CTA
+ * that reached that load first), so within a range the tasks keep descending
+ * work; C = min(tasks, SMs).
  * Without TT_CTA, BW_TASKS is in descending work order and persistent CTA b of
  * C takes records b, 2C-1-b, 2C+b, ... (the tensor-core and CUDA-core kernels).
  */

@@ -10,8 +10,6 @@
 // here from the lexicographically sorted page lists and their longest common
 // prefixes.
 #include <algorithm>
-#include <functional>
-#include <queue>
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -474,31 +472,47 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
       }
     }
     // Key-tile plans: the persistent kernel's CTAs take contiguous ranges of
-    // the table.  Each task, largest first, goes to the CTA with the least
-    // work so far (ties: the lowest CTA), and keeps that order inside its
-    // range: tt_cta[b] .. tt_cta[b + 1] for CTA b.  The work unit is the
-    // key-tile kernel's: whole 128-key tiles plus two for the task's own work.
-    std::vector<int32_t> tt_cta;
+    // the table.  Each task, largest first, goes to a CTA with the least work
+    // so far, and keeps that order inside its range: tt_cta[b] .. tt_cta[b + 1]
+    // for CTA b.  The work unit is the key-tile kernel's: whole 128-key tiles
+    // plus two for the task's own work.  Loads are small integers that only
+    // grow, so the CTAs sit in buckets by load (first in, first out: ties go
+    // to the CTA that reached the load first, CTA order at the start) and the
+    // lowest non-empty bucket only moves up: O(tasks + buckets).
+    std::vector<int32_t> tt_cta, owner;     // owner: CTA of each bw task (scattered at 7.)
     if (use_tt && !bw.empty()) {
       const int32_t C = (int32_t)std::min<int64_t>((int64_t)bw.size(), num_sms);
-      using Load = std::pair<int64_t, int32_t>;
-      std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
-      for (int32_t b = 0; b < C; ++b) least.push({0, b});
-      std::vector<int32_t> owner(bw.size());
-      tt_cta.assign((size_t)C + 1, 0);
+      std::vector<int32_t> w(bw.size());
+      int64_t total = 0, wmax = 0;
       for (size_t k = 0; k < bw.size(); ++k) {
-        const Load l = least.top();
-        least.pop();
-        owner[k] = l.second;
-        ++tt_cta[(size_t)l.second + 1];
-        least.push({l.first + ceil_div(bw[k].kv_end - bw[k].kv_begin, pps::kMmaKvTile) + 2,
-                    l.second});
+        w[k] = (int32_t)ceil_div(bw[k].kv_end - bw[k].kv_begin, pps::kMmaKvTile) + 2;
+        total += w[k];
+        wmax = std::max<int64_t>(wmax, w[k]);
+      }
+      // a CTA is picked at the least load (at most the mean), so every load
+      // stays below total / C + wmax + 1
+      const size_t nb = (size_t)(total / C + wmax + 2);
+      std::vector<int32_t> first(nb, -1), last(nb, -1), next((size_t)C, -1);
+      for (int32_t b = 0; b < C; ++b) next[b] = b + 1 < C ? b + 1 : -1;
+      first[0] = 0;
+      last[0] = C - 1;
+      owner.resize(bw.size());
+      tt_cta.assign((size_t)C + 1, 0);
+      size_t cur = 0;
+      for (size_t k = 0; k < bw.size(); ++k) {
+        while (first[cur] < 0) ++cur;
+        const int32_t b = first[cur];
+        first[cur] = next[b];
+        if (first[cur] < 0) last[cur] = -1;
+        owner[k] = b;
+        ++tt_cta[(size_t)b + 1];
+        const size_t to = cur + (size_t)w[k];
+        next[b] = -1;
+        if (last[to] < 0) first[to] = b;
+        else next[last[to]] = b;
+        last[to] = b;
       }
       for (int32_t b = 0; b < C; ++b) tt_cta[(size_t)b + 1] += tt_cta[b];
-      std::vector<int32_t> at(tt_cta.begin(), tt_cta.end() - 1);
-      std::vector<Task> grouped(bw.size());
-      for (size_t k = 0; k < bw.size(); ++k) grouped[(size_t)at[owner[k]]++] = bw[k];
-      bw.swap(grouped);
     }
     plan->shape.tt_ctas = tt_cta.empty() ? 0 : (int32_t)tt_cta.size() - 1;
 
@@ -568,12 +582,20 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
     plan->image = pps::host_buf_acquire((size_t)plan->image_ints);
     if (!plan->image.data) throw std::bad_alloc();
     int32_t* img = plan->image.data;
-    // Each section is copied in and the alignment gap after it zeroed.
+    // Each section is copied in (src null: already written) and the alignment
+    // gap after it zeroed.
     auto put = [&](int64_t at, const void* src, int64_t ints, int64_t end) {
-      if (ints) std::memcpy(img + at, src, (size_t)ints * 4);
+      if (ints && src) std::memcpy(img + at, src, (size_t)ints * 4);
       if (end > at + ints) std::memset(img + at + ints, 0, (size_t)(end - at - ints) * 4);
     };
-    put(L.bw_tasks, bw.data(), (int64_t)bw.size() * PPS_TASK_INTS, L.mma_tasks);
+    if (owner.empty()) {
+      put(L.bw_tasks, bw.data(), (int64_t)bw.size() * PPS_TASK_INTS, L.mma_tasks);
+    } else {                 // key-tile tables: each task at its place in its CTA's range
+      std::vector<int32_t> at(tt_cta.begin(), tt_cta.end() - 1);
+      Task* dst = reinterpret_cast<Task*>(img + L.bw_tasks);
+      for (size_t k = 0; k < bw.size(); ++k) dst[at[owner[k]]++] = bw[k];
+      put(L.bw_tasks, nullptr, (int64_t)bw.size() * PPS_TASK_INTS, L.mma_tasks);
+    }
     put(L.mma_tasks, mm.data(), (int64_t)mm.size() * PPS_TASK_INTS, L.rows);
     put(L.rows, rows.data(), (int64_t)rows.size(), L.pages);
     put(L.pages, page_indices, nnz, L.merge_tokens);
