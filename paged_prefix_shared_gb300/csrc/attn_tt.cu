@@ -659,17 +659,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
-    // V rows past the task's last position may hold anything (NaN included);
-    // P is 0 there, and 0 * NaN would poison O, so clear them.
-    auto clear_v_tail = [&](int st, int valid) {
+    // A tile with `valid` < 128 keys runs only the PV steps (16 keys each)
+    // that hold a valid key; the rest would multiply P = 0 by V rows that were
+    // not loaded.  Inside the last step, rows from `valid` to the next multiple
+    // of 16 are pool slots past the task's last position (the same page) and
+    // may hold anything, NaN included: 0 * NaN would poison O, so they are
+    // cleared (at most 15 rows of both 64-column blocks; whole 128-byte rows,
+    // so the swizzle does not matter).
+    auto clear_v_rows = [&](int st, int valid) {
       uint8_t* vt = smem + L::v_off + st * L::kv_tile;
-      const int rows = kTile - valid;
-      for (int idx = lane; idx < rows * 16; idx += 32) {
-        const int kb = idx / (rows * 8);
-        const int rem = idx - kb * rows * 8;
-        *reinterpret_cast<int4*>(vt + kb * 16384 + (valid + rem / 8) * 128 + (rem % 8) * 16) =
-            make_int4(0, 0, 0, 0);
-      }
+      const int nch = (((valid + 15) & ~15) - valid) * 8;   // 16-byte chunks per block
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb)
+        for (int i = lane; i < nch; i += 32)
+          *reinterpret_cast<int4*>(vt + kb * 16384 + (valid + (i >> 3)) * 128 + (i & 7) * 16) =
+              make_int4(0, 0, 0, 0);
       fence_proxy_async_smem();
       __syncwarp();
     };
@@ -729,16 +733,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(&bars.p_full[sb], (g >> 1) & 1)) { fail(); ok = false; break; }
         if (!warp_wait(&bars.v_full[st], (g / kStages) & 1)) { fail(); ok = false; break; }
         const int valid = min(kTile, task.kv_end - (task.kv_begin + j * kTile));
-        if (valid < kTile) clear_v_tail(st, valid);
+        const int nks = (valid + 15) >> 4;              // PV steps holding a valid key
+        if (valid & 15) clear_v_rows(st, valid);
         tc_fence_after();
         if (lane == 0) {
           const uint32_t vt = v_base + st * L::kv_tile;
           const uint32_t pt = p_base + sb * L::p_tile;
+          if (nks == kTile / 16) {                  // whole tile: back-to-back issue
 #pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks)
-            umma_ss(tm_o + ob * kRows, smem_desc(vt + ks * 2048, 16384, 1024),
-                    smem_desc(pt + ks * 1024, 1024, 512, kLayoutSwizzle64), id_pv,
-                    (j > 0 || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < kTile / 16; ++ks)
+              umma_ss(tm_o + ob * kRows, smem_desc(vt + ks * 2048, 16384, 1024),
+                      smem_desc(pt + ks * 1024, 1024, 512, kLayoutSwizzle64), id_pv,
+                      (j > 0 || ks > 0) ? 1u : 0u);
+          } else {
+#pragma unroll 1
+            for (int ks = 0; ks < nks; ++ks)
+              umma_ss(tm_o + ob * kRows, smem_desc(vt + ks * 2048, 16384, 1024),
+                      smem_desc(pt + ks * 1024, 1024, 512, kLayoutSwizzle64), id_pv,
+                      (j > 0 || ks > 0) ? 1u : 0u);
+          }
           umma_commit(smem_u32(&bars.v_empty[st]));
           umma_commit(smem_u32(&bars.p_empty[sb]));
           if (j == n - 1) umma_commit(smem_u32(&bars.o_done[ob]));
