@@ -241,14 +241,13 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
         }
         if (!any) cand.clear();
       }
-      // Lexicographic order of the page lists (by their first differing page
-      // id): every set of lists sharing a prefix is then one contiguous run.
+      // A lexicographic order of the page lists (page ids compared as their
+      // 4 bytes in memory order, one memcmp over the common length): every set
+      // of lists sharing a prefix is then one contiguous run.
       std::sort(cand.begin(), cand.end(), [&](int32_t a, int32_t b) {
         const int32_t n = std::min(full[a], full[b]);
-        const int32_t* pa = seq(a);
-        const int32_t* pb = seq(b);
-        const int32_t k = common_pages(pa, pb, n);
-        if (k < n) return pa[k] < pb[k];
+        const int c = std::memcmp(seq(a), seq(b), (size_t)n * 4);
+        if (c != 0) return c < 0;
         if (full[a] != full[b]) return full[a] < full[b];
         return a < b;
       });
