@@ -217,15 +217,23 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
     }
 
     // ---- 1. radix grouping over fully cached pages --------------------------------
+    // A request joins the grouping when its rows fill at most half a
+    // tensor-core tile.  A group saves shared-page reads only by packing the
+    // rows of several requests into fewer tiles; each grouped token pays fp32
+    // partials (~1 KB per query head, written and merged).  Decode and verify
+    // rows gain most; a prefill chunk of whole tiles gains nothing, so it reads
+    // the shared pages in its own tiles and writes its rows directly.  Plans
+    // without tensor-core tiles (16-row CUDA-core tiles) group every request.
     std::vector<int32_t> group_end(R, 0);
     std::vector<std::pair<std::vector<int32_t>, std::pair<int32_t, int32_t>>> groups;
     if (use_groups) {
+      const int64_t max_rows = use_mma ? pps::kMmaTaskRows / 2 : INT64_MAX;
       std::vector<int32_t> full(R, 0), cand;
       for (int32_t r = 0; r < R; ++r) {
         const int32_t q = q_indptr[r + 1] - q_indptr[r];
         const int32_t c = kv_len[r] - q;
         full[r] = c / P;
-        if (q > 0 && full[r] > 0) cand.push_back(r);
+        if (q > 0 && full[r] > 0 && (int64_t)q * G <= max_rows) cand.push_back(r);
       }
       auto seq = [&](int32_t r) { return page_indices + page_indptr[r]; };
       // A group needs two requests whose first cached pages are the same; with

@@ -63,11 +63,19 @@ def check_plan(pps, L, plan):
             pids = {pid + i for _, pid, i in lst}
             assert merged[t] == pids and len(pids) == per_head
             assert all(0 <= p < info["num_partials"] for p in pids)
-    # work-sorted (descending) inside each kernel class
+    # work-sorted (descending) inside each kernel class; key-tile tables in
+    # per-CTA ranges, each descending in 128-key tiles (+ 2 per task)
     G = L.num_q_heads // Hkv
+    off = plan.array("tt_cta")
     for name, rows_eff in (("bw_tasks", None), ("mma_tasks", 128)):
         tk = plan.array(name)
-        if len(tk):
+        if not len(tk):
+            continue
+        if name == "bw_tasks" and len(off):
+            w = -(-(tk[:, 5] - tk[:, 4]) // 128) + 2
+            for b in range(len(off) - 1):
+                assert (np.diff(w[off[b]:off[b + 1]]) <= 0).all()
+        else:
             w = (tk[:, 1] * G if rows_eff is None else rows_eff) * (tk[:, 5] - tk[:, 4])
             assert (np.diff(w) <= 0).all()
     return info
@@ -113,6 +121,32 @@ def test_groups_detected(pps):
     a = _plan(pps, wl.layout).info()["kv_bytes_read"]
     b = _plan(pps, wl.layout, flags=pps.PLAN_NO_GROUPS).info()["kv_bytes_read"]
     assert a < b
+
+
+def test_wide_prefill_rows_read_shared_pages_in_their_own_tiles(pps):
+    """A request whose rows fill more than half a tensor-core tile stays out of
+    the shared-prefix grouping (a group would only add fp32 partials to tiles
+    it already fills); narrower requests on the same pages still group.  Four
+    requests share a 4-page prefix at G = 4: two decode rows, a 32-token chunk
+    (128 rows: grouped) and a 33-token chunk (132 rows: alone).  CUDA-core-only
+    plans group all four."""
+    reqs = [([0], 20, [1]), ([0], 30, [1]), ([0], 40, [32]), ([0], 50, [33])]
+    L = workloads.build_workload("wide", num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                 page_size=16, shared_lens=[64], requests=reqs, seed=3,
+                                 values=False).layout
+    for flags, members in ((0, [0, 1, 2]), (pps.PLAN_CUDA_CORES_ONLY, [0, 1, 2, 3])):
+        plan = _plan(pps, L, flags=flags)
+        check_plan(pps, L, plan)
+        assert plan.info()["num_groups"] == 1
+        rows = plan.array("rows")
+        tasks = np.concatenate([plan.array("bw_tasks"), plan.array("mma_tasks")])
+        grp = tasks[(tasks[:, 6] == pps.NO_CAUSAL) & (tasks[:, 4] == 0) & (tasks[:, 5] == 64)]
+        toks = {int(t) for rec in grp for t in rows[rec[0]:rec[0] + rec[1]]}
+        want = {t for r in members for t in range(int(L.q_indptr[r]), int(L.q_indptr[r + 1]))}
+        assert toks == want
+        if 3 not in members:                   # request 3 reads the prefix itself
+            own = tasks[(tasks[:, 6] != pps.NO_CAUSAL) & (tasks[:, 3] == L.page_indptr[3])]
+            assert own.size and own[:, 4].min() == 0
 
 
 def test_unique_bytes_of_full_radix_workload(pps):
