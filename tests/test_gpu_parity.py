@@ -58,12 +58,14 @@ def small_cases():
         # each, masks inside the last KV tile, short contexts too)
         "tree_small_g4": lambda: _small_trees(),
         "tree_shared": lambda: _tree_shared(),
-        # KV ends at every kind of place inside a 128-key tile
+        # KV ends at every kind of place inside a 128-key tile (16- and
+        # 64-token pages: one or two page boxes per tile on the key-tile kernel)
         "tile_edges": lambda: _tile_edges(),
+        "tile_edges_p64": lambda: _tile_edges(page_size=64),
     }
 
 
-def _tile_edges():
+def _tile_edges(page_size=16):
     """Decode rows and 3-token verify rows whose KV ends 1, 15, 16, 17, 31, 32,
     33, 111, 112, 113, 127 and 128 keys into the last 128-key tile, after 0 to
     2 whole tiles: the number of 16-key PV steps that run and the rows zeroed
@@ -75,8 +77,9 @@ def _tile_edges():
         q = 3 if i % 2 and e >= 3 else 1
         kv = 128 * (i % 3) + e
         reqs.append(([], kv - q, [q]))
-    return workloads.build_workload("tile_edges", shared_lens=[], requests=reqs, seed=23,
-                                    **{k: v for k, v in KW.items() if k != "keep_segments"})
+    kw = {k: v for k, v in KW.items() if k != "keep_segments"}
+    kw["page_size"] = page_size
+    return workloads.build_workload("tile_edges", shared_lens=[], requests=reqs, seed=23, **kw)
 
 
 def _star_and_chains():
