@@ -471,6 +471,12 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
       sets.swap(sorted);
     }
     std::vector<Task> bw, mm;
+    {
+      size_t n_mma = 0;
+      for (const auto& ts : sets) n_mma += ts.mma ? 1 : 0;
+      bw.reserve((sets.size() - n_mma) * (size_t)num_kv_heads);
+      mm.reserve(n_mma * (size_t)num_kv_heads);
+    }
     for (const auto& ts : sets) {
       if (!ts.mma) plan->shape.bw_rows_max = std::max(plan->shape.bw_rows_max, ts.n_tok * G);
       for (int32_t h = 0; h < num_kv_heads; ++h) {
