@@ -335,9 +335,10 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
         else bw_kv += sp.end - sp.a;
       }
     }
-    // The bandwidth kernel is persistent (one CTA per SM taking the
-    // work-sorted tasks in symmetric round-robin order), so tasks only need to
-    // be small enough to give every SM about two of them: each task costs a
+    // The small-row kernels are persistent (one CTA per SM; the CUDA-core one
+    // takes the work-sorted tasks in symmetric round-robin order, the key-tile
+    // one its per-CTA range), so tasks only need to be small enough to give
+    // every SM about two of them: each task costs a
     // query load and a cross-warp merge, and a split request costs partials
     // and a merge.  Measured on GB300: 4096-token tasks beat 2048 (decode,
     // 256 requests) and 1024+ beat 352 (radix subtrees, 64 requests).
