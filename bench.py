@@ -392,7 +392,10 @@ def run_pps(args):
     L0 = steps[0]["L"]
     qo_bytes = sum(2 * s["L"].num_tokens * L0.num_q_heads * L0.head_dim * 2 for s in steps)
     kv_unique = sum(i["kv_bytes_unique"] for i in infos)
-    roof = roofline(pps, roof_ms, infos, qo_bytes, args.workload, sustained=len(steps) > 1)
+    # the committed DRAM records are for the full-size launches: a resized batch
+    # gets none (its key names the request count)
+    key = args.workload if not args.requests else f"{args.workload}[{args.requests} requests]"
+    roof = roofline(pps, roof_ms, infos, qo_bytes, key, sustained=len(steps) > 1)
 
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
