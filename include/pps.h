@@ -455,6 +455,12 @@ pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t* kv_len,
  * tasks, partial merge).  The plan may be destroyed as soon as the call
  * returns: the library keeps the table's host memory until the upload has
  * completed.  A plan may be run any number of times.
+ * The page-locked table buffers (plans, and the tables of pps_attn_step and
+ * pps_attn_step_host) come from a small library pool, each buffer reused once
+ * its last upload has completed.  When four buffers large enough for a request
+ * are still waiting for their uploads, pps_attn_plan and the step calls wait
+ * for the oldest instead of pinning more memory: the host runs at most a few
+ * steps ahead of the device.
  */
 pps_status pps_attn_run(const pps_plan* plan, const void* q, const pps_pool* pool, void* out,
                         void* workspace, size_t workspace_bytes, void* stream);
