@@ -100,6 +100,28 @@ def test_plan_covers_every_visible_key_once(pps, name, kw, flags):
         check_plan(pps, st.layout, plan)
 
 
+TT = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16, values=False)
+
+
+@pytest.mark.parametrize("num_sms", [1, 3, 152])
+@pytest.mark.parametrize("name,kw", [
+    ("decode_heavy", dict(num_requests=9, kv_lo=1, kv_hi=900, **TT)),
+    ("radix_sharing", dict(groups=2, root=128, branch=32, pairs=2, tail_lo=1, tail_hi=200, **TT)),
+    ("mixed_budget", dict(budget=300, prefill_q=150, prefill_cached=40, num_verify=5,
+                          mu=4.0, sigma=1.0, clip_lo=1, clip_hi=900, **TT)),
+    ("tree_verify", dict(num_requests=4, tree_size=8, kv_lo=1, kv_hi=700, **TT)),
+])
+def test_key_tile_plans_cover_every_visible_key_once(pps, name, kw, num_sms):
+    """The same coverage checks on plans whose small-row tasks run on the
+    key-tile kernel (head_dim 128): per-CTA ranges instead of one order."""
+    wl = workloads.make(name, **kw)
+    for st in wl.steps:
+        plan = _plan(pps, st.layout, num_sms=num_sms, tree_parent=st.layout.tree_parent)
+        assert plan.info()["small_rows_on_tensor"] == 1
+        check_plan(pps, st.layout, plan)
+        assert len(plan.array("tt_cta")) == min(num_sms, plan.info()["num_bw_tasks"]) + 1
+
+
 @pytest.mark.parametrize("chunk", [16, 48, 128])
 def test_forced_small_chunks_still_cover(pps, chunk):
     wl = workloads.make("mixed_budget", budget=120, prefill_q=40, prefill_cached=33, num_verify=4,
