@@ -154,6 +154,23 @@ def test_parity_small(pps, name, flags):
         assert mx <= MAX_ABS and mean <= MEAN_ABS, (s, mx, mean, plans[s].info())
 
 
+@pytest.mark.parametrize("num_sms", [1, 3])
+@pytest.mark.parametrize("name", ["decode_heavy", "radix_sharing", "mixed_budget", "tree_small_g4",
+                                  "tile_edges", "tile_edges_p64"])
+def test_parity_few_ctas(pps, name, num_sms):
+    """Plans for 1 and 3 persistent CTAs: every CTA runs a long range of tasks
+    back to back (query-row and output double buffers, QK across task ends,
+    deferred outputs), against the oracle."""
+    wl, (ref, _) = _small(name)
+    pps.get_device_error(clear=True)
+    outs, _, plans = run_workload(wl, num_sms=num_sms)
+    assert pps.get_device_error(clear=True) == 0
+    for s, (o, r) in enumerate(zip(outs, ref)):
+        assert torch.isfinite(o).all(), s
+        mx, mean = errors(o, r)
+        assert mx <= MAX_ABS and mean <= MEAN_ABS, (s, mx, mean, plans[s].info())
+
+
 @pytest.mark.parametrize("flags", [0, 4])
 @pytest.mark.parametrize("chunk", [512, 2048])
 def test_parity_long_tasks(pps, chunk, flags):
