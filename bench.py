@@ -4,17 +4,25 @@
 
 One step = the whole hot path over one batch: kv_append of the step's new
 rows, attn_plan on the host, attn_run (bandwidth tasks, tensor-core tasks,
-partial merge).  Default workload: 256 decode requests, 32/8 heads, head_dim
-128, page_size 16, cached length uniform in [512, 4096], seed 1 (2.4 GB of KV,
-larger than the 129 MB L2, so no flush is needed between steps).
+partial merge), issued as one pps_attn_step call per batch (a long-prefill
+step is its four causal chunks).
 
-Prints one JSON line.  ``value`` is tokens/s with inputs resident in HBM;
-``e2e`` is the same metric with every step's inputs copied from pinned host
-memory and the output copied back inside the timed region: one
-``pps_attn_step_host`` call per step (host rows and tables in, host rows out;
-for the serving loops, the same copies around the device calls).  Under torchrun
-each rank runs its own batch (weak scaling, no data-path collective).
-``--impl reference`` times the fp64 CPU oracle on a bounded sample instead.
+Without --workload the run measures every configuration of the attention path
+one after the other: tiny_mixed, decode_heavy, radix_sharing, mixed_budget and
+long_prefill.  The JSON line's own fields (value, e2e, roofline, clocks) are
+the headline configuration's, mixed_budget (8192 new tokens over ~44 GB of KV,
+the largest that fits one GPU); ``configs`` holds every configuration's full
+record, each with its own roofline, e2e and CPU baseline.  --workload NAME
+measures one workload alone (also the serving loops, the draft-tree batch and
+the projection GEMMs).
+
+``value`` is tokens/s with inputs resident in HBM; ``e2e`` is the same metric
+with every step's inputs copied from pinned host memory and the output copied
+back inside the timed region: one ``pps_attn_step_host`` call per batch (host
+rows and tables in, host rows out; for the serving loops, the same copies
+around the device calls).  Under torchrun each rank runs its own batch (weak
+scaling, no data-path collective).  ``--impl reference`` times the fp64 CPU
+oracle on a bounded sample instead.
 """
 from __future__ import annotations
 
@@ -230,32 +238,52 @@ def roofline(pps, roof_ms, infos, qo_bytes, workload, sustained):
 # ---------------------------------------------------------------------------
 
 
-def run_pps(args):
-    import numpy as np
+# The five configurations of the attention path, in the order the default run
+# measures them; the headline line is the largest one that fits one GPU.
+SUITE = ["tiny_mixed", "decode_heavy", "radix_sharing", "mixed_budget", "long_prefill"]
+HEADLINE = "mixed_budget"
+
+
+def init_device():
     import torch
-
     import paged_prefix_shared_gb300 as pps
-    import workloads
-
     rank, local_rank, world = dist_env()
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
     pps.build()
     pps.lib()
+    return torch.device("cuda", local_rank)
 
-    if args.workload == "decode_heavy":
-        wl = workloads.decode_heavy(seed=1 + 1000 * rank, device=dev,
-                                    num_requests=args.requests or 256)
-    elif args.workload == "long_prefill" and args.requests:
-        wl = workloads.long_prefill(device=dev, num_requests=args.requests)
-    elif args.workload == "tree_verify" and args.requests:
-        wl = workloads.tree_verify(device=dev, num_requests=args.requests)
-    else:
-        wl = workloads.make(args.workload, device=dev)
-    # device-resident inputs
+
+def make_attention_workload(name, args, dev, rank):
+    import workloads
+    if name == "decode_heavy":
+        return workloads.decode_heavy(seed=1 + 1000 * rank, device=dev,
+                                      num_requests=args.requests or 256)
+    if name == "long_prefill" and args.requests:
+        return workloads.long_prefill(device=dev, num_requests=args.requests)
+    if name == "tree_verify" and args.requests:
+        return workloads.tree_verify(device=dev, num_requests=args.requests)
+    kw = {} if rank == 0 else {"seed": {"tiny_mixed": 0, "radix_sharing": 2, "mixed_budget": 3,
+                                        "long_prefill": 4, "tree_verify": 5}[name] + 1000 * rank}
+    return workloads.make(name, device=dev, **kw)
+
+
+def measure_attention(name, args, dev, cpu_seconds):
+    """One configuration of the attention path: the record of its bench line.
+
+    Device-resident loop: one pps_attn_step call per step and chunk (tables
+    uploaded, new rows appended, batch planned on the host, attention), with
+    CUDA events around every kernel class.  e2e: one pps_attn_step_host call
+    per step and chunk (rows from page-locked host memory, output back)."""
+    import torch
+
+    import paged_prefix_shared_gb300 as pps
+
+    rank, local_rank, world = dist_env()
+    wl = make_attention_workload(name, args, dev, rank)
     # The library appends into a copy; the drawn pool stays as the generator
     # made it (the CPU baseline starts from it).  Re-appending the same rows
     # every step is idempotent.
@@ -263,41 +291,30 @@ def run_pps(args):
     steps = []
     for st in wl.steps:
         L = st.layout
-        tabs = {n: torch.as_tensor(getattr(L, n), dtype=torch.int32, device=dev)
-                for n in ("q_indptr", "cached_len", "page_indptr", "page_indices")}
         out = torch.empty_like(st.q)
+        call = pps.StepCall(pk, pv, st.q, st.k_new, st.v_new, L.q_indptr, L.kv_len,
+                            L.page_indptr, L.page_indices, out, tree_parent=L.tree_parent)
         plan = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices, L.num_q_heads,
                              L.num_kv_heads, L.head_dim, L.page_size, L.num_pages,
                              tree_parent=L.tree_parent)
-        info = plan.info()
-        ws = torch.empty(info["workspace_bytes"], dtype=torch.uint8, device=dev)
-        steps.append(dict(L=L, st=st, tabs=tabs, out=out, ws=ws, info=info))
+        steps.append(dict(L=L, st=st, out=out, call=call, info=plan.info()))
+        plan.destroy()
     stream = torch.cuda.current_stream()
     nk = pps.NUM_KERNEL_CLASSES
 
-    def one_step(ev=None):
-        # append (device tables resident), plan (host, every step), attention
+    def one_step(evs=None):
         for i, s in enumerate(steps):
-            L, st, t = s["L"], s["st"], s["tabs"]
-            pps.kv_append(pk, pv, st.k_new, st.v_new, t["q_indptr"], t["cached_len"],
-                          t["page_indptr"], t["page_indices"])
-            plan = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices,
-                                 L.num_q_heads, L.num_kv_heads, L.head_dim, L.page_size,
-                                 L.num_pages, tree_parent=L.tree_parent)
-            pps.attn_run(plan, st.q, pk, pv, s["out"], s["ws"],
-                         events=None if ev is None else ev[i])
+            s["call"](None if evs is None else evs[i])
 
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize()
 
-    # per-kernel events (one set per step per chunk) -> average launch duration
+    # per-kernel events (one set per step per chunk) -> average launch duration;
+    # created, recorded once and converted to C arrays outside the timed region
     ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2 * nk)] for _ in steps]
           for _ in range(args.steps)]
-    for per_step in ev:                 # torch creates events on first record: do it now,
-        for per_chunk in per_step:      # outside the timed region
-            for e in per_chunk:
-                e.record(stream)
+    evh = [[pps.event_array(per_chunk) for per_chunk in per_step] for per_step in ev]
     torch.cuda.synchronize()
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -309,7 +326,7 @@ def run_pps(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for k in range(args.steps):
-        one_step(ev[k])
+        one_step(evh[k])
     e1.record(stream)
     torch.cuda.synchronize()
     sampler.mark("t1")
@@ -318,12 +335,16 @@ def run_pps(args):
     clocks = sampler.stop()
     ms = e0.elapsed_time(e1) / args.steps
     ms_max = max_over_ranks(ms, world, dev)
-    kern_ms = [0.0] * nk
-    for k in range(args.steps):
-        for i in range(len(steps)):
-            for c in range(nk):
-                kern_ms[c] += ev[k][i][2 * c].elapsed_time(ev[k][i][2 * c + 1])
-    kern_ms = [x / args.steps for x in kern_ms]        # per step (summed over chunks)
+
+    def kernel_ms():
+        acc = [0.0] * nk
+        for k in range(args.steps):
+            for i in range(len(steps)):
+                for c in range(nk):
+                    acc[c] += ev[k][i][2 * c].elapsed_time(ev[k][i][2 * c + 1])
+        return [x / args.steps for x in acc]        # per step (summed over chunks)
+
+    kern_ms = kernel_ms()
 
     # ---- kernel times with a cold L2 (KV that L2 could partly hold) -----------------------
     # Each step is preceded by a write of a buffer four times the L2 size; only the
@@ -334,16 +355,11 @@ def run_pps(args):
     cold_ms = None
     if flush:
         fbuf = torch.empty(4 * l2_bytes // 4, dtype=torch.int32, device=dev)
-        cold = [0.0] * nk
         for k in range(args.steps):
             fbuf.fill_(k)
-            one_step(ev[k])
+            one_step(evh[k])
         torch.cuda.synchronize()
-        for k in range(args.steps):
-            for i in range(len(steps)):
-                for c in range(nk):
-                    cold[c] += ev[k][i][2 * c].elapsed_time(ev[k][i][2 * c + 1])
-        cold_ms = [x / args.steps for x in cold]
+        cold_ms = kernel_ms()
         del fbuf
     roof_ms = cold_ms if cold_ms is not None else kern_ms
 
@@ -352,25 +368,25 @@ def run_pps(args):
     value = total_tokens / (ms_max / 1e3)
 
     # ---- e2e: host buffers in, host result out, through the public API -------------------
-    # One pps_attn_step_host call per step: the step's rows and tables go from
-    # page-locked host memory to the device, through append, plan and attention,
-    # and the output rows come back, all enqueued by the library.
+    # One pps_attn_step_host call per step and chunk: the rows and tables go from
+    # page-locked host memory to the device, through append, plan and
+    # attention, and the output rows come back, all enqueued by the library.
     h = []
     for s in steps:
         st, L = s["st"], s["L"]
         host = {n: st.__dict__[n].cpu().pin_memory() for n in ("q", "k_new", "v_new")}
-        h.append(dict(host=host, out_h=torch.empty_like(s["out"], device="cpu").pin_memory()))
+        out_h = torch.empty_like(s["out"], device="cpu").pin_memory()
+        call = pps.StepCall(pk, pv, host["q"], host["k_new"], host["v_new"], L.q_indptr,
+                            L.kv_len, L.page_indptr, L.page_indices, out_h,
+                            tree_parent=L.tree_parent, host=True)
+        h.append(dict(host=host, out_h=out_h, call=call))
     tab_bytes = sum(4 * (3 * s["L"].num_requests + 2 + len(s["L"].page_indices)) for s in steps)
     bi = sum(v.numel() * v.element_size() for x in h for v in x["host"].values()) + tab_bytes
     bo = sum(x["out_h"].numel() * x["out_h"].element_size() for x in h)
 
     def e2e_step():
-        for s, x in zip(steps, h):
-            L = s["L"]
-            hq = x["host"]
-            pps.attn_step_host(pk, pv, hq["q"], hq["k_new"], hq["v_new"], L.q_indptr, L.kv_len,
-                               L.page_indptr, L.page_indices, x["out_h"],
-                               tree_parent=L.tree_parent)
+        for x in h:
+            x["call"]()
 
     for _ in range(max(3, args.warmup // 4)):
         e2e_step()
@@ -394,7 +410,7 @@ def run_pps(args):
     kv_unique = sum(i["kv_bytes_unique"] for i in infos)
     # the committed DRAM records are for the full-size launches: a resized batch
     # gets none (its key names the request count)
-    key = args.workload if not args.requests else f"{args.workload}[{args.requests} requests]"
+    key = name if not args.requests else f"{name}[{args.requests} requests]"
     roof = roofline(pps, roof_ms, infos, qo_bytes, key, sustained=len(steps) > 1)
 
     result = {
@@ -402,14 +418,16 @@ def run_pps(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, seeded layouts; no dataset)",
-        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}" +
+        "config": {"workload": f"{name}: {DESCRIPTIONS[name]}" +
                    (f" [{args.requests} requests]" if args.requests else ""),
                    "tokens_per_step": tokens, "kv_bytes_unique_per_step": kv_unique,
                    "l2": (f"step time warm (KV only {kv_unique / l2_bytes:.1f}x L2); kernel "
                           f"times for the roofline re-measured with a {4 * l2_bytes} B L2 flush "
                           f"before every step") if flush else
                    "inputs larger than L2 (KV > 4x the 129 MB L2), no flush",
-                   "parallelism": f"dp{world} (independent batch per GPU, no collective)"},
+                   "parallelism": f"dp{world} (independent batch per GPU, no collective)",
+                   "step_call": "pps_attn_step: one native call per step and chunk (tables "
+                                "uploaded, rows appended, batch planned on the host, attention)"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "ms_per_step": ms_e2e},
         "gpu_launches": launches,
@@ -426,7 +444,45 @@ def run_pps(args):
                      "tflops_total": sum(i["flops_total"] for i in infos) / (ms_max / 1e3) / 1e12},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(wl, budget_s=cpu_seconds)
+    del steps, h, pk, pv, wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return result
+
+
+def run_pps(args):
+    """One attention workload (--workload)."""
+    rank, _, world = dist_env()
+    dev = init_device()
+    result = measure_attention(args.workload, args, dev, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_suite(args):
+    """The default run: every configuration of the attention path, one after
+    the other on the same GPU; the line's own fields are the headline
+    configuration's (the largest that fits one GPU), ``configs`` holds every
+    configuration's full record."""
+    rank, _, world = dist_env()
+    dev = init_device()
+    recs = {}
+    for name in SUITE:
+        recs[name] = measure_attention(name, args, dev, args.cpu_seconds)
+    result = dict(recs[HEADLINE])
+    result["configs"] = {n: {k: v for k, v in r.items()
+                             if k not in ("metric", "unit", "n_gpus", "steps", "warmup",
+                                          "higher_is_better", "scaling", "vs_baseline", "dtype",
+                                          "data")}
+                         for n, r in recs.items()}
+    result["config"] = dict(result["config"])
+    result["config"]["suite"] = ("every configuration of the attention path measured in this "
+                                 "run (configs); the line's value, e2e and roofline are "
+                                 f"{HEADLINE}'s")
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -984,37 +1040,100 @@ def projections_cpu_baseline(a, ws, budget_s=15.0):
                       f"{os.environ.get('OPENBLAS_NUM_THREADS', 'all')} of {cores} cores"}
 
 
-def _oracle_sample_time(wl, reqs, step):
-    """Oracle wall time (s) and tokens for a subset of requests of one step."""
-    from oracle_run import oracle_steps
-    import workloads
-    sub = workloads.sub_workload(wl, step, reqs)
-    t0 = time.perf_counter()
-    oracle_steps(sub)
-    dt = time.perf_counter() - t0
-    return dt, sub.steps[step].layout.num_tokens
+class OracleSampler:
+    """Times the fp64 oracle, as it stands, on units of a workload: a unit is
+    one request's new rows at one step, taken in a fixed random order.  Setting a request up (its pages and
+    every step's new rows copied to the host, appended with the oracle's own
+    scatter) is not timed; the oracle's attention over the unit is.  A unit
+    of more than ``cap`` rows is timed on ``cap`` evenly spaced rows and its
+    time scaled to all of its rows."""
+
+    def __init__(self, wl, cap=64):
+        import numpy as np
+        self.wl, self.cap = wl, cap
+        self.last = len(wl.steps) - 1
+        L = wl.steps[self.last].layout
+        self.reqs = [r for r in range(L.num_requests)
+                     if any(int(st.layout.q_len[r]) > 0 for st in wl.steps)]
+        units = [(r, s) for r in self.reqs for s in range(len(wl.steps))
+                 if int(wl.steps[s].layout.q_len[r]) > 0]
+        # a fixed random order, so that any prefix of it samples the batch's mix
+        # (prefill chunks, verify drafts, decode rows) without favouring the first
+        perm = np.random.default_rng(12345).permutation(len(units))
+        self.units = [units[i] for i in perm]
+        self.pos = 0
+        self._req, self._sub, self._pools = None, None, None
+        self._done = {}
+        self.np = np
+
+    def _setup(self, r):
+        import oracle
+        import workloads
+        if self._req == r:
+            return
+        if r in self._done:
+            self._req, (self._sub, self._pools) = r, self._done[r]
+            return
+        sub = workloads.sub_workload(self.wl, self.last, [r])
+        pk, pv = sub.pool_k, sub.pool_v
+        for st in sub.steps:
+            L = st.layout
+            pk, pv = oracle.reference_scatter(pk, pv, st.k_new, st.v_new, L.q_indptr,
+                                              L.cached_len, L.page_indptr, L.page_indices,
+                                              L.page_size)
+        self._req, self._sub, self._pools = r, sub, (pk, pv)
+        if len(self._done) < 16:                 # requests set up so far, kept for the wrap
+            self._done[r] = (sub, (pk, pv))
+
+    def next_unit(self):
+        """(rows of the unit, rows timed, seconds timed) of the next unit (wrapping)."""
+        import oracle
+        np = self.np
+        r, s = self.units[self.pos % len(self.units)]
+        self.pos += 1
+        self._setup(r)
+        st = self._sub.steps[s]
+        L = st.layout
+        n = int(L.q_len[0])
+        sel = np.unique(np.linspace(0, n - 1, min(n, self.cap)).round().astype(np.int64))
+        pk, pv = self._pools
+        t0 = time.perf_counter()
+        oracle.paged_attention(st.q, pk, pv, L.q_indptr, L.kv_len, L.page_indptr,
+                               L.page_indices, L.page_size, L.sm_scale, L.num_kv_heads,
+                               tokens=sel, tree_parent=L.tree_parent)
+        return n, len(sel), time.perf_counter() - t0
+
+    def run(self, budget_s, min_units=1):
+        """Units until ``budget_s`` of timed oracle work (or four times that of
+        wall time, set-up included): (rows, estimated s, units, timed s)."""
+        rows, est, units, timed = 0, 0.0, 0, 0.0
+        w0 = time.perf_counter()
+        while units < min_units or (timed < budget_s and
+                                    time.perf_counter() - w0 < 4 * budget_s):
+            n, m, dt = self.next_unit()
+            rows += n
+            est += dt * n / m
+            timed += dt
+            units += 1
+            if units >= len(self.units) and timed >= 0.2 * budget_s:
+                break
+        return rows, est, units, timed
 
 
-def cpu_baseline(wl, budget_s=15.0, step=None):
+def cpu_baseline(wl, budget_s=15.0):
     """The fp64 oracle, as it stands, timed on this host on a bounded sample
-    of the same workload (whole requests, in order, until ~budget_s)."""
-    L = wl.steps[-1].layout
-    step = len(wl.steps) - 1 if step is None else step
+    of the same workload (OracleSampler units, in request order)."""
     cores = len(os.sched_getaffinity(0))
-    used, tok, secs = [], 0, 0.0
-    for r in range(L.num_requests):
-        if L.q_len[r] == 0:
-            continue
-        dt, n = _oracle_sample_time(wl, [r], step)
-        used.append(r)
-        tok += n
-        secs += dt
-        if secs >= budget_s:
-            break
-    return {"value": tok / secs if secs else None, "unit": "tokens/s", "cores": cores,
+    smp = OracleSampler(wl)
+    rows, est, units, timed = smp.run(budget_s)
+    L = wl.steps[-1].layout
+    return {"value": rows / est if est else None, "unit": "tokens/s", "cores": cores,
             "kind": "oracle",
-            "sample": f"{len(used)} of {L.num_requests} requests ({tok} new tokens, all their "
-                      f"rows, step {step}) in {secs:.1f} s; numpy fp64 with BLAS threads = "
+            "sample": f"{units} of {len(smp.units)} (request, step) units (fixed random order) of "
+                      f"{L.num_requests} "
+                      f"requests x {len(wl.steps)} step(s), {rows} new tokens; units of more than "
+                      f"{smp.cap} rows timed on {smp.cap} evenly spaced rows and scaled "
+                      f"({timed:.1f} s of oracle time); numpy fp64 with BLAS threads = "
                       f"{os.environ.get('OPENBLAS_NUM_THREADS', 'all')} of {cores} cores"}
 
 
@@ -1068,34 +1187,33 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0},
         }), flush=True)
         return
+    # The attention configurations: the same seeded workload as the GPU arm
+    # (drawn on the GPU when there is one, so the values are identical), the
+    # oracle timed on a bounded sample per step.
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    wl = workloads.make(args.workload, device=dev)
-    L = wl.steps[-1].layout
-    step = len(wl.steps) - 1
-    reqs = [r for r in range(L.num_requests) if L.q_len[r] > 0]
-    # calibrate: time per request, then size each step's sample to fit the budget
-    dt0, n0 = _oracle_sample_time(wl, reqs[:1], step)
-    per_step = max(0.05, args.cpu_seconds * 8 / max(1, args.steps + args.warmup))
-    m = max(1, min(len(reqs), int(per_step / max(dt0, 1e-6))))
-    for w in range(args.warmup):
-        _oracle_sample_time(wl, reqs[(w * m) % len(reqs):][:m] or reqs[:m], step)
-    tot_t, tot_tok = 0.0, 0
-    for k in range(args.steps):
-        sel = reqs[(k * m) % len(reqs):][:m] or reqs[:m]
-        dt, n = _oracle_sample_time(wl, sel, step)
-        tot_t += dt
-        tot_tok += n
-    value = tot_tok / tot_t
+    name = args.workload or HEADLINE
+    wl = make_attention_workload(name, args, dev, 0)
+    smp = OracleSampler(wl)
+    per_step = max(0.05, args.ref_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        smp.run(per_step)
+    rows, est, units, timed = 0, 0.0, 0, 0.0
+    for _ in range(args.steps):
+        n, e, u, t = smp.run(per_step)
+        rows, est, units, timed = rows + n, est + e, units + u, timed + t
+    value = rows / est
     cores = len(os.sched_getaffinity(0))
-    sample = (f"{m} of {L.num_requests} requests per step (consecutive, wrapping), fp64 numpy "
-              f"oracle on {cores} host cores")
+    sample = (f"per step about {per_step:.2f} s of oracle time: (request, step) units in a "
+              f"fixed random order, wrapping; units of more than {smp.cap} rows timed on {smp.cap} evenly "
+              f"spaced rows and scaled; {units} units, {rows} new tokens over {args.steps} timed "
+              f"steps; fp64 numpy oracle on {cores} host cores")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": est / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, seeded layouts; no dataset)",
-        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+        "config": {"workload": f"{name}: {DESCRIPTIONS[name]}",
                    "parallelism": "host cores, rank 0 only"},
         "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": sample, "value": value,
                          "unit": "tokens/s"},
@@ -1107,12 +1225,17 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="decode_heavy", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--workload", default=None, choices=sorted(DESCRIPTIONS),
+                    help="one workload; default: every configuration of the attention path "
+                         f"({', '.join(SUITE)}), headline {HEADLINE}")
     ap.add_argument("--impl", default="pps", choices=["pps", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=6.0,
+                    help="oracle time of the CPU baseline, per configuration")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="--impl reference: oracle time over all warm-up and timed steps")
     ap.add_argument("--flush-l2", default="auto", choices=["auto", "on", "off"],
                     help="re-time the kernels with an L2 flush before each step "
                          "(auto: when the unique KV is under 4x the L2 size)")
@@ -1128,6 +1251,8 @@ def main():
         run_cache_serving(args)
     elif args.workload == "projections":
         run_projections(args)
+    elif args.workload is None:
+        run_suite(args)
     else:
         run_pps(args)
 

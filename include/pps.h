@@ -48,8 +48,10 @@
  *  - Calls never throw and never abort.  They return PPS_OK (0) or a negative
  *    pps_status.  Argument errors are detected on the host before anything is
  *    enqueued.  Errors that only the GPU can see (a page id read from a device
- *    array that is out of range) are recorded in a device error word; read it
- *    with pps_get_device_error().  Kernels never trap.
+ *    array that is out of range) are recorded in a device error word: the
+ *    device's own (pps_get_device_error), or the one the caller registered for
+ *    the stream the work runs on (pps_set_stream_error_word).  Kernels never
+ *    trap.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Work is enqueued asynchronously on it.
  *  - Supported shapes: head_dim in {64, 128}; page_size in {16, 32, 64, 128};
@@ -441,6 +443,15 @@ pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t* kv_len,
 /*
  * pps_attn_run -- the mixed-batch attention.
  *
+ * Runs a plan's tile tasks as the XY-Serve review describes the attention of a
+ * P/D/V batch ("Core claim": one matmul-softmax-matmul meta-kernel over the
+ * task table, mask sparsity skipping invalid tiles; Fig. 10, the cube working
+ * on one tile while the vector unit runs the softmax of another), with the
+ * KV split into pieces whose partial softmaxes are merged exactly
+ * ("Assumptions & free parameters": online softmax with rescaling equals the
+ * plain softmax) and shared-prefix pages read once per group (SGLang review,
+ * "Core claim", RadixAttention).
+ *
  *  q          device bf16 [num_new_tokens, num_q_heads, head_dim].
  *  pool       host descriptor; its pages must already hold every row the step
  *             attends to (call pps_kv_append first for this step's rows).
@@ -628,8 +639,30 @@ pps_status pps_attn_step_host(const pps_pool* pool, const void* h_q, const void*
                               size_t scratch_bytes, size_t* out_scratch_bytes, void* stream);
 
 /* Reads the current device's error word into *code (0 = none); if `clear`
- * is nonzero, resets it to 0.  Synchronous (waits for the device). */
+ * is nonzero, resets it to 0.  Synchronous (waits for the device).  Work on a
+ * stream with its own error word (pps_set_stream_error_word) does not touch
+ * this one. */
 pps_status pps_get_device_error(int32_t* code, int32_t clear);
+
+/*
+ * Stream-scoped device error words.  Batches that run concurrently on
+ * different streams each need to know whether their own work failed (the
+ * XY-Serve review, "Assumptions & free parameters", keeps the block table
+ * consistent across requests; an error has to be traced to the batch whose
+ * tables caused it).  pps_set_stream_error_word registers a caller-owned
+ * device int32 (4-byte aligned, set to 0 by the caller before use) for
+ * `stream` on the current device: every later call that enqueues kernels on
+ * that stream (pps_kv_append, pps_copy_slots, the attention and step calls,
+ * pps_gemm_bf16) records its device-side errors (PPS_DEV_ERR_*) there, the
+ * first error of a run of calls winning, instead of in the device's word.
+ * d_word NULL removes the registration.  The word must stay valid while work
+ * that uses it is in flight; the library never frees it.
+ * pps_get_stream_error enqueues a read of the word on `stream` (and, if
+ * `clear` is nonzero, a reset to 0 behind it) and waits for the stream:
+ * *code = the stream's word, or the device's word when none is registered.
+ */
+pps_status pps_set_stream_error_word(void* stream, int32_t* d_word);
+pps_status pps_get_stream_error(void* stream, int32_t* code, int32_t clear);
 
 /*
  * pps_selftest_wait_timeout -- diagnostic for the kernels' bounded waits.

@@ -21,8 +21,8 @@ import numpy as np
 
 __all__ = [
     "PPSError", "Plan", "lib", "build", "kv_append", "attn_plan", "attn_run", "plan_destroy",
-    "attn_step_host", "attn_step",
-    "get_device_error", "launch_count", "status_string", "version", "LIB_PATH",
+    "attn_step_host", "attn_step", "StepCall", "event_array",
+    "get_device_error", "set_stream_error_word", "get_stream_error", "launch_count", "status_string", "version", "LIB_PATH",
     "PLAN_NO_GROUPS", "PLAN_CUDA_CORES_ONLY", "PLAN_SMALL_ROWS_CUDA_CORES", "KERNEL_BANDWIDTH", "KERNEL_TENSOR", "KERNEL_MERGE",
 ]
 
@@ -155,6 +155,10 @@ def lib():
                                 ctypes.c_float, ctypes.POINTER(_PlanOptions), vp, vp, sz,
                                 ctypes.POINTER(sz), vp, vp]
     L.pps_attn_step.restype = i32
+    L.pps_set_stream_error_word.argtypes = [vp, vp]
+    L.pps_set_stream_error_word.restype = i32
+    L.pps_get_stream_error.argtypes = [vp, ctypes.POINTER(i32), i32]
+    L.pps_get_stream_error.restype = i32
     L.pps_attn_run_noalloc.argtypes = [vp, vp, ctypes.POINTER(_Pool), vp, vp]
     L.pps_attn_run_noalloc.restype = i32
     L.pps_plan_destroy.argtypes = [vp]
@@ -350,6 +354,26 @@ def attn_run(plan: Plan, q, pool_k, pool_v, out, workspace, stream=None, events=
 def get_device_error(clear: bool = True) -> int:
     code = ctypes.c_int32()
     _check(lib().pps_get_device_error(ctypes.byref(code), int(bool(clear))), "pps_get_device_error")
+    return int(code.value)
+
+
+def set_stream_error_word(word, stream=None):
+    """pps_set_stream_error_word: device errors of later calls on `stream`
+    (default: the current stream) go to `word`, a one-element int32 CUDA
+    tensor the caller zeroes and keeps alive; None removes the registration."""
+    import torch
+    if word is not None and (not word.is_cuda or word.dtype != torch.int32 or word.numel() < 1):
+        raise PPSError("word must be an int32 CUDA tensor")
+    _check(lib().pps_set_stream_error_word(_stream(stream),
+                                           None if word is None else ctypes.c_void_p(word.data_ptr())),
+           "pps_set_stream_error_word")
+
+
+def get_stream_error(stream=None, clear: bool = True) -> int:
+    """pps_get_stream_error: the error word of `stream` (waits for the stream)."""
+    code = ctypes.c_int32()
+    _check(lib().pps_get_stream_error(_stream(stream), ctypes.byref(code), int(bool(clear))),
+           "pps_get_stream_error")
     return int(code.value)
 
 
@@ -754,6 +778,67 @@ def attn_step(pool_k, pool_v, q, k_new, v_new, q_indptr, kv_len, page_indptr, pa
             break
         _step_scratch[dev] = torch.empty(int(need.value * 1.25) + 256, dtype=torch.uint8, device=dev)
     _check(code, "pps_attn_step")
+
+
+class StepCall:
+    """One step of the attention path as a reusable native call:
+    pps_attn_step (device rows) or pps_attn_step_host (``host=True``: rows in
+    page-locked CPU tensors), with every argument marshalled once.  Each call
+    still uploads the tables, appends the rows, plans the batch on the host
+    and runs the attention: only the Python-side conversions are done up
+    front, for a loop that repeats one batch shape (a benchmark, or a caller
+    that rewrites the same host tables in place between steps).  The tensors
+    and arrays given here must stay alive and keep their addresses."""
+
+    def __init__(self, pool_k, pool_v, q, k_new, v_new, q_indptr, kv_len, page_indptr,
+                 page_indices, out, tree_parent=None, host=False, sm_scale=None, num_sms=0,
+                 bw_chunk_tokens=0, mma_chunk_tokens=0, flags=0, stream=None):
+        import torch
+        self._keep = [pool_k, pool_v, q, k_new, v_new, out]
+        self._pool = _pool(pool_k, pool_v)
+        tabs = [_host_addr(a) for a in (q_indptr, kv_len, page_indptr,
+                                        page_indices if len(page_indices) else np.zeros(1, np.int32))]
+        tp = None if tree_parent is None else \
+            _host_addr(tree_parent if len(tree_parent) else np.zeros(1, np.int32))
+        self._keep += [a for a, _ in tabs] + ([tp[0]] if tp else [])
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(pool_k.shape[3])
+        self._opts = _PlanOptions(int(num_sms), int(bw_chunk_tokens), int(mma_chunk_tokens),
+                                  int(flags))
+        bf = torch.bfloat16
+        rows = (lambda t: _host_ptr(t, bf)) if host else (lambda t: _dev(t, bf))
+        self._host = host
+        self._fn = lib().pps_attn_step_host if host else lib().pps_attn_step
+        self._args = [ctypes.byref(self._pool), rows(q), rows(k_new), rows(v_new),
+                      *[a for _, a in tabs], tp[1] if tp else None, len(tabs[1][0]),
+                      int(q.shape[1]), float(sm_scale), ctypes.byref(self._opts), rows(out)]
+        need = ctypes.c_size_t()
+        extra = [] if host else [None]
+        code = self._fn(*self._args, None, 0, ctypes.byref(need), _stream(stream), *extra)
+        if code != -4:
+            _check(code, "pps_attn_step" + ("_host" if host else ""))
+        self.scratch = torch.empty(max(int(need.value), 256), dtype=torch.uint8,
+                                   device=pool_k.device)
+        self._tail = [_dev(self.scratch), self.scratch.numel(), None, _stream(stream)]
+
+    def __call__(self, events=None):
+        """One step.  ``events``: None, or an ``event_array`` (device rows only)."""
+        if self._host:
+            code = self._fn(*self._args, *self._tail)
+        else:
+            code = self._fn(*self._args, *self._tail, events)
+        _check(code, "pps_attn_step" + ("_host" if self._host else ""))
+
+
+def event_array(events):
+    """2 * NUM_KERNEL_CLASSES torch.cuda.Event objects (or None) as the C array
+    of cudaEvent_t that pps_attn_run_events / pps_attn_step take."""
+    handles = []
+    for e in events:
+        if e is not None and not e.cuda_event:
+            e.record()          # torch creates the CUDA event on first record
+        handles.append(ctypes.c_void_p(e.cuda_event) if e is not None else None)
+    return (ctypes.c_void_p * (2 * NUM_KERNEL_CLASSES))(*handles)
 
 
 def gemm_bf16(a, w, c, stream=None):

@@ -25,12 +25,24 @@ constexpr int kMaxDevices = 64;
 int32_t* g_err_ptr[kMaxDevices] = {nullptr};
 std::mutex g_err_mu;
 
-// Device address of the error word on the current device (looked up once per device).
-int32_t* error_word(cudaError_t* status) {
+// Caller-owned error words registered for streams (pps_set_stream_error_word).
+struct StreamWord {
+  void* stream;
+  int dev;
+  int32_t* word;
+};
+std::vector<StreamWord> g_stream_words;
+
+// The error word for work enqueued on `stream` of the current device: the
+// caller's word registered for that stream, else the device's own word
+// (looked up once per device).
+int32_t* error_word(cudaError_t* status, void* stream) {
   int dev = 0;
   *status = cudaGetDevice(&dev);
   if (*status != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lk(g_err_mu);
+  for (const StreamWord& w : g_stream_words)
+    if (w.stream == stream && w.dev == dev) return w.word;
   if (!g_err_ptr[dev]) {
     void* p = nullptr;
     *status = cudaGetSymbolAddress(&p, g_pps_device_error);
@@ -61,7 +73,7 @@ pps_status run_impl(const pps_plan* plan, const void* q, const pps_pool* pool, v
       ((uintptr_t)pool->v & 15))
     return PPS_ERR_INVALID_ARGUMENT;
   cudaError_t e;
-  int32_t* err = error_word(&e);
+  int32_t* err = error_word(&e, stream);
   if (!err) return PPS_ERR_CUDA;
   auto st = (cudaStream_t)stream;
   auto rec = [&](int i) {
@@ -255,7 +267,7 @@ pps_status pps_kv_append(const pps_pool* pool, const void* k_new, const void* v_
       ((uintptr_t)pool->v & 15))
     return PPS_ERR_INVALID_ARGUMENT;
   cudaError_t e;
-  int32_t* err = error_word(&e);
+  int32_t* err = error_word(&e, stream);
   if (!err) return PPS_ERR_CUDA;
   return pps::launch_kv_append(*pool, k_new, v_new, q_indptr, cached_len, page_indptr,
                                page_indices, num_requests, num_new_tokens, err, stream)
@@ -272,7 +284,7 @@ pps_status pps_copy_slots(const pps_pool* pool, const int32_t* src_pages, const 
       ((uintptr_t)pool->v & 15))
     return PPS_ERR_INVALID_ARGUMENT;
   cudaError_t e;
-  int32_t* err = error_word(&e);
+  int32_t* err = error_word(&e, stream);
   if (!err) return PPS_ERR_CUDA;
   return pps::launch_copy_slots(*pool, src_pages, dst_pages, num_slots, count, err, stream)
              ? PPS_ERR_CUDA : PPS_OK;
@@ -285,7 +297,7 @@ pps_status pps_gemm_bf16(const void* a, const void* w, void* c, int32_t M, int32
   if (!a || !w || !c || ((uintptr_t)a & 15) || ((uintptr_t)w & 15) || ((uintptr_t)c & 15))
     return PPS_ERR_INVALID_ARGUMENT;
   cudaError_t e;
-  int32_t* err = error_word(&e);
+  int32_t* err = error_word(&e, stream);
   if (!err) return PPS_ERR_CUDA;
   return pps::launch_gemm_bf16(a, w, c, M, N, K, err, stream) ? PPS_ERR_CUDA : PPS_OK;
 }
@@ -451,11 +463,42 @@ pps_status pps_get_device_error(int32_t* code, int32_t clear) {
   return PPS_OK;
 }
 
+pps_status pps_set_stream_error_word(void* stream, int32_t* d_word) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PPS_ERR_CUDA;
+  if (d_word && ((uintptr_t)d_word & 3)) return PPS_ERR_INVALID_ARGUMENT;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  for (size_t i = 0; i < g_stream_words.size(); ++i)
+    if (g_stream_words[i].stream == stream && g_stream_words[i].dev == dev) {
+      if (d_word) {
+        g_stream_words[i].word = d_word;
+      } else {
+        g_stream_words.erase(g_stream_words.begin() + (ptrdiff_t)i);
+      }
+      return PPS_OK;
+    }
+  if (d_word) g_stream_words.push_back(StreamWord{stream, dev, d_word});
+  return PPS_OK;
+}
+
+pps_status pps_get_stream_error(void* stream, int32_t* code, int32_t clear) {
+  if (!code) return PPS_ERR_INVALID_ARGUMENT;
+  *code = 0;
+  cudaError_t e;
+  int32_t* w = error_word(&e, stream);
+  if (!w) return PPS_ERR_CUDA;
+  auto st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(code, w, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return PPS_ERR_CUDA;
+  if (clear && cudaMemsetAsync(w, 0, sizeof(int32_t), st) != cudaSuccess) return PPS_ERR_CUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? PPS_OK : PPS_ERR_CUDA;
+}
+
 pps_status pps_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
   if (limit_ns < 1000) limit_ns = 1000;
   if (limit_ns > 1000000000ull) limit_ns = 1000000000ull;
   cudaError_t e;
-  int32_t* err = error_word(&e);
+  int32_t* err = error_word(&e, stream);
   if (!err) return PPS_ERR_CUDA;
   wait_timeout_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(err, limit_ns);
   pps::count_launch();

@@ -272,6 +272,56 @@ def test_kv_append_flags_bad_page_id_on_device(pps):
     assert torch.isfinite(outs[0]).all()
 
 
+def test_stream_error_words_keep_each_batch_errors_apart(pps):
+    """Two batches on two streams, each stream with its own registered error
+    word: the bad page id in one stream's append tables shows in that stream's
+    word only; the other stream's word and the device's word stay 0."""
+    wl = workloads.tiny_mixed()
+    pk_a, pv_a, steps_a = to_device(wl)
+    pk_b, pv_b, steps_b = to_device(wl)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    wa = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wb = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    pps.get_device_error(clear=True)
+    pps.set_stream_error_word(wa, stream=sa)
+    pps.set_stream_error_word(wb, stream=sb)
+    try:
+        a, b = steps_a[0], steps_b[0]
+        bad = a["tabs"]["page_indices"].clone()
+        bad[:] = 10_000                              # every page id out of range
+        torch.cuda.synchronize()
+        with torch.cuda.stream(sa):
+            pps.kv_append(pk_a, pv_a, a["k_new"], a["v_new"], a["tabs"]["q_indptr"],
+                          a["tabs"]["cached_len"], a["tabs"]["page_indptr"], bad, stream=sa)
+        with torch.cuda.stream(sb):
+            pps.kv_append(pk_b, pv_b, b["k_new"], b["v_new"], b["tabs"]["q_indptr"],
+                          b["tabs"]["cached_len"], b["tabs"]["page_indptr"],
+                          b["tabs"]["page_indices"], stream=sb)
+            L = b["layout"]
+            plan = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices,
+                                 L.num_q_heads, L.num_kv_heads, L.head_dim, L.page_size,
+                                 pk_b.shape[0])
+            ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+            out = torch.full_like(b["q"], float("nan"))
+            pps.attn_run(plan, b["q"], pk_b, pv_b, out, ws, stream=sb)
+        assert pps.get_stream_error(stream=sa, clear=False) == 1   # PPS_DEV_ERR_APPEND_PAGE_ID
+        assert pps.get_stream_error(stream=sb, clear=False) == 0
+        torch.cuda.synchronize()
+        assert int(wa.item()) == 1 and int(wb.item()) == 0
+        assert pps.get_device_error(clear=True) == 0
+        assert torch.isfinite(out).all()
+        # clearing through the call resets the caller's word
+        assert pps.get_stream_error(stream=sa, clear=True) == 1
+        torch.cuda.synchronize()
+        assert int(wa.item()) == 0
+    finally:
+        pps.set_stream_error_word(None, stream=sa)
+        pps.set_stream_error_word(None, stream=sb)
+    # without a registration the stream reports the device's word again
+    assert pps.get_stream_error(stream=sa) == 0
+
+
 def test_run_rejects_small_workspace(pps):
     wl = workloads.tiny_mixed()
     pk, pv, steps = to_device(wl)
