@@ -58,8 +58,14 @@ bool pool_ok(const pps_pool* p) {
          (p->head_dim == 64 || p->head_dim == 128);
 }
 
+// What run_impl enqueues: the task-table upload, the kernels, or both (the
+// step calls upload before the append, so that the attention kernels follow
+// the append kernel directly and may start while it finishes).
+enum RunPhase { kRunAll, kRunUpload, kRunKernels };
+
 pps_status run_impl(const pps_plan* plan, const void* q, const pps_pool* pool, void* out,
-                    void* workspace, size_t workspace_bytes, void* stream, void* const* events) {
+                    void* workspace, size_t workspace_bytes, void* stream, void* const* events,
+                    RunPhase phase = kRunAll) {
   if (!plan || !pool || (plan->num_tokens > 0 && (!q || !out))) return PPS_ERR_INVALID_ARGUMENT;
   if (!pool_ok(pool)) return pool && (pool->head_dim != 64 && pool->head_dim != 128) ?
                                   PPS_ERR_UNSUPPORTED : PPS_ERR_INVALID_ARGUMENT;
@@ -81,16 +87,21 @@ pps_status run_impl(const pps_plan* plan, const void* q, const pps_pool* pool, v
     return cudaSuccess;
   };
   if (plan->num_tokens == 0) {
-    for (int i = 0; i < 2 * PPS_NUM_KERNEL_CLASSES; ++i)
-      if (rec(i) != cudaSuccess) return PPS_ERR_CUDA;
+    if (phase != kRunUpload)
+      for (int i = 0; i < 2 * PPS_NUM_KERNEL_CLASSES; ++i)
+        if (rec(i) != cudaSuccess) return PPS_ERR_CUDA;
     return PPS_OK;
   }
   char* ws = (char*)workspace;
-  // Asynchronous when the plan's table is page-locked; the buffer is not
-  // reused before this upload completes, so the plan may be destroyed at once.
-  e = cudaMemcpyAsync(ws, plan->image.data, (size_t)plan->image_ints * 4, cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return PPS_ERR_CUDA;
-  if (pps::host_buf_mark_use(plan->image, stream) != 0) return PPS_ERR_CUDA;
+  if (phase != kRunKernels) {
+    // Asynchronous when the plan's table is page-locked; the buffer is not
+    // reused before this upload completes, so the plan may be destroyed at once.
+    e = cudaMemcpyAsync(ws, plan->image.data, (size_t)plan->image_ints * 4, cudaMemcpyHostToDevice,
+                        st);
+    if (e != cudaSuccess) return PPS_ERR_CUDA;
+    if (pps::host_buf_mark_use(plan->image, stream) != 0) return PPS_ERR_CUDA;
+    if (phase == kRunUpload) return PPS_OK;
+  }
   const int32_t* base = (const int32_t*)ws;
   const auto& L = plan->layout;
   pps::DeviceTables t;
@@ -408,12 +419,16 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
             cudaSuccess;
   ok = ok && pps::host_buf_mark_use(tb, stream) == 0;
   pps::host_buf_release(tb);
-  // append, attend, rows out
+  // task table up, append, attend, rows out: the attention kernels directly
+  // follow the append kernel
   const int32_t* d_tab = (const int32_t*)(sc + off_tab);
-  if (ok) st = pps_kv_append(pool, dk, dv, d_tab, d_tab + R + 1, d_tab + 2 * R + 1,
-                             d_tab + 3 * R + 2, R, T, stream);
+  if (ok)
+    st = run_impl(plan, dq, pool, dout, sc + off_ws, al(ws_bytes), stream, events, kRunUpload);
   if (ok && st == PPS_OK)
-    st = run_impl(plan, dq, pool, dout, sc + off_ws, al(ws_bytes), stream, events);
+    st = pps_kv_append(pool, dk, dv, d_tab, d_tab + R + 1, d_tab + 2 * R + 1, d_tab + 3 * R + 2,
+                       R, T, stream);
+  if (ok && st == PPS_OK)
+    st = run_impl(plan, dq, pool, dout, sc + off_ws, al(ws_bytes), stream, events, kRunKernels);
   if (ok && st == PPS_OK && rows_on_host && T > 0)
     ok = cudaMemcpyAsync(out, sc + off_out, q_bytes, cudaMemcpyDeviceToHost, stm) == cudaSuccess;
   pps_plan_destroy(plan);

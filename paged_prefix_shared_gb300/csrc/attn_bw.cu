@@ -536,6 +536,10 @@ __global__ void __launch_bounds__(kBw2Threads, 1) bw2_attention_kernel(
     sm100::fence_mbar_init();
   }
   __syncthreads();
+  // Set-up done: let the next kernel of the stream be scheduled, then wait
+  // for the one before (the append writes the pool rows this kernel reads).
+  sm100::grid_dep_launch();
+  sm100::grid_dep_wait();
   auto fail = [&]() {
     atomicCAS(err, 0, PPS_DEV_ERR_WAIT_TIMEOUT);
     abort_flag = 1;
@@ -699,13 +703,14 @@ int launch_v2(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const 
       cudaSuccess)
     return (int)e;
   const int64_t grid = std::min<int64_t>(n, (int64_t)sms * std::max(per_sm, 1));
-  kern<<<(unsigned)grid, kBw2Threads, smem, st>>>(
-      t.bw_tasks, (int32_t)n, t.rows, t.pages, (const __nv_bfloat16*)q,
+  e = pps::launch_dependent(
+      kern, (unsigned)grid, kBw2Threads, smem, st, (const pps::Task*)t.bw_tasks, (int32_t)n,
+      (const int32_t*)t.rows, (const int32_t*)t.pages, (const __nv_bfloat16*)q,
       (const __nv_bfloat16*)pool.k, (const __nv_bfloat16*)pool.v, (__nv_bfloat16*)out, t.o_part,
       t.lse_part, t.tree_mask, err, s.num_q_heads, s.num_kv_heads, s.group, s.page_size,
       s.sm_scale * kLog2e);
   pps::count_launch();
-  return (int)cudaGetLastError();
+  return (int)e;
 }
 
 template <int D, int R>

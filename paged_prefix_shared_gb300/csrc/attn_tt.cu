@@ -507,6 +507,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tm = tmem_base;
   const uint32_t tm_o = tm + 2 * kRows;
+  // Set-up done: let the next kernel of the stream be scheduled, then wait
+  // for the one before (the append writes the pool rows this kernel reads).
+  grid_dep_launch();
+  grid_dep_wait();
 
   auto fail = [&]() {
     atomicCAS(p.err, 0, PPS_DEV_ERR_WAIT_TIMEOUT);
@@ -809,10 +813,10 @@ int launch_tt(const Shape& s, const DeviceTables& t, const void* q, const pps_po
   TtParams prm{t.bw_tasks, t.tt_cta, t.rows, t.pages, (const __nv_bfloat16*)q,
                (__nv_bfloat16*)out, t.o_part, t.lse_part, err, t.tree_mask, s.num_q_heads,
                s.group, s.page_size, s.sm_scale * 1.4426950408889634f};
-  tt_attention_kernel<TREE>
-      <<<(unsigned)grid, kThreads, TtLayout::smem_alloc, (cudaStream_t)stream>>>(mk, mv, prm);
+  e = launch_dependent(tt_attention_kernel<TREE>, (unsigned)grid, kThreads, TtLayout::smem_alloc,
+                       (cudaStream_t)stream, mk, mv, prm);
   count_launch();
-  return (int)cudaGetLastError();
+  return (int)e;
 }
 }  // namespace
 

@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include "pps_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace {
 
@@ -25,6 +26,9 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     const int32_t* __restrict__ page_indices, int32_t num_requests, int32_t num_tokens,
     int32_t num_kv_heads, int32_t page_size, int32_t num_pages, int32_t* __restrict__ err) {
   constexpr int kVec = D * 2 / 16;                  // int4 per row (8 or 16)
+  // the attention kernels that follow may be scheduled now (they wait for
+  // this grid's writes before reading the pool)
+  sm100::grid_dep_launch();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int t = warp / num_kv_heads;

@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include "pps_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace {
 
@@ -24,6 +25,7 @@ __global__ void __launch_bounds__(256) merge_kernel(
     const float* __restrict__ lse_part, __nv_bfloat16* __restrict__ out, int32_t num_q_heads,
     int64_t num_rows) {
   constexpr int kPer = D / 32;
+  sm100::grid_dep_wait();        // the partials of the attention kernels before it
   const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= num_rows) return;
@@ -68,16 +70,13 @@ int launch_merge(const Shape& s, const DeviceTables& t, int64_t num_merge_tokens
   auto st = (cudaStream_t)stream;
   const int64_t rows = num_merge_tokens * s.num_q_heads;
   const unsigned blocks = (unsigned)((rows * 32 + 255) / 256);
-  if (s.head_dim == 128)
-    merge_kernel<128><<<blocks, 256, 0, st>>>(t.merge_tokens, t.merge_indptr, t.merge_pids,
-                                               t.o_part, t.lse_part, (__nv_bfloat16*)out,
-                                               s.num_q_heads, rows);
-  else
-    merge_kernel<64><<<blocks, 256, 0, st>>>(t.merge_tokens, t.merge_indptr, t.merge_pids,
-                                              t.o_part, t.lse_part, (__nv_bfloat16*)out,
-                                              s.num_q_heads, rows);
+  auto kern = s.head_dim == 128 ? merge_kernel<128> : merge_kernel<64>;
+  const cudaError_t e = launch_dependent(
+      kern, blocks, 256, 0, st, (const int32_t*)t.merge_tokens, (const int32_t*)t.merge_indptr,
+      (const int32_t*)t.merge_pids, (const float*)t.o_part, (const float*)t.lse_part,
+      (__nv_bfloat16*)out, s.num_q_heads, rows);
   count_launch();
-  return (int)cudaGetLastError();
+  return (int)e;
 }
 
 }  // namespace pps

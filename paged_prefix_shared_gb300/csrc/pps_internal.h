@@ -146,6 +146,28 @@ namespace pps {
 bool make_pool_map(CUtensorMap* map, const void* base, const pps_pool& pool);
 #endif
 
+#if defined(__CUDACC__)
+// Launches `kern` on `stream` with programmatic stream serialization: it may
+// start (and run its set-up) while the previous kernel of the stream is still
+// running, and must call grid_dep_wait before it reads anything that kernel
+// writes.  Without a kernel just before it in the stream it runs as usual.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+#endif
+
 // SM count of the current device, or 0 when no device is usable.
 int device_sm_count();
 

@@ -81,6 +81,20 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// ---- programmatic dependent launch -------------------------------------------------------
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it in the stream is still running.  grid_dep_wait blocks
+// until that kernel has completed and its memory writes are visible (a no-op
+// when the kernel was launched without the attribute); grid_dep_launch lets
+// the next such kernel be scheduled as soon as every CTA of this one has
+// called it (or exited).
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- TMA ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int c0, int c1, int c2,
                                             int c3, uint32_t bar) {
@@ -249,6 +263,36 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 // region whose base is 1024-byte aligned (rows of 128 bytes).
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) {
   return r * 128u + ((c ^ (r & 7u)) << 4);
+}
+
+// ---- packed fp32 pairs (sm_100 family) ------------------------------------------------
+// Two fp32 values in one 64-bit register pair: {lo, hi}.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+// {a, b} = {x, y} * s2 + c2, both lanes rounded to nearest (one instruction).
+__device__ __forceinline__ void ffma2(float& a, float& b, float x, float y, uint64_t s2,
+                                      uint64_t c2) {
+  asm("{\n .reg .b64 u, v;\n mov.b64 u, {%2, %3};\n fma.rn.f32x2 v, u, %4, %5;\n"
+      " mov.b64 {%0, %1}, v;\n}\n"
+      : "=f"(a), "=f"(b)
+      : "f"(x), "f"(y), "l"(s2), "l"(c2));
+}
+// {a, b} += {x, y} (one instruction).
+__device__ __forceinline__ void fadd2(float& a, float& b, float x, float y) {
+  asm("{\n .reg .b64 u, v;\n mov.b64 u, {%0, %1};\n mov.b64 v, {%2, %3};\n"
+      " add.rn.f32x2 u, u, v;\n mov.b64 {%0, %1}, u;\n}\n"
+      : "+f"(a), "+f"(b)
+      : "f"(x), "f"(y));
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
