@@ -26,9 +26,9 @@
 //              output row or the partial (o, lse).
 //   warp 8     TMA producer: K and V tiles of 128 positions (one box per page
 //              and 64-column block, issued by one lane each) into a 2-stage ring.
-//   warp 9     MMA issuer (one thread): S_X = Q_X K^T (both K-major in shared
-//              memory) and O_X += P_X V (P from TMEM, V MN-major in shared
-//              memory), in the order PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1).
+//   warp 9     MMA issuer: S_X = Q_X K^T (both K-major in shared memory) and
+//              O_X += P_X V (P from TMEM, V MN-major in shared memory), in the
+//              order PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1).
 // TMEM (512 columns): S_A | S_B | O_A | O_B.  Every mbarrier wait is bounded;
 // on timeout the kernel records PPS_DEV_ERR_WAIT_TIMEOUT, stops issuing work,
 // drains what it issued and still frees TMEM.
@@ -54,6 +54,7 @@ constexpr int kThreads = 320;
 constexpr int kStages = 2;
 constexpr int kTile = 128;                    // KV positions per tile = query rows per tile
 constexpr float kRescaleThreshold = 8.f;      // log2 units
+constexpr float kRescaleSum = 256.f;          // 2^kRescaleThreshold
 
 struct MmaParams {
   const pps::Task* tasks;
@@ -271,76 +272,111 @@ __global__ void __launch_bounds__(kThreads, 1)
             vis[1] &= window64(trev, 127 - (lim - t0));
           }
         }
-        // Two passes over S in 32-column chunks, each a rolled loop: the whole
-        // softmax stays a few hundred instructions of code, so the warps that
-        // share its schedulers (the MMA issuer above all) keep their own
-        // instructions in the instruction cache.
-        // Pass 1: the row maximum of the visible scores.
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kTile; c0 += 32) {
-          uint32_t rr[32];
-          tmem_ld32(tm_s + lane_off + c0, rr);
-          tmem_wait_ld();
-          if (full) {
+        // One pass against the running reference: P = exp2(s * scale - m_ref),
+        // two columns per packed multiply-add, S read in two 64-column halves.
+        // Valid unless a score exceeds the reference by the threshold, which
+        // makes some P exceed 2^8 and so the row's sum: then (rarely, once a
+        // row has seen a tile) the exact two-pass path below.  The full-tile
+        // code is kept short: warps sharing a scheduler with the softmax (the
+        // MMA issuer above all) must keep their own instructions cached.
+        float rs0 = 0.f, rs1 = 0.f, alpha = 1.f, m_use = m_ref;
+        bool exact = __any_sync(0xffffffffu, m_ref == -INFINITY);
+        if (!exact) {
+          const uint64_t sc2 = f32x2(p.qk_scale, p.qk_scale);
+          const uint64_t nm2 = f32x2(-m_ref, -m_ref);
+          uint32_t pk[kTile / 2];                  // P row, bf16 pairs, stored once verified
 #pragma unroll
-            for (int c = 0; c < 32; c += 2)
-              mx = max3f(mx, __uint_as_float(rr[c]), __uint_as_float(rr[c + 1]));
-          } else {
-            const uint32_t vb = (uint32_t)((c0 < 64 ? vis[0] : vis[1]) >> (c0 & 63));
+          for (int h = 0; h < kTile; h += 64) {
+            uint32_t ra[32], rb[32];
+            tmem_ld32(tm_s + lane_off + h, ra);
+            tmem_ld32(tm_s + lane_off + h + 32, rb);
+            tmem_wait_ld();
+            if (full) {
+#pragma unroll
+              for (int c = 0; c < 64; c += 2) {
+                float a, bb;
+                ffma2(a, bb, __uint_as_float(c < 32 ? ra[c] : rb[c - 32]),
+                      __uint_as_float(c < 32 ? ra[c + 1] : rb[c - 31]), sc2, nm2);
+                a = ex2(a);
+                bb = ex2(bb);
+                fadd2(rs0, rs1, a, bb);
+                pk[(h + c) / 2] = pack_bf16(a, bb);
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 64; c += 2) {
+                const float sa = ((vis[(h + c) >> 6] >> ((h + c) & 63)) & 1ull)
+                                     ? __uint_as_float(c < 32 ? ra[c] : rb[c - 32]) : -INFINITY;
+                const float sb = ((vis[(h + c + 1) >> 6] >> ((h + c + 1) & 63)) & 1ull)
+                                     ? __uint_as_float(c < 32 ? ra[c + 1] : rb[c - 31]) : -INFINITY;
+                float a, bb;
+                ffma2(a, bb, sa, sb, sc2, nm2);
+                a = ex2(a);
+                bb = ex2(bb);
+                fadd2(rs0, rs1, a, bb);
+                pk[(h + c) / 2] = pack_bf16(a, bb);
+              }
+            }
+          }
+          exact = __any_sync(0xffffffffu, rs0 + rs1 > kRescaleSum);
+          if (!exact) {
+            // P over S's first 64 columns (S has been read in full above)
+#pragma unroll
+            for (int c0 = 0; c0 < kTile / 2; c0 += 16) {
+              uint32_t w[16];
+#pragma unroll
+              for (int c = 0; c < 16; ++c) w[c] = pk[c0 + c];
+              tmem_st16(tm_s + lane_off + c0, w);
+            }
+          }
+        }
+        if (exact) {
+          // Pass 1: the row maximum of the visible scores (rolled: rare code).
+          float mx = -INFINITY;
+#pragma unroll 1
+          for (int c0 = 0; c0 < kTile; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tm_s + lane_off + c0, rr);
+            tmem_wait_ld();
+            const uint32_t vb =
+                full ? ~0u : (uint32_t)((c0 < 64 ? vis[0] : vis[1]) >> (c0 & 63));
 #pragma unroll
             for (int c = 0; c < 32; ++c)
               if ((vb >> c) & 1u) mx = fmaxf(mx, __uint_as_float(rr[c]));
           }
-        }
-        // The reference moves (and O is rescaled) only on a row's first tile
-        // or when a score exceeds it by the threshold.
-        const float mxs = (mx == -INFINITY) ? -INFINITY : mx * p.qk_scale;
-        float alpha = 1.f, m_use = m_ref;
-        if (mxs > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mxs != -INFINITY)) {
-          m_use = fmaxf(mxs, m_ref);
-          alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_use);
-        }
-        // O rescale: the PV of this tile's previous KV tile completed before
-        // this S was delivered (one in-order tcgen05 stream; the commit behind
-        // s_full covers both).
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t rr[32];
-            tmem_ld32(tm_o + lane_off + c0, rr);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
-            tmem_st32(tm_o + lane_off + c0, rr);
+          const float mxs = (mx == -INFINITY) ? -INFINITY : mx * p.qk_scale;
+          if (mxs > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mxs != -INFINITY)) {
+            m_use = fmaxf(mxs, m_ref);
+            alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_use);
           }
-        }
-        // Pass 2: P = exp2(s * scale - m), two columns per packed
-        // multiply-add; chunk c0 is stored over columns c0/2 .. c0/2 + 15,
-        // all of which this pass has already read.
-        const float msub = (m_use == -INFINITY) ? 0.f : m_use;
-        const uint64_t sc2 = f32x2(p.qk_scale, p.qk_scale);
-        const uint64_t nm2 = f32x2(-msub, -msub);
-        float rs0 = 0.f, rs1 = 0.f;
+          // O rescale: the PV of this tile's previous KV tile completed before
+          // this S was delivered (one in-order tcgen05 stream; the commit behind
+          // s_full covers both).
+          if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < kTile; c0 += 32) {
-          uint32_t rr[32];
-          tmem_ld32(tm_s + lane_off + c0, rr);
-          tmem_wait_ld();
-          uint32_t w[16];
-          if (full) {
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t ro[32];
+              tmem_ld32(tm_o + lane_off + c0, ro);
+              tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              float a, bb;
-              ffma2(a, bb, __uint_as_float(rr[c]), __uint_as_float(rr[c + 1]), sc2, nm2);
-              a = ex2(a);
-              bb = ex2(bb);
-              fadd2(rs0, rs1, a, bb);
-              w[c / 2] = pack_bf16(a, bb);
+              for (int c = 0; c < 32; ++c) ro[c] = __float_as_uint(__uint_as_float(ro[c]) * alpha);
+              tmem_st32(tm_o + lane_off + c0, ro);
             }
-          } else {
-            // masked columns -inf before the exponent (their raw S may be NaN)
-            const uint32_t vb = (uint32_t)((c0 < 64 ? vis[0] : vis[1]) >> (c0 & 63));
+          }
+          // Pass 2: P = exp2(s * scale - m); chunk c0 is stored over columns
+          // c0/2 .. c0/2 + 15, all of which this pass has already read.
+          const float msub = (m_use == -INFINITY) ? 0.f : m_use;
+          const uint64_t sc2 = f32x2(p.qk_scale, p.qk_scale);
+          const uint64_t nm2 = f32x2(-msub, -msub);
+          rs0 = rs1 = 0.f;
+#pragma unroll 1
+          for (int c0 = 0; c0 < kTile; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tm_s + lane_off + c0, rr);
+            tmem_wait_ld();
+            const uint32_t vb =
+                full ? ~0u : (uint32_t)((c0 < 64 ? vis[0] : vis[1]) >> (c0 & 63));
+            uint32_t w[16];
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
               const float sa = ((vb >> c) & 1u) ? __uint_as_float(rr[c]) : -INFINITY;
@@ -352,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               fadd2(rs0, rs1, a, bb);
               w[c / 2] = pack_bf16(a, bb);
             }
+            tmem_st16(tm_s + lane_off + c0 / 2, w);
           }
-          tmem_st16(tm_s + lane_off + c0 / 2, w);
         }
         const float rs = rs0 + rs1;
         m_ref = m_use;
@@ -457,31 +493,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------- MMA issuer
-    // One thread does all of it.  The tensor core queues only a few MMAs, so
-    // every cycle the issuer spends between two groups (a warp-wide sync, a
-    // descriptor rebuilt from scratch) can leave the pipe empty: waits are
-    // single-thread, descriptors are a base plus a constant per K step, and
-    // lanes 1-31 wait at the end.
-    if (lane == 0) {
-      constexpr uint32_t id_qk = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t id_pv = idesc_bf16(128, D, 0, 1);
-      // Descriptor fields: address >> 4 in the low 14 bits; every operand
-      // address used below stays under 256 KB, so adding (offset >> 4) to a
-      // base descriptor never carries out of that field.
-      const uint64_t qd0 = smem_desc(q_base, 16, 1024);
-      const uint64_t kd0 = smem_desc(k_base, 16, 1024);
-      const uint64_t vd0 = smem_desc(v_base, 16384, 1024);
-      int it = 0;                                   // KV tiles consumed (ring position)
-      int px[2] = {0, 0};                           // phases consumed on p_full[X]
-      int qn = 0;                                   // phases consumed on q_full
-      bool ok = true;
-      auto wait1 = [&](uint64_t* bar, uint32_t parity) {
-        if (mbar_wait(smem_u32(bar), parity) && !abort_flag) return true;
-        fail();
-        ok = false;
-        return false;
-      };
-      auto qk = [&](int X, int st) {
+    // The whole warp runs the loop (waits, the V-tail clear); lane 0 issues.
+    // Descriptors are a base plus a constant per K step: the tensor core
+    // queues only a few MMAs, so time between two groups can empty the pipe.
+    constexpr uint32_t id_qk = idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t id_pv = idesc_bf16(128, D, 0, 1);
+    // Descriptor fields: address >> 4 in the low 14 bits; every operand address
+    // used below stays under 256 KB, so adding (offset >> 4) to a base
+    // descriptor never carries out of that field.
+    const uint64_t qd0 = smem_desc(q_base, 16, 1024);
+    const uint64_t kd0 = smem_desc(k_base, 16, 1024);
+    const uint64_t vd0 = smem_desc(v_base, 16384, 1024);
+    int it = 0;                                     // KV tiles consumed (ring position)
+    int px[2] = {0, 0};                             // phases consumed on p_full[X]
+    int qn = 0;                                     // phases consumed on q_full
+    bool ok = true;
+    int t;
+    auto qk = [&](int X, int st) {
+      tc_fence_after();
+      if (lane == 0) {
         const uint64_t qd = qd0 + (uint64_t)((X * Lay::kTileBytes) >> 4);
         const uint64_t kd = kd0 + (uint64_t)((st * Lay::kTileBytes) >> 4);
 #pragma unroll
@@ -490,10 +520,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ss(tm + X * 128, qd + off, kd + off, id_qk, ks > 0);
         }
         umma_commit(smem_u32(&bars.s_full[X]));
-      };
-      // O_X += P_X V over the first `steps` 16-key steps of the tile (a
-      // partial tile's steps past its last key are skipped).
-      auto pv = [&](int X, int st, int steps, bool first, bool last_of_task) {
+      }
+      __syncwarp();
+    };
+    // O_X += P_X V over the first `steps` 16-key steps of the tile (a partial
+    // tile's steps past its last key are skipped).
+    auto pv = [&](int X, int st, int steps, bool first, bool last_of_task) {
+      tc_fence_after();
+      if (lane == 0) {
         const uint64_t vd = vd0 + (uint64_t)((st * Lay::kTileBytes) >> 4);
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks)
@@ -501,71 +535,77 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_ts(tm + 256 + X * D, tm + X * 128 + ks * 8, vd + (uint64_t)(ks * 128), id_pv,
                     (!first || ks > 0) ? 1u : 0u);
         if (last_of_task) umma_commit(smem_u32(&bars.o_done[X]));
-      };
-      // V rows past the task's last position inside its last 16-key step may
-      // hold anything (NaN included); P is 0 there, and 0 * NaN would poison
-      // O, so clear them (at most 15 rows).
-      auto clear_v_tail = [&](int st, int valid) {
-        uint8_t* vt = smem + Lay::v_off + st * Lay::kTileBytes;
-        const int end = (valid + 15) & ~15;
-        for (int r = valid; r < end; ++r)
-#pragma unroll
-          for (int kb = 0; kb < KB; ++kb)
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<int4*>(vt + kb * 16384 + r * 128 + c * 16) = make_int4(0, 0, 0, 0);
-        fence_proxy_async_smem();
-      };
-      int t;
-      for (int ti = 0; ok && (t = snake_task(ti, b, nctas)) < p.num_tasks; ++ti) {
-        const pps::Task task = p.tasks[t];
-        const int nt[2] = {tile_range(task, 0, G).n_tiles, tile_range(task, 1, G).n_tiles};
-        const int n_tiles = max(nt[0], nt[1]);
-        if (!wait1(&bars.q_full, qn & 1)) break;
-        ++qn;
-        // QK of the first KV tile for both query tiles
-        {
-          const int st = it % kStages;
-          if (!wait1(&bars.k_full[st], (it / kStages) & 1)) break;
-          tc_fence_after();
-          for (int X = 0; X < 2; ++X)
-            if (nt[X] > 0) qk(X, st);
-          umma_commit(smem_u32(&bars.k_empty[st]));   // K_0 used by both QKs
-        }
-        for (int j = 0; ok && j < n_tiles; ++j) {
-          const int st = (it + j) % kStages;
-          const int stn = (it + j + 1) % kStages;
-          const bool next = j + 1 < n_tiles;
-          const int valid = min(kTile, task.kv_end - (task.kv_begin + j * kTile));
-          const int steps = (valid + 15) / 16;
-          bool v_ready = false, k_ready = false;
-          for (int X = 0; X < 2; ++X) {
-            if (j >= nt[X]) continue;
-            if (!wait1(&bars.p_full[X], px[X] & 1)) break;
-            ++px[X];
-            if (!v_ready) {
-              if (!wait1(&bars.v_full[st], ((it + j) / kStages) & 1)) break;
-              if (valid & 15) clear_v_tail(st, valid);
-              v_ready = true;
-            }
-            tc_fence_after();
-            pv(X, st, steps, j == 0, j + 1 == nt[X]);
-            if (j + 1 < nt[X]) {
-              if (!k_ready) {
-                if (!wait1(&bars.k_full[stn], ((it + j + 1) / kStages) & 1)) break;
-                tc_fence_after();
-                k_ready = true;
-              }
-              qk(X, stn);
-            }
+      }
+      __syncwarp();
+    };
+    // V rows past the task's last position inside its last 16-key step may
+    // hold anything (NaN included); P is 0 there, and 0 * NaN would poison O,
+    // so clear them (at most 15 rows).
+    auto clear_v_tail = [&](int st, int valid) {
+      uint8_t* vt = smem + Lay::v_off + st * Lay::kTileBytes;
+      const int rows = ((valid + 15) & ~15) - valid;
+      for (int idx = lane; idx < rows * 8 * KB; idx += 32) {
+        const int kb = idx / (rows * 8);
+        const int rem = idx - kb * rows * 8;
+        *reinterpret_cast<int4*>(vt + kb * 16384 + (valid + rem / 8) * 128 + (rem % 8) * 16) =
+            make_int4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    };
+    for (int ti = 0; ok && (t = snake_task(ti, b, nctas)) < p.num_tasks; ++ti) {
+      const pps::Task task = p.tasks[t];
+      const int nt[2] = {tile_range(task, 0, G).n_tiles, tile_range(task, 1, G).n_tiles};
+      const int n_tiles = max(nt[0], nt[1]);
+      if (!warp_wait(&bars.q_full, qn & 1)) { fail(); ok = false; break; }
+      ++qn;
+      // QK of the first KV tile for both query tiles
+      {
+        const int st = it % kStages;
+        if (!warp_wait(&bars.k_full[st], (it / kStages) & 1)) { fail(); ok = false; break; }
+        for (int X = 0; X < 2; ++X)
+          if (nt[X] > 0) qk(X, st);
+        tc_fence_after();
+        if (lane == 0) umma_commit(smem_u32(&bars.k_empty[st]));   // K_0 used by both QKs
+        __syncwarp();
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = (it + j) % kStages;
+        const int stn = (it + j + 1) % kStages;
+        const bool next = j + 1 < n_tiles;
+        const int valid = min(kTile, task.kv_end - (task.kv_begin + j * kTile));
+        const int steps = (valid + 15) / 16;
+        bool v_ready = false, k_ready = false;
+        for (int X = 0; X < 2; ++X) {
+          if (j >= nt[X]) continue;
+          if (!warp_wait(&bars.p_full[X], px[X] & 1)) { fail(); ok = false; break; }
+          ++px[X];
+          if (!v_ready) {
+            if (!warp_wait(&bars.v_full[st], ((it + j) / kStages) & 1)) { fail(); ok = false; break; }
+            if (valid & 15) clear_v_tail(st, valid);
+            v_ready = true;
           }
-          if (!ok) break;
+          pv(X, st, steps, j == 0, j + 1 == nt[X]);
+          if (j + 1 < nt[X]) {
+            if (!k_ready) {
+              if (!warp_wait(&bars.k_full[stn], ((it + j + 1) / kStages) & 1)) { fail(); ok = false; break; }
+              k_ready = true;
+            }
+            qk(X, stn);
+          }
+        }
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
           umma_commit(smem_u32(&bars.v_empty[st]));                 // V_j no longer needed
           if (next) umma_commit(smem_u32(&bars.k_empty[stn]));      // K_{j+1} used by its QKs
         }
-        it += n_tiles;
+        __syncwarp();
       }
-      // Every MMA this thread issued has completed before TMEM is freed.
+      it += n_tiles;
+    }
+    // Every MMA this warp issued has completed before TMEM is freed.
+    if (lane == 0) {
       umma_commit(smem_u32(&bars.drain));
       if (!mbar_wait(smem_u32(&bars.drain), 0)) fail();
     }
