@@ -38,6 +38,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <mutex>
 
 #include "pps_internal.h"
@@ -272,15 +273,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             vis[1] &= window64(trev, 127 - (lim - t0));
           }
         }
-        // One pass against the running reference: P = exp2(s * scale - m_ref),
+        // Hot path (a tile with every column visible, after the row's first):
+        // one pass against the running reference, P = exp2(s * scale - m_ref),
         // two columns per packed multiply-add, S read in two 64-column halves.
         // Valid unless a score exceeds the reference by the threshold, which
-        // makes some P exceed 2^8 and so the row's sum: then (rarely, once a
-        // row has seen a tile) the exact two-pass path below.  The full-tile
-        // code is kept short: warps sharing a scheduler with the softmax (the
-        // MMA issuer above all) must keep their own instructions cached.
+        // makes some P exceed 2^8 and so the row's sum.  Everything else
+        // (masked tiles, first tiles, a reference that must move) takes the
+        // exact two-pass path below, written as rolled loops.  The hot path is
+        // one straight block of code and the rest stays out of its way: the
+        // instruction cache is shared by every warp of a scheduler, and the MMA
+        // issuer stalls whenever the softmax code pushes its instructions out.
         float rs0 = 0.f, rs1 = 0.f, alpha = 1.f, m_use = m_ref;
-        bool exact = __any_sync(0xffffffffu, m_ref == -INFINITY);
+        bool exact = !__all_sync(0xffffffffu, full && m_ref != -INFINITY);
         if (!exact) {
           const uint64_t sc2 = f32x2(p.qk_scale, p.qk_scale);
           const uint64_t nm2 = f32x2(-m_ref, -m_ref);
@@ -291,31 +295,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tm_s + lane_off + h, ra);
             tmem_ld32(tm_s + lane_off + h + 32, rb);
             tmem_wait_ld();
-            if (full) {
 #pragma unroll
-              for (int c = 0; c < 64; c += 2) {
-                float a, bb;
-                ffma2(a, bb, __uint_as_float(c < 32 ? ra[c] : rb[c - 32]),
-                      __uint_as_float(c < 32 ? ra[c + 1] : rb[c - 31]), sc2, nm2);
-                a = ex2(a);
-                bb = ex2(bb);
-                fadd2(rs0, rs1, a, bb);
-                pk[(h + c) / 2] = pack_bf16(a, bb);
-              }
-            } else {
-#pragma unroll
-              for (int c = 0; c < 64; c += 2) {
-                const float sa = ((vis[(h + c) >> 6] >> ((h + c) & 63)) & 1ull)
-                                     ? __uint_as_float(c < 32 ? ra[c] : rb[c - 32]) : -INFINITY;
-                const float sb = ((vis[(h + c + 1) >> 6] >> ((h + c + 1) & 63)) & 1ull)
-                                     ? __uint_as_float(c < 32 ? ra[c + 1] : rb[c - 31]) : -INFINITY;
-                float a, bb;
-                ffma2(a, bb, sa, sb, sc2, nm2);
-                a = ex2(a);
-                bb = ex2(bb);
-                fadd2(rs0, rs1, a, bb);
-                pk[(h + c) / 2] = pack_bf16(a, bb);
-              }
+            for (int c = 0; c < 64; c += 2) {
+              float a, bb;
+              ffma2(a, bb, __uint_as_float(c < 32 ? ra[c] : rb[c - 32]),
+                    __uint_as_float(c < 32 ? ra[c + 1] : rb[c - 31]), sc2, nm2);
+              a = ex2(a);
+              bb = ex2(bb);
+              fadd2(rs0, rs1, a, bb);
+              pk[(h + c) / 2] = pack_bf16(a, bb);
             }
           }
           exact = __any_sync(0xffffffffu, rs0 + rs1 > kRescaleSum);
@@ -494,49 +482,78 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------- MMA issuer
     // The whole warp runs the loop (waits, the V-tail clear); lane 0 issues.
-    // Descriptors are a base plus a constant per K step: the tensor core
-    // queues only a few MMAs, so time between two groups can empty the pipe.
+    // The tensor core queues only a few MMAs and this warp shares its
+    // scheduler with two busy softmax warps, so an MMA must cost the issuer
+    // as few instructions as possible: every descriptor (per query tile or
+    // ring stage and K step) is built once into registers, and each issue
+    // instance is compiled for a fixed tile and stage.
     constexpr uint32_t id_qk = idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t id_pv = idesc_bf16(128, D, 0, 1);
-    // Descriptor fields: address >> 4 in the low 14 bits; every operand address
-    // used below stays under 256 KB, so adding (offset >> 4) to a base
-    // descriptor never carries out of that field.
-    const uint64_t qd0 = smem_desc(q_base, 16, 1024);
-    const uint64_t kd0 = smem_desc(k_base, 16, 1024);
-    const uint64_t vd0 = smem_desc(v_base, 16384, 1024);
+    constexpr int KS = D / 16;                      // K steps of QK
+    constexpr int VS = kTile / 16;                  // K steps of PV
+    uint64_t qdsc[2][KS], kdsc[kStages][KS], vdsc[kStages][VS];
+    uint32_t tS[2], tO[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      tS[x] = tm + x * 128;                         // S_x (P_x over its first 64 columns)
+      tO[x] = tm + 256 + x * D;                     // O_x
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks)
+        qdsc[x][ks] = smem_desc(q_base + x * Lay::kTileBytes + (ks / 4) * 16384 + (ks % 4) * 32,
+                                16, 1024);
+    }
+#pragma unroll
+    for (int st = 0; st < kStages; ++st) {
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks)
+        kdsc[st][ks] = smem_desc(k_base + st * Lay::kTileBytes + (ks / 4) * 16384 + (ks % 4) * 32,
+                                 16, 1024);
+#pragma unroll
+      for (int ks = 0; ks < VS; ++ks)
+        vdsc[st][ks] = smem_desc(v_base + st * Lay::kTileBytes + ks * 2048, 16384, 1024);
+    }
     int it = 0;                                     // KV tiles consumed (ring position)
     int px[2] = {0, 0};                             // phases consumed on p_full[X]
     int qn = 0;                                     // phases consumed on q_full
     bool ok = true;
     int t;
-    auto qk = [&](int X, int st) {
+    using I0 = std::integral_constant<int, 0>;
+    using I1 = std::integral_constant<int, 1>;
+    auto qk_at = [&](auto xc, auto sc) {
+      constexpr int X = decltype(xc)::value, ST = decltype(sc)::value;
       tc_fence_after();
       if (lane == 0) {
-        const uint64_t qd = qd0 + (uint64_t)((X * Lay::kTileBytes) >> 4);
-        const uint64_t kd = kd0 + (uint64_t)((st * Lay::kTileBytes) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t off = (uint64_t)(((ks / 4) * 16384 + (ks % 4) * 32) >> 4);
-          umma_ss(tm + X * 128, qd + off, kd + off, id_qk, ks > 0);
-        }
+        for (int ks = 0; ks < KS; ++ks) umma_ss(tS[X], qdsc[X][ks], kdsc[ST][ks], id_qk, ks > 0);
         umma_commit(smem_u32(&bars.s_full[X]));
       }
       __syncwarp();
     };
     // O_X += P_X V over the first `steps` 16-key steps of the tile (a partial
     // tile's steps past its last key are skipped).
-    auto pv = [&](int X, int st, int steps, bool first, bool last_of_task) {
+    auto pv_at = [&](auto xc, auto sc, int steps, bool first, bool last_of_task) {
+      constexpr int X = decltype(xc)::value, ST = decltype(sc)::value;
       tc_fence_after();
       if (lane == 0) {
-        const uint64_t vd = vd0 + (uint64_t)((st * Lay::kTileBytes) >> 4);
+        if (steps == VS && !first) {
 #pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          if (ks < steps)
-            umma_ts(tm + 256 + X * D, tm + X * 128 + ks * 8, vd + (uint64_t)(ks * 128), id_pv,
-                    (!first || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < VS; ++ks) umma_ts(tO[X], tS[X] + ks * 8, vdsc[ST][ks], id_pv, 1u);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < VS; ++ks)
+            if (ks < steps)
+              umma_ts(tO[X], tS[X] + ks * 8, vdsc[ST][ks], id_pv, (!first || ks > 0) ? 1u : 0u);
+        }
         if (last_of_task) umma_commit(smem_u32(&bars.o_done[X]));
       }
       __syncwarp();
+    };
+    auto qk = [&](auto xc, int st) {
+      if (st == 0) qk_at(xc, I0{}); else qk_at(xc, I1{});
+    };
+    auto pv = [&](auto xc, int st, int steps, bool first, bool last_of_task) {
+      if (st == 0) pv_at(xc, I0{}, steps, first, last_of_task);
+      else pv_at(xc, I1{}, steps, first, last_of_task);
     };
     // V rows past the task's last position inside its last 16-key step may
     // hold anything (NaN included); P is 0 there, and 0 * NaN would poison O,
@@ -553,6 +570,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
     };
+    // one query tile's step of KV tile j: PV_X(j), then QK_X(j + 1)
+    auto tile_step = [&](auto xc, int j, const int (&nt)[2], int st, int stn, int valid,
+                         bool& v_ready, bool& k_ready) {
+      constexpr int X = decltype(xc)::value;
+      if (j >= nt[X]) return true;
+      if (!warp_wait(&bars.p_full[X], px[X] & 1)) return false;
+      ++px[X];
+      if (!v_ready) {
+        if (!warp_wait(&bars.v_full[st], ((it + j) / kStages) & 1)) return false;
+        if (valid & 15) clear_v_tail(st, valid);
+        v_ready = true;
+      }
+      pv(xc, st, (valid + 15) / 16, j == 0, j + 1 == nt[X]);
+      if (j + 1 < nt[X]) {
+        if (!k_ready) {
+          if (!warp_wait(&bars.k_full[stn], ((it + j + 1) / kStages) & 1)) return false;
+          k_ready = true;
+        }
+        qk(xc, stn);
+      }
+      return true;
+    };
     for (int ti = 0; ok && (t = snake_task(ti, b, nctas)) < p.num_tasks; ++ti) {
       const pps::Task task = p.tasks[t];
       const int nt[2] = {tile_range(task, 0, G).n_tiles, tile_range(task, 1, G).n_tiles};
@@ -563,8 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int st = it % kStages;
         if (!warp_wait(&bars.k_full[st], (it / kStages) & 1)) { fail(); ok = false; break; }
-        for (int X = 0; X < 2; ++X)
-          if (nt[X] > 0) qk(X, st);
+        if (nt[0] > 0) qk(I0{}, st);
+        if (nt[1] > 0) qk(I1{}, st);
         tc_fence_after();
         if (lane == 0) umma_commit(smem_u32(&bars.k_empty[st]));   // K_0 used by both QKs
         __syncwarp();
@@ -574,27 +613,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int stn = (it + j + 1) % kStages;
         const bool next = j + 1 < n_tiles;
         const int valid = min(kTile, task.kv_end - (task.kv_begin + j * kTile));
-        const int steps = (valid + 15) / 16;
         bool v_ready = false, k_ready = false;
-        for (int X = 0; X < 2; ++X) {
-          if (j >= nt[X]) continue;
-          if (!warp_wait(&bars.p_full[X], px[X] & 1)) { fail(); ok = false; break; }
-          ++px[X];
-          if (!v_ready) {
-            if (!warp_wait(&bars.v_full[st], ((it + j) / kStages) & 1)) { fail(); ok = false; break; }
-            if (valid & 15) clear_v_tail(st, valid);
-            v_ready = true;
-          }
-          pv(X, st, steps, j == 0, j + 1 == nt[X]);
-          if (j + 1 < nt[X]) {
-            if (!k_ready) {
-              if (!warp_wait(&bars.k_full[stn], ((it + j + 1) / kStages) & 1)) { fail(); ok = false; break; }
-              k_ready = true;
-            }
-            qk(X, stn);
-          }
+        if (!tile_step(I0{}, j, nt, st, stn, valid, v_ready, k_ready) ||
+            !tile_step(I1{}, j, nt, st, stn, valid, v_ready, k_ready)) {
+          fail();
+          ok = false;
+          break;
         }
-        if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
           umma_commit(smem_u32(&bars.v_empty[st]));                 // V_j no longer needed
