@@ -293,7 +293,8 @@ def measure_attention(name, args, dev, cpu_seconds):
         L = st.layout
         out = torch.empty_like(st.q)
         call = pps.StepCall(pk, pv, st.q, st.k_new, st.v_new, L.q_indptr, L.kv_len,
-                            L.page_indptr, L.page_indices, out, tree_parent=L.tree_parent)
+                            L.page_indptr, L.page_indices, out, tree_parent=L.tree_parent,
+                            flags=pps.PLAN_FUSED_APPEND if args.fused_append else 0)
         plan = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices, L.num_q_heads,
                              L.num_kv_heads, L.head_dim, L.page_size, L.num_pages,
                              tree_parent=L.tree_parent)
@@ -337,6 +338,16 @@ def measure_attention(name, args, dev, cpu_seconds):
     clocks = sampler.stop()
     ms = e0.elapsed_time(e1) / args.steps
     ms_max = max_over_ranks(ms, world, dev)
+    # host cost of one step's calls with the GPU idle (plan, uploads, launches):
+    # inside the loop above the host may also wait for a staging buffer
+    hc = []
+    for k in range(min(args.steps, 20)):
+        torch.cuda.synchronize()
+        c0 = time.perf_counter()
+        one_step()
+        hc.append(time.perf_counter() - c0)
+    host_call_ms = statistics.median(hc) * 1e3
+    torch.cuda.synchronize()
     # the same steps again with events around every kernel class (per-kernel
     # times; the events are kept out of the step-time loop above)
     for k in range(args.steps):
@@ -437,11 +448,14 @@ def measure_attention(name, args, dev, cpu_seconds):
                    "inputs larger than L2 (KV > 4x the 129 MB L2), no flush",
                    "parallelism": f"dp{world} (independent batch per GPU, no collective)",
                    "step_call": "pps_attn_step: one native call per step and chunk (tables "
-                                "uploaded, rows appended, batch planned on the host, attention)"},
+                                "uploaded, rows appended, batch planned on the host, attention)" +
+                                ("; append fused into the first attention kernel"
+                                 if args.fused_append else "")},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "ms_per_step": ms_e2e},
         "gpu_launches": launches,
         "host_ms_per_step": host_ms,
+        "host_ms_per_call_idle_gpu": host_call_ms,
         "kernel_ms_per_step": {"bandwidth": kern_ms[0], "tensor": kern_ms[1], "merge": kern_ms[2]},
         "roofline": roof,
         **({"cold_l2": {"kernel_ms_per_step": dict(zip(("bandwidth", "tensor", "merge"), cold_ms)),
@@ -1250,6 +1264,9 @@ def main():
     ap.add_argument("--flush-l2", default="auto", choices=["auto", "on", "off"],
                     help="re-time the kernels with an L2 flush before each step "
                          "(auto: when the unique KV is under 4x the L2 size)")
+    ap.add_argument("--fused-append", action="store_true",
+                    help="device-resident steps with the append inside the first attention "
+                         "kernel (PPS_PLAN_FUSED_APPEND) instead of its own launch")
     ap.add_argument("--requests", type=int, default=0,
                     help="decode_heavy / long_prefill: number of requests (default 256 / 4); "
                          "for small profiling captures")

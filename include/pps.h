@@ -366,6 +366,7 @@ typedef struct pps_plan_options {
 #define PPS_PLAN_NO_GROUPS 1      /* do not merge shared-prefix pages into group tasks            */
 #define PPS_PLAN_CUDA_CORES_ONLY 2 /* route every task to the CUDA-core kernel (no tcgen05 tiles) */
 #define PPS_PLAN_SMALL_ROWS_CUDA_CORES 4 /* tasks of few rows on the CUDA-core kernel, not the key-tile one */
+#define PPS_PLAN_FUSED_APPEND 8    /* step calls: the first attention kernel appends the rows (no separate launch) */
 
 typedef struct pps_plan pps_plan;
 
@@ -593,6 +594,18 @@ pps_status pps_plan_get_array(const pps_plan* plan, int32_t which, const int32_t
  *  q, k_new, v_new, out  device bf16 rows as for pps_kv_append / pps_attn_run.
  *  host tables, scratch, errors: as pps_attn_step_host (its scratch holds only
  *  the tables and the plan's workspace here).
+ *
+ * With opts->flags & PPS_PLAN_FUSED_APPEND (this call and pps_attn_step_host)
+ * the append is not a launch of its own: the step's first attention kernel
+ * copies the rows into their pages in its set-up, every CTA taking a share,
+ * and all its CTAs wait for one another on a counter in the scratch before
+ * any reads the pool (XY-Serve review, "Core claim": the step's batch through
+ * one meta-kernel; the copy is the pps_kv_append definition, bit exact).  That
+ * kernel is launched cooperatively, so all its CTAs are resident at once; the
+ * wait is bounded, and one that runs out is recorded as
+ * PPS_DEV_ERR_WAIT_TIMEOUT.  It applies when the first kernel is the key-tile
+ * kernel (head_dim 128 small-row tasks) or the tensor-core kernel alone; other
+ * plans append with a separate launch as without the flag.
  */
 pps_status pps_attn_step(const pps_pool* pool, const void* q, const void* k_new, const void* v_new,
                          const int32_t* h_q_indptr, const int32_t* h_kv_len,

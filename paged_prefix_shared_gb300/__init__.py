@@ -23,7 +23,7 @@ __all__ = [
     "PPSError", "Plan", "lib", "build", "kv_append", "attn_plan", "attn_run", "plan_destroy",
     "attn_step_host", "attn_step", "StepCall", "event_array",
     "get_device_error", "set_stream_error_word", "get_stream_error", "launch_count", "status_string", "version", "LIB_PATH",
-    "PLAN_NO_GROUPS", "PLAN_CUDA_CORES_ONLY", "PLAN_SMALL_ROWS_CUDA_CORES", "KERNEL_BANDWIDTH", "KERNEL_TENSOR", "KERNEL_MERGE",
+    "PLAN_NO_GROUPS", "PLAN_CUDA_CORES_ONLY", "PLAN_SMALL_ROWS_CUDA_CORES", "PLAN_FUSED_APPEND", "KERNEL_BANDWIDTH", "KERNEL_TENSOR", "KERNEL_MERGE",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpps.so")
@@ -31,6 +31,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpps.so")
 PLAN_NO_GROUPS = 1
 PLAN_CUDA_CORES_ONLY = 2
 PLAN_SMALL_ROWS_CUDA_CORES = 4
+PLAN_FUSED_APPEND = 8
 KERNEL_BANDWIDTH, KERNEL_TENSOR, KERNEL_MERGE = 0, 1, 2
 NUM_KERNEL_CLASSES = 3
 TASK_INTS = 8

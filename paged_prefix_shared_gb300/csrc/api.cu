@@ -63,9 +63,16 @@ bool pool_ok(const pps_pool* p) {
 // the append kernel directly and may start while it finishes).
 enum RunPhase { kRunAll, kRunUpload, kRunKernels };
 
+// Whether the plan's first attention kernel can carry the step's append
+// (the key-tile kernel, or the tensor-core kernel when it runs alone).
+bool can_fuse_append(const pps_plan* plan) {
+  return plan->num_tokens > 0 &&
+         ((plan->num_bw > 0 && plan->shape.small_tt) || (plan->num_bw == 0 && plan->num_mma > 0));
+}
+
 pps_status run_impl(const pps_plan* plan, const void* q, const pps_pool* pool, void* out,
                     void* workspace, size_t workspace_bytes, void* stream, void* const* events,
-                    RunPhase phase = kRunAll) {
+                    RunPhase phase = kRunAll, const pps::AppendArgs* app = nullptr) {
   if (!plan || !pool || (plan->num_tokens > 0 && (!q || !out))) return PPS_ERR_INVALID_ARGUMENT;
   if (!pool_ok(pool)) return pool && (pool->head_dim != 64 && pool->head_dim != 128) ?
                                   PPS_ERR_UNSUPPORTED : PPS_ERR_INVALID_ARGUMENT;
@@ -116,14 +123,17 @@ pps_status run_impl(const pps_plan* plan, const void* q, const pps_pool* pool, v
   t.tt_cta = plan->shape.tt_ctas > 0 ? base + L.tt_cta : nullptr;
   t.o_part = (float*)(ws + plan->table_bytes);
   t.lse_part = (float*)(ws + plan->table_bytes + plan->partial_o_bytes);
+  t.sync = (int32_t*)(ws) + L.sync;
 
   if (rec(2 * PPS_KERNEL_BANDWIDTH) != cudaSuccess) return PPS_ERR_CUDA;
-  if (pps::launch_bw_attention(s, t, plan->num_bw, q, *pool, out, err, stream))
+  if (pps::launch_bw_attention(s, t, plan->num_bw, q, *pool, out, err, stream,
+                               plan->num_bw > 0 ? app : nullptr))
     return PPS_ERR_CUDA;
   if (rec(2 * PPS_KERNEL_BANDWIDTH + 1) != cudaSuccess) return PPS_ERR_CUDA;
   if (rec(2 * PPS_KERNEL_TENSOR) != cudaSuccess) return PPS_ERR_CUDA;
   if (plan->num_mma &&
-      pps::launch_mma_attention(s, t, plan->num_mma, q, *pool, out, err, stream))
+      pps::launch_mma_attention(s, t, plan->num_mma, q, *pool, out, err, stream,
+                                plan->num_bw == 0 ? app : nullptr))
     return PPS_ERR_CUDA;
   if (rec(2 * PPS_KERNEL_TENSOR + 1) != cudaSuccess) return PPS_ERR_CUDA;
   if (rec(2 * PPS_KERNEL_MERGE) != cudaSuccess) return PPS_ERR_CUDA;
@@ -420,15 +430,20 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
   ok = ok && pps::host_buf_mark_use(tb, stream) == 0;
   pps::host_buf_release(tb);
   // task table up, append, attend, rows out: the attention kernels directly
-  // follow the append kernel
+  // follow the append kernel, or (PPS_PLAN_FUSED_APPEND) the first of them
+  // appends the rows itself
   const int32_t* d_tab = (const int32_t*)(sc + off_tab);
+  const bool fused = opts && (opts->flags & PPS_PLAN_FUSED_APPEND) && can_fuse_append(plan);
+  const pps::AppendArgs app{dk, dv, d_tab, d_tab + R + 1, d_tab + 2 * R + 1, d_tab + 3 * R + 2,
+                            R, T};
   if (ok)
     st = run_impl(plan, dq, pool, dout, sc + off_ws, al(ws_bytes), stream, events, kRunUpload);
-  if (ok && st == PPS_OK)
+  if (ok && st == PPS_OK && !fused)
     st = pps_kv_append(pool, dk, dv, d_tab, d_tab + R + 1, d_tab + 2 * R + 1, d_tab + 3 * R + 2,
                        R, T, stream);
   if (ok && st == PPS_OK)
-    st = run_impl(plan, dq, pool, dout, sc + off_ws, al(ws_bytes), stream, events, kRunKernels);
+    st = run_impl(plan, dq, pool, dout, sc + off_ws, al(ws_bytes), stream, events, kRunKernels,
+                  fused ? &app : nullptr);
   if (ok && st == PPS_OK && rows_on_host && T > 0)
     ok = cudaMemcpyAsync(out, sc + off_out, q_bytes, cudaMemcpyDeviceToHost, stm) == cudaSuccess;
   pps_plan_destroy(plan);

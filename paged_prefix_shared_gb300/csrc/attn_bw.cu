@@ -737,9 +737,11 @@ int launch_t(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const v
 namespace pps {
 
 int launch_bw_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
-                        const pps_pool& pool, void* out, int32_t* err, void* stream) {
+                        const pps_pool& pool, void* out, int32_t* err, void* stream,
+                        const AppendArgs* app) {
   if (num_tasks == 0) return cudaSuccess;
-  if (s.small_tt) return launch_tt_attention(s, t, num_tasks, q, pool, out, err, stream);
+  if (s.small_tt) return launch_tt_attention(s, t, num_tasks, q, pool, out, err, stream, app);
+  if (app) return (int)cudaErrorInvalidValue;        // the CUDA-core kernels do not append
   auto st = (cudaStream_t)stream;
   // The planner caps rows per task at kBwMaxRows; pick the smallest instance.
   // Up to 8 rows: the pipelined v2 kernel; 9..16 rows (CUDA-core-only plans): v1.

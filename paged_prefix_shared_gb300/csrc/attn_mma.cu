@@ -43,6 +43,7 @@
 
 #include "pps_internal.h"
 #include "sm100_ptx.cuh"
+#include "append_dev.cuh"
 
 namespace {
 
@@ -72,6 +73,13 @@ struct MmaParams {
   int32_t G;
   int32_t page_size;
   float qk_scale;                             // sm_scale * log2(e)
+  // the step's rows to append first (num_tokens 0: none), into the pool
+  pps::AppendArgs append;
+  void* pool_k;
+  void* pool_v;
+  int32_t num_kv_heads;
+  int32_t num_pages;
+  int32_t* sync;
 };
 
 struct Bars {
@@ -194,6 +202,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // for the one before (the append writes the pool rows this kernel reads).
   grid_dep_launch();
   grid_dep_wait();
+  // The step's new K/V rows, when this launch carries the append: every CTA
+  // copies its share, then all wait for one another before any task reads
+  // the pool.
+  if (p.append.num_tokens > 0) {
+    pps_dev::append_rows<D>(p.append, reinterpret_cast<int4*>(p.pool_k),
+                            reinterpret_cast<int4*>(p.pool_v), p.num_kv_heads, p.page_size,
+                            p.num_pages, p.err, warp, lane, kThreads / 32);
+    pps_dev::grid_wait(p.sync, p.err);
+  }
 
   auto fail = [&]() {
     atomicCAS(p.err, 0, PPS_DEV_ERR_WAIT_TIMEOUT);
@@ -647,7 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 int launch_t(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const void* q,
-             const pps_pool& pool, void* out, int32_t* err, cudaStream_t st) {
+             const pps_pool& pool, void* out, int32_t* err, cudaStream_t st,
+             const pps::AppendArgs* app) {
   CUtensorMap mk, mv;
   if (!pps::make_pool_map(&mk, pool.k, pool) || !pps::make_pool_map(&mv, pool.v, pool))
     return (int)cudaErrorInvalidValue;
@@ -662,8 +680,14 @@ int launch_t(const pps::Shape& s, const pps::DeviceTables& t, int64_t n, const v
   const int64_t grid = std::min<int64_t>(n, sms);
   MmaParams prm{t.mma_tasks, (int32_t)n, t.rows, t.pages, (const __nv_bfloat16*)q,
                 (__nv_bfloat16*)out, t.o_part, t.lse_part, err, t.tree_mask, s.num_q_heads, s.group,
-                s.page_size, s.sm_scale * 1.4426950408889634f};
-  e = pps::launch_dependent(kern, (unsigned)grid, kThreads, Layout<D>::smem_alloc, st, mk, mv, prm);
+                s.page_size, s.sm_scale * 1.4426950408889634f,
+                app ? *app : pps::AppendArgs{}, pool.k, pool.v, pool.num_kv_heads,
+                pool.num_pages, t.sync};
+  // with the append every CTA must be resident at once (it waits for all)
+  e = app ? pps::launch_cooperative(kern, (unsigned)grid, kThreads, Layout<D>::smem_alloc, st, mk,
+                                    mv, prm)
+          : pps::launch_dependent(kern, (unsigned)grid, kThreads, Layout<D>::smem_alloc, st, mk, mv,
+                                  prm);
   pps::count_launch();
   return (int)e;
 }
@@ -733,11 +757,12 @@ bool make_pool_map(CUtensorMap* map, const void* base, const pps_pool& pool) {
 bool mma_path_available() { return true; }
 
 int launch_mma_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
-                         const pps_pool& pool, void* out, int32_t* err, void* stream) {
+                         const pps_pool& pool, void* out, int32_t* err, void* stream,
+                         const AppendArgs* app) {
   if (num_tasks == 0) return cudaSuccess;
   auto st = (cudaStream_t)stream;
-  if (s.head_dim == 128) return launch_t<128>(s, t, num_tasks, q, pool, out, err, st);
-  return launch_t<64>(s, t, num_tasks, q, pool, out, err, st);
+  if (s.head_dim == 128) return launch_t<128>(s, t, num_tasks, q, pool, out, err, st, app);
+  return launch_t<64>(s, t, num_tasks, q, pool, out, err, st, app);
 }
 
 }  // namespace pps

@@ -50,6 +50,7 @@
 
 #include "pps_internal.h"
 #include "sm100_ptx.cuh"
+#include "append_dev.cuh"
 
 namespace {
 
@@ -82,6 +83,13 @@ struct TtParams {
   int32_t G;
   int32_t page_size;
   float qk_scale;                            // sm_scale * log2(e)
+  // the step's rows to append first (num_tokens 0: none), into the pool
+  pps::AppendArgs append;
+  void* pool_k;
+  void* pool_v;
+  int32_t num_kv_heads;
+  int32_t num_pages;
+  int32_t* sync;
 };
 
 struct TtBars {
@@ -511,6 +519,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // for the one before (the append writes the pool rows this kernel reads).
   grid_dep_launch();
   grid_dep_wait();
+  // The step's new K/V rows, when this launch carries the append: every CTA
+  // copies its share, then all wait for one another before any task reads
+  // the pool.
+  if (p.append.num_tokens > 0) {
+    pps_dev::append_rows<D>(p.append, reinterpret_cast<int4*>(p.pool_k),
+                            reinterpret_cast<int4*>(p.pool_v), p.num_kv_heads, p.page_size,
+                            p.num_pages, p.err, warp, lane, kThreads / 32);
+    pps_dev::grid_wait(p.sync, p.err);
+  }
 
   auto fail = [&]() {
     atomicCAS(p.err, 0, PPS_DEV_ERR_WAIT_TIMEOUT);
@@ -791,7 +808,7 @@ namespace pps {
 namespace {
 template <bool TREE>
 int launch_tt(const Shape& s, const DeviceTables& t, const void* q, const pps_pool& pool,
-              void* out, int32_t* err, void* stream) {
+              void* out, int32_t* err, void* stream, const AppendArgs* app) {
   CUtensorMap mk, mv;
   if (!make_pool_map(&mk, pool.k, pool) || !make_pool_map(&mv, pool.v, pool))
     return (int)cudaErrorInvalidValue;
@@ -812,20 +829,26 @@ int launch_tt(const Shape& s, const DeviceTables& t, const void* q, const pps_po
   if (grid <= 0 || !t.tt_cta) return (int)cudaErrorInvalidValue;
   TtParams prm{t.bw_tasks, t.tt_cta, t.rows, t.pages, (const __nv_bfloat16*)q,
                (__nv_bfloat16*)out, t.o_part, t.lse_part, err, t.tree_mask, s.num_q_heads,
-               s.group, s.page_size, s.sm_scale * 1.4426950408889634f};
-  e = launch_dependent(tt_attention_kernel<TREE>, (unsigned)grid, kThreads, TtLayout::smem_alloc,
-                       (cudaStream_t)stream, mk, mv, prm);
+               s.group, s.page_size, s.sm_scale * 1.4426950408889634f,
+               app ? *app : AppendArgs{}, pool.k, pool.v, pool.num_kv_heads, pool.num_pages,
+               t.sync};
+  // with the append every CTA must be resident at once (it waits for all)
+  e = app ? launch_cooperative(tt_attention_kernel<TREE>, (unsigned)grid, kThreads,
+                               TtLayout::smem_alloc, (cudaStream_t)stream, mk, mv, prm)
+          : launch_dependent(tt_attention_kernel<TREE>, (unsigned)grid, kThreads,
+                             TtLayout::smem_alloc, (cudaStream_t)stream, mk, mv, prm);
   count_launch();
   return (int)e;
 }
 }  // namespace
 
 int launch_tt_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
-                        const pps_pool& pool, void* out, int32_t* err, void* stream) {
+                        const pps_pool& pool, void* out, int32_t* err, void* stream,
+                        const AppendArgs* app) {
   if (num_tasks == 0) return cudaSuccess;
   if (s.head_dim != D) return (int)cudaErrorInvalidValue;
-  return t.tree_mask ? launch_tt<true>(s, t, q, pool, out, err, stream)
-                     : launch_tt<false>(s, t, q, pool, out, err, stream);
+  return t.tree_mask ? launch_tt<true>(s, t, q, pool, out, err, stream, app)
+                     : launch_tt<false>(s, t, q, pool, out, err, stream, app);
 }
 
 }  // namespace pps

@@ -590,6 +590,7 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
     L.merge_pids = off;    off += al((int64_t)m_pid.size());
     L.tree_mask = off;     off += plan->has_tree ? al(2LL * T) : 0;
     L.tt_cta = off;        off += al((int64_t)tt_cta.size());
+    L.sync = off;          off += 64;             // zeros: a counter for grid-wide waits
     L.total_ints = off;
     plan->layout = L;
     plan->image_ints = std::max<int64_t>(off, 64);
@@ -617,7 +618,8 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
     put(L.merge_indptr, m_ptr.data(), (int64_t)m_ptr.size(), L.merge_pids);
     put(L.merge_pids, m_pid.data(), (int64_t)m_pid.size(), L.tree_mask);
     put(L.tree_mask, tmask.data(), plan->has_tree ? 2LL * T : 0, L.tt_cta);
-    put(L.tt_cta, tt_cta.data(), (int64_t)tt_cta.size(), plan->image_ints);
+    put(L.tt_cta, tt_cta.data(), (int64_t)tt_cta.size(), L.sync);
+    put(L.sync, nullptr, 0, plan->image_ints);
 
     plan->num_bw = (int64_t)bw.size();
     plan->num_mma = (int64_t)mm.size();

@@ -35,6 +35,7 @@ struct TableLayout {
   int64_t merge_tokens = 0, merge_indptr = 0, merge_pids = 0;
   int64_t tree_mask = 0;   // 2 ints per new token, only when the plan has a draft tree
   int64_t tt_cta = 0;      // key-tile plans: per-CTA task ranges, CTAs + 1 offsets
+  int64_t sync = 0;        // 64 zero ints: the counter of a grid-wide wait
   int64_t total_ints = 0;
 };
 
@@ -54,6 +55,21 @@ struct DeviceTables {
   const int32_t* tt_cta;
   float* o_part;     // [num_partials, Hq, d]
   float* lse_part;   // [num_partials, Hq] (log2 domain)
+  int32_t* sync;     // zero at the start of every run (uploaded with the table)
+};
+
+// The step's new K/V rows, appended by the first attention kernel of the
+// step itself (the append fused into the attention launch): rows as for
+// pps_kv_append, tables on the device.
+struct AppendArgs {
+  const void* k_new;
+  const void* v_new;
+  const int32_t* q_indptr;
+  const int32_t* cached_len;
+  const int32_t* page_indptr;
+  const int32_t* page_indices;
+  int32_t num_requests;
+  int32_t num_tokens;
 };
 
 struct Shape {
@@ -122,15 +138,21 @@ int launch_copy_slots(const pps_pool& pool, const int32_t* src_pages, const int3
 int launch_gemm_bf16(const void* a, const void* w, void* c, int32_t M, int32_t N, int32_t K,
                      int32_t* err, void* stream);
 
+// `app`: as launch_mma_attention; only the key-tile kernel (s.small_tt) takes it.
 int launch_bw_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
-                        const pps_pool& pool, void* out, int32_t* err, void* stream);
+                        const pps_pool& pool, void* out, int32_t* err, void* stream,
+                        const AppendArgs* app = nullptr);
 
+// `app` (may be null): the step's rows to append before any task reads the
+// pool (one grid-wide wait; the kernel is then launched cooperatively).
 int launch_mma_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
-                         const pps_pool& pool, void* out, int32_t* err, void* stream);
+                         const pps_pool& pool, void* out, int32_t* err, void* stream,
+                         const AppendArgs* app = nullptr);
 
 // Small-row tasks (the bandwidth task list) on the key-tile tensor kernel.
 int launch_tt_attention(const Shape& s, const DeviceTables& t, int64_t num_tasks, const void* q,
-                        const pps_pool& pool, void* out, int32_t* err, void* stream);
+                        const pps_pool& pool, void* out, int32_t* err, void* stream,
+                        const AppendArgs* app = nullptr);
 
 int launch_merge(const Shape& s, const DeviceTables& t, int64_t num_merge_tokens, void* out,
                  void* stream);
@@ -162,6 +184,24 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsigned blo
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// Launches `kern` cooperatively: every CTA is resident at once (or the launch
+// fails), as a grid-wide wait inside the kernel requires.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cooperative(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                               cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, args...);
