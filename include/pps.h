@@ -635,9 +635,17 @@ pps_status pps_attn_step(const pps_pool* pool, const void* q, const void* k_new,
  *                        stream reaches the end of this step.
  *  d_scratch             device, 256-byte aligned, scratch_bytes long; the size
  *                        it needs is written to *out_scratch_bytes (may be NULL).
- * Everything is enqueued on `stream`; page-locked host rows make the copies
- * asynchronous, and every host buffer must stay valid until the stream has
- * passed this step.  The host tables are read before the call returns.
+ *                        It holds two slots of input rows taken in turn, the
+ *                        output rows, the tables and the plan's workspace; it
+ *                        must not be used by other work while steps are in flight.
+ * The copies of the input rows run on a stream of the library's own (one per
+ * device), so that the rows of the next call travel while this call's
+ * kernels run; the step's kernels on `stream` wait for them, and a slot is
+ * written again only once the kernels that read it have finished.  The rest
+ * (table upload, append, attention, the output copy) is enqueued on `stream`.
+ * Page-locked host rows make the copies asynchronous, and every host buffer
+ * must stay valid until the stream has passed this step.  The host tables are
+ * read before the call returns.
  * The row copies start before the host plans, so on PPS_ERR_WORKSPACE (scratch
  * missing, misaligned or smaller than needed) or a planning error only the
  * scratch may have been written; the pool is untouched.

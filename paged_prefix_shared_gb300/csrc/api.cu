@@ -338,6 +338,36 @@ pps_status pps_attn_run_events(const pps_plan* plan, const void* q, const pps_po
 
 namespace {
 
+// The host-to-device row copies of pps_attn_step_host run on a stream of the
+// library's own, into one of two row slots of the scratch taken in turn, so
+// the next step's rows travel while this step's kernels run.  A slot is
+// written again only after the kernels that read it (event `free`), and the
+// step's kernels wait for their slot's copies (event `in`).
+struct RowCopier {
+  cudaStream_t copy = nullptr;
+  cudaEvent_t in[2] = {nullptr, nullptr};
+  cudaEvent_t free[2] = {nullptr, nullptr};
+  bool used[2] = {false, false};
+  uint64_t calls = 0;
+};
+std::mutex g_copier_mu;
+RowCopier g_copier[kMaxDevices];
+
+// The current device's copier (created on first use), or null.
+RowCopier* row_copier() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  RowCopier& c = g_copier[dev];
+  if (!c.copy) {
+    if (cudaStreamCreateWithFlags(&c.copy, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    for (int i = 0; i < 2; ++i)
+      if (cudaEventCreateWithFlags(&c.in[i], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&c.free[i], cudaEventDisableTiming) != cudaSuccess)
+        return nullptr;
+  }
+  return &c;
+}
+
 // One step: rows on the host (copied into scratch first) or already on the
 // device; host tables uploaded through a page-locked staging buffer; append,
 // plan, attention; rows out (to the host, or left in the caller's device
@@ -366,9 +396,11 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
   const int64_t nnz = R > 0 ? h_page_indptr[R] : 0;
   if (nnz < 0 || (nnz > 0 && !h_page_indices)) return PPS_ERR_INVALID_ARGUMENT;
   const size_t tab_ints = (size_t)(R + 1) + R + (R + 1) + (size_t)nnz;
-  const size_t rows = rows_on_host ? al(q_bytes) * 2 + al(kv_bytes) * 2 : 0;
-  const size_t off_q = 0, off_k = al(q_bytes), off_v = off_k + al(kv_bytes),
-               off_out = off_v + al(kv_bytes), off_tab = rows, off_ws = off_tab + al(tab_ints * 4);
+  // host rows: two input slots (q, k, v each) and one output area
+  const size_t slot_bytes = al(q_bytes) + 2 * al(kv_bytes);
+  const size_t rows = rows_on_host ? 2 * slot_bytes + al(q_bytes) : 0;
+  const size_t off_k = al(q_bytes), off_v = off_k + al(kv_bytes), off_out = 2 * slot_bytes,
+               off_tab = rows, off_ws = off_tab + al(tab_ints * 4);
   auto plan_for = [&](pps_plan** pl, size_t* ws) {
     return pps_attn_plan_tree(h_q_indptr, h_kv_len, h_page_indptr, h_page_indices, h_tree_parent,
                               R, num_q_heads, pool->num_kv_heads, pool->head_dim, pool->page_size,
@@ -390,16 +422,29 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
   const void* dk = k_new;
   const void* dv = v_new;
   void* dout = out;
+  RowCopier* rc = nullptr;
+  int slot = 0;
   if (rows_on_host) {
-    // rows in (only the scratch is written until the plan is known)
-    if (T > 0 &&
-        (cudaMemcpyAsync(sc + off_q, q, q_bytes, cudaMemcpyHostToDevice, stm) != cudaSuccess ||
-         cudaMemcpyAsync(sc + off_k, k_new, kv_bytes, cudaMemcpyHostToDevice, stm) != cudaSuccess ||
-         cudaMemcpyAsync(sc + off_v, v_new, kv_bytes, cudaMemcpyHostToDevice, stm) != cudaSuccess))
+    // rows in, on the copier's stream into the next slot (only the scratch is
+    // written until the plan is known); the step's kernels wait for them
+    std::lock_guard<std::mutex> lk(g_copier_mu);
+    rc = row_copier();
+    if (!rc) return PPS_ERR_CUDA;
+    slot = (int)(rc->calls++ & 1);
+    char* sl = sc + slot * slot_bytes;
+    if (rc->used[slot] && cudaStreamWaitEvent(rc->copy, rc->free[slot], 0) != cudaSuccess)
       return PPS_ERR_CUDA;
-    dq = sc + off_q;
-    dk = sc + off_k;
-    dv = sc + off_v;
+    if (T > 0 &&
+        (cudaMemcpyAsync(sl, q, q_bytes, cudaMemcpyHostToDevice, rc->copy) != cudaSuccess ||
+         cudaMemcpyAsync(sl + off_k, k_new, kv_bytes, cudaMemcpyHostToDevice, rc->copy) != cudaSuccess ||
+         cudaMemcpyAsync(sl + off_v, v_new, kv_bytes, cudaMemcpyHostToDevice, rc->copy) != cudaSuccess))
+      return PPS_ERR_CUDA;
+    if (cudaEventRecord(rc->in[slot], rc->copy) != cudaSuccess ||
+        cudaStreamWaitEvent(stm, rc->in[slot], 0) != cudaSuccess)
+      return PPS_ERR_CUDA;
+    dq = sl;
+    dk = sl + off_k;
+    dv = sl + off_v;
     dout = sc + off_out;
   }
   // the plan, from the host tables (checks them all)
@@ -444,6 +489,12 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
   if (ok && st == PPS_OK)
     st = run_impl(plan, dq, pool, dout, sc + off_ws, al(ws_bytes), stream, events, kRunKernels,
                   fused ? &app : nullptr);
+  if (rows_on_host) {
+    // the slot may be written again once this step's kernels have read it
+    std::lock_guard<std::mutex> lk(g_copier_mu);
+    if (cudaEventRecord(rc->free[slot], stm) == cudaSuccess) rc->used[slot] = true;
+    else ok = false;
+  }
   if (ok && st == PPS_OK && rows_on_host && T > 0)
     ok = cudaMemcpyAsync(out, sc + off_out, q_bytes, cudaMemcpyDeviceToHost, stm) == cudaSuccess;
   pps_plan_destroy(plan);
