@@ -632,17 +632,27 @@ pps_status pps_attn_step(const pps_pool* pool, const void* q, const void* k_new,
  *                        NULL); each request's new tokens are its last q_len
  *                        positions (cached_len = kv_len - q_len).
  *  h_out                 host bf16 [T, num_q_heads, head_dim], written when the
- *                        stream reaches the end of this step.
+ *                        stream reaches the end of this step.  When h_out is
+ *                        page-locked memory mapped for the device
+ *                        (cudaHostAlloc / cudaHostRegister) and tensor-core
+ *                        tiles write at most half of the rows, the step's
+ *                        kernels write it directly and no copy follows them;
+ *                        otherwise the rows come back by a copy on `stream`
+ *                        after the kernels.
  *  d_scratch             device, 256-byte aligned, scratch_bytes long; the size
  *                        it needs is written to *out_scratch_bytes (may be NULL).
- *                        It holds two slots of input rows taken in turn, the
- *                        output rows, the tables and the plan's workspace; it
- *                        must not be used by other work while steps are in flight.
+ *                        It holds two slots of input rows taken in turn, room
+ *                        for the output rows, the tables and the plan's workspace; it
+ *                        must not be used by other work while steps are in
+ *                        flight, and steps that share it are issued on one
+ *                        stream (steps on other streams take scratch of their own).
  * The copies of the input rows run on a stream of the library's own (one per
- * device), so that the rows of the next call travel while this call's
- * kernels run; the step's kernels on `stream` wait for them, and a slot is
- * written again only once the kernels that read it have finished.  The rest
- * (table upload, append, attention, the output copy) is enqueued on `stream`.
+ * scratch buffer, up to 32 kept; the least recently used one is retired,
+ * after the work it fences has finished, when a 33rd scratch comes), so that
+ * the rows of the next call travel while this call's kernels run; the step's
+ * kernels on `stream` wait for them, and a slot is written again only once
+ * the kernels that read it have finished.  The rest (table upload, append,
+ * attention, any output copy) is enqueued on `stream`.
  * Page-locked host rows make the copies asynchronous, and every host buffer
  * must stay valid until the stream has passed this step.  The host tables are
  * read before the call returns.

@@ -342,30 +342,77 @@ namespace {
 // library's own, into one of two row slots of the scratch taken in turn, so
 // the next step's rows travel while this step's kernels run.  A slot is
 // written again only after the kernels that read it (event `free`), and the
-// step's kernels wait for their slot's copies (event `in`).
+// step's kernels wait for their slot's copies (event `in`).  The state is kept
+// per scratch buffer (device, address), so steps on several streams, each with
+// its own scratch, never wait on one another's events.
 struct RowCopier {
+  int dev = -1;
+  const void* scratch = nullptr;
+  uint64_t last_use = 0;
   cudaStream_t copy = nullptr;
   cudaEvent_t in[2] = {nullptr, nullptr};
   cudaEvent_t free[2] = {nullptr, nullptr};
   bool used[2] = {false, false};
   uint64_t calls = 0;
 };
+constexpr int kMaxCopiers = 32;
 std::mutex g_copier_mu;
-RowCopier g_copier[kMaxDevices];
+RowCopier g_copier[kMaxCopiers];
+uint64_t g_copier_clock = 0;
 
-// The current device's copier (created on first use), or null.
-RowCopier* row_copier() {
+// The copier of `scratch` on the current device; a new scratch takes a free
+// entry, else the least recently used one once the work it fenced has
+// finished.  Null on a CUDA error.  Called with g_copier_mu held.
+RowCopier* row_copier(const void* scratch) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  RowCopier& c = g_copier[dev];
-  if (!c.copy) {
-    if (cudaStreamCreateWithFlags(&c.copy, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  RowCopier* pick = nullptr;
+  for (RowCopier& c : g_copier)
+    if (c.dev == dev && c.scratch == scratch) { pick = &c; break; }
+  if (!pick) {
+    for (RowCopier& c : g_copier)
+      if (!pick || c.last_use < pick->last_use) pick = &c;
+    RowCopier& c = *pick;
+    if (c.copy) {
+      // the entry's own resources belong to its device; wait for what they fence
+      int cur = dev;
+      if (cudaSetDevice(c.dev) != cudaSuccess) return nullptr;
+      bool ok = cudaStreamSynchronize(c.copy) == cudaSuccess;
+      for (int i = 0; i < 2; ++i) ok = ok && cudaEventSynchronize(c.free[i]) == cudaSuccess;
+      cudaStreamDestroy(c.copy);
+      for (int i = 0; i < 2; ++i) { cudaEventDestroy(c.in[i]); cudaEventDestroy(c.free[i]); }
+      c = RowCopier{};
+      if (cudaSetDevice(cur) != cudaSuccess || !ok) return nullptr;
+    }
+    bool ok = cudaStreamCreateWithFlags(&c.copy, cudaStreamNonBlocking) == cudaSuccess;
     for (int i = 0; i < 2; ++i)
-      if (cudaEventCreateWithFlags(&c.in[i], cudaEventDisableTiming) != cudaSuccess ||
-          cudaEventCreateWithFlags(&c.free[i], cudaEventDisableTiming) != cudaSuccess)
-        return nullptr;
+      ok = ok && cudaEventCreateWithFlags(&c.in[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&c.free[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      if (c.copy) cudaStreamDestroy(c.copy);
+      for (int i = 0; i < 2; ++i) {
+        if (c.in[i]) cudaEventDestroy(c.in[i]);
+        if (c.free[i]) cudaEventDestroy(c.free[i]);
+      }
+      c = RowCopier{};
+      return nullptr;
+    }
+    c.dev = dev;
+    c.scratch = scratch;
   }
-  return &c;
+  pick->last_use = ++g_copier_clock;
+  return pick;
+}
+
+// The address by which the current device reaches host byte `p`, if `p` lies
+// in page-locked host memory mapped for it; else null.
+void* device_view_of_host(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();                      // not a CUDA pointer: clear the error
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
 
 // One step: rows on the host (copied into scratch first) or already on the
@@ -424,11 +471,13 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
   void* dout = out;
   RowCopier* rc = nullptr;
   int slot = 0;
+  void* host_out = nullptr;
+  bool out_direct = false;
   if (rows_on_host) {
     // rows in, on the copier's stream into the next slot (only the scratch is
     // written until the plan is known); the step's kernels wait for them
     std::lock_guard<std::mutex> lk(g_copier_mu);
-    rc = row_copier();
+    rc = row_copier(d_scratch);
     if (!rc) return PPS_ERR_CUDA;
     slot = (int)(rc->calls++ & 1);
     char* sl = sc + slot * slot_bytes;
@@ -446,6 +495,13 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
     dk = sl + off_k;
     dv = sl + off_v;
     dout = sc + off_out;
+    // output rows in page-locked host memory the device can address (first
+    // and last byte mapped for this device)?
+    if (T > 0) {
+      void* d0 = device_view_of_host(out);
+      void* d1 = device_view_of_host((const char*)out + q_bytes - 1);
+      if (d0 && d1 == (char*)d0 + q_bytes - 1) host_out = d0;
+    }
   }
   // the plan, from the host tables (checks them all)
   pps_plan* plan = nullptr;
@@ -457,6 +513,20 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
   if (scratch_bytes < need) {
     pps_plan_destroy(plan);
     return PPS_ERR_WORKSPACE;
+  }
+  // Output rows into mapped host memory straight from the kernels, so no
+  // copy follows the step -- unless tensor-core tiles write most of them: that
+  // kernel's epilogue stalls on stores that cross to host memory (a
+  // long-prefill step, all rows on tensor-core tiles, measured 37 -> 41 ms).
+  // Those batches, and host memory the device cannot address, get the rows
+  // through scratch and a copy on `stream`.
+  int64_t mma_rows = 0;
+  const int32_t* mt = plan->image.data + plan->layout.mma_tasks;
+  for (int64_t i = 0; i < plan->num_mma; ++i) mma_rows += mt[i * PPS_TASK_INTS + 1];
+  mma_rows *= plan->shape.group;
+  if (host_out && 2 * mma_rows <= (int64_t)T * num_q_heads) {
+    dout = host_out;
+    out_direct = true;
   }
   // tables (q_indptr, cached_len = kv_len - q_len, page CSR) through one
   // page-locked staging buffer, reused only after this upload completes
@@ -495,7 +565,7 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
     if (cudaEventRecord(rc->free[slot], stm) == cudaSuccess) rc->used[slot] = true;
     else ok = false;
   }
-  if (ok && st == PPS_OK && rows_on_host && T > 0)
+  if (ok && st == PPS_OK && rows_on_host && T > 0 && !out_direct)
     ok = cudaMemcpyAsync(out, sc + off_out, q_bytes, cudaMemcpyDeviceToHost, stm) == cudaSuccess;
   pps_plan_destroy(plan);
   if (!ok) return PPS_ERR_CUDA;

@@ -86,3 +86,66 @@ def test_step_host_scratch_checks(pps):
     with pytest.raises(pps.PPSError):
         pps.attn_step_host(pk, pv, st.q.cuda(), st.k_new.cpu(), st.v_new.cpu(), L.q_indptr,
                            L.kv_len, L.page_indptr, L.page_indices, out)
+
+
+def _host_rows(st):
+    pin = lambda t: t.cpu().contiguous().pin_memory()
+    out = torch.full(tuple(st.q.shape), float("nan"), dtype=torch.bfloat16).pin_memory()
+    return pin(st.q), pin(st.k_new), pin(st.v_new), out
+
+
+def test_step_host_back_to_back_one_scratch(pps):
+    """Six chunked-prefill steps enqueued with no synchronization between them,
+    one scratch: the input rows of step n+2 go into the slot step n's kernels
+    read, so every output is right only if that copy waited for them."""
+    import workloads
+    wl = workloads.long_prefill(num_requests=2, chunk=300, num_chunks=6, num_q_heads=32,
+                                num_kv_heads=8, head_dim=128, page_size=64, keep_segments=False)
+    dev_in = to_device(wl)
+    outs, (pk, pv), _ = run_workload(wl, device_inputs=dev_in)
+    pk2, pv2 = wl.pool_k.to("cuda", copy=True), wl.pool_v.to("cuda", copy=True)
+    rows = [_host_rows(st) for st in wl.steps]
+    scratch = torch.empty(128 << 20, dtype=torch.uint8, device="cuda")
+    pps.get_device_error(clear=True)
+    for st, (q, k, v, out) in zip(wl.steps, rows):
+        L = st.layout
+        pps.attn_step_host(pk2, pv2, q, k, v, L.q_indptr, L.kv_len, L.page_indptr, L.page_indices,
+                           out, scratch=scratch)
+    torch.cuda.synchronize()
+    assert pps.get_device_error(clear=True) == 0
+    for s, (_, _, _, out) in enumerate(rows):
+        assert torch.equal(out.view(torch.int16), outs[s].cpu().view(torch.int16)), s
+    assert torch.equal(pk2.view(torch.int16), pk.view(torch.int16))
+    assert torch.equal(pv2.view(torch.int16), pv.view(torch.int16))
+
+
+def test_step_host_two_streams(pps):
+    """Two independent batches (own pool, scratch and stream) with their steps
+    interleaved call by call: each stream's results match its batch's device
+    calls, whatever the other stream does meanwhile."""
+    import workloads
+    mk = lambda seed: workloads.long_prefill(num_requests=2, chunk=200, num_chunks=4,
+                                             num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                             page_size=16, keep_segments=False, seed=seed)
+    wls = [mk(11), mk(12)]
+    refs, pools, rows, scratches, streams = [], [], [], [], []
+    for wl in wls:
+        outs, _, _ = run_workload(wl, device_inputs=to_device(wl))
+        refs.append(outs)
+        pools.append((wl.pool_k.to("cuda", copy=True), wl.pool_v.to("cuda", copy=True)))
+        rows.append([_host_rows(st) for st in wl.steps])
+        scratches.append(torch.empty(128 << 20, dtype=torch.uint8, device="cuda"))
+        streams.append(torch.cuda.Stream())
+    torch.cuda.synchronize()
+    pps.get_device_error(clear=True)
+    for s in range(len(wls[0].steps)):
+        for b, wl in enumerate(wls):
+            L = wl.steps[s].layout
+            q, k, v, out = rows[b][s]
+            pps.attn_step_host(*pools[b], q, k, v, L.q_indptr, L.kv_len, L.page_indptr,
+                               L.page_indices, out, scratch=scratches[b], stream=streams[b])
+    torch.cuda.synchronize()
+    assert pps.get_device_error(clear=True) == 0
+    for b in range(2):
+        for s, (_, _, _, out) in enumerate(rows[b]):
+            assert torch.equal(out.view(torch.int16), refs[b][s].cpu().view(torch.int16)), (b, s)
