@@ -9,16 +9,29 @@
 // (the virtual padding), nothing padded is ever read from or written to HBM,
 // and the epilogue stores only rows < M and columns < N.
 //
-// Persistent kernel, one CTA per SM (192 threads) taking output tiles b,
-// b + grid, ...:
-//   warp 0     TMA producer: per 64-wide K block, the A tile (128 x 64) and the
-//              W tile (256 x 64), 128-byte swizzle, into a 4-stage ring;
-//   warp 1     MMA issuer: 4 x tcgen05.mma (M 128, N 256, K 16) per K block into
-//              one of two TMEM accumulators (2 x 256 columns), so the epilogue
-//              of one tile overlaps the MMAs of the next;
-//   warps 2-5  epilogue: TMEM -> registers -> bf16 -> global, row = TMEM lane.
+// Persistent kernel on CTA pairs (clusters of two CTAs, one CTA per SM): a
+// pair computes 256 x 256 output tiles p, p + pairs, ... with tcgen05 MMAs of
+// M = 256 issued by the even CTA (.cta_group::2): each CTA stages its own 128
+// rows of A and its own 128 rows of W per K block, and each CTA's TMEM holds
+// its 128 rows of the accumulator.  Per K block an SM thus writes 32 KB into
+// shared memory and its tensor core reads 32 KB there, against 48 + 48 KB for
+// a 128 x 256 tile on one SM -- the shared-memory traffic, not the MMA rate,
+// bounded that form.  192 threads per CTA:
+//   warp 0     TMA producer: per 64-wide K block, this CTA's A rows (128 x 64)
+//              and W rows (128 x 64), 128-byte swizzle, into a 6-stage ring;
+//              completion is signalled on the even CTA's barrier, which
+//              expects both CTAs' bytes;
+//   warp 1     (even CTA) MMA issuer: 4 x tcgen05.mma (M 256, N 256, K 16) per K
+//              block into one of two TMEM accumulators (2 x 256 columns), so the
+//              epilogue of one tile overlaps the MMAs of the next; its commits
+//              free the stage and announce the accumulator in both CTAs;
+//   warps 2-5  epilogue: TMEM -> registers -> bf16 -> global, row = TMEM lane;
+//              both CTAs' epilogue warps release the accumulator on the even
+//              CTA's barrier.
 // Every mbarrier wait is bounded; on timeout the kernel records
-// PPS_DEV_ERR_WAIT_TIMEOUT, stops, drains what it issued and frees TMEM.
+// PPS_DEV_ERR_WAIT_TIMEOUT and stops issuing.  No thread returns early: all of
+// both CTAs meet at the closing cluster barrier, after the MMAs have drained,
+// before the TMEM is freed.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -34,19 +47,23 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
-constexpr int kABytes = kBM * kBK * 2;              // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;              // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kBM = 128;                          // A rows per CTA (256 per pair)
+constexpr int kBN = 256;                          // C columns per pair tile
+constexpr int kBNh = kBN / 2;                     // W rows per CTA
+constexpr int kBK = 64, kStages = 6;
+constexpr int kABytes = kBM * kBK * 2;            // 16 KB
+constexpr int kBBytes = kBNh * kBK * 2;           // 16 KB
+constexpr int kStageBytes = kABytes + kBBytes;    // per CTA
 constexpr int kSmemAlloc = kStages * kStageBytes + 1024;
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
+constexpr uint16_t kPairMask = 0x3;
 
 struct GemmBars {
   uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tw,
                      __nv_bfloat16* __restrict__ c, int M, int N, int K, int32_t* err) {
   extern __shared__ uint8_t smem_raw[];
@@ -55,8 +72,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_base;
   __shared__ volatile int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();          // 0: issues the MMAs
+  const int pair = (int)(blockIdx.x >> 1), pairs = (int)(gridDim.x >> 1);
   const int ntn = (N + kBN - 1) / kBN;
-  const int tiles = ((M + kBM - 1) / kBM) * ntn;
+  const int tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ntn;
   const int nkb = (K + kBK - 1) / kBK;
 
   if (threadIdx.x == 0) {
@@ -66,18 +85,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bars.acc_full[b]), 1);
-      mbar_init(smem_u32(&bars.acc_empty[b]), kEpiWarps);
+      mbar_init(smem_u32(&bars.acc_empty[b]), 2 * kEpiWarps);
     }
     mbar_init(smem_u32(&bars.drain), 1);
     abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_base), 512);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&tmem_base), 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();                                   // the peer's barriers are initialised
   tc_fence_after();
   const uint32_t tm = tmem_base;
   auto fail = [&]() {
@@ -97,70 +117,77 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-      const int m0 = (t / ntn) * kBM, n0 = (t % ntn) * kBN;
+    for (int t = pair; ok && t < tiles; t += pairs) {
+      const int m0 = (t / ntn) * (2 * kBM) + (int)rank * kBM;
+      const int n0 = (t % ntn) * kBN + (int)rank * kBNh;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const int s = it % kStages, use = it / kStages;
         if (!warp_wait(&bars.empty[s], (use - 1) & 1, use > 0)) { fail(); ok = false; break; }
         if (lane == 0) {
-          const uint32_t fb = smem_u32(&bars.full[s]);
+          const uint32_t fb = mapa_shared(smem_u32(&bars.full[s]), 0);
           const uint32_t base = smem_u32(smem + s * kStageBytes);
-          mbar_expect_tx(fb, kStageBytes);
-          tma_load_2d(base, &ta, kb * kBK, m0, fb);
-          tma_load_2d(base + kABytes, &tw, kb * kBK, n0, fb);
+          if (rank == 0) mbar_expect_tx(smem_u32(&bars.full[s]), 2 * kStageBytes);
+          tma_load_2d_pair(base, &ta, kb * kBK, m0, fb);
+          tma_load_2d_pair(base + kABytes, &tw, kb * kBK, n0, fb);
         }
         __syncwarp();
       }
     }
-    // every load started lands before the CTA may exit
-    if (lane == 0) {
+    // the even CTA sees every load of both CTAs land before the pair may exit
+    // (the odd CTA's loads are counted on the even CTA's barriers)
+    if (rank == 0 && lane == 0) {
       const uint64_t lim = ok ? 2000000000ull : 10000000ull;
       for (int j = (it > kStages ? it - kStages : 0); j < it; ++j)
         mbar_wait(smem_u32(&bars.full[j % kStages]), (j / kStages) & 1, lim);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16(kBM, kBN, 0, 0);
-    int it = 0, tc = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++tc) {
-      const int b = tc & 1, use_b = tc >> 1;
-      if (!warp_wait(&bars.acc_empty[b], (use_b - 1) & 1, use_b > 0)) { fail(); ok = false; break; }
-      tc_fence_after();
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int s = it % kStages;
-        if (!warp_wait(&bars.full[s], (it / kStages) & 1)) { fail(); ok = false; break; }
+    if (rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16(2 * kBM, kBN, 0, 0);
+      int it = 0, tc = 0;
+      bool ok = true;
+      for (int t = pair; ok && t < tiles; t += pairs, ++tc) {
+        const int b = tc & 1, use_b = tc >> 1;
+        if (!warp_wait(&bars.acc_empty[b], (use_b - 1) & 1, use_b > 0)) { fail(); ok = false; break; }
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a0 = smem_u32(smem + s * kStageBytes), w0 = a0 + kABytes;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!warp_wait(&bars.full[s], (it / kStages) & 1)) { fail(); ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a0 = smem_u32(smem + s * kStageBytes), w0 = a0 + kABytes;
 #pragma unroll
-          for (int ks = 0; ks < kBK / 16; ++ks)
-            umma_ss(tm + b * kBN, smem_desc(a0 + ks * 32, 16, 1024),
-                    smem_desc(w0 + ks * 32, 16, 1024), idesc, (kb > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(smem_u32(&bars.empty[s]));        // stage free once these MMAs finish
+            for (int ks = 0; ks < kBK / 16; ++ks)
+              umma_ss_pair(tm + b * kBN, smem_desc(a0 + ks * 32, 16, 1024),
+                           smem_desc(w0 + ks * 32, 16, 1024), idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+            // the stage is free in both CTAs once these MMAs finish
+            umma_commit_pair_mc(smem_u32(&bars.empty[s]), kPairMask);
+          }
+          __syncwarp();
         }
+        if (!ok) break;
+        if (lane == 0) umma_commit_pair_mc(smem_u32(&bars.acc_full[b]), kPairMask);
         __syncwarp();
       }
-      if (!ok) break;
-      if (lane == 0) umma_commit(smem_u32(&bars.acc_full[b]));
+      if (lane == 0) {
+        umma_commit_pair(smem_u32(&bars.drain));
+        if (!mbar_wait(smem_u32(&bars.drain), 0)) fail();
+      }
       __syncwarp();
     }
-    if (lane == 0) {
-      umma_commit(smem_u32(&bars.drain));
-      if (!mbar_wait(smem_u32(&bars.drain), 0)) fail();
-    }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------- epilogue
     const int quarter = warp & 3;                       // TMEM lanes this warp may read
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int r = quarter * 32 + lane;                  // row within the tile
+    const int r = quarter * 32 + lane;                  // row within this CTA's half
+    const uint32_t empty0 = mapa_shared(smem_u32(&bars.acc_empty[0]), 0);
+    const uint32_t empty1 = mapa_shared(smem_u32(&bars.acc_empty[1]), 0);
     int tc = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++tc) {
+    for (int t = pair; t < tiles; t += pairs, ++tc) {
       const int b = tc & 1, use_b = tc >> 1;
       if (!warp_wait(&bars.acc_full[b], use_b & 1)) { fail(); break; }
       tc_fence_after();
-      const int m = (t / ntn) * kBM + r, n0 = (t % ntn) * kBN;
+      const int m = (t / ntn) * (2 * kBM) + (int)rank * kBM + r, n0 = (t % ntn) * kBN;
 #pragma unroll 1
       for (int c0 = 0; c0 < kBN; c0 += 32) {
         uint32_t rr[32];
@@ -182,15 +209,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars.acc_empty[b]));
+      if (lane == 0) mbar_arrive_cluster(b ? empty1 : empty0);
     }
   }
 
+  // All MMAs of the pair have completed (the even CTA's drain), so both CTAs'
+  // shared memory and TMEM may go.
   tc_fence_before();
   __syncthreads();
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tm, 512);
+    tmem_dealloc_pair(tm, 512);
   }
 }
 
@@ -230,7 +260,7 @@ int launch_gemm_bf16(const void* a, const void* w, void* c, int32_t M, int32_t N
                      int32_t* err, void* stream) {
   if (M == 0) return cudaSuccess;
   CUtensorMap ma, mw;
-  if (!make_map(&ma, a, M, K, kBM) || !make_map(&mw, w, N, K, kBN))
+  if (!make_map(&ma, a, M, K, kBM) || !make_map(&mw, w, N, K, kBNh))
     return (int)cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
@@ -239,8 +269,8 @@ int launch_gemm_bf16(const void* a, const void* w, void* c, int32_t M, int32_t N
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return (int)e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return (int)e;
-  const int64_t tiles = (int64_t)((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
-  const int64_t grid = std::min<int64_t>(tiles, sms);
+  const int64_t tiles = (int64_t)((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kBN - 1) / kBN);
+  const int64_t grid = 2 * std::min<int64_t>(tiles, sms / 2);     // CTA pairs
   gemm_bf16_kernel<<<(unsigned)grid, kThreads, kSmemAlloc, (cudaStream_t)stream>>>(
       ma, mw, (__nv_bfloat16*)c, M, N, K, err);
   count_launch();
