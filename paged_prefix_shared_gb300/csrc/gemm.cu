@@ -25,9 +25,11 @@
 //              block into one of two TMEM accumulators (2 x 256 columns), so the
 //              epilogue of one tile overlaps the MMAs of the next; its commits
 //              free the stage and announce the accumulator in both CTAs;
-//   warps 2-5  epilogue: TMEM -> registers -> bf16 -> global, row = TMEM lane;
-//              both CTAs' epilogue warps release the accumulator on the even
-//              CTA's barrier.
+//   warps 2-5  epilogue: TMEM -> registers -> bf16 -> a 32 x 32 staging box in
+//              shared memory (64-byte swizzle, two per warp) -> TMA store, row
+//              = TMEM lane; the store writes whole 64-byte row pieces and
+//              leaves out rows >= M and columns >= N; both CTAs' epilogue warps
+//              release the accumulator on the even CTA's barrier.
 // Every mbarrier wait is bounded; on timeout the kernel records
 // PPS_DEV_ERR_WAIT_TIMEOUT and stops issuing.  No thread returns early: all of
 // both CTAs meet at the closing cluster barrier, after the MMAs have drained,
@@ -54,7 +56,10 @@ constexpr int kBK = 64, kStages = 6;
 constexpr int kABytes = kBM * kBK * 2;            // 16 KB
 constexpr int kBBytes = kBNh * kBK * 2;           // 16 KB
 constexpr int kStageBytes = kABytes + kBBytes;    // per CTA
-constexpr int kSmemAlloc = kStages * kStageBytes + 1024;
+constexpr int kEpiBox = 32;                       // output box: 32 rows x 32 columns
+constexpr int kEpiBoxBytes = kEpiBox * kEpiBox * 2;  // 2 KB
+constexpr int kRingBytes = kStages * kStageBytes;
+constexpr int kSmemAlloc = kRingBytes + 4 * 2 * kEpiBoxBytes + 1024;
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
 constexpr uint16_t kPairMask = 0x3;
@@ -65,7 +70,7 @@ struct GemmBars {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tw,
-                     __nv_bfloat16* __restrict__ c, int M, int N, int K, int32_t* err) {
+                     const __grid_constant__ CUtensorMap tc, int M, int N, int K, int32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ GemmBars bars;
@@ -179,38 +184,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- epilogue
     const int quarter = warp & 3;                       // TMEM lanes this warp may read
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int r = quarter * 32 + lane;                  // row within this CTA's half
     const uint32_t empty0 = mapa_shared(smem_u32(&bars.acc_empty[0]), 0);
     const uint32_t empty1 = mapa_shared(smem_u32(&bars.acc_empty[1]), 0);
-    int tc = 0;
-    for (int t = pair; t < tiles; t += pairs, ++tc) {
-      const int b = tc & 1, use_b = tc >> 1;
+    // two staging boxes per warp; with the 64-byte swizzle, 16-byte piece j of
+    // row r sits at r * 64 + ((j ^ (r / 2 % 4)) * 16), so the 32 lanes' stores
+    // of one piece each fill four distinct bank lines
+    const uint32_t stage0 = smem_u32(smem + kRingBytes) + (uint32_t)(quarter * 2 * kEpiBoxBytes);
+    const uint32_t row_off = (uint32_t)lane * 64u;
+    const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
+    if (lane == 0) prefetch_tmap(&tc);
+    int tc_i = 0, box = 0;
+    for (int t = pair; t < tiles; t += pairs, ++tc_i) {
+      const int b = tc_i & 1, use_b = tc_i >> 1;
       if (!warp_wait(&bars.acc_full[b], use_b & 1)) { fail(); break; }
       tc_fence_after();
-      const int m = (t / ntn) * (2 * kBM) + (int)rank * kBM + r, n0 = (t % ntn) * kBN;
+      const int m_box = (t / ntn) * (2 * kBM) + (int)rank * kBM + quarter * 32;
+      const int n0 = (t % ntn) * kBN;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
+      for (int c0 = 0; c0 < kBN; c0 += 32, ++box) {
         uint32_t rr[32];
         tmem_ld32(tm + b * kBN + lane_off + c0, rr);
+        const uint32_t buf = stage0 + (uint32_t)(box & 1) * kEpiBoxBytes;
+        if (box >= 2) {
+          // the store issued from this box two rounds ago has read it
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+        }
         tmem_wait_ld();
-        if (m < M) {
-          __nv_bfloat16* dst = c + (size_t)m * N + n0 + c0;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (n0 + c0 + 8 * j >= N) break;
-            int4 v;
-            v.x = (int)pack_bf16(__uint_as_float(rr[8 * j + 0]), __uint_as_float(rr[8 * j + 1]));
-            v.y = (int)pack_bf16(__uint_as_float(rr[8 * j + 2]), __uint_as_float(rr[8 * j + 3]));
-            v.z = (int)pack_bf16(__uint_as_float(rr[8 * j + 4]), __uint_as_float(rr[8 * j + 5]));
-            v.w = (int)pack_bf16(__uint_as_float(rr[8 * j + 6]), __uint_as_float(rr[8 * j + 7]));
-            *reinterpret_cast<int4*>(dst + 8 * j) = v;
-          }
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t x = pack_bf16(__uint_as_float(rr[8 * j + 0]), __uint_as_float(rr[8 * j + 1]));
+          const uint32_t y = pack_bf16(__uint_as_float(rr[8 * j + 2]), __uint_as_float(rr[8 * j + 3]));
+          const uint32_t z = pack_bf16(__uint_as_float(rr[8 * j + 4]), __uint_as_float(rr[8 * j + 5]));
+          const uint32_t w = pack_bf16(__uint_as_float(rr[8 * j + 6]), __uint_as_float(rr[8 * j + 7]));
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           buf + row_off + ((((uint32_t)j) ^ sw) << 4)),
+                       "r"(x), "r"(y), "r"(z), "r"(w)
+                       : "memory");
+        }
+        fence_proxy_async_smem();                       // visible to the TMA store
+        __syncwarp();
+        if (lane == 0) {
+          if (m_box < M && n0 + c0 < N) tma_store_2d(&tc, n0 + c0, m_box, buf);
+          bulk_commit_group();
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(b ? empty1 : empty0);
     }
+    // the stores have read their boxes and written C before the CTA exits
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
   }
 
   // All MMAs of the pair have completed (the even CTA's drain), so both CTAs'
@@ -238,17 +263,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Row-major [rows, K] bf16 matrix; box = 64 columns x box_rows rows, 128-byte
-// swizzle (the UMMA K-major layout); out-of-range elements read as zero.
-bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
+// Row-major [rows, cols] bf16 matrix; box = box_cols x box_rows, the given
+// swizzle (128-byte: the UMMA K-major layout of the operands); out-of-range
+// elements read as zero and are not written.
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows,
+              int box_cols = kBK, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -259,8 +286,9 @@ namespace pps {
 int launch_gemm_bf16(const void* a, const void* w, void* c, int32_t M, int32_t N, int32_t K,
                      int32_t* err, void* stream) {
   if (M == 0) return cudaSuccess;
-  CUtensorMap ma, mw;
-  if (!make_map(&ma, a, M, K, kBM) || !make_map(&mw, w, N, K, kBNh))
+  CUtensorMap ma, mw, mc;
+  if (!make_map(&ma, a, M, K, kBM) || !make_map(&mw, w, N, K, kBNh) ||
+      !make_map(&mc, c, M, N, kEpiBox, kEpiBox, CU_TENSOR_MAP_SWIZZLE_64B))
     return (int)cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
@@ -272,7 +300,7 @@ int launch_gemm_bf16(const void* a, const void* w, void* c, int32_t M, int32_t N
   const int64_t tiles = (int64_t)((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kBN - 1) / kBN);
   const int64_t grid = 2 * std::min<int64_t>(tiles, sms / 2);     // CTA pairs
   gemm_bf16_kernel<<<(unsigned)grid, kThreads, kSmemAlloc, (cudaStream_t)stream>>>(
-      ma, mw, (__nv_bfloat16*)c, M, N, K, err);
+      ma, mw, mc, M, N, K, err);
   count_launch();
   return (int)cudaGetLastError();
 }
