@@ -13,15 +13,17 @@
 // pair computes 256 x 256 output tiles p, p + pairs, ... with tcgen05 MMAs of
 // M = 256 issued by the even CTA (.cta_group::2): each CTA stages its own 128
 // rows of A and its own 128 rows of W per K block, and each CTA's TMEM holds
-// its 128 rows of the accumulator.  Per K block an SM thus writes 32 KB into
+// its 128 rows of the accumulator.  Per 64 of K an SM thus writes 32 KB into
 // shared memory and its tensor core reads 32 KB there, against 48 + 48 KB for
-// a 128 x 256 tile on one SM -- the shared-memory traffic, not the MMA rate,
-// bounded that form.  192 threads per CTA:
-//   warp 0     TMA producer: per 64-wide K block, this CTA's A rows (128 x 64)
-//              and W rows (128 x 64), 128-byte swizzle, into a 6-stage ring;
+// a 128 x 256 tile on one SM.  A stage holds 128 of K: the MMA warp waits on a
+// stage barrier once per 8 MMAs, since that wait, not the data, is what kept
+// the tensor pipe idle with 64-deep stages.  192 threads per CTA:
+//   warp 0     TMA producer: per 128-wide K block, this CTA's A rows (128 x 128)
+//              and W rows (128 x 128), each as two 64-column boxes with
+//              128-byte swizzle, into a 3-stage ring (64 KB a stage);
 //              completion is signalled on the even CTA's barrier, which
 //              expects both CTAs' bytes;
-//   warp 1     (even CTA) MMA issuer: 4 x tcgen05.mma (M 256, N 256, K 16) per K
+//   warp 1     (even CTA) MMA issuer: 8 x tcgen05.mma (M 256, N 256, K 16) per K
 //              block into one of two TMEM accumulators (2 x 256 columns), so the
 //              epilogue of one tile overlaps the MMAs of the next; its commits
 //              free the stage and announce the accumulator in both CTAs;
@@ -52,9 +54,11 @@ using namespace sm100;
 constexpr int kBM = 128;                          // A rows per CTA (256 per pair)
 constexpr int kBN = 256;                          // C columns per pair tile
 constexpr int kBNh = kBN / 2;                     // W rows per CTA
-constexpr int kBK = 64, kStages = 6;
-constexpr int kABytes = kBM * kBK * 2;            // 16 KB
-constexpr int kBBytes = kBNh * kBK * 2;           // 16 KB
+constexpr int kBK = 128, kStages = 3;             // K block: two 64-column boxes per operand
+constexpr int kSub = kBK / 64;
+constexpr int kSubA = kBM * 64 * 2, kSubB = kBNh * 64 * 2;   // 16 KB each
+constexpr int kABytes = kSub * kSubA;             // 32 KB
+constexpr int kBBytes = kSub * kSubB;             // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;    // per CTA
 constexpr int kEpiBox = 32;                       // output box: 32 rows x 32 columns
 constexpr int kEpiBoxBytes = kEpiBox * kEpiBox * 2;  // 2 KB
@@ -132,8 +136,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t fb = mapa_shared(smem_u32(&bars.full[s]), 0);
           const uint32_t base = smem_u32(smem + s * kStageBytes);
           if (rank == 0) mbar_expect_tx(smem_u32(&bars.full[s]), 2 * kStageBytes);
-          tma_load_2d_pair(base, &ta, kb * kBK, m0, fb);
-          tma_load_2d_pair(base + kABytes, &tw, kb * kBK, n0, fb);
+#pragma unroll
+          for (int h = 0; h < kSub; ++h) {
+            tma_load_2d_pair(base + h * kSubA, &ta, kb * kBK + h * 64, m0, fb);
+            tma_load_2d_pair(base + kABytes + h * kSubB, &tw, kb * kBK + h * 64, n0, fb);
+          }
         }
         __syncwarp();
       }
@@ -163,8 +170,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t a0 = smem_u32(smem + s * kStageBytes), w0 = a0 + kABytes;
 #pragma unroll
             for (int ks = 0; ks < kBK / 16; ++ks)
-              umma_ss_pair(tm + b * kBN, smem_desc(a0 + ks * 32, 16, 1024),
-                           smem_desc(w0 + ks * 32, 16, 1024), idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+              umma_ss_pair(tm + b * kBN, smem_desc(a0 + (ks / 4) * kSubA + (ks % 4) * 32, 16, 1024),
+                           smem_desc(w0 + (ks / 4) * kSubB + (ks % 4) * 32, 16, 1024), idesc,
+                           (kb > 0 || ks > 0) ? 1u : 0u);
             // the stage is free in both CTAs once these MMAs finish
             umma_commit_pair_mc(smem_u32(&bars.empty[s]), kPairMask);
           }
@@ -267,7 +275,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // swizzle (128-byte: the UMMA K-major layout of the operands); out-of-range
 // elements read as zero and are not written.
 bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows,
-              int box_cols = kBK, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+              int box_cols = 64, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
