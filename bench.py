@@ -1030,7 +1030,8 @@ def run_projections(args):
                 "d2h_bytes_per_step": sum(M * N * 2 for N in shapes), "ms_per_step": ms_e2e},
         "gpu_launches": launches,
         "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
-                     "frac": tf / peak, "traffic": None, "kernel": "tcgen05 projection GEMM",
+                     "frac": tf / peak, "traffic": traffic_record("gemm.cu", "projections"),
+                     "kernel": "tcgen05 projection GEMM",
                      "algorithmic": f"{flops:.4g} FLOP per step (2*M*N*K, QKV and O)",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json, burst)"},
         "library_gemm_ms": {"qkv": cub[0], "o": cub[1],
