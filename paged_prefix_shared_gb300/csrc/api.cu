@@ -529,8 +529,15 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
     out_direct = true;
   }
   // tables (q_indptr, cached_len = kv_len - q_len, page CSR) through one
-  // page-locked staging buffer, reused only after this upload completes
-  pps::HostBuf tb = pps::host_buf_acquire(std::max<size_t>(tab_ints, 1));
+  // page-locked staging buffer, reused only after this upload completes; for
+  // a plan whose task table is small, the task table rides in the same copy
+  // (scratch holds them back to back), one copy-engine round trip fewer ahead
+  // of the append
+  const size_t tab_span = off_ws - off_tab;               // the tables, 256-byte rounded
+  const size_t img_bytes = (size_t)plan->image_ints * 4;
+  const bool one_copy = T > 0 && img_bytes <= ((size_t)1 << 20);
+  const size_t stage_ints = one_copy ? (tab_span + img_bytes) / 4 : tab_ints;
+  pps::HostBuf tb = pps::host_buf_acquire(std::max<size_t>(stage_ints, 1));
   if (!tb.data) {
     pps_plan_destroy(plan);
     return PPS_ERR_NO_MEMORY;
@@ -540,8 +547,12 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
   for (int32_t r = 0; r < R; ++r) t[R + 1 + r] = h_kv_len[r] - (h_q_indptr[r + 1] - h_q_indptr[r]);
   if (R > 0) std::memcpy(t + 2 * R + 1, h_page_indptr, (size_t)(R + 1) * 4);
   if (nnz) std::memcpy(t + 3 * R + 2, h_page_indices, (size_t)nnz * 4);
-  bool ok = cudaMemcpyAsync(sc + off_tab, t, tab_ints * 4, cudaMemcpyHostToDevice, stm) ==
-            cudaSuccess;
+  if (one_copy) {
+    std::memset(t + tab_ints, 0, tab_span - tab_ints * 4);
+    std::memcpy(t + tab_span / 4, plan->image.data, img_bytes);
+  }
+  bool ok = cudaMemcpyAsync(sc + off_tab, t, one_copy ? tab_span + img_bytes : tab_ints * 4,
+                            cudaMemcpyHostToDevice, stm) == cudaSuccess;
   ok = ok && pps::host_buf_mark_use(tb, stream) == 0;
   pps::host_buf_release(tb);
   // task table up, append, attend, rows out: the attention kernels directly
@@ -551,7 +562,7 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
   const bool fused = opts && (opts->flags & PPS_PLAN_FUSED_APPEND) && can_fuse_append(plan);
   const pps::AppendArgs app{dk, dv, d_tab, d_tab + R + 1, d_tab + 2 * R + 1, d_tab + 3 * R + 2,
                             R, T};
-  if (ok)
+  if (ok && !one_copy)
     st = run_impl(plan, dq, pool, dout, sc + off_ws, al(ws_bytes), stream, events, kRunUpload);
   if (ok && st == PPS_OK && !fused)
     st = pps_kv_append(pool, dk, dv, d_tab, d_tab + R + 1, d_tab + 2 * R + 1, d_tab + 3 * R + 2,

@@ -25,31 +25,48 @@ __global__ void __launch_bounds__(256) merge_kernel(
     const float* __restrict__ lse_part, __nv_bfloat16* __restrict__ out, int32_t num_q_heads,
     int64_t num_rows) {
   constexpr int kPer = D / 32;
-  sm100::grid_dep_wait();        // the partials of the attention kernels before it
   const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (wid >= num_rows) return;
-  const int m = (int)(wid / num_q_heads), h = (int)(wid - (int64_t)m * num_q_heads);
-  const int t = tokens[m];
-  const int a = indptr[m], b = indptr[m + 1];
+  const bool live = wid < num_rows;
+  const int m = live ? (int)(wid / num_q_heads) : 0;
+  const int h = live ? (int)(wid - (int64_t)m * num_q_heads) : 0;
+  // The merge lists were uploaded before the step's kernels ran, so they are
+  // read while the attention kernel before this one finishes; only the
+  // partials wait for it.
+  // (the first three partial ids are read ahead; a token rarely has more)
+  int t = 0, a = 0, b = 0, p0 = 0, p1 = 0, p2 = 0;
+  if (live) {
+    t = __ldg(tokens + m);
+    a = __ldg(indptr + m);
+    b = __ldg(indptr + m + 1);
+    if (a < b) p0 = __ldg(pids + a);
+    if (a + 1 < b) p1 = __ldg(pids + a + 1);
+    if (a + 2 < b) p2 = __ldg(pids + a + 2);
+  }
+  sm100::grid_dep_wait();        // the partials of the attention kernels before it
+  if (!live) return;
+  auto pid_at = [&](int i) {
+    const int d = i - a;
+    return d == 0 ? p0 : d == 1 ? p1 : d == 2 ? p2 : __ldg(pids + i);
+  };
   float M = -INFINITY;
-  for (int i = a; i < b; ++i) M = fmaxf(M, __ldg(lse_part + (size_t)pids[i] * num_q_heads + h));
+  for (int i = a; i < b; ++i) M = fmaxf(M, lse_part[(size_t)pid_at(i) * num_q_heads + h]);
   float acc[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
   float wsum = 0.f;
   for (int i = a; i < b; ++i) {
-    const size_t row = (size_t)pids[i] * num_q_heads + h;
-    const float l = __ldg(lse_part + row);
+    const size_t row = (size_t)pid_at(i) * num_q_heads + h;
+    const float l = lse_part[row];
     const float w = (l == -INFINITY) ? 0.f : exp2f(l - M);
     wsum += w;
     const float* src = o_part + row * D + lane * kPer;
     if constexpr (kPer == 4) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(src));
+      const float4 v = *reinterpret_cast<const float4*>(src);
       acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
     } else {
       static_assert(kPer == 2, "head_dim 64 or 128");
-      const float2 v = __ldg(reinterpret_cast<const float2*>(src));
+      const float2 v = *reinterpret_cast<const float2*>(src);
       acc[0] += w * v.x; acc[1] += w * v.y;
     }
   }
