@@ -149,3 +149,35 @@ def test_step_host_two_streams(pps):
     for b in range(2):
         for s, (_, _, _, out) in enumerate(rows[b]):
             assert torch.equal(out.view(torch.int16), refs[b][s].cpu().view(torch.int16)), (b, s)
+
+
+def test_step_with_large_task_table(pps):
+    """4096 decode rows: a task table over 1 MB, which the step calls upload
+    apart from the step's tables (smaller ones ride in the same copy).  The
+    device-row and host-row steps must match the separate calls bit for bit."""
+    import workloads
+    wl = workloads.decode_heavy(num_requests=4096, kv_lo=16, kv_hi=80, num_q_heads=32,
+                                num_kv_heads=8, head_dim=128, page_size=16, keep_segments=False)
+    L = wl.steps[0].layout
+    plan = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices, L.num_q_heads,
+                         L.num_kv_heads, L.head_dim, L.page_size, L.num_pages)
+    assert plan.info()["table_bytes"] > 1 << 20
+    dev_in = to_device(wl)
+    outs, (pk, pv), _ = run_workload(wl, device_inputs=dev_in)
+    st = dev_in[2][0]
+    for host in (False, True):
+        pk2, pv2 = wl.pool_k.to("cuda", copy=True), wl.pool_v.to("cuda", copy=True)
+        pps.get_device_error(clear=True)
+        if host:
+            q, k, v, out = _host_rows(wl.steps[0])
+            pps.attn_step_host(pk2, pv2, q, k, v, L.q_indptr, L.kv_len, L.page_indptr,
+                               L.page_indices, out)
+        else:
+            out = torch.full_like(st["q"], float("nan"))
+            pps.attn_step(pk2, pv2, st["q"], st["k_new"], st["v_new"], L.q_indptr, L.kv_len,
+                          L.page_indptr, L.page_indices, out)
+        torch.cuda.synchronize()
+        assert pps.get_device_error(clear=True) == 0
+        assert torch.equal(out.cpu().view(torch.int16), outs[0].cpu().view(torch.int16)), host
+        assert torch.equal(pk2.view(torch.int16), pk.view(torch.int16))
+        assert torch.equal(pv2.view(torch.int16), pv.view(torch.int16))
