@@ -165,6 +165,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ Bars bars;
   __shared__ uint32_t tmem_base;
   __shared__ volatile int abort_flag;
+  // The CTA's next task, read during the current one (see the softmax warps):
+  // its record per tile, and per softmax thread its token (-1: padding row),
+  // query head and draft-tree lookback mask.
+  __shared__ pps::Task next_task[2];
+  __shared__ int2 next_row[kSoftmaxWarps * 32];
+  __shared__ unsigned long long next_mask[kSoftmaxWarps * 32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x, nctas = gridDim.x;
@@ -232,21 +238,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tm_o = tm + 256 + X * D;         // O_X
     uint8_t* q_tile = smem + Lay::q_off + X * Lay::kTileBytes;
     int sx = 0, ox = 0;                             // phases consumed on s_full[X] / o_done[X]
+    // A task switch costs a CTA ~10 us of mostly idle tensor core (epilogue,
+    // Q rows, first S): the chain of dependent loads task -> token -> Q row
+    // alone took ~3 us.  So during a task, after its first tile, each thread
+    // reads the next task's record, its token and mask into shared memory
+    // (`meta`), and once this tile's last QK has completed (the last s_full)
+    // it starts the copy of its next Q row into the now free Q tile (`q_pref`).
+    bool meta = false, q_pref = false;
     for (int ti = 0;; ++ti) {
       const int t = snake_task(ti, b, nctas);
       // Both warpgroups start a task together (and stop together): neither can
       // run a task ahead and complete the next task's q_full phase alone.
       if (softmax_barrier_or(t >= p.num_tasks || abort_flag)) break;
-      const pps::Task task = p.tasks[t];
+      const pps::Task task = meta ? next_task[X] : p.tasks[t];
       const TileRange tr = tile_range(task, X, G);
       const int r = X * 128 + m;                    // row within the task
       const bool real = m < tr.rows;
       const int i = r / G, g = r - (r / G) * G;
       const int h = task.kv_head * G + g;
-      const int tok = real ? p.rows[task.row_off + i] : 0;
+      const int tok = meta ? max(next_row[tid].x, 0) : (real ? p.rows[task.row_off + i] : 0);
+      const unsigned long long tmask_pre = meta ? next_mask[tid] : ~0ull;
       // Q row -> swizzled shared memory (zeros for padding rows).  Every MMA of
       // the previous task completed before its epilogues, which precede this.
-      {
+      if (q_pref) {
+        cp_async_wait_all();
+      } else {
         const int4* src = reinterpret_cast<const int4*>(p.q + ((size_t)tok * p.num_q_heads + h) * D);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
@@ -254,6 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<int4*>(q_tile + (c / 8) * 16384 + sw128(m, c % 8)) = v;
         }
       }
+      const bool had_meta = meta;
+      meta = q_pref = false;
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -265,7 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // before the row's own one is visible.  Kept bit-reversed so the
       // visibility of a tile's columns is a shifted window of it.
       const unsigned long long tmask =
-          (p.tree_mask && real && task.causal != PPS_NO_CAUSAL) ? p.tree_mask[tok] : ~0ull;
+          had_meta ? tmask_pre
+                   : ((p.tree_mask && real && task.causal != PPS_NO_CAUSAL) ? p.tree_mask[tok] : ~0ull);
       const bool trow = tmask != ~0ull;
       const unsigned long long trev = __brevll(tmask);
       // Padding rows see no key: any finite reference keeps their P at 0 and
@@ -275,6 +294,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < tr.n_tiles; ++j, ++sx) {
         const int t0 = task.kv_begin + j * kTile;
         if (!warp_wait(&bars.s_full[X], sx & 1)) { fail(); ok = false; break; }
+        if (meta && j + 1 == tr.n_tiles) {
+          // this tile's last QK has completed: Q_X is free for the next task
+          const int2 nr = next_row[tid];
+          const char* src = reinterpret_cast<const char*>(
+              p.q + ((size_t)max(nr.x, 0) * p.num_q_heads + nr.y) * D);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c)
+            cp_async16(smem_u32(q_tile + (c / 8) * 16384 + sw128(m, c % 8)), src + c * 16,
+                       nr.x >= 0 ? 16u : 0u);
+          q_pref = true;
+        }
         tc_fence_after();
         const int bound = min(task.kv_end - t0, lim - t0 + 1);     // columns c < bound visible
         // the row's tree window [lim - 63, lim] reaches into this tile
@@ -403,6 +433,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[X]));
+        if (j == 0) {
+          // the next task's record, token and mask, read while the tensor
+          // core runs this tile's PV and the next QK
+          const int tn = snake_task(ti + 1, b, nctas);
+          if (tn < p.num_tasks) {
+            const pps::Task nt = p.tasks[tn];
+            const TileRange ntr = tile_range(nt, X, G);
+            const bool nreal = m < ntr.rows;
+            const int ni = r / G;
+            const int ntok = nreal ? p.rows[nt.row_off + ni] : -1;
+            next_row[tid] = make_int2(ntok, nt.kv_head * G + g);
+            next_mask[tid] = (p.tree_mask && nreal && nt.causal != PPS_NO_CAUSAL)
+                                 ? p.tree_mask[ntok] : ~0ull;
+            if (m == 0) next_task[X] = nt;
+            meta = true;
+          }
+        }
       }
       if (!ok) continue;                            // the next task barrier sees the abort
       // epilogue: O / l once the task's last PV on this tile is done
@@ -445,6 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (real && !direct) p.lse_part[prow] = l_sum > 0.f ? m_ref + __log2f(l_sum) : -INFINITY;
       tc_fence_before();       // the O reads finish before the next task's first PV
     }
+    cp_async_wait_all();       // a prefetched row of a task that never started
   } else if (warp == kProducerWarp) {
     // ------------------------------------------------------------- TMA producer
     // Lane 0 arms a stage's barrier with the tile's byte count, then one lane
