@@ -288,16 +288,18 @@ def measure_attention(name, args, dev, cpu_seconds):
     # made it (the CPU baseline starts from it).  Re-appending the same rows
     # every step is idempotent.
     pk, pv = wl.pool_k.clone(), wl.pool_v.clone()
+    flags = (pps.PLAN_FUSED_APPEND if args.fused_append else 0) | \
+        (pps.PLAN_SMALL_ROWS_CUDA_CORES if args.small_rows_cuda_cores else 0)
     steps = []
     for st in wl.steps:
         L = st.layout
         out = torch.empty_like(st.q)
         call = pps.StepCall(pk, pv, st.q, st.k_new, st.v_new, L.q_indptr, L.kv_len,
                             L.page_indptr, L.page_indices, out, tree_parent=L.tree_parent,
-                            flags=pps.PLAN_FUSED_APPEND if args.fused_append else 0)
+                            flags=flags)
         plan = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices, L.num_q_heads,
                              L.num_kv_heads, L.head_dim, L.page_size, L.num_pages,
-                             tree_parent=L.tree_parent)
+                             tree_parent=L.tree_parent, flags=flags & ~pps.PLAN_FUSED_APPEND)
         steps.append(dict(L=L, st=st, out=out, call=call, info=plan.info()))
         plan.destroy()
     stream = torch.cuda.current_stream()
@@ -396,7 +398,7 @@ def measure_attention(name, args, dev, cpu_seconds):
         out_h = torch.empty_like(s["out"], device="cpu").pin_memory()
         call = pps.StepCall(pk, pv, host["q"], host["k_new"], host["v_new"], L.q_indptr,
                             L.kv_len, L.page_indptr, L.page_indices, out_h,
-                            tree_parent=L.tree_parent, host=True)
+                            tree_parent=L.tree_parent, host=True, flags=flags)
         h.append(dict(host=host, out_h=out_h, call=call))
     tab_bytes = sum(4 * (3 * s["L"].num_requests + 2 + len(s["L"].page_indices)) for s in steps)
     bi = sum(v.numel() * v.element_size() for x in h for v in x["host"].values()) + tab_bytes
@@ -450,7 +452,9 @@ def measure_attention(name, args, dev, cpu_seconds):
                    "step_call": "pps_attn_step: one native call per step and chunk (tables "
                                 "uploaded, rows appended, batch planned on the host, attention)" +
                                 ("; append fused into the first attention kernel"
-                                 if args.fused_append else "")},
+                                 if args.fused_append else "") +
+                                ("; small-row tasks on the CUDA-core kernel"
+                                 if args.small_rows_cuda_cores else "")},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "ms_per_step": ms_e2e},
         "gpu_launches": launches,
@@ -1265,6 +1269,9 @@ def main():
     ap.add_argument("--flush-l2", default="auto", choices=["auto", "on", "off"],
                     help="re-time the kernels with an L2 flush before each step "
                          "(auto: when the unique KV is under 4x the L2 size)")
+    ap.add_argument("--small-rows-cuda-cores", action="store_true",
+                    help="small-row tasks on the CUDA-core split-KV kernel "
+                         "(PPS_PLAN_SMALL_ROWS_CUDA_CORES) instead of the key-tile kernel")
     ap.add_argument("--fused-append", action="store_true",
                     help="device-resident steps with the append inside the first attention "
                          "kernel (PPS_PLAN_FUSED_APPEND) instead of its own launch")
