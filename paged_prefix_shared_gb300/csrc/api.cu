@@ -72,7 +72,8 @@ bool can_fuse_append(const pps_plan* plan) {
 
 pps_status run_impl(const pps_plan* plan, const void* q, const pps_pool* pool, void* out,
                     void* workspace, size_t workspace_bytes, void* stream, void* const* events,
-                    RunPhase phase = kRunAll, const pps::AppendArgs* app = nullptr) {
+                    RunPhase phase = kRunAll, const pps::AppendArgs* app = nullptr,
+                    cudaEvent_t split_done = nullptr) {
   if (!plan || !pool || (plan->num_tokens > 0 && (!q || !out))) return PPS_ERR_INVALID_ARGUMENT;
   if (!pool_ok(pool)) return pool && (pool->head_dim != 64 && pool->head_dim != 128) ?
                                   PPS_ERR_UNSUPPORTED : PPS_ERR_INVALID_ARGUMENT;
@@ -131,10 +132,23 @@ pps_status run_impl(const pps_plan* plan, const void* q, const pps_pool* pool, v
     return PPS_ERR_CUDA;
   if (rec(2 * PPS_KERNEL_BANDWIDTH + 1) != cudaSuccess) return PPS_ERR_CUDA;
   if (rec(2 * PPS_KERNEL_TENSOR) != cudaSuccess) return PPS_ERR_CUDA;
-  if (plan->num_mma &&
-      pps::launch_mma_attention(s, t, plan->num_mma, q, *pool, out, err, stream,
-                                plan->num_bw == 0 ? app : nullptr))
+  if (split_done && plan->num_mma_first > 0 && !app) {
+    // output split: the tasks of the first requests, then (with `split_done`
+    // recorded between) the rest, so the first rows can leave while the
+    // rest are computed
+    pps::DeviceTables t2 = t;
+    t2.mma_tasks = t.mma_tasks + plan->num_mma_first;
+    if (pps::launch_mma_attention(s, t, plan->num_mma_first, q, *pool, out, err, stream,
+                                  nullptr) ||
+        cudaEventRecord(split_done, st) != cudaSuccess ||
+        pps::launch_mma_attention(s, t2, plan->num_mma - plan->num_mma_first, q, *pool, out, err,
+                                  stream, nullptr))
+      return PPS_ERR_CUDA;
+  } else if (plan->num_mma &&
+             pps::launch_mma_attention(s, t, plan->num_mma, q, *pool, out, err, stream,
+                                       plan->num_bw == 0 ? app : nullptr)) {
     return PPS_ERR_CUDA;
+  }
   if (rec(2 * PPS_KERNEL_TENSOR + 1) != cudaSuccess) return PPS_ERR_CUDA;
   if (rec(2 * PPS_KERNEL_MERGE) != cudaSuccess) return PPS_ERR_CUDA;
   if (pps::launch_merge(s, t, plan->num_merge_tokens, out, stream)) return PPS_ERR_CUDA;
@@ -354,6 +368,10 @@ struct RowCopier {
   cudaEvent_t free[2] = {nullptr, nullptr};
   bool used[2] = {false, false};
   uint64_t calls = 0;
+  // output split: the first requests' rows go back on `out` once their
+  // tensor-core launch is done (`split`), while the rest are computed
+  cudaStream_t out = nullptr;
+  cudaEvent_t split = nullptr, out_done = nullptr;
 };
 constexpr int kMaxCopiers = 32;
 std::mutex g_copier_mu;
@@ -377,19 +395,29 @@ RowCopier* row_copier(const void* scratch) {
       // the entry's own resources belong to its device; wait for what they fence
       int cur = dev;
       if (cudaSetDevice(c.dev) != cudaSuccess) return nullptr;
-      bool ok = cudaStreamSynchronize(c.copy) == cudaSuccess;
+      bool ok = cudaStreamSynchronize(c.copy) == cudaSuccess &&
+                cudaStreamSynchronize(c.out) == cudaSuccess;
       for (int i = 0; i < 2; ++i) ok = ok && cudaEventSynchronize(c.free[i]) == cudaSuccess;
       cudaStreamDestroy(c.copy);
+      cudaStreamDestroy(c.out);
       for (int i = 0; i < 2; ++i) { cudaEventDestroy(c.in[i]); cudaEventDestroy(c.free[i]); }
+      cudaEventDestroy(c.split);
+      cudaEventDestroy(c.out_done);
       c = RowCopier{};
       if (cudaSetDevice(cur) != cudaSuccess || !ok) return nullptr;
     }
-    bool ok = cudaStreamCreateWithFlags(&c.copy, cudaStreamNonBlocking) == cudaSuccess;
+    bool ok = cudaStreamCreateWithFlags(&c.copy, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&c.split, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&c.out_done, cudaEventDisableTiming) == cudaSuccess;
     for (int i = 0; i < 2; ++i)
       ok = ok && cudaEventCreateWithFlags(&c.in[i], cudaEventDisableTiming) == cudaSuccess &&
            cudaEventCreateWithFlags(&c.free[i], cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
       if (c.copy) cudaStreamDestroy(c.copy);
+      if (c.out) cudaStreamDestroy(c.out);
+      if (c.split) cudaEventDestroy(c.split);
+      if (c.out_done) cudaEventDestroy(c.out_done);
       for (int i = 0; i < 2; ++i) {
         if (c.in[i]) cudaEventDestroy(c.in[i]);
         if (c.free[i]) cudaEventDestroy(c.free[i]);
@@ -448,10 +476,20 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
   const size_t rows = rows_on_host ? 2 * slot_bytes + al(q_bytes) : 0;
   const size_t off_k = al(q_bytes), off_v = off_k + al(kv_bytes), off_out = 2 * slot_bytes,
                off_tab = rows, off_ws = off_tab + al(tab_ints * 4);
+  // Host rows with a large output from several requests: the planner puts
+  // the tensor-core tasks of the first half of the tokens' requests first, so
+  // those rows can go back to the host while the rest are computed (the
+  // device-to-host copy after the kernels is otherwise the one part of a
+  // host-row step nothing overlaps).
+  int32_t split_req = 0;
+  if (rows_on_host && R >= 2 && T > 0 && q_bytes >= ((size_t)16 << 20)) {
+    split_req = 1;
+    while (split_req < R - 1 && h_q_indptr[split_req] < T / 2) ++split_req;
+  }
   auto plan_for = [&](pps_plan** pl, size_t* ws) {
-    return pps_attn_plan_tree(h_q_indptr, h_kv_len, h_page_indptr, h_page_indices, h_tree_parent,
-                              R, num_q_heads, pool->num_kv_heads, pool->head_dim, pool->page_size,
-                              pool->num_pages, sm_scale, opts, pl, ws);
+    return pps::plan_tree(h_q_indptr, h_kv_len, h_page_indptr, h_page_indices, h_tree_parent, R,
+                          num_q_heads, pool->num_kv_heads, pool->head_dim, pool->page_size,
+                          pool->num_pages, sm_scale, opts, split_req, pl, ws);
   };
   if (!d_scratch || scratch_bytes < off_ws || ((uintptr_t)d_scratch & 255)) {
     // report the whole size (rows, tables and the plan's workspace); nothing enqueued
@@ -567,17 +605,33 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
   if (ok && st == PPS_OK && !fused)
     st = pps_kv_append(pool, dk, dv, d_tab, d_tab + R + 1, d_tab + 2 * R + 1, d_tab + 3 * R + 2,
                        R, T, stream);
+  const bool split_out = rows_on_host && !out_direct && !fused && plan->num_mma_first > 0;
   if (ok && st == PPS_OK)
     st = run_impl(plan, dq, pool, dout, sc + off_ws, al(ws_bytes), stream, events, kRunKernels,
-                  fused ? &app : nullptr);
+                  fused ? &app : nullptr, split_out ? rc->split : nullptr);
   if (rows_on_host) {
     // the slot may be written again once this step's kernels have read it
     std::lock_guard<std::mutex> lk(g_copier_mu);
     if (cudaEventRecord(rc->free[slot], stm) == cudaSuccess) rc->used[slot] = true;
     else ok = false;
   }
-  if (ok && st == PPS_OK && rows_on_host && T > 0 && !out_direct)
-    ok = cudaMemcpyAsync(out, sc + off_out, q_bytes, cudaMemcpyDeviceToHost, stm) == cudaSuccess;
+  if (ok && st == PPS_OK && rows_on_host && T > 0 && !out_direct) {
+    if (split_out) {
+      // rows [0, split_tokens) on the copier's output stream once their launch
+      // has finished; the stream reaches the end of this step after both copies
+      const size_t b1 = (size_t)plan->split_tokens * num_q_heads * D * 2;
+      std::lock_guard<std::mutex> lk(g_copier_mu);
+      ok = cudaStreamWaitEvent(rc->out, rc->split, 0) == cudaSuccess &&
+           cudaMemcpyAsync(out, sc + off_out, b1, cudaMemcpyDeviceToHost, rc->out) ==
+               cudaSuccess &&
+           cudaEventRecord(rc->out_done, rc->out) == cudaSuccess &&
+           cudaMemcpyAsync((char*)out + b1, sc + off_out + b1, q_bytes - b1,
+                           cudaMemcpyDeviceToHost, stm) == cudaSuccess &&
+           cudaStreamWaitEvent(stm, rc->out_done, 0) == cudaSuccess;
+    } else {
+      ok = cudaMemcpyAsync(out, sc + off_out, q_bytes, cudaMemcpyDeviceToHost, stm) == cudaSuccess;
+    }
+  }
   pps_plan_destroy(plan);
   if (!ok) return PPS_ERR_CUDA;
   return st;

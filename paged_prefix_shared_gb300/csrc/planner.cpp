@@ -124,6 +124,18 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
                                          int32_t head_dim, int32_t page_size, int32_t num_pages,
                                          float sm_scale, const pps_plan_options* opts,
                                          pps_plan** out_plan, size_t* out_workspace_bytes) {
+  return pps::plan_tree(q_indptr, kv_len, page_indptr, page_indices, tree_parent, num_requests,
+                        num_q_heads, num_kv_heads, head_dim, page_size, num_pages, sm_scale, opts,
+                        0, out_plan, out_workspace_bytes);
+}
+
+pps_status pps::plan_tree(const int32_t* q_indptr, const int32_t* kv_len,
+                          const int32_t* page_indptr, const int32_t* page_indices,
+                          const int32_t* tree_parent, int32_t num_requests, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                          int32_t num_pages, float sm_scale, const pps_plan_options* opts,
+                          int32_t split_request, pps_plan** out_plan,
+                          size_t* out_workspace_bytes) {
   if (out_plan) *out_plan = nullptr;
   if (out_workspace_bytes) *out_workspace_bytes = 0;
   if (!out_plan || !out_workspace_bytes || num_requests < 0 || !q_indptr || !page_indptr ||
@@ -448,7 +460,14 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
 
     // ---- 5. sort by work (descending), deterministic ties ---------------------------
     // Order: bandwidth before tensor-core sets, then work descending, then
-    // (key, tile, chunk), which identify a set, so the order is total.
+    // (key, tile, chunk), which identify a set, so the order is total.  A
+    // split request puts the tensor-core sets of the requests before it first
+    // (each half in work order), when the split can hold: tensor-core sets
+    // only, every one private to a request (no shared-prefix group), no
+    // partials.
+    bool split = split_request > 0 && split_request < R;
+    for (size_t k = 0; split && k < sets.size(); ++k)
+      split = sets[k].mma && sets[k].key < R && direct[k];
     {
       struct SortKey {
         uint64_t a, b;
@@ -457,7 +476,9 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
       std::vector<SortKey> keys(sets.size());
       for (size_t k = 0; k < sets.size(); ++k) {
         const TaskSet& t = sets[k];
-        keys[k].a = ((uint64_t)t.mma << 63) | (((uint64_t)1 << 62) - 1 - (uint64_t)t.work);
+        const uint64_t late = split && t.key >= split_request ? 1 : 0;
+        keys[k].a = ((uint64_t)t.mma << 63) | (late << 62) |
+                    (((uint64_t)1 << 61) - 1 - (uint64_t)t.work);
         keys[k].b = ((uint64_t)(uint32_t)t.key << 32) | (uint32_t)t.tile;
         keys[k].c = (uint32_t)t.chunk;
         keys[k].idx = (uint32_t)k;
@@ -623,6 +644,14 @@ extern "C" pps_status pps_attn_plan_tree(const int32_t* q_indptr, const int32_t*
 
     plan->num_bw = (int64_t)bw.size();
     plan->num_mma = (int64_t)mm.size();
+    if (split) {
+      int64_t first = 0;
+      for (const auto& ts : sets) first += ts.key < split_request ? num_kv_heads : 0;
+      if (first > 0 && first < plan->num_mma) {
+        plan->num_mma_first = first;
+        plan->split_tokens = q_indptr[split_request];
+      }
+    }
     plan->num_partials = next_pid;
     plan->num_merge_tokens = (int64_t)m_tok.size();
     plan->num_merge_pids = (int64_t)m_pid.size();

@@ -97,12 +97,31 @@ int host_buf_mark_use(const HostBuf& b, void* stream);
 
 }  // namespace pps
 
+namespace pps {
+// pps_attn_plan_tree, with the tensor-core tasks of requests [0, split_request)
+// ordered first when split_request > 0 and the batch allows an output split
+// (tensor-core tasks only, no shared-prefix groups, no partials); see
+// pps_plan::num_mma_first.
+pps_status plan_tree(const int32_t* q_indptr, const int32_t* kv_len, const int32_t* page_indptr,
+                     const int32_t* page_indices, const int32_t* tree_parent,
+                     int32_t num_requests, int32_t num_q_heads, int32_t num_kv_heads,
+                     int32_t head_dim, int32_t page_size, int32_t num_pages, float sm_scale,
+                     const pps_plan_options* opts, int32_t split_request, pps_plan** out_plan,
+                     size_t* out_workspace_bytes);
+}  // namespace pps
+
 struct pps_plan {
   pps::Shape shape;
   int32_t num_requests = 0;
   int32_t num_tokens = 0;
   int32_t num_groups = 0;
   int64_t num_bw = 0, num_mma = 0, num_partials = 0, num_merge_tokens = 0, num_merge_pids = 0;
+  // Output split (plans made with a split request only): the first
+  // num_mma_first tensor-core tasks hold every row of the requests before
+  // split_request and nothing else, so those rows (tokens [0, split_tokens))
+  // are final once a launch over just those tasks has completed.  0: no split.
+  int64_t num_mma_first = 0;
+  int32_t split_tokens = 0;
   int64_t num_rows = 0, num_pages_listed = 0;
   int32_t num_tree_requests = 0;   // requests with a non-chain draft tree
   bool has_tree = false;           // table holds the per-token tree masks

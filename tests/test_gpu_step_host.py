@@ -181,3 +181,37 @@ def test_step_with_large_task_table(pps):
         assert torch.equal(out.cpu().view(torch.int16), outs[0].cpu().view(torch.int16)), host
         assert torch.equal(pk2.view(torch.int16), pk.view(torch.int16))
         assert torch.equal(pv2.view(torch.int16), pv.view(torch.int16))
+
+
+def test_step_host_split_output_copy(pps):
+    """Host-row prefill steps whose output (over 16 MB, several requests, only
+    tensor-core tasks, no groups, no partials) goes back in two parts: the
+    first requests' rows leave after a tensor-core launch over just their
+    tasks, the rest after the second.  Outputs and pool must match the
+    separate calls bit for bit, steps enqueued back to back."""
+    import workloads
+    wl = workloads.long_prefill(num_requests=4, chunk=640, num_chunks=3, num_q_heads=32,
+                                num_kv_heads=8, head_dim=128, page_size=64, keep_segments=False)
+    for st in wl.steps:
+        L = st.layout
+        assert st.q.numel() * 2 >= 16 << 20
+        info = pps.attn_plan(L.q_indptr, L.kv_len, L.page_indptr, L.page_indices, L.num_q_heads,
+                             L.num_kv_heads, L.head_dim, L.page_size, L.num_pages).info()
+        assert info["num_bw_tasks"] == 0 and info["num_merge_tokens"] == 0
+        assert info["num_groups"] == 0
+    dev_in = to_device(wl)
+    outs, (pk, pv), _ = run_workload(wl, device_inputs=dev_in)
+    pk2, pv2 = wl.pool_k.to("cuda", copy=True), wl.pool_v.to("cuda", copy=True)
+    rows = [_host_rows(st) for st in wl.steps]
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    pps.get_device_error(clear=True)
+    for st, (q, k, v, out) in zip(wl.steps, rows):
+        L = st.layout
+        pps.attn_step_host(pk2, pv2, q, k, v, L.q_indptr, L.kv_len, L.page_indptr, L.page_indices,
+                           out, scratch=scratch)
+    torch.cuda.synchronize()
+    assert pps.get_device_error(clear=True) == 0
+    for s, (_, _, _, out) in enumerate(rows):
+        assert torch.equal(out.view(torch.int16), outs[s].cpu().view(torch.int16)), s
+    assert torch.equal(pk2.view(torch.int16), pk.view(torch.int16))
+    assert torch.equal(pv2.view(torch.int16), pv.view(torch.int16))
