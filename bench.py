@@ -618,8 +618,9 @@ class CacheServer:
         return self._run_batch(kv_len, cached, page_indptr, page_indices, copies, events)
 
     def _run_batch(self, kv_len, cached, page_indptr, page_indices, copies, events=None):
-        """Device side of a step: copy-on-write copies, kv_append of positions
-        [cached, kv_len) of every request, attn_plan and attn_run."""
+        """Device side of a step: copy-on-write copies, then one pps_attn_step
+        call (append of positions [cached, kv_len) of every request, plan,
+        attention), or in the end-to-end run one pps_attn_step_host call."""
         import numpy as np
         torch, pps = self.torch, self.pps
         R = len(kv_len)
@@ -639,44 +640,48 @@ class CacheServer:
             used |= {c[0], c[1]}
         if cur:
             waves.append(cur)
-        # one upload of every table of the step
-        parts = [q_indptr, cached, page_indptr, page_indices] + \
-            [np.array(w, np.int32).T.reshape(-1) for w in waves]
-        sizes = [len(a) for a in parts]
-        flat = np.concatenate(parts).astype(np.int32)
-        hb = self.nstep & 1
-        self.nstep += 1
-        if self.h_ev[hb] is not None:
-            self.h_ev[hb].synchronize()
-        self.h_tab[hb][:len(flat)].copy_(torch.from_numpy(flat))
-        self.d_tab[:len(flat)].copy_(self.h_tab[hb][:len(flat)], non_blocking=True)
-        self.h_ev[hb] = torch.cuda.Event()
-        self.h_ev[hb].record()
-        views, off = [], 0
-        for n in sizes:
-            views.append(self.d_tab[off:off + n])
-            off += n
-        d_qi, d_cached, d_pi, d_px = views[:4]
-        for w, v in zip(waves, views[4:]):
-            n = len(w)
-            pps.copy_slots(self.pk, self.pv, v[:n], v[n:2 * n], v[2 * n:3 * n])
+        # the copy-on-write tables in one upload (the step call uploads its own)
+        if waves:
+            parts = [np.array(w, np.int32).T.reshape(-1) for w in waves]
+            flat = np.concatenate(parts).astype(np.int32)
+            hb = self.nstep & 1
+            self.nstep += 1
+            if self.h_ev[hb] is not None:
+                self.h_ev[hb].synchronize()
+            self.h_tab[hb][:len(flat)].copy_(torch.from_numpy(flat))
+            self.d_tab[:len(flat)].copy_(self.h_tab[hb][:len(flat)], non_blocking=True)
+            self.h_ev[hb] = torch.cuda.Event()
+            self.h_ev[hb].record()
+            off = 0
+            for w, a in zip(waves, parts):
+                n = len(w)
+                v = self.d_tab[off:off + 3 * n]
+                pps.copy_slots(self.pk, self.pv, v[:n], v[n:2 * n], v[2 * n:3 * n])
+                off += len(a)
         if self.io is not None:
+            # end to end: the step's rows from page-locked host memory and its
+            # output rows back, through the one-call host-row step
             hq, hk, hv, ho = self.io
-            self.q[:T].copy_(hq[:T], non_blocking=True)
-            self.rows_k[:T].copy_(hk[:T], non_blocking=True)
-            self.rows_v[:T].copy_(hv[:T], non_blocking=True)
-        pps.kv_append(self.pk, self.pv, self.rows_k[:T], self.rows_v[:T], d_qi, d_cached, d_pi,
-                      d_px)
+            t1 = time.perf_counter()
+            pps.attn_step_host(self.pk, self.pv, hq[:T], hk[:T], hv[:T], q_indptr, kv_len,
+                               page_indptr, page_indices, ho[:T])
+            self.host_s += time.perf_counter() - t1
+            return T, R, None, len(copies)
+        # the step's append, plan and attention: one pps_attn_step call; the
+        # tables are kept so the plan's figures for the roofline can be taken
+        # after the timed loop
         t1 = time.perf_counter()
-        plan = pps.attn_plan(q_indptr, kv_len, page_indptr, page_indices, self.Hq, self.Hkv,
-                             self.D, self.P, self.num_pages)
+        pps.attn_step(self.pk, self.pv, self.q[:T], self.rows_k[:T], self.rows_v[:T], q_indptr,
+                      kv_len, page_indptr, page_indices, self.out[:T], scratch=self.ws,
+                      events=events)
         self.host_s += time.perf_counter() - t1
-        if plan.workspace_bytes > self.ws.numel():
-            raise RuntimeError("workspace buffer too small")
-        pps.attn_run(plan, self.q[:T], self.pk, self.pv, self.out[:T], self.ws, events=events)
-        if self.io is not None:
-            self.io[3][:T].copy_(self.out[:T], non_blocking=True)
-        return T, R, plan.info(), len(copies)
+        return T, R, (q_indptr, kv_len.copy(), page_indptr.copy(), page_indices.copy()), \
+            len(copies)
+
+    def plan_info(self, tables):
+        q_indptr, kv_len, page_indptr, page_indices = tables
+        return self.pps.attn_plan(q_indptr, kv_len, page_indptr, page_indices, self.Hq, self.Hkv,
+                                  self.D, self.P, self.num_pages).info()
 
 
 class EngineServer(CacheServer):
@@ -826,7 +831,8 @@ def run_cache_serving(args):
     kern_ms = [sum(ev[k][2 * c].elapsed_time(ev[k][2 * c + 1]) for k in range(args.steps))
                / args.steps for c in range(nk)]
 
-    # e2e: the step's Q/K/V rows come from pinned host memory, outputs go back
+    # e2e: the step's Q/K/V rows come from pinned host memory, outputs go back,
+    # one pps_attn_step_host call per step (after the step's copy-on-write copies)
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype).pin_memory().copy_(t.cpu())
     srv.io = (pin(srv.q), pin(srv.rows_k), pin(srv.rows_v),
               torch.empty(srv.out.shape, dtype=srv.out.dtype).pin_memory())
@@ -848,6 +854,7 @@ def run_cache_serving(args):
     ms_e2e = max_over_ranks(f0.elapsed_time(f1) / k_e2e, world, dev)
     e2e_value = sum_over_ranks(tok_e2e, world, dev) / (ms_e2e * k_e2e / 1e3)
 
+    infos = [srv.plan_info(t) for t in infos]        # the timed steps' plans, planned again
     avg = lambda key: sum(i[key] for i in infos) / len(infos)
     avg_infos = [{k: avg(k) for k in ("kv_bytes_unique", "kv_bytes_bw", "flops_mma", "small_rows_on_tensor",
                                       "kv_bytes_read", "flops_total")}]
