@@ -19,10 +19,11 @@ the projection GEMMs).
 ``value`` is tokens/s with inputs resident in HBM; ``e2e`` is the same metric
 with every step's inputs copied from pinned host memory and the output copied
 back inside the timed region: one ``pps_attn_step_host`` call per batch (host
-rows and tables in, host rows out; for the serving loops, the same copies
-around the device calls).  Under torchrun each rank runs its own batch (weak
-scaling, no data-path collective).  ``--impl reference`` times the fp64 CPU
-oracle on a bounded sample instead.
+rows and tables in, host rows out; the serving loops make the same call after
+each step's cache or engine calls; the projection GEMMs copy their activations
+in and outputs out around the GEMM calls).  Under torchrun each rank runs its
+own batch (weak scaling, no data-path collective).  ``--impl reference`` times
+the fp64 CPU oracle on a bounded sample instead.
 """
 from __future__ import annotations
 
