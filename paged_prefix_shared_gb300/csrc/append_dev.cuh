@@ -17,6 +17,26 @@
 
 namespace pps_dev {
 
+// The request of new token t, the last r with q_indptr[r] <= t (empty requests
+// have equal consecutive offsets, so this is the one that holds t), found by a
+// whole warp: each round its 32 lanes probe 32 evenly spaced offsets at once
+// and the range shrinks 32-fold, so a 256-request batch takes 2 dependent
+// loads instead of the 8 of a one-thread bisection.  The caller has checked
+// q_indptr[0] <= t < q_indptr[num_requests]; every lane gets the answer.
+__device__ __forceinline__ int request_of_token(const int32_t* q_indptr, int num_requests,
+                                                int t, int lane) {
+  int lo = 0, hi = num_requests;                    // q_indptr[lo] <= t < q_indptr[hi]
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) >> 5;
+    const int probe = lo + (lane + 1) * step;
+    const bool le = probe < hi && __ldg(q_indptr + probe) <= t;
+    const int c = __popc(__ballot_sync(0xffffffffu, le));   // probes <= t: a prefix of lanes
+    hi = min(hi, lo + (c + 1) * step);
+    lo += c * step;
+  }
+  return lo;
+}
+
 // One warp per (new token, kv head) item, items strided over every warp of the
 // grid; the caller's `nwarps` warps of this CTA take part (warps 0..nwarps-1).
 template <int D>
@@ -36,12 +56,7 @@ __device__ __noinline__ void append_rows(const pps::AppendArgs& a, int4* pool_k,
       if (lane == 0) atomicCAS(err, 0, PPS_DEV_ERR_APPEND_REQUEST);
       continue;
     }
-    int lo = 0, hi = a.num_requests;                 // q_indptr[lo] <= t < q_indptr[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (a.q_indptr[mid] <= t) lo = mid; else hi = mid;
-    }
-    const int r = lo;
+    const int r = request_of_token(a.q_indptr, a.num_requests, t, lane);
     const int p = a.cached_len[r] + (t - a.q_indptr[r]);
     const int pi = p / page_size;
     if (p < 0 || pi >= a.page_indptr[r + 1] - a.page_indptr[r]) {

@@ -11,6 +11,7 @@
 
 #include "pps_internal.h"
 #include "sm100_ptx.cuh"
+#include "append_dev.cuh"
 
 namespace {
 
@@ -35,16 +36,11 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
   const int h = warp - t * num_kv_heads;
   if (t >= num_tokens) return;
   // request of token t: last r with q_indptr[r] <= t
-  int lo = 0, hi = num_requests;                    // invariant: q_indptr[lo] <= t < q_indptr[hi]
   if (q_indptr[0] > t || q_indptr[num_requests] <= t) {
     if (lane == 0) set_error(err, PPS_DEV_ERR_APPEND_REQUEST);
     return;
   }
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (q_indptr[mid] <= t) lo = mid; else hi = mid;
-  }
-  const int r = lo;
+  const int r = pps_dev::request_of_token(q_indptr, num_requests, t, lane);
   const int p = cached_len[r] + (t - q_indptr[r]);
   const int pi = p / page_size;
   const int npg = page_indptr[r + 1] - page_indptr[r];
