@@ -586,10 +586,11 @@ pps_status pps_plan_get_array(const pps_plan* plan, int32_t which, const int32_t
 /*
  * pps_attn_step -- one whole step with the rows already on the device and the
  * tables on the host: the tables are uploaded (through a page-locked staging
- * buffer) into d_scratch, the new K/V rows appended (pps_kv_append), the batch
- * planned (pps_attn_plan_tree) and attended (pps_attn_run, or
- * pps_attn_run_events when `events` is not NULL).  The same operations as the
- * three device-side calls, in one native call per step.
+ * buffer) into d_scratch, the new K/V rows appended (the pps_kv_append
+ * scatter, each new token's page and slot taken on the host from the tables
+ * the plan has checked), the batch planned (pps_attn_plan_tree) and attended
+ * (pps_attn_run, or pps_attn_run_events when `events` is not NULL).  The same
+ * operations as the three device-side calls, in one native call per step.
  *
  *  q, k_new, v_new, out  device bf16 rows as for pps_kv_append / pps_attn_run.
  *  host tables, scratch, errors: as pps_attn_step_host (its scratch holds only

@@ -470,7 +470,10 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
   const size_t kv_bytes = (size_t)T * pool->num_kv_heads * D * 2;
   const int64_t nnz = R > 0 ? h_page_indptr[R] : 0;
   if (nnz < 0 || (nnz > 0 && !h_page_indices)) return PPS_ERR_INVALID_ARGUMENT;
-  const size_t tab_ints = (size_t)(R + 1) + R + (R + 1) + (size_t)nnz;
+  // tables: q_indptr, cached_len, page_indptr, page_indices, then (8-byte
+  // aligned) each new token's {page, slot} for the append
+  const size_t slots_off = ((size_t)(R + 1) + R + (R + 1) + (size_t)nnz + 1) & ~(size_t)1;
+  const size_t tab_ints = slots_off + 2 * (size_t)T;
   // host rows: two input slots (q, k, v each) and one output area
   const size_t slot_bytes = al(q_bytes) + 2 * al(kv_bytes);
   const size_t rows = rows_on_host ? 2 * slot_bytes + al(q_bytes) : 0;
@@ -585,6 +588,22 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
   for (int32_t r = 0; r < R; ++r) t[R + 1 + r] = h_kv_len[r] - (h_q_indptr[r + 1] - h_q_indptr[r]);
   if (R > 0) std::memcpy(t + 2 * R + 1, h_page_indptr, (size_t)(R + 1) * 4);
   if (nnz) std::memcpy(t + 3 * R + 2, h_page_indices, (size_t)nnz * 4);
+  // every new token's destination; the plan has checked the page lists
+  // (long enough for kv_len, ids in range)
+  {
+    const int32_t P = pool->page_size;
+    int32_t* ds = t + slots_off;
+    for (int32_t r = 0; r < R; ++r) {
+      const int32_t q0 = h_q_indptr[r], c = h_kv_len[r] - (h_q_indptr[r + 1] - q0);
+      const int32_t* pl = h_page_indices + h_page_indptr[r];
+      for (int32_t j = q0; j < h_q_indptr[r + 1]; ++j) {
+        const int32_t pos = c + (j - q0);
+        ds[2 * (size_t)j] = pl[pos / P];
+        ds[2 * (size_t)j + 1] = pos % P;
+      }
+    }
+    if (slots_off > (size_t)(3 * R + 2) + (size_t)nnz) t[slots_off - 1] = 0;   // the pad word
+  }
   if (one_copy) {
     std::memset(t + tab_ints, 0, tab_span - tab_ints * 4);
     std::memcpy(t + tab_span / 4, plan->image.data, img_bytes);
@@ -602,9 +621,11 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
                             R, T};
   if (ok && !one_copy)
     st = run_impl(plan, dq, pool, dout, sc + off_ws, al(ws_bytes), stream, events, kRunUpload);
-  if (ok && st == PPS_OK && !fused)
-    st = pps_kv_append(pool, dk, dv, d_tab, d_tab + R + 1, d_tab + 2 * R + 1, d_tab + 3 * R + 2,
-                       R, T, stream);
+  if (ok && st == PPS_OK && !fused && T > 0) {
+    if (((uintptr_t)dk & 15) || ((uintptr_t)dv & 15)) st = PPS_ERR_INVALID_ARGUMENT;
+    else if (pps::launch_kv_append_slots(*pool, dk, dv, d_tab + slots_off, T, stream))
+      st = PPS_ERR_CUDA;
+  }
   const bool split_out = rows_on_host && !out_direct && !fused && plan->num_mma_first > 0;
   if (ok && st == PPS_OK)
     st = run_impl(plan, dq, pool, dout, sc + off_ws, al(ws_bytes), stream, events, kRunKernels,

@@ -65,6 +65,29 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
   }
 }
 
+// The same scatter with each new token's (page, slot) computed on the host from
+// the step's checked tables (the step calls): one warp per (token, kv head),
+// one dependent load before the copy instead of a request search and two
+// table lookups.
+template <int D>
+__global__ void __launch_bounds__(256) kv_append_slots_kernel(
+    int4* __restrict__ pool_k, int4* __restrict__ pool_v, const int4* __restrict__ k_new,
+    const int4* __restrict__ v_new, const int2* __restrict__ dst_slots, int32_t num_tokens,
+    int32_t num_kv_heads, int32_t page_size) {
+  constexpr int kVec = D * 2 / 16;
+  sm100::grid_dep_launch();
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int t = warp / num_kv_heads;
+  const int h = warp - t * num_kv_heads;
+  if (t >= num_tokens) return;
+  const int2 ps = __ldg(dst_slots + t);              // {page, slot}
+  const size_t dst = (((size_t)ps.x * num_kv_heads + h) * page_size + ps.y) * kVec;
+  const size_t src = ((size_t)t * num_kv_heads + h) * kVec;
+  if (lane < kVec) pool_k[dst + lane] = __ldg(k_new + src + lane);
+  else if (lane < 2 * kVec) pool_v[dst + lane - kVec] = __ldg(v_new + src + lane - kVec);
+}
+
 // Copy-on-write of a partly reused page: slots [0, n) of every kv head of page
 // src go to the same slots of page dst (K and V), one warp per (copy, kv head,
 // slot).  A page id out of range or a slot count outside [0, page_size] is
@@ -113,6 +136,22 @@ int launch_copy_slots(const pps_pool& pool, const int32_t* src_pages, const int3
     copy_slots_kernel<64><<<(unsigned)blocks, threads, 0, s>>>(
         (int4*)pool.k, (int4*)pool.v, src_pages, dst_pages, num_slots, count, pool.num_kv_heads,
         pool.page_size, pool.num_pages, err);
+  count_launch();
+  return (int)cudaGetLastError();
+}
+
+int launch_kv_append_slots(const pps_pool& pool, const void* k_new, const void* v_new,
+                           const int32_t* dst_slots, int32_t num_new_tokens, void* stream) {
+  const int64_t warps = (int64_t)num_new_tokens * pool.num_kv_heads;
+  if (warps == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (warps * 32 + threads - 1) / threads;
+  auto s = (cudaStream_t)stream;
+  auto kern = pool.head_dim == 128 ? kv_append_slots_kernel<128> : kv_append_slots_kernel<64>;
+  kern<<<(unsigned)blocks, threads, 0, s>>>((int4*)pool.k, (int4*)pool.v, (const int4*)k_new,
+                                            (const int4*)v_new,
+                                            reinterpret_cast<const int2*>(dst_slots),
+                                            num_new_tokens, pool.num_kv_heads, pool.page_size);
   count_launch();
   return (int)cudaGetLastError();
 }

@@ -146,6 +146,9 @@ namespace pps {
 
 // Kernel launchers (defined in the .cu files).  All return cudaSuccess (0) or
 // the launch error.  `err` is the device error word of the current device.
+// dst_slots: device int32 pairs {page, slot} per new token (8-byte aligned).
+int launch_kv_append_slots(const pps_pool& pool, const void* k_new, const void* v_new,
+                           const int32_t* dst_slots, int32_t num_new_tokens, void* stream);
 int launch_kv_append(const pps_pool& pool, const void* k_new, const void* v_new,
                      const int32_t* q_indptr, const int32_t* cached_len,
                      const int32_t* page_indptr, const int32_t* page_indices,
