@@ -619,7 +619,7 @@ pps_status pps_attn_step(const pps_pool* pool, const void* q, const void* k_new,
 /*
  * pps_attn_step_host -- one whole step from host memory: the step's new K/V
  * rows, query rows and tables are copied to device scratch, the K/V rows are
- * appended to the pool (pps_kv_append), the batch is planned (pps_attn_plan_tree
+ * appended to the pool (as in pps_attn_step), the batch is planned (pps_attn_plan_tree
  * on the host tables) and attended (pps_attn_run), and the output rows are
  * copied back.  The same operations as the device-side calls, in one native
  * call, for a caller that keeps its batch on the host (the XY-Serve review's
