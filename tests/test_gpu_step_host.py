@@ -215,3 +215,28 @@ def test_step_host_split_output_copy(pps):
         assert torch.equal(out.view(torch.int16), outs[s].cpu().view(torch.int16)), s
     assert torch.equal(pk2.view(torch.int16), pk.view(torch.int16))
     assert torch.equal(pv2.view(torch.int16), pv.view(torch.int16))
+
+
+def test_step_host_many_scratch_buffers(pps):
+    """The library keeps copy streams and slot events for up to 32 scratch
+    buffers and retires the least recently used one (after the work it fences)
+    when another comes: 40 steps, each with a scratch of its own, all kept
+    alive so every address is new, give the separate calls' output each time."""
+    wl = small_cases()["decode_heavy"]()
+    st = wl.steps[0]
+    L = st.layout
+    dev_in = to_device(wl)
+    outs, _, _ = run_workload(wl, device_inputs=dev_in)
+    q, k, v, _ = _host_rows(st)
+    keep = []
+    for i in range(40):
+        pk, pv = wl.pool_k.to("cuda", copy=True), wl.pool_v.to("cuda", copy=True)
+        out = torch.full(tuple(st.q.shape), float("nan"), dtype=torch.bfloat16).pin_memory()
+        scratch = torch.empty(8 << 20, dtype=torch.uint8, device="cuda")
+        keep.append((pk, pv, out, scratch))
+        pps.attn_step_host(pk, pv, q, k, v, L.q_indptr, L.kv_len, L.page_indptr,
+                           L.page_indices, out, scratch=scratch)
+    torch.cuda.synchronize()
+    assert pps.get_device_error(clear=True) == 0
+    for i, (_, _, out, _) in enumerate(keep):
+        assert torch.equal(out.view(torch.int16), outs[0].cpu().view(torch.int16)), i
