@@ -642,7 +642,7 @@ pps_status pps_attn_step(const pps_pool* pool, const void* q, const void* k_new,
  *                        kernels.  When the output exceeds 16 MB, comes from
  *                        two or more requests and only tensor-core tasks with
  *                        no partials compute it, the tasks of the requests
- *                        holding the first half of the tokens run in a launch
+ *                        holding the first three quarters of the tokens run in a launch
  *                        of their own and their rows travel back (on a
  *                        stream of the library's own) while the rest are
  *                        computed; `stream` waits for that copy at the end
