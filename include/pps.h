@@ -639,14 +639,14 @@ pps_status pps_attn_step(const pps_pool* pool, const void* q, const void* k_new,
  *                        tiles write at most half of the rows, the step's
  *                        kernels write it directly and no copy follows them;
  *                        otherwise the rows come back by copies after the
- *                        kernels.  When the output exceeds 16 MB, comes from
- *                        two or more requests and only tensor-core tasks with
- *                        no partials compute it, the tasks of the requests
- *                        holding the first three quarters of the tokens run in a launch
- *                        of their own and their rows travel back (on a
- *                        stream of the library's own) while the rest are
- *                        computed; `stream` waits for that copy at the end
- *                        of the step.
+ *                        kernels.  When h_out is page-locked, the output
+ *                        exceeds 16 MB and comes from two or more requests,
+ *                        all on tensor-core tasks with no partials, the tasks
+ *                        of the requests holding the first three quarters of
+ *                        the tokens run in a launch of their own and their
+ *                        rows travel back (on a stream of the library's own)
+ *                        while the rest are computed; `stream` waits for that
+ *                        copy at the end of the step.
  *  d_scratch             device, 256-byte aligned, scratch_bytes long; the size
  *                        it needs is written to *out_scratch_bytes (may be NULL).
  *                        It holds two slots of input rows taken in turn, room

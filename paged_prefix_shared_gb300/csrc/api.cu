@@ -485,13 +485,17 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
   // are computed (the device-to-host copy after the kernels is otherwise the
   // one part of a host-row step nothing overlaps; a long-prefill step measured
   // 35.1-35.8 ms with the split at half the tokens, 34.3-35.6 at three
-  // quarters, 37.1-38.1 without).
-  int32_t split_req = 0;
-  if (rows_on_host && R >= 2 && T > 0 && q_bytes >= ((size_t)16 << 20)) {
-    split_req = 1;
-    while (split_req < R - 1 && h_q_indptr[split_req] < T / 4 * 3) ++split_req;
-  }
-  auto plan_for = [&](pps_plan** pl, size_t* ws) {
+  // quarters, 37.1-38.1 without).  Page-locked output only: a copy into
+  // pageable memory would hold the host until the first launch is done.
+  auto split_request = [&](bool locked_out) {
+    int32_t r1 = 0;
+    if (rows_on_host && locked_out && R >= 2 && T > 0 && q_bytes >= ((size_t)16 << 20)) {
+      r1 = 1;
+      while (r1 < R - 1 && h_q_indptr[r1] < T / 4 * 3) ++r1;
+    }
+    return r1;
+  };
+  auto plan_for = [&](pps_plan** pl, size_t* ws, int32_t split_req) {
     return pps::plan_tree(h_q_indptr, h_kv_len, h_page_indptr, h_page_indices, h_tree_parent, R,
                           num_q_heads, pool->num_kv_heads, pool->head_dim, pool->page_size,
                           pool->num_pages, sm_scale, opts, split_req, pl, ws);
@@ -500,7 +504,7 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
     // report the whole size (rows, tables and the plan's workspace); nothing enqueued
     pps_plan* probe = nullptr;
     size_t ws = 0;
-    const pps_status ps = plan_for(&probe, &ws);
+    const pps_status ps = plan_for(&probe, &ws, 0);
     if (ps != PPS_OK) return ps;
     pps_plan_destroy(probe);
     if (out_scratch_bytes) *out_scratch_bytes = off_ws + al(ws);
@@ -549,7 +553,7 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
   // the plan, from the host tables (checks them all)
   pps_plan* plan = nullptr;
   size_t ws_bytes = 0;
-  pps_status st = plan_for(&plan, &ws_bytes);
+  pps_status st = plan_for(&plan, &ws_bytes, split_request(host_out != nullptr));
   if (st != PPS_OK) return st;
   const size_t need = off_ws + al(ws_bytes);
   if (out_scratch_bytes) *out_scratch_bytes = need;
@@ -628,7 +632,8 @@ pps_status step_impl(const pps_pool* pool, const void* q, const void* k_new, con
     else if (pps::launch_kv_append_slots(*pool, dk, dv, d_tab + slots_off, T, stream))
       st = PPS_ERR_CUDA;
   }
-  const bool split_out = rows_on_host && !out_direct && !fused && plan->num_mma_first > 0;
+  const bool split_out = rows_on_host && host_out && !out_direct && !fused &&
+                         plan->num_mma_first > 0;
   if (ok && st == PPS_OK)
     st = run_impl(plan, dq, pool, dout, sc + off_ws, al(ws_bytes), stream, events, kRunKernels,
                   fused ? &app : nullptr, split_out ? rc->split : nullptr);
