@@ -183,12 +183,14 @@ def test_step_with_large_task_table(pps):
         assert torch.equal(pv2.view(torch.int16), pv.view(torch.int16))
 
 
-def test_step_host_split_output_copy(pps):
+@pytest.mark.parametrize("locked", [True, False])
+def test_step_host_split_output_copy(pps, locked):
     """Host-row prefill steps whose output (over 16 MB, several requests, only
-    tensor-core tasks, no groups, no partials) goes back in two parts: the
-    first requests' rows leave after a tensor-core launch over just their
-    tasks, the rest after the second.  Outputs and pool must match the
-    separate calls bit for bit, steps enqueued back to back."""
+    tensor-core tasks, no groups, no partials) goes back in two parts when the
+    output is page-locked: the first requests' rows leave after a tensor-core
+    launch over just their tasks, the rest after the second (pageable output:
+    one copy after one launch).  Outputs and pool must match the separate
+    calls bit for bit, steps enqueued back to back."""
     import workloads
     wl = workloads.long_prefill(num_requests=4, chunk=640, num_chunks=3, num_q_heads=32,
                                 num_kv_heads=8, head_dim=128, page_size=64, keep_segments=False)
@@ -203,6 +205,9 @@ def test_step_host_split_output_copy(pps):
     outs, (pk, pv), _ = run_workload(wl, device_inputs=dev_in)
     pk2, pv2 = wl.pool_k.to("cuda", copy=True), wl.pool_v.to("cuda", copy=True)
     rows = [_host_rows(st) for st in wl.steps]
+    if not locked:
+        rows = [(q, k, v, torch.full(tuple(o.shape), float("nan"), dtype=torch.bfloat16))
+                for q, k, v, o in rows]
     scratch = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     pps.get_device_error(clear=True)
     for st, (q, k, v, out) in zip(wl.steps, rows):
