@@ -33,7 +33,10 @@ def _check(got, ref):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 8, 8), (127, 256, 64), (128, 256, 128), (129, 264, 72),
-                                   (300, 520, 200), (5, 1024, 4096), (4101, 1024, 512)])
+                                   (300, 520, 200), (5, 1024, 4096), (4101, 1024, 512),
+                                   # around a CTA pair's 256 x 256 tile and its 128-deep K block
+                                   (255, 256, 128), (256, 512, 192), (257, 520, 136),
+                                   (513, 8, 256), (384, 768, 4224)])
 def test_gemm_matches_oracle(pps, M, N, K):
     a, w = _inputs(M, N, K, M + N + K)
     c = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
