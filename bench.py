@@ -369,15 +369,25 @@ def measure_attention(name, args, dev, cpu_seconds):
 
     # ---- kernel times with a cold L2 (KV that L2 could partly hold) -----------------------
     # Each step is preceded by a write of a buffer four times the L2 size; only the
-    # per-kernel events count, so the flush itself is never timed.
+    # per-kernel events count, so the flush itself is never timed.  The write leaves
+    # L2 full of dirty lines, whose write-back then lands inside the next kernel (up to
+    # 129 MB of writes the kernel never made), so the roofline times are taken with the
+    # buffer also read back after its write: L2 then holds clean lines of the flush
+    # buffer and none of the step's data.  The dirty-L2 times are reported beside them.
     l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129e6)
     kv_unique0 = sum(s["info"]["kv_bytes_unique"] for s in steps)
     flush = args.flush_l2 == "on" or (args.flush_l2 == "auto" and kv_unique0 < 4 * l2_bytes)
-    cold_ms = None
+    cold_ms = dirty_ms = None
     if flush:
         fbuf = torch.empty(4 * l2_bytes // 4, dtype=torch.int32, device=dev)
         for k in range(args.steps):
             fbuf.fill_(k)
+            one_step(evh[k])
+        torch.cuda.synchronize()
+        dirty_ms = kernel_ms()
+        for k in range(args.steps):
+            fbuf.fill_(k)
+            fbuf.sum(dtype=torch.int64)
             one_step(evh[k])
         torch.cuda.synchronize()
         cold_ms = kernel_ms()
@@ -447,7 +457,8 @@ def measure_attention(name, args, dev, cpu_seconds):
                    "tokens_per_step": tokens, "kv_bytes_unique_per_step": kv_unique,
                    "l2": (f"step time warm (KV only {kv_unique / l2_bytes:.1f}x L2); kernel "
                           f"times for the roofline re-measured with a {4 * l2_bytes} B L2 flush "
-                          f"before every step") if flush else
+                          f"before every step (the buffer written, then read back so that L2 "
+                          f"holds no dirty lines)") if flush else
                    "inputs larger than L2 (KV > 4x the 129 MB L2), no flush",
                    "parallelism": f"dp{world} (independent batch per GPU, no collective)",
                    "step_call": "pps_attn_step: one native call per step and chunk (tables "
@@ -466,7 +477,10 @@ def measure_attention(name, args, dev, cpu_seconds):
         **({"cold_l2": {"kernel_ms_per_step": dict(zip(("bandwidth", "tensor", "merge"), cold_ms)),
                         "attention_unique_gbs": kv_unique / (max(cold_ms[0], cold_ms[1])
                                                              + cold_ms[2]) * 1e3 / 1e9,
-                        "flush_bytes": 4 * l2_bytes}} if cold_ms is not None else {}),
+                        "flush_bytes": 4 * l2_bytes, "flush": "write, then read back",
+                        "kernel_ms_per_step_dirty_l2": dict(zip(("bandwidth", "tensor", "merge"),
+                                                                dirty_ms))}}
+           if cold_ms is not None else {}),
         "clocks": clocks,
         "achieved": {"kv_unique_gbs": kv_unique / (ms_max / 1e3) / 1e9,
                      "attention_unique_gbs": kv_unique / (max(kern_ms[0], kern_ms[1]) + kern_ms[2])

@@ -587,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto qk_at = [&](auto xc, auto sc) {
       constexpr int X = decltype(xc)::value, ST = decltype(sc)::value;
       tc_fence_after();
-      if (lane == 0) {
+      if (elect_one()) {
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) umma_ss(tS[X], qdsc[X][ks], kdsc[ST][ks], id_qk, ks > 0);
         umma_commit(smem_u32(&bars.s_full[X]));
@@ -599,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto pv_at = [&](auto xc, auto sc, int steps, bool first, bool last_of_task) {
       constexpr int X = decltype(xc)::value, ST = decltype(sc)::value;
       tc_fence_after();
-      if (lane == 0) {
+      if (elect_one()) {
         if (steps == VS && !first) {
 #pragma unroll
           for (int ks = 0; ks < VS; ++ks) umma_ts(tO[X], tS[X] + ks * 8, vdsc[ST][ks], id_pv, 1u);
@@ -670,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nt[0] > 0) qk(I0{}, st);
         if (nt[1] > 0) qk(I1{}, st);
         tc_fence_after();
-        if (lane == 0) umma_commit(smem_u32(&bars.k_empty[st]));   // K_0 used by both QKs
+        if (elect_one()) umma_commit(smem_u32(&bars.k_empty[st]));   // K_0 used by both QKs
         __syncwarp();
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
@@ -686,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        if (lane == 0) {
+        if (elect_one()) {
           umma_commit(smem_u32(&bars.v_empty[st]));                 // V_j no longer needed
           if (next) umma_commit(smem_u32(&bars.k_empty[stn]));      // K_{j+1} used by its QKs
         }
@@ -695,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       it += n_tiles;
     }
     // Every MMA this warp issued has completed before TMEM is freed.
-    if (lane == 0) {
+    if (elect_one()) {
       umma_commit(smem_u32(&bars.drain));
       if (!mbar_wait(smem_u32(&bars.drain), 0)) fail();
     }

@@ -664,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = g % kStages;
       if (!warp_wait(&bars.k_full[st], (g / kStages) & 1)) return false;
       tc_fence_after();
-      if (lane == 0) {
+      if (elect_one()) {
         const uint32_t kt = k_base + st * L::kv_tile;
         const uint32_t qt = q_base + qb * L::q_tile;
 #pragma unroll
@@ -720,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           return false;
         }
         if (q_n == 0) {                             // no QK reads the buffer
-          if (lane == 0) umma_commit(smem_u32(&bars.q_empty[q_ti & 1]));
+          if (elect_one()) umma_commit(smem_u32(&bars.q_empty[q_ti & 1]));
           __syncwarp();
         }
       }
@@ -730,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
       }
       if (q_j == q_n - 1) {                         // the task's last QK: its buffer frees
-        if (lane == 0) umma_commit(smem_u32(&bars.q_empty[q_ti & 1]));
+        if (elect_one()) umma_commit(smem_u32(&bars.q_empty[q_ti & 1]));
         __syncwarp();
       }
       ++q_j;
@@ -745,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = n_tiles_of(task);
       const int ob = ti & 1;
       if (n == 0) {                                 // nothing accumulated: O is ready now
-        if (lane == 0) umma_commit(smem_u32(&bars.o_done[ob]));
+        if (elect_one()) umma_commit(smem_u32(&bars.o_done[ob]));
         __syncwarp();
         continue;
       }
@@ -757,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nks = (valid + 15) >> 4;              // PV steps holding a valid key
         if (valid & 15) clear_v_rows(st, valid);
         tc_fence_after();
-        if (lane == 0) {
+        if (elect_one()) {
           const uint32_t vt = v_base + st * L::kv_tile;
           const uint32_t pt = p_base + sb * L::p_tile;
           if (nks == kTile / 16) {                  // whole tile: back-to-back issue
@@ -786,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       gt += n;
     }
     // Every MMA this warp issued has completed before TMEM is freed.
-    if (lane == 0) {
+    if (elect_one()) {
       umma_commit(smem_u32(&bars.drain));
       if (!mbar_wait(smem_u32(&bars.drain), 0)) fail();
     }

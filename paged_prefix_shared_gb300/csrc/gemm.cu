@@ -132,7 +132,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const int s = it % kStages, use = it / kStages;
         if (!warp_wait(&bars.empty[s], (use - 1) & 1, use > 0)) { fail(); ok = false; break; }
-        if (lane == 0) {
+        if (elect_one()) {
           const uint32_t fb = mapa_shared(smem_u32(&bars.full[s]), 0);
           const uint32_t base = smem_u32(smem + s * kStageBytes);
           if (rank == 0) mbar_expect_tx(smem_u32(&bars.full[s]), 2 * kStageBytes);
@@ -166,7 +166,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int s = it % kStages;
           if (!warp_wait(&bars.full[s], (it / kStages) & 1)) { fail(); ok = false; break; }
           tc_fence_after();
-          if (lane == 0) {
+          if (elect_one()) {
             const uint32_t a0 = smem_u32(smem + s * kStageBytes), w0 = a0 + kABytes;
 #pragma unroll
             for (int ks = 0; ks < kBK / 16; ++ks)
@@ -179,10 +179,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
         if (!ok) break;
-        if (lane == 0) umma_commit_pair_mc(smem_u32(&bars.acc_full[b]), kPairMask);
+        if (elect_one()) umma_commit_pair_mc(smem_u32(&bars.acc_full[b]), kPairMask);
         __syncwarp();
       }
-      if (lane == 0) {
+      if (elect_one()) {
         umma_commit_pair(smem_u32(&bars.drain));
         if (!mbar_wait(smem_u32(&bars.drain), 0)) fail();
       }

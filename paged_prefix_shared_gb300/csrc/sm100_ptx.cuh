@@ -68,6 +68,21 @@ __device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity,
   }
 }
 
+// One lane of a converged warp (the lowest active one, the same lane every
+// time): the lane that issues a warp's tcgen05 MMAs and commits.  Unlike a
+// plain lane-0 test, the compiler knows exactly one thread runs the branch, so
+// warp-uniform operands (descriptors, TMEM addresses) reach the MMA
+// instructions without per-thread handling; the MMA issuer runs markedly
+// faster this way.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n .reg .pred P;\n .reg .b32 r;\n elect.sync r|P, 0xffffffff;\n"
+      " selp.b32 %0, 1, 0, P;\n}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ---- proxies / fences ------------------------------------------------------------
 // Generic-proxy writes to shared memory become visible to the async proxy
 // (TMA, tensor core) after this fence.
