@@ -370,7 +370,7 @@ __device__ __forceinline__ bool bw_consume(const pps::Task& task, int nrows, int
     const int wi = g / kBw2Consumers;
     const int s = warp * kStagesPerWarp + wi % kStagesPerWarp;
     const bool got =
-        sm100::mbar_wait(sm100::smem_u32(&sh.full[s]), (wi / kStagesPerWarp) & 1) && !*sh.abort_flag;
+        sm100::mbar_wait_live(sm100::smem_u32(&sh.full[s]), (wi / kStagesPerWarp) & 1, sh.abort_flag);
     if (!__all_sync(0xffffffffu, got)) {
       if (lane == 0) {
         atomicCAS(sh.err, 0, PPS_DEV_ERR_WAIT_TIMEOUT);

@@ -224,9 +224,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // A wait whose outcome is the same for every lane of the warp (the warp then
   // goes on to warp-collective tcgen05 ld/st together, or leaves together).
-  auto warp_wait = [&](uint64_t* bar, uint32_t parity, bool needed = true) {
+  // The abort flag is read only when the phase has not completed at the first
+  // poll (a shared-memory load in every wait slowed the MMA issuer).
+  auto warp_wait = [&](uint64_t* bar, uint32_t parity, bool needed = true) -> bool {
+    if (__all_sync(0xffffffffu, !needed || mbar_try_wait(smem_u32(bar), parity))) return true;
     const bool ok = (!needed || mbar_wait(smem_u32(bar), parity)) && !abort_flag;
-    return __all_sync(0xffffffffu, ok);
+    return __all_sync(0xffffffffu, ok) != 0;
   };
 
   if (warp < kSoftmaxWarps) {
@@ -549,34 +552,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp runs the loop (waits, the V-tail clear); lane 0 issues.
     // The tensor core queues only a few MMAs and this warp shares its
     // scheduler with two busy softmax warps, so an MMA must cost the issuer
-    // as few instructions as possible: every descriptor (per query tile or
-    // ring stage and K step) is built once into registers, and each issue
-    // instance is compiled for a fixed tile and stage.
+    // as few instructions as possible.  Each issue instance is compiled for a
+    // fixed tile and stage; inside the elected branch the descriptors are the
+    // stage's base descriptor plus the K step's constant offset, values the
+    // compiler keeps uniform (holding all 48 descriptors in per-thread
+    // registers made every MMA slower to issue), and no wait of this warp
+    // reads the abort flag unless it has to block.
     constexpr uint32_t id_qk = idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t id_pv = idesc_bf16(128, D, 0, 1);
     constexpr int KS = D / 16;                      // K steps of QK
     constexpr int VS = kTile / 16;                  // K steps of PV
-    uint64_t qdsc[2][KS], kdsc[kStages][KS], vdsc[kStages][VS];
     uint32_t tS[2], tO[2];
 #pragma unroll
     for (int x = 0; x < 2; ++x) {
       tS[x] = tm + x * 128;                         // S_x (P_x over its first 64 columns)
       tO[x] = tm + 256 + x * D;                     // O_x
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks)
-        qdsc[x][ks] = smem_desc(q_base + x * Lay::kTileBytes + (ks / 4) * 16384 + (ks % 4) * 32,
-                                16, 1024);
     }
-#pragma unroll
-    for (int st = 0; st < kStages; ++st) {
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks)
-        kdsc[st][ks] = smem_desc(k_base + st * Lay::kTileBytes + (ks / 4) * 16384 + (ks % 4) * 32,
-                                 16, 1024);
-#pragma unroll
-      for (int ks = 0; ks < VS; ++ks)
-        vdsc[st][ks] = smem_desc(v_base + st * Lay::kTileBytes + ks * 2048, 16384, 1024);
-    }
+    // descriptor of K step ks: the base descriptor plus the step's offset / 16
+    auto koff = [](int ks) { return (uint64_t)(((ks / 4) * 16384 + (ks % 4) * 32) >> 4); };
     int it = 0;                                     // KV tiles consumed (ring position)
     int px[2] = {0, 0};                             // phases consumed on p_full[X]
     int qn = 0;                                     // phases consumed on q_full
@@ -588,8 +581,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int X = decltype(xc)::value, ST = decltype(sc)::value;
       tc_fence_after();
       if (elect_one()) {
+        const uint64_t qd = smem_desc(q_base + X * Lay::kTileBytes, 16, 1024);
+        const uint64_t kd = smem_desc(k_base + ST * Lay::kTileBytes, 16, 1024);
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) umma_ss(tS[X], qdsc[X][ks], kdsc[ST][ks], id_qk, ks > 0);
+        for (int ks = 0; ks < KS; ++ks)
+          umma_ss(tS[X], qd + koff(ks), kd + koff(ks), id_qk, ks > 0);
         umma_commit(smem_u32(&bars.s_full[X]));
       }
       __syncwarp();
@@ -600,14 +596,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int X = decltype(xc)::value, ST = decltype(sc)::value;
       tc_fence_after();
       if (elect_one()) {
+        const uint64_t vd = smem_desc(v_base + ST * Lay::kTileBytes, 16384, 1024);
         if (steps == VS && !first) {
 #pragma unroll
-          for (int ks = 0; ks < VS; ++ks) umma_ts(tO[X], tS[X] + ks * 8, vdsc[ST][ks], id_pv, 1u);
+          for (int ks = 0; ks < VS; ++ks) umma_ts(tO[X], tS[X] + ks * 8, vd + (uint64_t)(ks * 128), id_pv, 1u);
         } else {
 #pragma unroll
           for (int ks = 0; ks < VS; ++ks)
             if (ks < steps)
-              umma_ts(tO[X], tS[X] + ks * 8, vdsc[ST][ks], id_pv, (!first || ks > 0) ? 1u : 0u);
+              umma_ts(tO[X], tS[X] + ks * 8, vd + (uint64_t)(ks * 128), id_pv, (!first || ks > 0) ? 1u : 0u);
         }
         if (last_of_task) umma_commit(smem_u32(&bars.o_done[X]));
       }

@@ -281,7 +281,7 @@ __device__ __forceinline__ bool softmax_tiles(const SmCtx& c, const pps::Task& t
   for (int j = 0; j < n; ++j, ++gt) {
     const int sb = gt & 1;
     const int t0 = task.kv_begin + j * kTile;
-    bool got = mbar_wait(smem_u32(&c.bars->s_full[sb]), (gt >> 1) & 1) && !*c.abort_flag;
+    bool got = mbar_wait_live(smem_u32(&c.bars->s_full[sb]), (gt >> 1) & 1, c.abort_flag);
     // the P^T buffer sb is free once the PV two tiles back has completed
     if (gt >= 2) got = got && mbar_wait(smem_u32(&c.bars->p_empty[sb]), ((gt - 2) >> 1) & 1);
     if (softmax_or(!got)) {
@@ -425,7 +425,7 @@ __device__ __forceinline__ bool softmax_output(const SmCtx& c, const pps::Task& 
   const int t = c.t;
   const int n = n_tiles_of(task), nrows = task.n_tok * p.G;
   bool got = true;
-  if (n > 0) got = mbar_wait(smem_u32(&c.bars->o_done[ti & 1]), (ti >> 1) & 1) && !*c.abort_flag;
+  if (n > 0) got = mbar_wait_live(smem_u32(&c.bars->o_done[ti & 1]), (ti >> 1) & 1, c.abort_flag);
   if (softmax_or(!got)) {
     if (t == 0) sm_fail(c);
     return false;
@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     abort_flag = 1;
   };
   auto warp_wait = [&](uint64_t* bar, uint32_t parity, bool needed = true) {
-    const bool ok = (!needed || mbar_wait(smem_u32(bar), parity)) && !abort_flag;
+    const bool ok = !needed || mbar_wait_live(smem_u32(bar), parity, &abort_flag);
     return __all_sync(0xffffffffu, ok);
   };
 

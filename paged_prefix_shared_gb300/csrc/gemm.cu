@@ -114,7 +114,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     abort_flag = 1;
   };
   auto warp_wait = [&](uint64_t* bar, uint32_t parity, bool needed = true) {
-    const bool ok = (!needed || mbar_wait(smem_u32(bar), parity)) && !abort_flag;
+    const bool ok = !needed || mbar_wait_live(smem_u32(bar), parity, &abort_flag);
     return __all_sync(0xffffffffu, ok);
   };
 

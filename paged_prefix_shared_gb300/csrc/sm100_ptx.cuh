@@ -51,6 +51,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// A wait that also gives up when another warp of the CTA has raised `abort`.
+// The flag is read only when the phase has not completed at the first poll:
+// a warp whose barriers keep completing runs on (it blocks, and sees the flag,
+// at its first wait that does not), and the common path costs no shared-memory
+// load.
+__device__ __forceinline__ bool mbar_wait_live(uint32_t bar, uint32_t parity,
+                                               const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait(bar, parity) && !*abort;
+}
+
 // The same wait for a warp with nothing else to do meanwhile (a loader that
 // runs a task ahead): it sleeps between polls instead of spinning, leaving the
 // issue slots of its scheduler to the warps on the critical path.
