@@ -632,18 +632,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
     };
-    // one query tile's step of KV tile j: PV_X(j), then QK_X(j + 1)
+    // one query tile's step of KV tile j: PV_X(j), then QK_X(j + 1) (V_j has
+    // been waited for already)
     auto tile_step = [&](auto xc, int j, const int (&nt)[2], int st, int stn, int valid,
-                         bool& v_ready, bool& k_ready) {
+                         bool& k_ready) {
       constexpr int X = decltype(xc)::value;
       if (j >= nt[X]) return true;
       if (!warp_wait(&bars.p_full[X], px[X] & 1)) return false;
       ++px[X];
-      if (!v_ready) {
-        if (!warp_wait(&bars.v_full[st], ((it + j) / kStages) & 1)) return false;
-        if (valid & 15) clear_v_tail(st, valid);
-        v_ready = true;
-      }
       pv(xc, st, (valid + 15) / 16, j == 0, j + 1 == nt[X]);
       if (j + 1 < nt[X]) {
         if (!k_ready) {
@@ -670,14 +666,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (elect_one()) umma_commit(smem_u32(&bars.k_empty[st]));   // K_0 used by both QKs
         __syncwarp();
       }
+      // V_j is waited for (and its tail cleared) at the end of step j - 1, where
+      // the wait's latency hides behind the MMAs just queued
+      auto v_wait = [&](int j) -> bool {
+        const int sj = (it + j) % kStages;
+        if (!warp_wait(&bars.v_full[sj], ((it + j) / kStages) & 1)) return false;
+        const int vj = min(kTile, task.kv_end - (task.kv_begin + j * kTile));
+        if (vj & 15) clear_v_tail(sj, vj);
+        return true;
+      };
+      if (n_tiles > 0 && !v_wait(0)) { fail(); ok = false; break; }
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = (it + j) % kStages;
         const int stn = (it + j + 1) % kStages;
         const bool next = j + 1 < n_tiles;
         const int valid = min(kTile, task.kv_end - (task.kv_begin + j * kTile));
-        bool v_ready = false, k_ready = false;
-        if (!tile_step(I0{}, j, nt, st, stn, valid, v_ready, k_ready) ||
-            !tile_step(I1{}, j, nt, st, stn, valid, v_ready, k_ready)) {
+        bool k_ready = false;
+        if (!tile_step(I0{}, j, nt, st, stn, valid, k_ready) ||
+            !tile_step(I1{}, j, nt, st, stn, valid, k_ready)) {
           fail();
           ok = false;
           break;
@@ -688,6 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (next) umma_commit(smem_u32(&bars.k_empty[stn]));      // K_{j+1} used by its QKs
         }
         __syncwarp();
+        if (next && !v_wait(j + 1)) { fail(); ok = false; break; }
       }
       it += n_tiles;
     }
