@@ -333,6 +333,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // one straight block of code and the rest stays out of its way: the
         // instruction cache is shared by every warp of a scheduler, and the MMA
         // issuer stalls whenever the softmax code pushes its instructions out.
+        // A row's first tile with every column visible: its maximum becomes
+        // the reference, and the tile takes the hot path.
+        if (__all_sync(0xffffffffu, full && m_ref == -INFINITY)) {
+          float mx = -INFINITY;
+#pragma unroll 1
+          for (int c0 = 0; c0 < kTile; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tm_s + lane_off + c0, rr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(rr[c]));
+          }
+          m_ref = mx * p.qk_scale;
+        }
         float rs0 = 0.f, rs1 = 0.f, alpha = 1.f, m_use = m_ref;
         bool exact = !__all_sync(0xffffffffu, full && m_ref != -INFINITY);
         if (!exact) {
