@@ -479,11 +479,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
       const bool direct = task.out_pid < 0;
       const size_t prow = direct ? 0 : (size_t)(task.out_pid + i) * p.num_q_heads + h;
+      // With G a multiple of 4, the 4 lanes of each lane quad hold one token's
+      // 4 consecutive heads, rows that are contiguous in the output: a 4 x 4
+      // transpose of 16-byte pieces across the quad lets every store of the
+      // warp write 64 contiguous bytes per quad instead of 16 scattered ones.
+      const bool quads = direct && (G & 3) == 0;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t rr[32];
         tmem_ld32(tm_o + lane_off + c0, rr);
         tmem_wait_ld();
+        if (quads) {
+          int4 pc[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t* v = rr + 8 * q;
+            pc[q].x = (int)pack_bf16(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv);
+            pc[q].y = (int)pack_bf16(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
+            pc[q].z = (int)pack_bf16(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv);
+            pc[q].w = (int)pack_bf16(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv);
+          }
+          const int k = lane & 3;
+          auto xchg = [&](int4& a, int4& b, bool hi, int mask) {
+            // send b (hi lanes send a), receive into the slot that was sent
+            int4 s = hi ? a : b, r;
+            r.x = __shfl_xor_sync(0xffffffffu, s.x, mask);
+            r.y = __shfl_xor_sync(0xffffffffu, s.y, mask);
+            r.z = __shfl_xor_sync(0xffffffffu, s.z, mask);
+            r.w = __shfl_xor_sync(0xffffffffu, s.w, mask);
+            if (hi) a = r; else b = r;
+          };
+          xchg(pc[0], pc[2], (k & 2) != 0, 2);
+          xchg(pc[1], pc[3], (k & 2) != 0, 2);
+          xchg(pc[0], pc[1], (k & 1) != 0, 1);
+          xchg(pc[2], pc[3], (k & 1) != 0, 1);
+          // lane k now holds piece k of the quad's rows 0..3
+          if (real) {
+            __nv_bfloat16* grp = p.out + ((size_t)tok * p.num_q_heads + (h - k)) * D + c0 + 8 * k;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) *reinterpret_cast<int4*>(grp + (size_t)q * D) = pc[q];
+          }
+          continue;
+        }
         if (real) {
           if (direct) {
             __nv_bfloat16* dst = p.out + ((size_t)tok * p.num_q_heads + h) * D + c0;
