@@ -15,7 +15,7 @@
 // tree rows (Fig. 8, tree-based speculation) also mask the draft positions
 // that are not their ancestors, in the KV tiles their 64-key window reaches.
 //
-// Warp roles (320 threads, one persistent CTA per SM taking tasks in
+// Warp roles (352 threads, one persistent CTA per SM taking tasks in
 // symmetric round-robin order over the work-sorted list):
 //   warps 0-3  softmax A, warps 4-7 softmax B: thread m of a warpgroup owns
 //              query row m = TMEM lane m.  It loads its Q row into 128-byte
@@ -24,8 +24,11 @@
 //              rescale in TMEM, only when a score exceeds that reference by more
 //              than 2^8), writes P as bf16 over S's own columns, and writes the
 //              output row or the partial (o, lse).
-//   warp 8     TMA producer: K and V tiles of 128 positions (one box per page
-//              and 64-column block, issued by one lane each) into a 2-stage ring.
+//   warps 8/10 TMA producers of K and of V: tiles of 128 positions (one box
+//              per page and 64-column block, issued by one lane each) into a
+//              2-stage ring each.  Two warps, so that a K tile whose stage has
+//              freed never queues behind the V tile's issue (with 16-position
+//              pages a tile is 16 boxes).
 //   warp 9     MMA issuer: S_X = Q_X K^T (both K-major in shared memory) and
 //              O_X += P_X V (P from TMEM, V MN-major in shared memory), in the
 //              order PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1).
@@ -52,7 +55,8 @@ using namespace sm100;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kProducerVWarp = 10;
+constexpr int kThreads = 352;
 constexpr int kStages = 2;
 constexpr int kTile = 128;                    // KV positions per tile = query rows per tile
 constexpr float kRescaleThreshold = 8.f;      // log2 units
@@ -547,15 +551,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();       // the O reads finish before the next task's first PV
     }
     cp_async_wait_all();       // a prefetched row of a task that never started
-  } else if (warp == kProducerWarp) {
-    // ------------------------------------------------------------- TMA producer
-    // Lane 0 arms a stage's barrier with the tile's byte count, then one lane
-    // per (page, 64-column block) issues its box: a single issuing thread
-    // cannot issue small TMA loads fast enough to keep the tensor core fed.
-    if (lane == 0) {
-      prefetch_tmap(&tmk);
-      prefetch_tmap(&tmv);
-    }
+  } else if (warp == kProducerWarp || warp == kProducerVWarp) {
+    // ------------------------------------------------------------- TMA producers
+    // (K in warp 8, V in warp 10.)  Lane 0 arms a stage's barrier with the
+    // tile's byte count, then one lane per (page, 64-column block) issues its
+    // box: a single issuing thread cannot issue small TMA loads fast enough to
+    // keep the tensor core fed.
+    const bool is_k = warp == kProducerWarp;
+    const CUtensorMap* map = is_k ? &tmk : &tmv;
+    const uint32_t ring = is_k ? k_base : v_base;
+    uint64_t* full = is_k ? bars.k_full : bars.v_full;
+    uint64_t* empty = is_k ? bars.k_empty : bars.v_empty;
+    if (lane == 0) prefetch_tmap(map);
     const int P = p.page_size;
     const uint32_t box_bytes = (uint32_t)P * 128u;
     int it = 0;                                     // KV tiles loaded by this CTA
@@ -573,20 +580,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pg = lane / KB, kb = lane % KB;
         const bool mine = lane < npg * KB;
         const int page = mine ? p.pages[task.page_off + (t0 + pg * P) / P] : 0;
-        const uint32_t kf = smem_u32(&bars.k_full[st]);
-        if (!warp_wait(&bars.k_empty[st], (use - 1) & 1, use > 0)) { fail(); ok = false; break; }
-        if (lane == 0) mbar_expect_tx(kf, bytes);
+        const uint32_t fb = smem_u32(&full[st]);
+        if (!warp_wait(&empty[st], (use - 1) & 1, use > 0)) { fail(); ok = false; break; }
+        if (lane == 0) mbar_expect_tx(fb, bytes);
         __syncwarp();
         if (mine)
-          tma_load_4d(k_base + st * Lay::kTileBytes + kb * 16384 + pg * P * 128, &tmk, kb * 64, 0,
-                      task.kv_head, page, kf);
-        const uint32_t vf = smem_u32(&bars.v_full[st]);
-        if (!warp_wait(&bars.v_empty[st], (use - 1) & 1, use > 0)) { fail(); ok = false; break; }
-        if (lane == 0) mbar_expect_tx(vf, bytes);
-        __syncwarp();
-        if (mine)
-          tma_load_4d(v_base + st * Lay::kTileBytes + kb * 16384 + pg * P * 128, &tmv, kb * 64, 0,
-                      task.kv_head, page, vf);
+          tma_load_4d(ring + st * Lay::kTileBytes + kb * 16384 + pg * P * 128, map, kb * 64, 0,
+                      task.kv_head, page, fb);
       }
     }
     // every load this CTA started lands before it may exit
@@ -594,13 +594,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t lim = ok ? 2000000000ull : 10000000ull;
       for (int j = (it > kStages ? it - kStages : 0); j < it; ++j) {
         const int st = j % kStages, use = j / kStages;
-        mbar_wait(smem_u32(&bars.k_full[st]), use & 1, lim);
-        mbar_wait(smem_u32(&bars.v_full[st]), use & 1, lim);
+        mbar_wait(smem_u32(&full[st]), use & 1, lim);
       }
     }
   } else {
     // ------------------------------------------------------------- MMA issuer
-    // The whole warp runs the loop (waits, the V-tail clear); lane 0 issues.
+    // The whole warp runs the loop (waits, the V-tail clear); one elected lane
+    // issues the MMAs and commits.
     // The tensor core queues only a few MMAs and this warp shares its
     // scheduler with two busy softmax warps, so an MMA must cost the issuer
     // as few instructions as possible.  Each issue instance is compiled for a
