@@ -351,8 +351,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           m_ref = mx * p.qk_scale;
         }
+        // A masked tile after the row's first: -inf over the invisible
+        // columns of S (chunks with every column visible are skipped), and
+        // the tile takes the hot path like a full one.
+        bool masked = false;
+        if (!full && __all_sync(0xffffffffu, m_ref != -INFINITY)) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < kTile; c0 += 32) {
+            const uint32_t vb = (uint32_t)((c0 < 64 ? vis[0] : vis[1]) >> (c0 & 63));
+            if (__any_sync(0xffffffffu, vb != ~0u)) {
+              uint32_t rr[32];
+              tmem_ld32(tm_s + lane_off + c0, rr);
+              tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                if (!((vb >> c) & 1u)) rr[c] = 0xff800000u;
+              tmem_st32(tm_s + lane_off + c0, rr);
+            }
+          }
+          tmem_wait_st();
+          masked = true;
+        }
         float rs0 = 0.f, rs1 = 0.f, alpha = 1.f, m_use = m_ref;
-        bool exact = !__all_sync(0xffffffffu, full && m_ref != -INFINITY);
+        bool exact = !__all_sync(0xffffffffu, (full || masked) && m_ref != -INFINITY);
         if (!exact) {
           const uint64_t sc2 = f32x2(p.qk_scale, p.qk_scale);
           const uint64_t nm2 = f32x2(-m_ref, -m_ref);
