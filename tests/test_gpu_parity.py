@@ -45,6 +45,15 @@ def small_cases():
                                                   num_verify=3, mu=4.0, sigma=1.0, clip_lo=1,
                                                   clip_hi=700, num_q_heads=4, num_kv_heads=4,
                                                   head_dim=128, page_size=128),
+        # prefill chunks written directly by tensor-core tiles at G = 1 and 2:
+        # the rows of a lane quad are not one token's heads there, so they take
+        # the per-row stores instead of the quad transpose
+        "g2_prefill": lambda: workloads.long_prefill(num_requests=2, chunk=200, num_chunks=2,
+                                                     num_q_heads=8, num_kv_heads=4, head_dim=128,
+                                                     page_size=64),
+        "g1_prefill_d64": lambda: workloads.long_prefill(num_requests=2, chunk=150, num_chunks=2,
+                                                         num_q_heads=4, num_kv_heads=4,
+                                                         head_dim=64, page_size=32),
         # draft trees: 40-token trees (tensor-core tiles of 160 rows), 64-token
         # trees at G = 8 (two tasks per tree), 8-token trees at G = 1 (bandwidth
         # kernel), and trees behind a shared prefix (group tasks + tree tasks)
