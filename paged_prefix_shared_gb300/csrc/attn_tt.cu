@@ -533,9 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     atomicCAS(p.err, 0, PPS_DEV_ERR_WAIT_TIMEOUT);
     abort_flag = 1;
   };
-  auto warp_wait = [&](uint64_t* bar, uint32_t parity, bool needed = true) {
-    const bool ok = !needed || mbar_wait_live(smem_u32(bar), parity, &abort_flag);
-    return __all_sync(0xffffffffu, ok);
+  auto warp_wait = [&](uint64_t* bar, uint32_t parity, bool needed = true) -> bool {
+    if (__all_sync(0xffffffffu, !needed || mbar_try_wait(smem_u32(bar), parity))) return true;
+    const bool ok = (!needed || mbar_wait(smem_u32(bar), parity)) && !abort_flag;
+    return __all_sync(0xffffffffu, ok) != 0;
   };
 
   if (warp < 4) {
@@ -665,14 +666,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(&bars.k_full[st], (g / kStages) & 1)) return false;
       tc_fence_after();
       if (elect_one()) {
-        const uint32_t kt = k_base + st * L::kv_tile;
-        const uint32_t qt = q_base + qb * L::q_tile;
+        const uint64_t kd = smem_desc(k_base + st * L::kv_tile, 16, 1024);
+        const uint64_t qd = smem_desc(q_base + qb * L::q_tile, 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t ka = (ks / 4) * 16384 + (ks % 4) * 32;
           const uint32_t qa = (ks / 4) * L::q_block + (ks % 4) * 32;
-          umma_ss(tm + (g & 1) * kRows, smem_desc(kt + ka, 16, 1024), smem_desc(qt + qa, 16, 1024),
-                  id_qk, ks > 0);
+          umma_ss(tm + (g & 1) * kRows, kd + (ka >> 4), qd + (qa >> 4), id_qk, ks > 0);
         }
         umma_commit(smem_u32(&bars.s_full[g & 1]));
         umma_commit(smem_u32(&bars.k_empty[st]));
@@ -758,20 +758,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (valid & 15) clear_v_rows(st, valid);
         tc_fence_after();
         if (elect_one()) {
-          const uint32_t vt = v_base + st * L::kv_tile;
-          const uint32_t pt = p_base + sb * L::p_tile;
+          const uint64_t vd = smem_desc(v_base + st * L::kv_tile, 16384, 1024);
+          const uint64_t pd = smem_desc(p_base + sb * L::p_tile, 1024, 512, kLayoutSwizzle64);
           if (nks == kTile / 16) {                  // whole tile: back-to-back issue
 #pragma unroll
             for (int ks = 0; ks < kTile / 16; ++ks)
-              umma_ss(tm_o + ob * kRows, smem_desc(vt + ks * 2048, 16384, 1024),
-                      smem_desc(pt + ks * 1024, 1024, 512, kLayoutSwizzle64), id_pv,
-                      (j > 0 || ks > 0) ? 1u : 0u);
+              umma_ss(tm_o + ob * kRows, vd + (uint64_t)(ks * 128), pd + (uint64_t)(ks * 64),
+                      id_pv, (j > 0 || ks > 0) ? 1u : 0u);
           } else {
 #pragma unroll 1
             for (int ks = 0; ks < nks; ++ks)
-              umma_ss(tm_o + ob * kRows, smem_desc(vt + ks * 2048, 16384, 1024),
-                      smem_desc(pt + ks * 1024, 1024, 512, kLayoutSwizzle64), id_pv,
-                      (j > 0 || ks > 0) ? 1u : 0u);
+              umma_ss(tm_o + ob * kRows, vd + (uint64_t)(ks * 128), pd + (uint64_t)(ks * 64),
+                      id_pv, (j > 0 || ks > 0) ? 1u : 0u);
           }
           umma_commit(smem_u32(&bars.v_empty[st]));
           umma_commit(smem_u32(&bars.p_empty[sb]));
