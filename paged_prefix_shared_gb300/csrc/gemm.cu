@@ -113,9 +113,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     atomicCAS(err, 0, PPS_DEV_ERR_WAIT_TIMEOUT);
     abort_flag = 1;
   };
-  auto warp_wait = [&](uint64_t* bar, uint32_t parity, bool needed = true) {
-    const bool ok = !needed || mbar_wait_live(smem_u32(bar), parity, &abort_flag);
-    return __all_sync(0xffffffffu, ok);
+  auto warp_wait = [&](uint64_t* bar, uint32_t parity, bool needed = true) -> bool {
+    if (__all_sync(0xffffffffu, !needed || mbar_try_wait(smem_u32(bar), parity))) return true;
+    const bool ok = (!needed || mbar_wait(smem_u32(bar), parity)) && !abort_flag;
+    return __all_sync(0xffffffffu, ok) != 0;
   };
 
   if (warp == 0) {
@@ -167,11 +168,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!warp_wait(&bars.full[s], (it / kStages) & 1)) { fail(); ok = false; break; }
           tc_fence_after();
           if (elect_one()) {
-            const uint32_t a0 = smem_u32(smem + s * kStageBytes), w0 = a0 + kABytes;
+            const uint32_t a0 = smem_u32(smem + s * kStageBytes);
+            const uint64_t ad = smem_desc(a0, 16, 1024), wd = smem_desc(a0 + kABytes, 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < kBK / 16; ++ks)
-              umma_ss_pair(tm + b * kBN, smem_desc(a0 + (ks / 4) * kSubA + (ks % 4) * 32, 16, 1024),
-                           smem_desc(w0 + (ks / 4) * kSubB + (ks % 4) * 32, 16, 1024), idesc,
+              umma_ss_pair(tm + b * kBN, ad + (uint64_t)(((ks / 4) * kSubA + (ks % 4) * 32) >> 4),
+                           wd + (uint64_t)(((ks / 4) * kSubB + (ks % 4) * 32) >> 4), idesc,
                            (kb > 0 || ks > 0) ? 1u : 0u);
             // the stage is free in both CTAs once these MMAs finish
             umma_commit_pair_mc(smem_u32(&bars.empty[s]), kPairMask);
